@@ -1,0 +1,192 @@
+"""Seeded synthetic inputs for the selective scan and the recurrent state update.
+
+Shared by the CUDA path's tests/benchmark and by the oracle's tests; it holds none of the
+scan's arithmetic. Every array comes from numpy's PCG64 (``SeedSequence(seed).spawn``, one
+child stream per array role, so adding or dropping an optional array never shifts the
+others). Normal draws are made in float32 and rounded once, round-to-nearest-even, to the
+I/O dtype by torch; the oracle reads exactly the bits the GPU reads.
+
+Workloads (Bt = batch, D = channels "d_inner", L = sequence length, N = state size):
+
+* ``tiny``      1 x 4 x 64, N=4, fp32; no gate, D-skip = 1.
+* ``block512``  1 x 512 x 1024, N=16, bf16; z ~ N(0,1) gate; D-skip ~ N(0,1).
+                (d_model 256, expand 2: the usage example of "Python Mamba: an
+                underrated state-space model tool".)
+* ``m130``      8 x 1536 x 2048, N=16, bf16; z ~ N(0,1) gate; D-skip = 1.
+                (d_model 768, expand 2: the 130M row of the model-size table on
+                atcfu.com "Mamba" source-analysis page.)
+* ``long128k``  1 x 1536 x 131072, N=64, bf16; u an AR(1) series (rho 0.9, unit
+                variance); no gate; D-skip = 1; the final state is returned.
+                (N=64 for >100K tokens follows the d_state advice on the
+                "Python Mamba" page.)
+* ``decode``    256 x 5120, N=16, 64 successive single-token steps from an N(0,1)
+                fp32 state (d_inner of the 2.8B row, 2 x 2560).
+
+In every scan workload A[d, n] = -(n+1) (the S4D-real initialisation, A_log = log(1..N),
+of "From RNN to Mamba", section 3.3); u, B, C ~ N(0,1) unless stated; the raw step
+``delta`` ~ N(0, 0.5^2) (0.5 is the standard deviation); the per-channel step bias is
+log(expm1(x)) with x = exp(U[ln 1e-3, ln 1e-1]), i.e. the bias whose softplus lands
+log-uniformly in [1e-3, 1e-1] (same page, section 3.3; range from "Mamba model analysis",
+intelliparadigm.com, section 3.2). For the decode workload the step ``dt`` is handed to
+the kernel already positive, so the recipe draws it as softplus(N(0, 0.5^2) + bias) in
+float64 (numpy's logaddexp) and rounds it to bf16.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+# child-stream roles
+_R_BIAS, _R_DELTA, _R_U, _R_B, _R_C, _R_D, _R_Z, _R_STATE = range(8)
+
+
+@dataclass(frozen=True)
+class ScanConfig:
+    name: str
+    Bt: int
+    D: int
+    L: int
+    N: int
+    io: str = "bf16"             # "f32" or "bf16" for u, delta, B, C, z, y
+    gate: bool = False           # z present
+    dskip: Optional[str] = "ones"  # "ones", "normal" or None (no D-skip)
+    u_kind: str = "normal"       # "normal" or "ar1"
+    bias: bool = True            # delta_bias present
+    softplus: bool = True
+    last_state: bool = False
+    seed: int = 0
+
+    @property
+    def elements(self) -> int:
+        return self.Bt * self.D * self.L * self.N
+
+
+@dataclass(frozen=True)
+class DecodeConfig:
+    name: str
+    Bt: int
+    D: int
+    N: int
+    steps: int
+    gate: bool = True
+    dskip: Optional[str] = "ones"
+    seed: int = 4
+
+
+TINY = ScanConfig("tiny", 1, 4, 64, 4, io="f32", gate=False, dskip="ones", seed=0)
+BLOCK512 = ScanConfig("block512", 1, 512, 1024, 16, gate=True, dskip="normal", seed=1)
+M130 = ScanConfig("m130", 8, 1536, 2048, 16, gate=True, dskip="ones", seed=2)
+LONG128K = ScanConfig("long128k", 1, 1536, 131072, 64, gate=False, dskip="ones",
+                      u_kind="ar1", last_state=True, seed=3)
+DECODE = DecodeConfig("decode", 256, 5120, 16, 64, seed=4)
+
+SCAN_CONFIGS: Dict[str, ScanConfig] = {c.name: c for c in (TINY, BLOCK512, M130, LONG128K)}
+
+
+def _streams(seed: int):
+    return [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(8)]
+
+
+def _to_io(a32: np.ndarray, io: str) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a32, dtype=np.float32))
+    return t.to(torch.bfloat16) if io == "bf16" else t
+
+
+def _bias(rng, D: int) -> np.ndarray:
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    x = np.exp(rng.uniform(lo, hi, size=D))
+    return np.log(np.expm1(x)).astype(np.float32)
+
+
+def s4d_real_A(D: int, N: int) -> torch.Tensor:
+    """A[d, n] = -(n + 1)."""
+    return -torch.arange(1, N + 1, dtype=torch.float32).repeat(D, 1).contiguous()
+
+
+def _ar1(rng, rows: int, L: int, rho: float = 0.9) -> np.ndarray:
+    eps = rng.standard_normal((rows, L), dtype=np.float32)
+    out = np.empty((rows, L), dtype=np.float32)
+    k = np.float32(math.sqrt(1.0 - rho * rho))
+    out[:, 0] = eps[:, 0]
+    prev = out[:, 0].copy()
+    r = np.float32(rho)
+    for t in range(1, L):
+        prev = r * prev + k * eps[:, t]
+        out[:, t] = prev
+    return out
+
+
+def scan_inputs(cfg: ScanConfig, seed: Optional[int] = None, **overrides) -> Dict[str, object]:
+    """Inputs of one scan call as CPU tensors (time-contiguous layouts):
+    u, delta, z: [Bt, D, L] (io dtype); B, C: [Bt, N, L] (io dtype); A: [D, N] fp32;
+    D, delta_bias: [D] fp32 (or None); plus the flags ``delta_softplus`` and ``last_state``."""
+    if overrides:
+        cfg = replace(cfg, **overrides)
+    seed = cfg.seed if seed is None else seed
+    s = _streams(seed)
+    Bt, D, L, N = cfg.Bt, cfg.D, cfg.L, cfg.N
+    out: Dict[str, object] = {"cfg": cfg, "seed": seed}
+    out["A"] = s4d_real_A(D, N)
+    out["delta_bias"] = torch.from_numpy(_bias(s[_R_BIAS], D)) if cfg.bias else None
+    out["delta"] = _to_io(0.5 * s[_R_DELTA].standard_normal((Bt, D, L), dtype=np.float32), cfg.io)
+    if cfg.u_kind == "ar1":
+        u = _ar1(s[_R_U], Bt * D, L).reshape(Bt, D, L)
+    else:
+        u = s[_R_U].standard_normal((Bt, D, L), dtype=np.float32)
+    out["u"] = _to_io(u, cfg.io)
+    out["B"] = _to_io(s[_R_B].standard_normal((Bt, N, L), dtype=np.float32), cfg.io)
+    out["C"] = _to_io(s[_R_C].standard_normal((Bt, N, L), dtype=np.float32), cfg.io)
+    if cfg.dskip == "ones":
+        out["D"] = torch.ones(D, dtype=torch.float32)
+    elif cfg.dskip == "normal":
+        out["D"] = torch.from_numpy(s[_R_D].standard_normal(D, dtype=np.float32))
+    else:
+        out["D"] = None
+    out["z"] = (_to_io(s[_R_Z].standard_normal((Bt, D, L), dtype=np.float32), cfg.io)
+                if cfg.gate else None)
+    out["delta_softplus"] = cfg.softplus
+    out["last_state"] = cfg.last_state
+    return out
+
+
+def decode_inputs(cfg: DecodeConfig = DECODE, seed: Optional[int] = None, steps: Optional[int] = None,
+                  **overrides) -> Dict[str, object]:
+    """Inputs of ``steps`` successive single-token updates as CPU tensors:
+    state0 [Bt, D, N] fp32; x, dt, z: [S, Bt, D] bf16; B, C: [S, Bt, N] bf16;
+    A [D, N] fp32; D [D] fp32 (or None)."""
+    if overrides:
+        cfg = replace(cfg, **overrides)
+    seed = cfg.seed if seed is None else seed
+    S = cfg.steps if steps is None else steps
+    s = _streams(seed)
+    Bt, D, N = cfg.Bt, cfg.D, cfg.N
+    bias = _bias(s[_R_BIAS], D).astype(np.float64)
+    raw = 0.5 * s[_R_DELTA].standard_normal((S, Bt, D), dtype=np.float32).astype(np.float64)
+    dt = np.logaddexp(0.0, raw + bias[None, None, :]).astype(np.float32)
+    out: Dict[str, object] = {"cfg": cfg, "seed": seed, "steps": S}
+    out["A"] = s4d_real_A(D, N)
+    out["state0"] = torch.from_numpy(s[_R_STATE].standard_normal((Bt, D, N), dtype=np.float32))
+    out["x"] = _to_io(s[_R_U].standard_normal((S, Bt, D), dtype=np.float32), "bf16")
+    out["dt"] = _to_io(dt, "bf16")
+    out["B"] = _to_io(s[_R_B].standard_normal((S, Bt, N), dtype=np.float32), "bf16")
+    out["C"] = _to_io(s[_R_C].standard_normal((S, Bt, N), dtype=np.float32), "bf16")
+    out["z"] = (_to_io(s[_R_Z].standard_normal((S, Bt, D), dtype=np.float32), "bf16")
+                if cfg.gate else None)
+    if cfg.dskip == "ones":
+        out["D"] = torch.ones(D, dtype=torch.float32)
+    elif cfg.dskip == "normal":
+        out["D"] = torch.from_numpy(s[_R_D].standard_normal(D, dtype=np.float32))
+    else:
+        out["D"] = None
+    return out
+
+
+def as_f64(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
+    """Exact float64 copy of a CPU/GPU tensor's values (bf16 and fp32 embed exactly)."""
+    if t is None:
+        return None
+    return t.detach().to("cpu").to(torch.float64).numpy()
