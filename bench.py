@@ -1,0 +1,394 @@
+#!/usr/bin/env python
+"""Benchmark of the selective scan (Mamba S6) on B300: one JSON line.
+
+A step is one selective-scan call over the whole workload (default: the long-sequence
+scan, batch 1 x 1536 channels x 131072 steps x 64 states, bf16 I/O, fp32 state, final
+state returned), inputs resident in HBM. `value` is scan elements (batch*dim*L*N) per
+second over all ranks; each rank scans its own copy (weak scaling, no collective on the
+data path). The line also carries the recurrent-step (decode) throughput, the roofline of
+the step against the MUFU exp2 peak, the fp64 CPU oracle timed on this host's cores, an
+end-to-end number through the host-buffer C-ABI entry point, and the SM clocks sampled
+during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long128k|m130|block512]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from selective_state_space_153_b300 import gen  # noqa: E402
+
+SM_COUNT = 148
+EX2_PER_CLK_SM = 32          # measured on B300: MUFU ex2.approx.f32 issue rate per SM per clock
+FALLBACK_HBM_GBS = 6400.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum of the dominant scan kernel per launch from the
+# ncu capture summarised in profiles/ (None until a capture of the current kernel exists).
+TRAFFIC_BYTES_PER_LAUNCH = None
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long128k", choices=list(gen.SCAN_CONFIGS))
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "sm_max_mhz": 2032.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------- distributed
+def dist_setup(n):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- clocks (NVML)
+class ClockSampler:
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, cuda_index):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self._stop = threading.Event()
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            props = torch.cuda.get_device_properties(cuda_index)
+            self.h = pynvml.nvmlDeviceGetHandleByUUID("GPU-" + str(props.uuid))
+            self.nv = pynvml
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # noqa: BLE001
+            self.ok = False
+            self.err = repr(e)[:120]
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                self.reasons |= int(self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h))
+            except Exception:
+                pass
+            time.sleep(0.02)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
+                    "reasons": ["unavailable: " + getattr(self, "err", "no samples")], "samples": 0}
+        names = [v for k, v in self.REASONS.items() if self.reasons & k and v != "gpu_idle"]
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------- oracle timing
+def oracle_rate(inp, target_s, nthreads):
+    """fp64 oracle on a bounded sample of channels (full sequence): elements/s."""
+    import oracle
+    cfg = inp["cfg"]
+    f = gen.as_f64
+
+    def run(chs):
+        bs = np.array([c[0] for c in chs]); ds = np.array([c[1] for c in chs])
+        rows = lambda t: None if t is None else t[torch.as_tensor(bs), torch.as_tensor(ds), :].to(torch.float64).numpy()  # noqa: E731
+        args = (rows(inp["u"]), rows(inp["delta"]), f(inp["A"])[ds], f(inp["B"]), f(inp["C"]), bs)
+        kw = dict(D=None if inp["D"] is None else f(inp["D"])[ds], z=rows(inp["z"]),
+                  delta_bias=None if inp["delta_bias"] is None else f(inp["delta_bias"])[ds],
+                  delta_softplus=inp["delta_softplus"], nthreads=nthreads)
+        t = time.perf_counter()
+        oracle.scan_rows(*args, **kw)
+        return time.perf_counter() - t
+
+    allch = [(b, d) for b in range(cfg.Bt) for d in range(cfg.D)]
+    t1 = run(allch[:1])
+    k = int(max(1, min(len(allch), round(target_s * nthreads / max(t1, 1e-6)))))
+    k = max(min(k, len(allch)), 1)
+    step = max(1, len(allch) // k)
+    chs = allch[::step][:k]
+    t = run(chs)
+    elems = len(chs) * cfg.L * cfg.N
+    return elems / t, len(chs), min(nthreads, len(chs)), t
+
+
+# ---------------------------------------------------------------------------- our arm
+def bench_ours(args, rank, ws, local):
+    from selective_state_space_153_b300 import ssm
+    ssm.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg = gen.SCAN_CONFIGS[args.workload]
+    inp = gen.scan_inputs(cfg)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(g["u"])
+    last = torch.empty((cfg.Bt, cfg.D, cfg.N), dtype=torch.float32, device=dev) if cfg.last_state else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                               delta_bias=g["delta_bias"], delta_softplus=cfg.softplus, y=y, last_state=last,
+                               stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert ssm.stream_status(stream) == ssm.SSM_OK
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with sampler:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, ws)
+    assert ssm.stream_status(stream) == ssm.SSM_OK
+
+    elems = cfg.elements
+    esz = 2 if cfg.io == "bf16" else 4
+    io_bytes = (cfg.Bt * cfg.D * cfg.L * esz * (3 + (1 if cfg.gate else 0))      # u, delta, (z), y
+                + 2 * cfg.Bt * cfg.N * cfg.L * esz + cfg.D * cfg.N * 4 + 2 * cfg.D * 4
+                + (cfg.Bt * cfg.D * cfg.N * 4 if cfg.last_state else 0))
+    t_step = ms_max / args.steps / 1e3
+    peaks, peak_kind = measured_peaks()
+    clocks = sampler.summary()
+    sm_max = float(peaks.get("sm_max_mhz", 2032.0))
+    ex2_peak = SM_COUNT * EX2_PER_CLK_SM * sm_max * 1e6 / 1e9          # Gexp/s at the max SM clock
+    achieved = elems / t_step / 1e9
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    launches_per_step = 3 if ssm.workspace_bytes(cfg.Bt, cfg.D, cfg.L, cfg.N,
+                                                ssm.SSM_BF16 if cfg.io == "bf16" else ssm.SSM_F32) > 0 else 1
+    out = {
+        "metric": "scan elements/s (B*D*L*N/s); fraction of the max(HBM, SFU) roofline; decode tok/s",
+        "value": ws * elems / t_step, "unit": "elem/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 compute, bf16 io" if cfg.io == "bf16" else "f32",
+        "data": "synthetic (seeded generator, PCG64)",
+        "config": {"workload": f"{cfg.name}: selective scan Bt={cfg.Bt} D={cfg.D} L={cfg.L} N={cfg.N} "
+                               f"io={cfg.io} gate={cfg.gate} last_state={cfg.last_state}",
+                   "batch": cfg.Bt, "dim": cfg.D, "seqlen": cfg.L, "dstate": cfg.N,
+                   "l2": "inputs larger than L2 (%.0f MB per step)" % (io_bytes / 1e6)},
+        "tokens_per_s": ws * cfg.Bt * cfg.L / t_step,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": ex2_peak, "unit": "Gexp/s",
+                     "frac": achieved / ex2_peak, "traffic": TRAFFIC_BYTES_PER_LAUNCH,
+                     "peak_source": f"MUFU ex2 {EX2_PER_CLK_SM}/clk/SM x {SM_COUNT} SMs x {sm_max:.0f} MHz",
+                     "kernel": "whole scan call (%d launch%s)" % (launches_per_step, "es" if launches_per_step > 1 else ""),
+                     "hbm": {"achieved_gbs": io_bytes / t_step / 1e9, "peak_gbs": hbm, "peak_kind": peak_kind,
+                             "frac": io_bytes / t_step / 1e9 / hbm},
+                     "frac_at_sampled_clock": (achieved / (SM_COUNT * EX2_PER_CLK_SM * clocks["sm_mhz"] * 1e6 / 1e9)
+                                               if clocks["sm_mhz"] else None)},
+        "clocks": clocks,
+        "gpu_launches": args.steps * launches_per_step,
+    }
+    # end to end: host buffers through the C ABI, copies inside the timed region
+    if not args.no_e2e:
+        pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        yh = torch.empty_like(pin["u"]).pin_memory()
+        lh = torch.empty((cfg.Bt, cfg.D, cfg.N), dtype=torch.float32).pin_memory() if cfg.last_state else None
+
+        def host_step():
+            ssm.selective_scan_fwd_host(pin["u"], pin["delta"], pin["A"], pin["B"], pin["C"], D=pin["D"], z=pin["z"],
+                                        delta_bias=pin["delta_bias"], delta_softplus=cfg.softplus, y=yh,
+                                        last_state=lh)
+        host_step()
+        ke = max(2, min(args.steps, 5))
+        barrier(ws)
+        t = time.perf_counter()
+        for _ in range(ke):
+            host_step()
+        te = max_over_ranks(time.perf_counter() - t, ws)
+        h2d = sum(v.numel() * v.element_size() for k, v in pin.items()
+                  if isinstance(v, torch.Tensor) and k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias"))
+        d2h = yh.numel() * yh.element_size() + (lh.numel() * 4 if lh is not None else 0)
+        out["e2e"] = {"value": ws * elems * ke / te, "unit": "elem/s", "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "ms_per_step": te / ke * 1e3,
+                      "entry": "ssm_selective_scan_fwd_host (pinned host buffers)"}
+        del pin, yh
+    if not args.no_decode:
+        out["decode"] = bench_decode(dev)
+        out["gpu_launches"] += out["decode"]["launches"]
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        nthreads = os.cpu_count() or 1
+        rate, nch, cores, secs = oracle_rate(inp, args.cpu_seconds, nthreads)
+        out["cpu_baseline"] = {"value": rate, "unit": "elem/s", "cores": cores, "kind": "oracle",
+                               "sample": f"{nch} of {cfg.Bt * cfg.D} channels, full L={cfg.L}, N={cfg.N}, "
+                                         f"fp64 sequential C, {cores} threads, {secs:.1f} s"}
+    return out
+
+
+def bench_decode(dev):
+    """Recurrent step at batch 256 x 5120 channels x 16 states: tok/s = batch / step time,
+    L2 flushed before every timed step (the 84 MB state would otherwise stay in L2)."""
+    from selective_state_space_153_b300 import ssm
+    cfg = gen.DECODE
+    d = gen.decode_inputs(cfg)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    st = g["state0"].clone()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ys = torch.empty((cfg.steps, cfg.Bt, cfg.D), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream()
+
+    def one(i):
+        ssm.state_update(st, g["x"][i], g["dt"][i], g["A"], g["B"][i], g["C"][i], D=g["D"], z=g["z"][i], y=ys[i],
+                         stream=s)
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    times = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(cfg.steps)]
+    for i in range(cfg.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(s)
+        one(i)
+        ev[i][1].record(s)
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in ev]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(cfg.steps):
+        one(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    b2b = e0.elapsed_time(e1) / cfg.steps
+    med = statistics.median(times)
+    bytes_step = (2 * cfg.Bt * cfg.D * cfg.N * 4 + 4 * cfg.Bt * cfg.D * 2 + 2 * cfg.Bt * cfg.N * 2
+                  + cfg.D * cfg.N * 4 + cfg.D * 4)
+    peaks, kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    return {"workload": f"decode Bt={cfg.Bt} D={cfg.D} N={cfg.N}, {cfg.steps} successive steps",
+            "tok_per_s": cfg.Bt / (med / 1e3), "ms_per_step": med,
+            "roofline": {"bound": "hbm", "achieved": bytes_step / (med / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": bytes_step / (med / 1e3) / 1e9 / hbm, "peak_kind": kind,
+                         "bytes_per_step": bytes_step, "l2": "flushed (256 MB write) before each timed step"},
+            "back_to_back_tok_per_s": cfg.Bt / (b2b / 1e3), "launches": 2 * cfg.steps}
+
+
+# ---------------------------------------------------------------------------- reference arm
+def bench_reference(args, rank, ws):
+    """The fp64 CPU oracle as it stands, on this host's cores: each step scans a bounded
+    sample of the workload's channels over the full sequence."""
+    if rank != 0:
+        return None
+    import oracle
+    cfg = gen.SCAN_CONFIGS[args.workload]
+    inp = gen.scan_inputs(cfg)
+    nthreads = os.cpu_count() or 1
+    rate1, _, _, t1 = oracle_rate(inp, 0.0, nthreads)   # one channel, to size the sample
+    per_ch = t1
+    k = int(max(1, min(cfg.Bt * cfg.D, round(2.0 * nthreads / max(per_ch, 1e-6)))))
+    f = gen.as_f64
+    allch = [(b, d) for b in range(cfg.Bt) for d in range(cfg.D)]
+    chs = allch[:: max(1, len(allch) // k)][:k]
+    bs = np.array([c[0] for c in chs]); ds = np.array([c[1] for c in chs])
+    rows = lambda t: None if t is None else t[torch.as_tensor(bs), torch.as_tensor(ds), :].to(torch.float64).numpy()  # noqa: E731
+    a = (rows(inp["u"]), rows(inp["delta"]), f(inp["A"])[ds], f(inp["B"]), f(inp["C"]), bs)
+    kw = dict(D=None if inp["D"] is None else f(inp["D"])[ds], z=rows(inp["z"]),
+              delta_bias=None if inp["delta_bias"] is None else f(inp["delta_bias"])[ds],
+              delta_softplus=inp["delta_softplus"], nthreads=nthreads)
+    for _ in range(args.warmup):
+        oracle.scan_rows(*a, **kw)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scan_rows(*a, **kw)
+    el = time.perf_counter() - t
+    elems = len(chs) * cfg.L * cfg.N
+    v = elems * args.steps / el
+    cores = min(nthreads, len(chs))
+    sample = f"{len(chs)} of {cfg.Bt * cfg.D} channels per step, full L={cfg.L}, N={cfg.N}, fp64 sequential C"
+    return {"impl": "reference", "metric": "scan elements/s (B*D*L*N/s); fraction of the max(HBM, SFU) roofline; decode tok/s",
+            "value": v, "unit": "elem/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded generator, PCG64)",
+            "config": {"workload": f"{cfg.name}: selective scan Bt={cfg.Bt} D={cfg.D} L={cfg.L} N={cfg.N} io={cfg.io}",
+                       "batch": cfg.Bt, "dim": cfg.D, "seqlen": cfg.L, "dstate": cfg.N},
+            "cpu_baseline": {"value": v, "unit": "elem/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        out = bench_reference(args, rank, ws)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    rank, ws, local = dist_setup(args.gpus)
+    out = bench_ours(args, rank, ws, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

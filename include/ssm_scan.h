@@ -1,0 +1,170 @@
+/*
+ * ssm_scan.h -- C ABI of a B300 (sm_103a) selective state-space scan library (Mamba "S6").
+ *
+ * What is computed. For every batch row b, channel d and state n, with the step
+ *     dt[b,d,t] = softplus(delta[b,d,t] + delta_bias[d])   (or without softplus / bias)
+ * the discretised diagonal system
+ *     A_bar = exp(dt * A[d,n]),   B_bar * u = dt * B[b,n,t] * u[b,d,t]
+ *     h[b,d,n,t] = A_bar * h[b,d,n,t-1] + dt * B[b,n,t] * u[b,d,t],   h[.,.,.,-1] = 0
+ *     y[b,d,t]   = (sum_n C[b,n,t] * h[b,d,n,t] + D[d] * u[b,d,t]) * SiLU(z[b,d,t])
+ * This is the per-timestep loop of section 3.2 of "From RNN to Mamba: state-space model
+ * principles and long-sequence modelling in practice" (lmnt.cn): A_bar = exp(dt*A),
+ * B_bar = dt*B_t, h = A_bar*h + B_bar*x_t, y_t = sum(h*C_t), then y + x*D and the SiLU(z)
+ * gate; A diagonal per section 2.2; softplus of a biased projection for dt per section 3.3
+ * (softplus(x) = log(1 + e^x): "Mamba architecture principles and industrial long-text
+ * practice", jsqmd.com, section 2.2). The recurrent single-token step used at inference
+ * (lmnt.cn section 5.3: one fixed-size fp32 state, advanced token by token) is
+ * ssm_state_update.
+ *
+ * Readings the library fixes where the pages are silent:
+ *   - B_bar*u = dt*B*u (the page's code), not the exact zero-order hold (A_bar-1)/A*B.
+ *   - softplus(v) = v for v > 20, else log(1 + exp(v)) (beta = 1).
+ *   - y at t uses the state after the update at t.
+ *   - B and C are shared by all channels of a batch row: [batch][dstate][seqlen].
+ *
+ * Layouts (row-major, last index contiguous; every tensor is dense with no stride gaps):
+ *   u, delta, z, y : [batch][dim][seqlen]   io dtype (fp32 or bf16)
+ *   B, C           : [batch][dstate][seqlen] io dtype
+ *   A              : [dim][dstate]           fp32
+ *   D, delta_bias  : [dim]                   fp32
+ *   last_state     : [batch][dim][dstate]    fp32
+ * Precision: inputs are read in their stored precision, everything is computed in fp32
+ * (state, discretisation, readout), and y is rounded once (round-to-nearest-even) to the
+ * io dtype. exp uses the hardware base-2 exponential (ex2.approx) on dt*A*log2(e).
+ *
+ * Ownership: the caller owns every buffer; the library never frees or retains a caller
+ * pointer after the call returns. Device pointers must be device memory of the current
+ * CUDA device. Alignment: the scan's u, delta, z, y, B, C, last_state and the state
+ * update's state and A must be 16-byte aligned; the scan's A, D, delta_bias and the state
+ * update's per-token vectors (x, dt, z, y, B, C) and D need only their element alignment.
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream)
+ * unless stated otherwise.
+ *
+ * Errors: arguments are checked on the host before anything is launched; on any error
+ * nothing is launched and nothing is written. Launch failures return SSM_ERR_CUDA
+ * (cudaGetLastError). Errors raised while a kernel runs (the bounded waits of the
+ * L-parallel scan) are recorded in a device status word that ssm_stream_status() reads.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_NULL = 1,        /* a required pointer is NULL */
+    SSM_ERR_SHAPE = 2,       /* a dimension is negative, dstate < 1, or sizes overflow */
+    SSM_ERR_DTYPE = 3,       /* io_dtype is not one of ssm_dtype_t */
+    SSM_ERR_ALIGN = 4,       /* a pointer is not aligned as required (see Alignment) */
+    SSM_ERR_UNSUPPORTED = 5, /* dstate > SSM_MAX_DSTATE, or no device / wrong architecture */
+    SSM_ERR_CUDA = 6,        /* a CUDA runtime call failed */
+    SSM_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up (see ssm_stream_status) */
+    SSM_ERR_WORKSPACE = 8    /* workspace missing or too small */
+} ssm_status_t;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
+
+/* batch, dim (channels, "d_inner"), seqlen (L) and dstate (N) of a call, and the dtype of
+ * u, delta, B, C, z and y (the state, A, D and delta_bias are always fp32). */
+typedef struct {
+    int64_t batch, dim, seqlen, dstate;
+    ssm_dtype_t io_dtype;
+} ssm_dims_t;
+
+#define SSM_MAX_DSTATE 128
+
+/*
+ * Selective scan forward (lmnt.cn "From RNN to Mamba", section 3.2, the loop; the
+ * associative prefix-scan form of section 2.2 and of jsqmd.com section 3.4 lets the GPU
+ * split the sequence): computes y (and optionally the final state) as defined above.
+ *   dims            batch, dim, seqlen, dstate, io dtype. batch, dim or seqlen may be 0
+ *                   (nothing to compute; last_state, if given and seqlen == 0, is zeroed).
+ *   u, delta        device, [batch][dim][seqlen], io dtype. delta is the raw step.
+ *   A               device, [dim][dstate] fp32 (diagonal of the state matrix; any real).
+ *   B, C            device, [batch][dstate][seqlen], io dtype.
+ *   D               device, [dim] fp32, or NULL for no skip term.
+ *   z               device, [batch][dim][seqlen] io dtype, or NULL for no gate.
+ *   delta_bias      device, [dim] fp32 added to delta before the softplus, or NULL.
+ *   delta_softplus  nonzero: dt = softplus(delta + bias); zero: dt = delta + bias.
+ *   y               device, [batch][dim][seqlen] io dtype, written.
+ *   last_state      device, [batch][dim][dstate] fp32, written with h at t = seqlen-1,
+ *                   or NULL.
+ *   stream          cudaStream_t the work is queued on.
+ * Sequences are split into chunks processed in parallel when batch*dim alone cannot fill
+ * the GPU; the chunk states then pass through a workspace that the library allocates
+ * stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`) unless one was given with
+ * ssm_selective_scan_fwd_ws.
+ */
+ssm_status_t ssm_selective_scan_fwd(const ssm_dims_t *dims, const void *u, const void *delta,
+                                    const float *A, const void *B, const void *C,
+                                    const float *D, const void *z, const float *delta_bias,
+                                    int delta_softplus, void *y, float *last_state,
+                                    void *stream);
+
+/* Bytes of device workspace ssm_selective_scan_fwd_ws needs for `dims` (0 if none). */
+size_t ssm_selective_scan_workspace_bytes(const ssm_dims_t *dims);
+
+/* As ssm_selective_scan_fwd, with a caller-owned device workspace (16-byte aligned, at
+ * least ssm_selective_scan_workspace_bytes(dims) bytes; it may be NULL when that is 0).
+ * The workspace must not be used by anything else until the call has completed on
+ * `stream`. Returns SSM_ERR_WORKSPACE if it is too small. */
+ssm_status_t ssm_selective_scan_fwd_ws(const ssm_dims_t *dims, const void *u,
+                                       const void *delta, const float *A, const void *B,
+                                       const void *C, const float *D, const void *z,
+                                       const float *delta_bias, int delta_softplus, void *y,
+                                       float *last_state, void *workspace,
+                                       size_t workspace_bytes, void *stream);
+
+/*
+ * Recurrent single-token step (lmnt.cn "From RNN to Mamba", section 5.3; the section 3.2
+ * loop body for one timestep), in place on the state:
+ *     state[b,d,n] = exp(dt[b,d]*A[d,n]) * state[b,d,n] + dt[b,d]*B[b,n]*x[b,d]
+ *     y[b,d]       = (sum_n C[b,n]*state[b,d,n] + D[d]*x[b,d]) * SiLU(z[b,d])
+ *   dims        batch, dim, dstate, io dtype (seqlen is ignored).
+ *   state       device, [batch][dim][dstate] fp32, read and overwritten.
+ *   x, dt       device, [batch][dim] io dtype; dt is the final positive step (no bias,
+ *               no softplus applied here).
+ *   A           device, [dim][dstate] fp32.   B, C: device, [batch][dstate] io dtype.
+ *   D           device, [dim] fp32 or NULL.   z: device, [batch][dim] io dtype or NULL.
+ *   y           device, [batch][dim] io dtype, written.
+ */
+ssm_status_t ssm_state_update(const ssm_dims_t *dims, float *state, const void *x,
+                              const void *dt, const float *A, const void *B, const void *C,
+                              const float *D, const void *z, void *y, void *stream);
+
+/*
+ * Host-buffer scan: the same computation as ssm_selective_scan_fwd, with every array in
+ * HOST memory (pinned memory gives the fastest copies). The call copies the inputs to the
+ * device, scans, copies y (and last_state) back, and returns when the results are in the
+ * host buffers. Device buffers are allocated stream-ordered on `stream` and freed before
+ * returning. The channels are processed in blocks so that copies in both directions
+ * overlap the scans of neighbouring blocks. Same argument meanings and errors as
+ * ssm_selective_scan_fwd (alignment is not required of host pointers).
+ */
+ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u,
+                                         const void *delta, const float *A, const void *B,
+                                         const void *C, const float *D, const void *z,
+                                         const float *delta_bias, int delta_softplus,
+                                         void *y, float *last_state, void *stream);
+
+/* Synchronises `stream` and returns (then clears) the library's device status word:
+ * SSM_OK, SSM_ERR_TIMEOUT if a bounded device-side wait gave up since the last check, or
+ * SSM_ERR_CUDA if the synchronisation itself failed. */
+ssm_status_t ssm_stream_status(void *stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *ssm_status_string(ssm_status_t status);
+
+/* Library ABI version: (major << 16) | minor. */
+int ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

@@ -1,0 +1,87 @@
+// Recurrent single-token step (section 5.3 of "From RNN to Mamba", lmnt.cn: inference
+// advances one fixed-size fp32 state per channel token by token; the update is the body
+// of the section 3.2 loop for one timestep):
+//   state = exp(dt*A) * state + dt*B*x ;  y = (sum_n C*state + D*x) * SiLU(z).
+// Memory-bound: the fp32 state is read and written once. Vector path (N % 4 == 0): one
+// thread per (b, d, 4 consecutive states) with 16-byte state loads/stores, the y partials
+// reduced across the N/4 lanes of a channel with shuffles (N/4 must divide 32, i.e.
+// N in {4, 8, 16, 32, 64, 128}); otherwise one thread per (b, d) walking all states.
+#pragma once
+#include "common.cuh"
+
+namespace ssm {
+
+struct DecodeParams {
+    float *state;
+    const void *x, *dt, *B, *C, *z;
+    const float *A, *D;
+    void *y;
+    int64_t Bt, Dm, N;
+};
+
+template <typename IO, int LPC>  // LPC: lanes per channel = N/4
+__global__ void __launch_bounds__(256) decode_vec_kernel(const DecodeParams p) {
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t chan = gid / LPC;   // b*Dm + d
+    const int q = (int)(gid % LPC);
+    const bool valid = chan < p.Bt * p.Dm;
+    const int64_t cl = valid ? chan : 0;
+    const int64_t b = cl / p.Dm, d = cl % p.Dm;
+    float acc = 0.0f;
+    float xv = 0.0f, zv = 0.0f;
+    if (valid) {
+        const IO *X = reinterpret_cast<const IO *>(p.x);
+        const IO *DT = reinterpret_cast<const IO *>(p.dt);
+        const IO *Bm = reinterpret_cast<const IO *>(p.B);
+        const IO *Cm = reinterpret_cast<const IO *>(p.C);
+        xv = io_traits<IO>::to_f(X[cl]);
+        const float dt = io_traits<IO>::to_f(DT[cl]);
+        if (p.z != nullptr) zv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.z)[cl]);
+        float4 *sp = reinterpret_cast<float4 *>(p.state + cl * p.N) + q;
+        float4 s = __ldcs(sp);
+        const float4 a4 = __ldg(reinterpret_cast<const float4 *>(p.A + d * p.N) + q);
+        const int64_t nb = b * p.N + 4 * q;
+        const float b0 = io_traits<IO>::to_f(Bm[nb]), b1 = io_traits<IO>::to_f(Bm[nb + 1]);
+        const float b2 = io_traits<IO>::to_f(Bm[nb + 2]), b3 = io_traits<IO>::to_f(Bm[nb + 3]);
+        const float c0 = io_traits<IO>::to_f(Cm[nb]), c1 = io_traits<IO>::to_f(Cm[nb + 1]);
+        const float c2 = io_traits<IO>::to_f(Cm[nb + 2]), c3 = io_traits<IO>::to_f(Cm[nb + 3]);
+        const float dx = dt * xv, dl = dt * kLog2e;
+        s.x = fmaf(ex2(dl * a4.x), s.x, dx * b0);
+        s.y = fmaf(ex2(dl * a4.y), s.y, dx * b1);
+        s.z = fmaf(ex2(dl * a4.z), s.z, dx * b2);
+        s.w = fmaf(ex2(dl * a4.w), s.w, dx * b3);
+        __stcs(sp, s);
+        acc = fmaf(c0, s.x, fmaf(c1, s.y, fmaf(c2, s.z, c3 * s.w)));
+    }
+#pragma unroll
+    for (int o = LPC / 2; o >= 1; o /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (valid && q == 0) {
+        float yv = acc + (p.D != nullptr ? p.D[d] * xv : 0.0f);
+        if (p.z != nullptr) yv *= silu_f(zv);
+        store_io(reinterpret_cast<IO *>(p.y) + cl, yv);
+    }
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(256) decode_scalar_kernel(const DecodeParams p) {
+    const int64_t cl = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (cl >= p.Bt * p.Dm) return;
+    const int64_t b = cl / p.Dm, d = cl % p.Dm;
+    const IO *Bm = reinterpret_cast<const IO *>(p.B);
+    const IO *Cm = reinterpret_cast<const IO *>(p.C);
+    const float xv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.x)[cl]);
+    const float dt = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.dt)[cl]);
+    const float dx = dt * xv, dl = dt * kLog2e;
+    float acc = 0.0f;
+    for (int64_t n = 0; n < p.N; ++n) {
+        float s = p.state[cl * p.N + n];
+        s = fmaf(ex2(dl * p.A[d * p.N + n]), s, dx * io_traits<IO>::to_f(Bm[b * p.N + n]));
+        p.state[cl * p.N + n] = s;
+        acc = fmaf(io_traits<IO>::to_f(Cm[b * p.N + n]), s, acc);
+    }
+    float yv = acc + (p.D != nullptr ? p.D[d] * xv : 0.0f);
+    if (p.z != nullptr) yv *= silu_f(io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.z)[cl]));
+    store_io(reinterpret_cast<IO *>(p.y) + cl, yv);
+}
+
+}  // namespace ssm

@@ -1,0 +1,180 @@
+"""Thin Python binding of the C ABI in include/ssm_scan.h (libssm_scan.so), by ctypes.
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels. Tensors are torch tensors (device memory for the device entry points, host
+memory for ``selective_scan_fwd_host``); their raw pointers are passed through unchanged.
+There is no CPU fallback: if the library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssm_scan.so")
+
+SSM_OK, SSM_ERR_NULL, SSM_ERR_SHAPE, SSM_ERR_DTYPE, SSM_ERR_ALIGN = 0, 1, 2, 3, 4
+SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = 5, 6, 7, 8
+SSM_F32, SSM_BF16 = 0, 1
+MAX_DSTATE = 128
+
+# every symbol include/ssm_scan.h declares
+EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_workspace_bytes",
+           "ssm_selective_scan_fwd_ws", "ssm_state_update", "ssm_selective_scan_fwd_host",
+           "ssm_stream_status", "ssm_status_string", "ssm_version")
+
+
+class SsmDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("io_dtype", ctypes.c_int)]
+
+
+class SsmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def load(path: str = LIB_PATH):
+    """Load libssm_scan.so (raises if it is missing: build it with
+    ``python -m selective_state_space_153_b300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"CUDA library not built: {path}")
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(SsmDims)
+    scan_args = [dp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp]
+    lib.ssm_selective_scan_fwd.argtypes = scan_args + [_vp]
+    lib.ssm_selective_scan_fwd.restype = ctypes.c_int
+    lib.ssm_selective_scan_fwd_ws.argtypes = scan_args + [_vp, ctypes.c_size_t, _vp]
+    lib.ssm_selective_scan_fwd_ws.restype = ctypes.c_int
+    lib.ssm_selective_scan_fwd_host.argtypes = scan_args + [_vp]
+    lib.ssm_selective_scan_fwd_host.restype = ctypes.c_int
+    lib.ssm_selective_scan_workspace_bytes.argtypes = [dp]
+    lib.ssm_selective_scan_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssm_state_update.argtypes = [dp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.ssm_state_update.restype = ctypes.c_int
+    lib.ssm_stream_status.argtypes = [_vp]
+    lib.ssm_stream_status.restype = ctypes.c_int
+    lib.ssm_status_string.argtypes = [ctypes.c_int]
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_version.argtypes = []
+    lib.ssm_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().ssm_status_string(int(code)).decode()
+
+
+def _io_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    if t.dtype == torch.float32:
+        return SSM_F32
+    raise TypeError(f"io dtype must be bfloat16 or float32, got {t.dtype}")
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return _vp(t.data_ptr())
+
+
+def _stream_ptr(stream) -> Optional[ctypes.c_void_p]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _vp(stream.cuda_stream) if hasattr(stream, "cuda_stream") else _vp(int(stream))
+
+
+def dims(batch, dim, seqlen, dstate, io) -> SsmDims:
+    return SsmDims(int(batch), int(dim), int(seqlen), int(dstate), int(io))
+
+
+def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                       y=None, last_state=None, return_last_state=False, stream=None,
+                       workspace=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Device scan. u, delta, z [Bt, D, L]; B, C [Bt, N, L] (io dtype); A [D, N], D, bias [D]
+    fp32. Returns (y, last_state or None). ``workspace``: optional uint8 device tensor for
+    ssm_selective_scan_fwd_ws."""
+    lib = load()
+    Bt, Dm, L = u.shape
+    N = A.shape[1]
+    io = _io_code(u)
+    if y is None:
+        y = torch.empty_like(u)
+    if return_last_state and last_state is None:
+        last_state = torch.empty((Bt, Dm, N), dtype=torch.float32, device=u.device)
+    dm = dims(Bt, Dm, L, N, io)
+    args = [ctypes.byref(dm), _p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+            int(bool(delta_softplus)), _p(y), _p(last_state)]
+    if workspace is None:
+        rc = lib.ssm_selective_scan_fwd(*args, _stream_ptr(stream))
+    else:
+        rc = lib.ssm_selective_scan_fwd_ws(*args, _p(workspace), workspace.numel() * workspace.element_size(),
+                                           _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SsmError(rc, "ssm_selective_scan_fwd")
+    return y, last_state
+
+
+def workspace_bytes(Bt, Dm, L, N, io=SSM_BF16) -> int:
+    return int(load().ssm_selective_scan_workspace_bytes(ctypes.byref(dims(Bt, Dm, L, N, io))))
+
+
+def selective_scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                            y=None, last_state=None, return_last_state=False, stream=None):
+    """Host-buffer scan: every tensor on the CPU (pinned for speed); copies in, scans on
+    the GPU, copies out, returns when the results are in the host tensors."""
+    lib = load()
+    Bt, Dm, L = u.shape
+    N = A.shape[1]
+    io = _io_code(u)
+    if y is None:
+        y = torch.empty_like(u)
+    if return_last_state and last_state is None:
+        last_state = torch.empty((Bt, Dm, N), dtype=torch.float32)
+    dm = dims(Bt, Dm, L, N, io)
+    rc = lib.ssm_selective_scan_fwd_host(ctypes.byref(dm), _p(u), _p(delta), _p(A), _p(B), _p(C), _p(D),
+                                         _p(z), _p(delta_bias), int(bool(delta_softplus)), _p(y),
+                                         _p(last_state), _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SsmError(rc, "ssm_selective_scan_fwd_host")
+    return y, last_state
+
+
+def state_update(state, x, dt, A, B, C, D=None, z=None, y=None, stream=None) -> torch.Tensor:
+    """In-place recurrent step on ``state`` [Bt, D, N] fp32; x, dt, z [Bt, D]; B, C [Bt, N]
+    (io dtype); A [D, N]; D [D]. Returns y [Bt, D]."""
+    lib = load()
+    Bt, Dm, N = state.shape
+    io = _io_code(x)
+    if y is None:
+        y = torch.empty_like(x)
+    dm = dims(Bt, Dm, 1, N, io)
+    rc = lib.ssm_state_update(ctypes.byref(dm), _p(state), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D),
+                              _p(z), _p(y), _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SsmError(rc, "ssm_state_update")
+    return y
+
+
+def stream_status(stream=None) -> int:
+    return int(load().ssm_stream_status(_stream_ptr(stream)))
+
+
+def version() -> Tuple[int, int]:
+    v = int(load().ssm_version())
+    return v >> 16, v & 0xFFFF

@@ -1,0 +1,99 @@
+"""The C-ABI library loads, exports every symbol include/ssm_scan.h declares, and rejects bad
+arguments on the host with the documented status codes (no GPU needed: nothing is
+launched on an argument error)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_153_b300 import build, ssm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ssm.load()
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z_]+)\s*\(", txt)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(ssm.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    for code in range(9):
+        s = ssm.status_string(code)
+        assert s.startswith("SSM_")
+    assert ssm.status_string(99) == "SSM_ERR_UNKNOWN"
+    assert ssm.version() == (1, 0)
+
+
+A = ctypes.c_void_p(0x1000)      # fake, 16-byte aligned "device" pointers: never dereferenced
+MIS = ctypes.c_void_p(0x1002)    # misaligned
+
+
+def call_scan(lib, d, u=A, delta=A, Am=A, B=A, C=A, D=None, z=None, bias=None, y=A, last=None):
+    return lib.ssm_selective_scan_fwd(ctypes.byref(d) if d is not None else None, u, delta, Am, B, C, D, z,
+                                      bias, 1, y, last, None)
+
+
+def test_scan_argument_errors(lib):
+    d = ssm.dims(1, 4, 64, 4, ssm.SSM_F32)
+    assert call_scan(lib, None) == ssm.SSM_ERR_NULL
+    assert call_scan(lib, d, u=None) == ssm.SSM_ERR_NULL
+    assert call_scan(lib, d, C=None) == ssm.SSM_ERR_NULL
+    assert call_scan(lib, d, y=None) == ssm.SSM_ERR_NULL
+    assert call_scan(lib, d, u=MIS) == ssm.SSM_ERR_ALIGN
+    assert call_scan(lib, d, z=MIS) == ssm.SSM_ERR_ALIGN
+    assert call_scan(lib, d, last=MIS) == ssm.SSM_ERR_ALIGN
+    assert call_scan(lib, ssm.dims(-1, 4, 64, 4, 0)) == ssm.SSM_ERR_SHAPE
+    assert call_scan(lib, ssm.dims(1, 4, -3, 4, 0)) == ssm.SSM_ERR_SHAPE
+    assert call_scan(lib, ssm.dims(1, 4, 64, 0, 0)) == ssm.SSM_ERR_SHAPE
+    assert call_scan(lib, ssm.dims(1, 4, 64, 4, 7)) == ssm.SSM_ERR_DTYPE
+    assert call_scan(lib, ssm.dims(1, 4, 64, ssm.MAX_DSTATE + 1, 0)) == ssm.SSM_ERR_UNSUPPORTED
+    assert call_scan(lib, ssm.dims(1 << 40, 1 << 20, 1 << 20, 4, 0)) == ssm.SSM_ERR_SHAPE
+    # empty batch/dim: nothing to do, OK without touching the GPU
+    assert call_scan(lib, ssm.dims(0, 4, 64, 4, 0), u=None, delta=None, y=None) == ssm.SSM_OK
+    assert call_scan(lib, ssm.dims(2, 0, 64, 4, 0), u=None, delta=None, y=None) == ssm.SSM_OK
+
+
+def test_state_update_argument_errors(lib):
+    d = ssm.dims(2, 8, 1, 16, ssm.SSM_BF16)
+    f = lib.ssm_state_update
+    assert f(None, A, A, A, A, A, A, None, None, A, None) == ssm.SSM_ERR_NULL
+    assert f(ctypes.byref(d), None, A, A, A, A, A, None, None, A, None) == ssm.SSM_ERR_NULL
+    assert f(ctypes.byref(d), A, A, A, A, A, A, None, None, None, None) == ssm.SSM_ERR_NULL
+    assert f(ctypes.byref(d), MIS, A, A, A, A, A, None, None, A, None) == ssm.SSM_ERR_ALIGN
+    assert f(ctypes.byref(ssm.dims(2, 8, 1, 0, 1)), A, A, A, A, A, A, None, None, A, None) == ssm.SSM_ERR_SHAPE
+    assert f(ctypes.byref(ssm.dims(0, 8, 1, 16, 1)), None, None, None, None, None, None, None, None, None, None) == ssm.SSM_OK
+
+
+def test_workspace_query(lib):
+    # a long single-row sequence is split into chunks and needs a workspace; a wide batch does not
+    assert ssm.workspace_bytes(1, 1536, 131072, 64) > 0
+    assert ssm.workspace_bytes(8, 1536, 2048, 16) == 0
+    assert ssm.workspace_bytes(0, 1536, 2048, 16) == 0
+    assert lib.ssm_selective_scan_workspace_bytes(None) == 0
+
+
+def test_ws_entry_rejects_small_workspace(lib):
+    d = ssm.dims(1, 1536, 131072, 64, ssm.SSM_BF16)
+    need = ssm.workspace_bytes(1, 1536, 131072, 64)
+    assert need > 0
+    rc = lib.ssm_selective_scan_fwd_ws(ctypes.byref(d), A, A, A, A, A, None, None, None, 1, A, None,
+                                       MIS, need, None)
+    assert rc == ssm.SSM_ERR_ALIGN

@@ -1,0 +1,221 @@
+"""GPU (C ABI) against the fp64 oracle, element by element, on seeded inputs."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import TOL, compare_scan, gpu_scan, sample_channels, to_dev
+from selective_state_space_153_b300 import build, gen, ssm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build.build()
+    ssm.load()
+
+
+# ---- the workloads ------------------------------------------------------------------------
+def test_tiny_fp32():
+    inp = gen.scan_inputs(gen.TINY)
+    y, h = gpu_scan(inp)
+    compare_scan(inp, y, h)
+
+
+def test_block512_bf16_full():
+    inp = gen.scan_inputs(gen.BLOCK512)
+    y, h = gpu_scan(inp)
+    compare_scan(inp, y, h)
+
+
+def test_m130_full_size_sampled():
+    inp = gen.scan_inputs(gen.M130)
+    y, h = gpu_scan(inp)
+    compare_scan(inp, y, h, channels=sample_channels(8, 1536, 48))
+
+
+def test_long128k_full_size_sampled():
+    inp = gen.scan_inputs(gen.LONG128K)
+    y, h = gpu_scan(inp)
+    assert torch.isfinite(y.float()).all()
+    compare_scan(inp, y, h, channels=sample_channels(1, 1536, 12, seed=3))
+
+
+# ---- shapes and options -------------------------------------------------------------------
+CASES = [
+    # Bt, D, L, N, io, gate, dskip, bias, softplus
+    (1, 1, 1, 1, "f32", False, "ones", True, True),
+    (1, 5, 7, 3, "f32", True, "normal", True, True),
+    (2, 37, 33, 16, "f32", True, None, False, False),
+    (1, 3, 100, 17, "bf16", False, "ones", True, True),
+    (3, 9, 129, 64, "bf16", True, "normal", True, True),
+    (1, 40, 257, 100, "f32", True, "ones", True, True),
+    (2, 33, 96, 128, "bf16", False, None, True, True),
+    (1, 130, 64, 8, "bf16", True, "ones", True, False),
+    (2, 64, 1000, 32, "f32", True, "normal", True, True),
+    (1, 7, 4097, 4, "f32", False, "ones", True, True),
+]
+
+
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,bias,sp", CASES)
+def test_shapes(Bt, D, L, N, io, gate, dskip, bias, sp):
+    cfg = gen.ScanConfig("case", Bt, D, L, N, io=io, gate=gate, dskip=dskip, bias=bias, softplus=sp, seed=L + N)
+    inp = gen.scan_inputs(cfg)
+    if not sp:  # without the softplus the raw step itself must be a positive step
+        inp["delta"] = (inp["delta"].float().abs() * 0.2).to(inp["delta"].dtype)
+        if inp["delta_bias"] is not None:
+            inp["delta_bias"] = torch.full_like(inp["delta_bias"], 0.01)
+    y, h = gpu_scan(inp)
+    compare_scan(inp, y, h)
+
+
+@pytest.mark.parametrize("plan", ["16,4,5", "16,4,1", "4,4,3", "16,8,2", "8,1,7"])
+def test_forced_plans(plan, monkeypatch):
+    N = {"16,4,5": 64, "16,4,1": 64, "4,4,3": 16, "16,8,2": 128, "8,1,7": 8}[plan]
+    monkeypatch.setenv("SSM_PLAN", plan)
+    cfg = gen.ScanConfig("plan", 2, 40, 1111, N, io="bf16", gate=True, dskip="normal", seed=5)
+    inp = gen.scan_inputs(cfg)
+    y, h = gpu_scan(inp)
+    compare_scan(inp, y, h)
+
+
+def test_chunked_fp32_long_decay():
+    # small steps keep the state alive across chunk boundaries
+    cfg = gen.ScanConfig("chunks", 1, 16, 6000, 16, io="f32", gate=False, dskip="ones", seed=9)
+    inp = gen.scan_inputs(cfg)
+    inp["delta_bias"] = torch.full_like(inp["delta_bias"], -6.0)
+    y, h = gpu_scan(inp)
+    assert ssm.workspace_bytes(1, 16, 6000, 16, ssm.SSM_F32) > 0
+    compare_scan(inp, y, h)
+
+
+def test_empty_inputs():
+    d = "cuda"
+    A = -torch.ones(4, 4, device=d)
+    for (Bt, Dm, L) in [(0, 4, 8), (1, 0, 8)]:
+        u = torch.empty(Bt, Dm, L, device=d)
+        y, _ = ssm.selective_scan_fwd(u, u, A[:Dm], torch.empty(Bt, 4, L, device=d), torch.empty(Bt, 4, L, device=d))
+        assert y.numel() == 0
+    u = torch.empty(2, 4, 0, device=d)
+    st = torch.full((2, 4, 4), 7.0, device=d)
+    y, st2 = ssm.selective_scan_fwd(u, u, A, torch.empty(2, 4, 0, device=d), torch.empty(2, 4, 0, device=d),
+                                    last_state=st)
+    torch.cuda.synchronize()
+    assert torch.equal(st, torch.zeros_like(st))
+
+
+def test_misaligned_pointer_rejected():
+    d = "cuda"
+    buf = torch.zeros(1 * 4 * 64 + 1, device=d)
+    u = buf[1:].view(1, 4, 64)
+    good = torch.zeros(1, 4, 64, device=d)
+    A = -torch.ones(4, 4, device=d)
+    B = torch.zeros(1, 4, 64, device=d)
+    with pytest.raises(ssm.SsmError) as e:
+        ssm.selective_scan_fwd(u, good, A, B, B)
+    assert e.value.code == ssm.SSM_ERR_ALIGN
+
+
+def test_caller_workspace_and_stream():
+    inp = gen.scan_inputs(gen.BLOCK512)
+    need = ssm.workspace_bytes(1, 512, 1024, 16)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    y, h = gpu_scan(inp, stream=s, workspace=ws)
+    compare_scan(inp, y, h)
+    small = torch.empty(max(need // 2, 16), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ssm.SsmError) as e:
+        gpu_scan(inp, workspace=small)
+    assert e.value.code == ssm.SSM_ERR_WORKSPACE
+    assert ssm.stream_status(s) == ssm.SSM_OK
+
+
+@pytest.mark.parametrize("cfg", [gen.BLOCK512, gen.ScanConfig("h", 3, 70, 333, 16, io="f32", gate=True, seed=8)],
+                         ids=["block512", "ragged_f32"])
+def test_host_buffer_entry(cfg):
+    inp = gen.scan_inputs(cfg)
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    yh, hh = ssm.selective_scan_fwd_host(pin["u"], pin["delta"], pin["A"], pin["B"], pin["C"], D=pin["D"],
+                                         z=pin["z"], delta_bias=pin["delta_bias"], return_last_state=True)
+    assert yh.device.type == "cpu" and hh.device.type == "cpu"
+    compare_scan(inp, yh, hh)
+
+
+# ---- decode ---------------------------------------------------------------------------------
+def _decode_gpu(inp, steps):
+    g = to_dev(inp)
+    st = g["state0"].clone()
+    ys = []
+    for s in range(steps):
+        ys.append(ssm.state_update(st, g["x"][s], g["dt"][s], g["A"], g["B"][s], g["C"][s], D=g["D"],
+                                   z=None if g["z"] is None else g["z"][s]))
+    torch.cuda.synchronize()
+    return torch.stack(ys, -1), st
+
+
+def _decode_oracle(inp, rows, steps):
+    f = gen.as_f64
+    st = f(inp["state0"])[rows]
+    sm = np.abs(st)
+    ys, yms = [], []
+    for s in range(steps):
+        y, st, ym, sm = oracle.state_update(st, f(inp["x"][s])[rows], f(inp["dt"][s])[rows], f(inp["A"]),
+                                            f(inp["B"][s])[rows], f(inp["C"][s])[rows], D=f(inp["D"]),
+                                            z=None if inp["z"] is None else f(inp["z"][s])[rows],
+                                            smag=sm, with_mag=True)
+        ys.append(y)
+        yms.append(ym)
+    return np.stack(ys, -1), st, np.stack(yms, -1), sm
+
+
+def test_decode_full_size_sampled_rows():
+    inp = gen.decode_inputs(gen.DECODE)
+    y, st = _decode_gpu(inp, 64)
+    rows = [0, 97, 255]
+    yo, so, ym, sm = _decode_oracle(inp, rows, 64)
+    assert oracle.rel_err(y[rows].float().cpu().numpy(), yo, ym) <= TOL["bf16"]
+    assert oracle.rel_err(st[rows].cpu().numpy(), so, sm) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("N,gate,dskip,io", [(16, True, "ones", "bf16"), (5, False, None, "bf16"),
+                                            (64, True, "normal", "bf16"), (128, False, "ones", "bf16"),
+                                            (4, True, "ones", "f32"), (7, True, "normal", "f32")])
+def test_decode_shapes(N, gate, dskip, io):
+    inp = gen.decode_inputs(gen.DECODE, Bt=3, D=50, N=N, gate=gate, dskip=dskip, steps=9)
+    if io == "f32":
+        for k in ("x", "dt", "B", "C", "z"):
+            if inp[k] is not None:
+                inp[k] = inp[k].float()
+    y, st = _decode_gpu(inp, 9)
+    rows = [0, 1, 2]
+    yo, so, ym, sm = _decode_oracle(inp, rows, 9)
+    tol = TOL[io]
+    assert oracle.rel_err(y.float().cpu().numpy(), yo, ym) <= tol
+    assert oracle.rel_err(st.cpu().numpy(), so, sm) <= tol
+
+
+def test_scan_then_decode_equals_longer_scan():
+    """A scan of L steps then k recurrent steps from its final state equals the oracle's
+    scan of L+k steps (softplus folded: the decode step takes the final dt)."""
+    cfg = gen.ScanConfig("sd", 2, 24, 300, 16, io="f32", gate=True, dskip="ones", softplus=False, bias=False, seed=21)
+    inp = gen.scan_inputs(cfg)
+    inp["delta"] = inp["delta"].abs() * 0.1
+    L, k = 280, 20
+    first = {kk: (v[..., :L].contiguous() if isinstance(v, torch.Tensor) and v.dim() == 3 else v) for kk, v in inp.items()}
+    y1, h1 = gpu_scan(first)
+    g = to_dev(inp)
+    st = h1.clone()
+    ys = []
+    for t in range(L, L + k):
+        ys.append(ssm.state_update(st, g["u"][..., t].contiguous(), g["delta"][..., t].contiguous(), g["A"],
+                                   g["B"][..., t].contiguous(), g["C"][..., t].contiguous(), D=g["D"],
+                                   z=g["z"][..., t].contiguous()))
+    torch.cuda.synchronize()
+    y_all = torch.cat([y1, torch.stack(ys, -1)], -1)
+    compare_scan(inp, y_all, st)
