@@ -96,53 +96,64 @@ def max_over_ranks(x, ws):
 
 # ---------------------------------------------------------------------------- clocks (NVML)
 class ClockSampler:
-    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
-               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
-               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    """Samples SM clock and clock-event reasons with nvidia-smi during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, cuda_index):
-        self.samples, self.reasons, self.max_mhz = [], 0, None
-        self._stop = threading.Event()
-        self.ok = False
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ssm_clocks_{os.getpid()}_{cuda_index}.csv")
         try:
-            import pynvml
-            pynvml.nvmlInit()
             props = torch.cuda.get_device_properties(cuda_index)
-            self.h = pynvml.nvmlDeviceGetHandleByUUID("GPU-" + str(props.uuid))
-            self.nv = pynvml
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # noqa: BLE001
-            self.ok = False
-            self.err = repr(e)[:120]
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                self.reasons |= int(self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h))
-            except Exception:
-                pass
-            time.sleep(0.02)
+            self.uuid = "GPU-" + str(props.uuid)
+        except Exception:  # noqa: BLE001
+            self.uuid = None
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
-            self.t.start()
+        import subprocess
+        if self.uuid is None:
+            return self
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:  # noqa: BLE001
+            self.proc = None
         return self
 
     def __exit__(self, *a):
-        if self.ok:
-            self._stop.set()
-            self.t.join()
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+            self.f.close()
 
     def summary(self):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
-                    "reasons": ["unavailable: " + getattr(self, "err", "no samples")], "samples": 0}
-        names = [v for k, v in self.REASONS.items() if self.reasons & k and v != "gpu_idle"]
-        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
-                "reasons": names, "samples": len(self.samples)}
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable: nvidia-smi"], "samples": 0}
+        mhz, mx, reasons, pw = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                mhz.append(float(f[0])); mx = float(f[1]); pw.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(statistics.median(mhz)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz), "power_w_max": max(pw) if pw else None}
 
 
 # ---------------------------------------------------------------------------- oracle timing
