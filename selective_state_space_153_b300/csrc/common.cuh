@@ -104,4 +104,22 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// Transposed butterfly over the G lanes of a channel: on entry v[i] is this lane's partial
+// for timestep tb+i (i < G); on exit v[0] is the full sum for timestep tb + (lane % G).
+template <int G>
+__device__ __forceinline__ float group_reduce_transpose(float (&v)[G], int lane) {
+#pragma unroll
+    for (int h = G / 2; h >= 1; h /= 2) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float lo = v[i], hi = v[i + h];
+            const float send = upper ? lo : hi;
+            const float keep = upper ? hi : lo;
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+        }
+    }
+    return v[0];
+}
+
 }  // namespace ssm

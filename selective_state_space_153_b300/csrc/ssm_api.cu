@@ -9,10 +9,15 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <cuda.h>
+#include <mutex>
+
 #include "ssm_scan.h"
 #include "common.cuh"
+#include "ptx.cuh"
 #include "decode.cuh"
 #include "scan_seq.cuh"
+#include "scan_tc.cuh"
 
 namespace {
 
@@ -22,7 +27,6 @@ using namespace ssm;
 constexpr int kTile = 32;
 constexpr int kWarps = 4;
 
-__device__ int g_device_status = 0;  // written only by bounded device-side waits
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -90,7 +94,7 @@ ScanPlan plan_scan(const ssm_dims_t &d) {
     return p;
 }
 
-size_t scan_workspace_bytes(const ssm_dims_t &d, const ScanPlan &p) {
+size_t seq_workspace_bytes(const ssm_dims_t &d, const ScanPlan &p) {
     if (p.nchunks <= 1) return 0;
     const size_t BD = (size_t)(d.batch * d.dim), npad = (size_t)(p.nper * p.g);
     const size_t agg_h = (size_t)p.nchunks * BD * npad * 4, agg_s = (size_t)p.nchunks * BD * 4;
@@ -147,6 +151,148 @@ bool plan_supported(const ScanPlan &pl) {
     }
 }
 
+// ---- persistent TMEM-replay path ---------------------------------------------------------
+struct TcPlan {
+    bool use = false;
+    int G = 4, NG = 0, groups_per_b = 0, nseg = 1, seg_tiles = 1, ntiles = 0;
+    int64_t Lp = 0;
+    size_t off_carry = 0, off_bc = 0, bytes = 0, ctrl_bytes = 0;
+};
+
+bool env_is(const char *name, const char *val) {
+    const char *e = std::getenv(name);
+    return e != nullptr && std::strcmp(e, val) == 0;
+}
+
+TcPlan plan_tc(const ssm_dims_t &d) {
+    TcPlan t;
+    if (env_is("SSM_KERNEL", "seq")) return t;
+    const size_t esz = io_size(d.io_dtype);
+    if (((size_t)d.seqlen * esz) % 16 != 0) return t;                       // TMA row strides
+    if (d.seqlen >= (int64_t)1 << 30 || d.dim >= (int64_t)1 << 30 || d.batch >= (int64_t)1 << 30) return t;
+    const int64_t N = d.dstate;
+    t.G = N <= 16 ? 1 : (N <= 32 ? 2 : (N <= 64 ? 4 : 8));
+    const int cpw = 32 / t.G;
+    t.groups_per_b = (int)((d.dim + cpw - 1) / cpw);
+    const int64_t ng = d.batch * t.groups_per_b;
+    t.ntiles = (int)((d.seqlen + kTcT - 1) / kTcT);
+    const int64_t sms = sm_count();
+    const bool forced = env_is("SSM_KERNEL", "tc");
+    if (ng >= (int64_t)1 << 24) return t;
+    if (!forced && (ng < sms || t.ntiles < 4)) return t;
+    t.NG = (int)ng;
+    int64_t nseg = (16 * sms + ng - 1) / ng;
+    nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, t.ntiles));
+    t.seg_tiles = (int)((t.ntiles + nseg - 1) / nseg);
+    t.nseg = (t.ntiles + t.seg_tiles - 1) / t.seg_tiles;
+    t.Lp = (int64_t)t.ntiles * kTcT;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    t.ctrl_bytes = up((size_t)(1 + t.NG) * 4);
+    t.off_carry = t.ctrl_bytes;
+    t.off_bc = t.off_carry + up((size_t)t.NG * 2 * 512 * 4);
+    t.bytes = t.off_bc + up((size_t)d.batch * t.Lp * 2 * 16 * t.G * 4);
+    t.use = true;
+    return t;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// [Bt][Dm][L] io tensor, box [1][CPW][T]
+bool make_map(CUtensorMap *m, const void *base, const ssm_dims_t &d, int cpw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const size_t esz = io_size(d.io_dtype);
+    const cuuint64_t dims[3] = {(cuuint64_t)d.seqlen, (cuuint64_t)d.dim, (cuuint64_t)d.batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)(d.seqlen * esz), (cuuint64_t)(d.seqlen * d.dim * esz)};
+    const cuuint32_t box[3] = {(cuuint32_t)kTcT, (cuuint32_t)cpw, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, d.io_dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename IO, int G>
+cudaError_t launch_tc_t(const TcParams &prm, cudaStream_t s) {
+    using Cfg = TcCfg<IO, G>;
+    auto k = scan_tc_kernel<IO, G>;
+    static unsigned long long attr_set = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set |= 1ull << dev;
+    }
+    k<<<(unsigned)sm_count(), Cfg::W * 32, Cfg::SMEM, s>>>(prm);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_tc(int G, const TcParams &prm, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_tc_t<IO, 1>(prm, s);
+        case 2: return launch_tc_t<IO, 2>(prm, s);
+        case 4: return launch_tc_t<IO, 4>(prm, s);
+        case 8: return launch_tc_t<IO, 8>(prm, s);
+        default: return cudaErrorInvalidConfiguration;
+    }
+}
+
+ssm_status_t run_scan_tc(const ssm_dims_t &d, const TcPlan &t, const void *u, const void *delta, const float *A,
+                         const void *B, const void *C, const float *D, const void *z, const float *delta_bias,
+                         int delta_softplus, void *y, float *last_state, char *ws, cudaStream_t s) {
+    TcParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    const int cpw = 32 / t.G;
+    if (!make_map(&prm.map_u, u, d, cpw) || !make_map(&prm.map_delta, delta, d, cpw) ||
+        !make_map(&prm.map_z, z ? z : u, d, cpw) || !make_map(&prm.map_y, y, d, cpw))
+        return SSM_ERR_CUDA;
+    prm.bc = reinterpret_cast<const float *>(ws + t.off_bc);
+    prm.A = A; prm.D = D; prm.bias = delta_bias; prm.last_state = last_state;
+    prm.ctrl = reinterpret_cast<int *>(ws);
+    prm.carry = reinterpret_cast<float *>(ws + t.off_carry);
+    prm.Bt = d.batch; prm.Dm = d.dim; prm.L = d.seqlen; prm.N = d.dstate; prm.Lp = t.Lp;
+    prm.NG = t.NG; prm.groups_per_b = t.groups_per_b; prm.nseg = t.nseg; prm.seg_tiles = t.seg_tiles;
+    prm.ntiles = t.ntiles; prm.has_z = z != nullptr; prm.softplus = delta_softplus ? 1 : 0;
+    prm.spin_limit = 1u << 24;
+    prm.force_timeout = 0;
+    if (env_is("SSM_TEST_FORCE_TIMEOUT", "1")) { prm.force_timeout = 1; prm.spin_limit = 256; }
+    if (cudaMemsetAsync(ws, 0, t.ctrl_bytes, s) != cudaSuccess) return SSM_ERR_CUDA;
+    const int NP = 16 * t.G;
+    float *bc = reinterpret_cast<float *>(ws + t.off_bc);
+    const dim3 pg((unsigned)(t.Lp / 32), (unsigned)d.batch);
+    const size_t psm = (size_t)2 * NP * 33 * 4;
+    if (d.io_dtype == SSM_BF16)
+        bc_prep_kernel<bf16><<<pg, 256, psm, s>>>(static_cast<const bf16 *>(B), static_cast<const bf16 *>(C), bc,
+                                                  d.dstate, d.seqlen, t.Lp, NP);
+    else
+        bc_prep_kernel<float><<<pg, 256, psm, s>>>(static_cast<const float *>(B), static_cast<const float *>(C), bc,
+                                                   d.dstate, d.seqlen, t.Lp, NP);
+    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    const cudaError_t e = d.io_dtype == SSM_BF16 ? launch_tc<bf16>(t.G, prm, s) : launch_tc<float>(t.G, prm, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 __global__ void zero_f32_kernel(float *p, int64_t n) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) p[i] = 0.0f;
 }
@@ -181,9 +327,22 @@ ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, 
         }
         return SSM_OK;
     }
+    const TcPlan tp = plan_tc(d);
+    if (tp.use) {
+        char *w = static_cast<char *>(workspace);
+        bool alloc = false;
+        if (w == nullptr || ws_bytes < tp.bytes) {
+            if (!own_ws) return SSM_ERR_WORKSPACE;
+            if (cudaMallocAsync(reinterpret_cast<void **>(&w), tp.bytes, s) != cudaSuccess) return SSM_ERR_CUDA;
+            alloc = true;
+        }
+        const ssm_status_t r = run_scan_tc(d, tp, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, w, s);
+        if (alloc) cudaFreeAsync(w, s);
+        return r;
+    }
     const ScanPlan pl = plan_scan(d);
     if (!plan_supported(pl)) return SSM_ERR_UNSUPPORTED;
-    const size_t need = scan_workspace_bytes(d, pl);
+    const size_t need = seq_workspace_bytes(d, pl);
     bool allocated = false;
     if (need > 0) {
         if (workspace == nullptr || ws_bytes < need) {
@@ -247,7 +406,9 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_dims_t *dims, const void *u, const
 size_t ssm_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
-    return scan_workspace_bytes(*dims, plan_scan(*dims));
+    const TcPlan tp = plan_tc(*dims);
+    if (tp.use) return tp.bytes;
+    return seq_workspace_bytes(*dims, plan_scan(*dims));
 }
 
 ssm_status_t ssm_selective_scan_fwd_ws(const ssm_dims_t *dims, const void *u, const void *delta,
@@ -398,10 +559,10 @@ ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, 
 ssm_status_t ssm_stream_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSM_ERR_CUDA;
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, ssm::g_ssm_status, sizeof(int)) != cudaSuccess) return SSM_ERR_CUDA;
     if (v != 0) {
         const int zero = 0;
-        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return SSM_ERR_CUDA;
+        if (cudaMemcpyToSymbol(ssm::g_ssm_status, &zero, sizeof(int)) != cudaSuccess) return SSM_ERR_CUDA;
         return static_cast<ssm_status_t>(v);
     }
     return SSM_OK;

@@ -219,3 +219,50 @@ def test_scan_then_decode_equals_longer_scan():
     torch.cuda.synchronize()
     y_all = torch.cat([y1, torch.stack(ys, -1)], -1)
     compare_scan(inp, y_all, st)
+
+
+# ---- persistent tensor-memory path, forced on small shapes -------------------------------------
+TC_CASES = [
+    # Bt, D, L, N, io, gate, dskip
+    (1, 8, 128, 64, "bf16", False, "ones"),
+    (2, 37, 1000, 16, "bf16", True, "normal"),
+    (1, 20, 4096, 64, "f32", True, "ones"),
+    (3, 9, 520, 128, "bf16", False, None),
+    (1, 50, 2048, 32, "bf16", True, "ones"),
+    (2, 33, 64, 5, "f32", False, "normal"),
+    (1, 64, 8192, 64, "bf16", False, "ones"),
+]
+
+
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip", TC_CASES)
+def test_tc_forced_shapes(Bt, D, L, N, io, gate, dskip, monkeypatch):
+    monkeypatch.setenv("SSM_KERNEL", "tc")
+    cfg = gen.ScanConfig("tc", Bt, D, L, N, io=io, gate=gate, dskip=dskip, seed=D + L)
+    inp = gen.scan_inputs(cfg)
+    y, h = gpu_scan(inp)
+    assert ssm.stream_status() == ssm.SSM_OK
+    compare_scan(inp, y, h)
+
+
+def test_tc_bounded_wait_reports_timeout(monkeypatch):
+    """The carry wait between segments gives up after a bounded spin on a flag that is never
+    set (test hook), records SSM_ERR_TIMEOUT, and the next call runs normally."""
+    monkeypatch.setenv("SSM_KERNEL", "tc")
+    cfg = gen.ScanConfig("to", 1, 16, 2048, 16, io="bf16", gate=False, seed=4)
+    inp = gen.scan_inputs(cfg)
+    monkeypatch.setenv("SSM_TEST_FORCE_TIMEOUT", "1")
+    gpu_scan(inp)
+    assert ssm.stream_status() == ssm.SSM_ERR_TIMEOUT
+    assert ssm.stream_status() == ssm.SSM_OK          # reading clears it
+    monkeypatch.delenv("SSM_TEST_FORCE_TIMEOUT")
+    y, h = gpu_scan(inp)
+    assert ssm.stream_status() == ssm.SSM_OK
+    compare_scan(inp, y, h)
+
+
+def test_seq_forced_long(monkeypatch):
+    monkeypatch.setenv("SSM_KERNEL", "seq")
+    cfg = gen.ScanConfig("seqlong", 1, 40, 20000, 64, io="bf16", gate=True, seed=6)
+    inp = gen.scan_inputs(cfg)
+    y, h = gpu_scan(inp)
+    compare_scan(inp, y, h)
