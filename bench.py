@@ -85,6 +85,12 @@ def barrier(ws):
         dist.barrier()
 
 
+def weak_scaling_value(units_per_rank, ws, max_seconds_per_step):
+    """Whole-job throughput: every rank processes its own copy of the workload (weak
+    scaling), so the job's units per step are ws * units_per_rank, over the slowest rank."""
+    return ws * units_per_rank / max_seconds_per_step
+
+
 def max_over_ranks(x, ws):
     if ws == 1:
         return x
@@ -237,7 +243,7 @@ def bench_ours(args, rank, ws, local):
                                                 ssm.SSM_BF16 if cfg.io == "bf16" else ssm.SSM_F32) > 0 else 1
     out = {
         "metric": "scan elements/s (B*D*L*N/s); fraction of the max(HBM, SFU) roofline; decode tok/s",
-        "value": ws * elems / t_step, "unit": "elem/s", "n_gpus": ws, "steps": args.steps,
+        "value": weak_scaling_value(elems, ws, t_step), "unit": "elem/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 compute, bf16 io" if cfg.io == "bf16" else "f32",
         "data": "synthetic (seeded generator, PCG64)",
