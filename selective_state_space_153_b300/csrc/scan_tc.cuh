@@ -44,7 +44,8 @@ constexpr int kTcK = 8;       // steps per warp per tile
 constexpr int kTcT = kTcWarps * kTcK;
 
 struct TcParams {
-    CUtensorMap map_u, map_delta, map_z, map_y;   // 3-D [Bt][Dm][L] io-dtype tensors
+    CUtensorMap map_u, map_delta, map_z, map_y;   // 3-D [Bt][Dm][L] io-dtype tensors, box [1][CPW][T]
+    CUtensorMap map_y8;                            // y with a box of 8 steps (per-warp stores)
     const float *bc;                               // [Bt][Lp][2*NP] fp32: B row then C row
     const float *A, *D, *bias;
     float *last_state;
@@ -55,7 +56,11 @@ struct TcParams {
     int has_z, softplus;
     uint32_t spin_limit;
     int force_timeout;                             // test hook: wait for a flag nothing sets
+    int cpw, np;                                   // geometry the host planned (checked on entry)
 };
+
+// Status recorded when a launch's planned geometry does not match the kernel's
+constexpr int kStatusBadGeometry = 5;   // SSM_ERR_UNSUPPORTED
 
 template <typename IO, int G>
 struct TcCfg {
@@ -74,6 +79,8 @@ struct TcCfg {
     // one CTA per SM: the kernel owns all 512 tensor-memory columns
     static constexpr size_t SMEM = BYTES > 120 * 1024 ? BYTES : 120 * 1024;
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "G");
+    // every shared-memory buffer a TMA tensor copy reads or writes starts on 128 bytes
+    static_assert(RAW_ARR % 128 == 0 && OFF_RAW % 128 == 0 && OFF_Y % 128 == 0, "TMA smem alignment");
 };
 
 // B, C [Bt][N][L] io -> bc [Bt][Lp][2*NP] fp32 (zero beyond N and L), 32 timesteps per block.
@@ -117,6 +124,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1) scan_tc_kernel(const __grid_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = lane / G, g = lane % G;
     constexpr size_t ARR = (size_t)CPW * T;
+    if (p.cpw != CPW || p.np != NP) {   // tile sizes of the TMA boxes would not match expect_tx
+        if (tid == 0) set_status(kStatusBadGeometry);
+        return;
+    }
 
     if (warp == 0) tmem_alloc(s_tmem, 512);
     if (tid == 0) {

@@ -18,6 +18,7 @@
 #include "decode.cuh"
 #include "scan_seq.cuh"
 #include "scan_tc.cuh"
+#include "scan_tp.cuh"
 
 namespace {
 
@@ -154,6 +155,9 @@ bool plan_supported(const ScanPlan &pl) {
 // ---- persistent TMEM-replay path ---------------------------------------------------------
 struct TcPlan {
     bool use = false;
+    bool pipelined = true;   // scan_tp_kernel (default, dstate <= 64) or scan_tc_kernel
+    int T = kTpT;
+    int cpw = 8, np = 64;    // channels per group, padded states
     int G = 4, NG = 0, groups_per_b = 0, nseg = 1, seg_tiles = 1, ntiles = 0;
     int64_t Lp = 0;
     size_t off_carry = 0, off_bc = 0, bytes = 0, ctrl_bytes = 0;
@@ -171,13 +175,26 @@ TcPlan plan_tc(const ssm_dims_t &d) {
     if (((size_t)d.seqlen * esz) % 16 != 0) return t;                       // TMA row strides
     if (d.seqlen >= (int64_t)1 << 30 || d.dim >= (int64_t)1 << 30 || d.batch >= (int64_t)1 << 30) return t;
     const int64_t N = d.dstate;
-    t.G = N <= 16 ? 1 : (N <= 32 ? 2 : (N <= 64 ? 4 : 8));
-    const int cpw = 32 / t.G;
+    // pipelined kernel: GP = 8-state groups per channel pair (N <= 64), 64/GP channels per group;
+    // otherwise the barrier-phased kernel: G = 16-state groups per channel, 32/G channels
+    // (fp32 with N <= 8 would need 64-channel groups whose tiles do not fit shared memory)
+    t.pipelined = !env_is("SSM_KERNEL", "tc") && N <= 64 && !(N <= 8 && d.io_dtype == SSM_F32);
+    if (t.pipelined) {
+        t.G = N <= 8 ? 1 : (N <= 16 ? 2 : (N <= 32 ? 4 : 8));
+        t.cpw = 64 / t.G;
+        t.np = 8 * t.G;
+    } else {
+        t.G = N <= 16 ? 1 : (N <= 32 ? 2 : (N <= 64 ? 4 : 8));
+        t.cpw = 32 / t.G;
+        t.np = 16 * t.G;
+    }
+    const int cpw = t.cpw;
     t.groups_per_b = (int)((d.dim + cpw - 1) / cpw);
     const int64_t ng = d.batch * t.groups_per_b;
-    t.ntiles = (int)((d.seqlen + kTcT - 1) / kTcT);
+    t.T = t.pipelined ? kTpT : kTcT;
+    t.ntiles = (int)((d.seqlen + t.T - 1) / t.T);
     const int64_t sms = sm_count();
-    const bool forced = env_is("SSM_KERNEL", "tc");
+    const bool forced = env_is("SSM_KERNEL", "tc") || env_is("SSM_KERNEL", "tp");
     if (ng >= (int64_t)1 << 24) return t;
     if (!forced && (ng < sms || t.ntiles < 4)) return t;
     t.NG = (int)ng;
@@ -185,12 +202,12 @@ TcPlan plan_tc(const ssm_dims_t &d) {
     nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, t.ntiles));
     t.seg_tiles = (int)((t.ntiles + nseg - 1) / nseg);
     t.nseg = (t.ntiles + t.seg_tiles - 1) / t.seg_tiles;
-    t.Lp = (int64_t)t.ntiles * kTcT;
+    t.Lp = (int64_t)t.ntiles * t.T;
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     t.ctrl_bytes = up((size_t)(1 + t.NG) * 4);
     t.off_carry = t.ctrl_bytes;
     t.off_bc = t.off_carry + up((size_t)t.NG * 2 * 512 * 4);
-    t.bytes = t.off_bc + up((size_t)d.batch * t.Lp * 2 * 16 * t.G * 4);
+    t.bytes = t.off_bc + up((size_t)d.batch * t.Lp * 2 * t.np * 4);
     t.use = true;
     return t;
 }
@@ -213,14 +230,14 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [Bt][Dm][L] io tensor, box [1][CPW][T]
-bool make_map(CUtensorMap *m, const void *base, const ssm_dims_t &d, int cpw) {
+// [Bt][Dm][L] io tensor, box [1][CPW][box_t]
+bool make_map(CUtensorMap *m, const void *base, const ssm_dims_t &d, int cpw, int box_t) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const size_t esz = io_size(d.io_dtype);
     const cuuint64_t dims[3] = {(cuuint64_t)d.seqlen, (cuuint64_t)d.dim, (cuuint64_t)d.batch};
     const cuuint64_t strides[2] = {(cuuint64_t)(d.seqlen * esz), (cuuint64_t)(d.seqlen * d.dim * esz)};
-    const cuuint32_t box[3] = {(cuuint32_t)kTcT, (cuuint32_t)cpw, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)box_t, (cuuint32_t)cpw, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(m, d.io_dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -247,8 +264,37 @@ cudaError_t launch_tc_t(const TcParams &prm, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <typename IO, int G>
+cudaError_t launch_tp_t(const TcParams &prm, cudaStream_t s) {
+    using Cfg = TpCfg<IO, G>;
+    auto k = scan_tp_kernel<IO, G>;
+    static unsigned long long attr_set = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set |= 1ull << dev;
+    }
+    k<<<(unsigned)sm_count(), Cfg::W * 32, Cfg::SMEM, s>>>(prm);
+    return cudaGetLastError();
+}
+
 template <typename IO>
-cudaError_t launch_tc(int G, const TcParams &prm, cudaStream_t s) {
+cudaError_t launch_tc(bool pipelined, int G, const TcParams &prm, cudaStream_t s) {
+    if (pipelined) {
+        switch (G) {
+            case 1:
+                if constexpr (tp_bytes<IO, 1>(2) <= kSmemLimit) return launch_tp_t<IO, 1>(prm, s);
+                return cudaErrorInvalidConfiguration;
+            case 2: return launch_tp_t<IO, 2>(prm, s);
+            case 4: return launch_tp_t<IO, 4>(prm, s);
+            case 8: return launch_tp_t<IO, 8>(prm, s);
+            default: return cudaErrorInvalidConfiguration;
+        }
+    }
     switch (G) {
         case 1: return launch_tc_t<IO, 1>(prm, s);
         case 2: return launch_tc_t<IO, 2>(prm, s);
@@ -263,9 +309,10 @@ ssm_status_t run_scan_tc(const ssm_dims_t &d, const TcPlan &t, const void *u, co
                          int delta_softplus, void *y, float *last_state, char *ws, cudaStream_t s) {
     TcParams prm;
     std::memset(&prm, 0, sizeof(prm));
-    const int cpw = 32 / t.G;
-    if (!make_map(&prm.map_u, u, d, cpw) || !make_map(&prm.map_delta, delta, d, cpw) ||
-        !make_map(&prm.map_z, z ? z : u, d, cpw) || !make_map(&prm.map_y, y, d, cpw))
+    const int cpw = t.cpw;
+    if (!make_map(&prm.map_u, u, d, cpw, t.T) || !make_map(&prm.map_delta, delta, d, cpw, t.T) ||
+        !make_map(&prm.map_z, z ? z : u, d, cpw, t.T) || !make_map(&prm.map_y, y, d, cpw, t.T) ||
+        !make_map(&prm.map_y8, y, d, cpw, 8))
         return SSM_ERR_CUDA;
     prm.bc = reinterpret_cast<const float *>(ws + t.off_bc);
     prm.A = A; prm.D = D; prm.bias = delta_bias; prm.last_state = last_state;
@@ -274,11 +321,13 @@ ssm_status_t run_scan_tc(const ssm_dims_t &d, const TcPlan &t, const void *u, co
     prm.Bt = d.batch; prm.Dm = d.dim; prm.L = d.seqlen; prm.N = d.dstate; prm.Lp = t.Lp;
     prm.NG = t.NG; prm.groups_per_b = t.groups_per_b; prm.nseg = t.nseg; prm.seg_tiles = t.seg_tiles;
     prm.ntiles = t.ntiles; prm.has_z = z != nullptr; prm.softplus = delta_softplus ? 1 : 0;
+    prm.cpw = t.cpw;
+    prm.np = t.np;
     prm.spin_limit = 1u << 24;
     prm.force_timeout = 0;
     if (env_is("SSM_TEST_FORCE_TIMEOUT", "1")) { prm.force_timeout = 1; prm.spin_limit = 256; }
     if (cudaMemsetAsync(ws, 0, t.ctrl_bytes, s) != cudaSuccess) return SSM_ERR_CUDA;
-    const int NP = 16 * t.G;
+    const int NP = t.np;
     float *bc = reinterpret_cast<float *>(ws + t.off_bc);
     const dim3 pg((unsigned)(t.Lp / 32), (unsigned)d.batch);
     const size_t psm = (size_t)2 * NP * 33 * 4;
@@ -289,7 +338,8 @@ ssm_status_t run_scan_tc(const ssm_dims_t &d, const TcPlan &t, const void *u, co
         bc_prep_kernel<float><<<pg, 256, psm, s>>>(static_cast<const float *>(B), static_cast<const float *>(C), bc,
                                                    d.dstate, d.seqlen, t.Lp, NP);
     if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-    const cudaError_t e = d.io_dtype == SSM_BF16 ? launch_tc<bf16>(t.G, prm, s) : launch_tc<float>(t.G, prm, s);
+    const cudaError_t e = d.io_dtype == SSM_BF16 ? launch_tc<bf16>(t.pipelined, t.G, prm, s)
+                                                 : launch_tc<float>(t.pipelined, t.G, prm, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

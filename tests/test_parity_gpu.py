@@ -234,9 +234,10 @@ TC_CASES = [
 ]
 
 
+@pytest.mark.parametrize("kernel", ["tp", "tc"])
 @pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip", TC_CASES)
-def test_tc_forced_shapes(Bt, D, L, N, io, gate, dskip, monkeypatch):
-    monkeypatch.setenv("SSM_KERNEL", "tc")
+def test_tc_forced_shapes(Bt, D, L, N, io, gate, dskip, kernel, monkeypatch):
+    monkeypatch.setenv("SSM_KERNEL", kernel)
     cfg = gen.ScanConfig("tc", Bt, D, L, N, io=io, gate=gate, dskip=dskip, seed=D + L)
     inp = gen.scan_inputs(cfg)
     y, h = gpu_scan(inp)
@@ -244,10 +245,11 @@ def test_tc_forced_shapes(Bt, D, L, N, io, gate, dskip, monkeypatch):
     compare_scan(inp, y, h)
 
 
-def test_tc_bounded_wait_reports_timeout(monkeypatch):
+@pytest.mark.parametrize("kernel", ["tp", "tc"])
+def test_tc_bounded_wait_reports_timeout(kernel, monkeypatch):
     """The carry wait between segments gives up after a bounded spin on a flag that is never
     set (test hook), records SSM_ERR_TIMEOUT, and the next call runs normally."""
-    monkeypatch.setenv("SSM_KERNEL", "tc")
+    monkeypatch.setenv("SSM_KERNEL", kernel)
     cfg = gen.ScanConfig("to", 1, 16, 2048, 16, io="bf16", gate=False, seed=4)
     inp = gen.scan_inputs(cfg)
     monkeypatch.setenv("SSM_TEST_FORCE_TIMEOUT", "1")
