@@ -120,6 +120,46 @@ ssm_status_t ssm_selective_scan_fwd_ws(const ssm_dims_t *dims, const void *u,
                                        float *last_state, void *workspace,
                                        size_t workspace_bytes, void *stream);
 
+/* Size of the library's fixed device scratch used by ssm_selective_scan_fwd_noalloc. */
+#define SSM_SCRATCH_MAX_BYTES ((size_t)16 * 1024 * 1024)
+
+/*
+ * As ssm_selective_scan_fwd, but it never allocates device memory: the chunk carries,
+ * the persistent kernel's control words and the prepared B/C live in one fixed scratch
+ * array of SSM_SCRATCH_MAX_BYTES per device, compiled into the library. The method has
+ * no counterpart on the pages: this is a calling convention, not a step of the scan.
+ *
+ * For callers that cannot allocate at call time:
+ *   - a program whose device memory is held by another allocator (a framework's caching
+ *     pool), where a stream-ordered allocation from the driver's default pool can fail for
+ *     lack of memory although the framework has free blocks;
+ *   - a device or driver configuration without stream-ordered memory pools
+ *     (cudaDevAttrMemoryPoolsSupported is 0), where cudaMallocAsync is not available;
+ *   - plain C callers with no allocator of their own that cannot size a workspace and
+ *     keep it alive until each call has completed on the stream.
+ *
+ * Scratch size: returns SSM_ERR_WORKSPACE, before any CUDA work is queued, when
+ * ssm_selective_scan_workspace_bytes(dims) exceeds SSM_SCRATCH_MAX_BYTES. For example,
+ * 8 x 1536 x 2048 x 16 needs 3.5 MiB and fits; 1 x 1536 x 131072 x 64 needs about 65 MiB
+ * and is rejected. Use ssm_selective_scan_fwd_ws for those.
+ * Zero state: the control words at the start of the scratch (the persistent kernel's
+ * work ticket and per-segment carry flags) must be zero when that kernel starts; every
+ * call clears them on `stream` (cudaMemsetAsync) before its launch. Everything else in
+ * the scratch is written before it is read within the call.
+ * First use: the first call on each device resolves the scratch's device address with
+ * cudaGetSymbolAddress, which may load the library's module. Make that first call before
+ * any stream capture begins. A failure there returns SSM_ERR_CUDA.
+ * Concurrency: there is ONE scratch per device. Calls whose GPU work overlaps on the same
+ * device race on it, whichever streams or host threads issue them, and give wrong results.
+ * Queue such calls on one stream, or order them with events.
+ * Arguments, layout and the other status codes are those of ssm_selective_scan_fwd.
+ */
+ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_dims_t *dims, const void *u,
+                                            const void *delta, const float *A, const void *B,
+                                            const void *C, const float *D, const void *z,
+                                            const float *delta_bias, int delta_softplus,
+                                            void *y, float *last_state, void *stream);
+
 /*
  * Recurrent single-token step (lmnt.cn "From RNN to Mamba", section 5.3; the section 3.2
  * loop body for one timestep), in place on the state:

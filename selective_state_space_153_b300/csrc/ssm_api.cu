@@ -439,6 +439,42 @@ ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, 
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+// ---- fixed scratch for ssm_selective_scan_fwd_noalloc -------------------------------------
+// Callers that cannot allocate device memory at call time (their memory is held by another
+// allocator's pool, their device has no stream-ordered pools, or they are plain C code with
+// nothing to own a workspace) get the chunk carries, control words and prepared B/C from this
+// array instead. One copy exists per device, in the module's own global memory; it is only
+// ever passed to run_scan as a caller workspace, so no code path allocates on its behalf.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_SCRATCH_MAX_BYTES];
+
+constexpr int kScratchDevices = 64;   // devices whose scratch address is cached
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kScratchDevices] = {};
+
+// Device address of the current device's scratch, resolved with cudaGetSymbolAddress at
+// first use on that device (which may load the module: outside any stream capture).
+ssm_status_t scratch_address(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    const bool cached = dev >= 0 && dev < kScratchDevices;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (cached && g_scratch_addr[dev] != nullptr) {
+        *out = g_scratch_addr[dev];
+        return SSM_OK;
+    }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();   // do not leave the error for the next launch check to find
+        return SSM_ERR_CUDA;
+    }
+    if (cached) g_scratch_addr[dev] = p;
+    *out = p;
+    return SSM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -471,6 +507,26 @@ ssm_status_t ssm_selective_scan_fwd_ws(const ssm_dims_t *dims, const void *u, co
     if (workspace != nullptr && !aligned16(workspace)) return SSM_ERR_ALIGN;
     return run_scan(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
                     workspace, workspace_bytes, false, static_cast<cudaStream_t>(stream));
+}
+
+ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_dims_t *dims, const void *u, const void *delta,
+                                            const float *A, const void *B, const void *C,
+                                            const float *D, const void *z, const float *delta_bias,
+                                            int delta_softplus, void *y, float *last_state,
+                                            void *stream) {
+    ssm_status_t st = scan_checks(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
+    if (st != SSM_OK) return st;
+    const size_t need = ssm_selective_scan_workspace_bytes(dims);
+    if (need > SSM_SCRATCH_MAX_BYTES) return SSM_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (need > 0) {
+        st = scratch_address(&scratch);
+        if (st != SSM_OK) return st;
+    }
+    // own_ws = false: run_scan may only use the scratch, never allocate a replacement
+    return run_scan(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
+                    scratch, need > 0 ? SSM_SCRATCH_MAX_BYTES : 0, false,
+                    static_cast<cudaStream_t>(stream));
 }
 
 ssm_status_t ssm_state_update(const ssm_dims_t *dims, float *state, const void *x, const void *dt,

@@ -20,11 +20,13 @@ SSM_OK, SSM_ERR_NULL, SSM_ERR_SHAPE, SSM_ERR_DTYPE, SSM_ERR_ALIGN = 0, 1, 2, 3, 
 SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = 5, 6, 7, 8
 SSM_F32, SSM_BF16 = 0, 1
 MAX_DSTATE = 128
+SCRATCH_MAX_BYTES = 16 * 1024 * 1024   # SSM_SCRATCH_MAX_BYTES: the no-alloc entry's fixed scratch
 
 # every symbol include/ssm_scan.h declares
 EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_workspace_bytes",
            "ssm_selective_scan_fwd_ws", "ssm_state_update", "ssm_selective_scan_fwd_host",
-           "ssm_stream_status", "ssm_status_string", "ssm_version")
+           "ssm_stream_status", "ssm_status_string", "ssm_version",
+           "ssm_selective_scan_fwd_noalloc")
 
 
 class SsmDims(ctypes.Structure):
@@ -58,6 +60,8 @@ def load(path: str = LIB_PATH):
     lib.ssm_selective_scan_fwd_ws.argtypes = scan_args + [_vp, ctypes.c_size_t, _vp]
     lib.ssm_selective_scan_fwd_ws.restype = ctypes.c_int
     lib.ssm_selective_scan_fwd_host.argtypes = scan_args + [_vp]
+    lib.ssm_selective_scan_fwd_noalloc.argtypes = scan_args + [_vp]
+    lib.ssm_selective_scan_fwd_noalloc.restype = ctypes.c_int
     lib.ssm_selective_scan_fwd_host.restype = ctypes.c_int
     lib.ssm_selective_scan_workspace_bytes.argtypes = [dp]
     lib.ssm_selective_scan_workspace_bytes.restype = ctypes.c_size_t
@@ -127,6 +131,32 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
                                            _stream_ptr(stream))
     if rc != SSM_OK:
         raise SsmError(rc, "ssm_selective_scan_fwd")
+    return y, last_state
+
+
+def selective_scan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                               y=None, last_state=None, return_last_state=False, stream=None
+                               ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Device scan through ssm_selective_scan_fwd_noalloc: no device allocation inside the
+    library; its scratch is the library's fixed per-device array of SCRATCH_MAX_BYTES.
+    Raises SsmError (SSM_ERR_WORKSPACE) for a shape whose scratch exceeds that size. Calls
+    that overlap on the GPU share the scratch and race: keep them on one stream."""
+    lib = load()
+    Bt, Dm, L = u.shape
+    N = A.shape[1]
+    io = _io_code(u)
+    if y is None:
+        y = torch.empty_like(u)
+    if return_last_state and last_state is None:
+        last_state = torch.empty((Bt, Dm, N), dtype=torch.float32, device=u.device)
+    dm = dims(Bt, Dm, L, N, io)
+    rc = lib.ssm_selective_scan_fwd_noalloc(ctypes.byref(dm), _p(u), _p(delta), _p(A), _p(B), _p(C), _p(D),
+                                            _p(z), _p(delta_bias), int(bool(delta_softplus)), _p(y),
+                                            _p(last_state), _stream_ptr(stream))
+    if rc != SSM_OK:
+        need = workspace_bytes(Bt, Dm, L, N, io)
+        raise SsmError(rc, f"ssm_selective_scan_fwd_noalloc (scratch needed {need} B, "
+                           f"fixed size {SCRATCH_MAX_BYTES} B)")
     return y, last_state
 
 
