@@ -41,6 +41,22 @@ FALLBACK_HBM_GBS = 6400.0
 TRAFFIC_BYTES_PER_LAUNCH = None
 
 
+def count_kernel_launches(fn):
+    """Kernels launched by one call of fn, counted by the CUDA activity profiler (memsets and
+    copies excluded). None if the profiler is unavailable."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+        kern = [n for n in names if not n.lower().startswith(("memset", "memcpy"))]
+        return len(kern), sorted(set(kern))
+    except Exception:  # noqa: BLE001
+        return None, []
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -239,8 +255,10 @@ def bench_ours(args, rank, ws, local):
     ex2_peak = SM_COUNT * EX2_PER_CLK_SM * sm_max * 1e6 / 1e9          # Gexp/s at the max SM clock
     achieved = elems / t_step / 1e9
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    launches_per_step = 3 if ssm.workspace_bytes(cfg.Bt, cfg.D, cfg.L, cfg.N,
-                                                ssm.SSM_BF16 if cfg.io == "bf16" else ssm.SSM_F32) > 0 else 1
+    launches_per_step, kernel_names = count_kernel_launches(step)
+    if launches_per_step is None:   # profiler unavailable: the planner's count for this shape
+        launches_per_step = 2 if ssm.workspace_bytes(cfg.Bt, cfg.D, cfg.L, cfg.N,
+                                                    ssm.SSM_BF16 if cfg.io == "bf16" else ssm.SSM_F32) > 0 else 1
     out = {
         "metric": "scan elements/s (B*D*L*N/s); fraction of the max(HBM, SFU) roofline; decode tok/s",
         "value": weak_scaling_value(elems, ws, t_step), "unit": "elem/s", "n_gpus": ws, "steps": args.steps,
@@ -262,6 +280,7 @@ def bench_ours(args, rank, ws, local):
                                                if clocks["sm_mhz"] else None)},
         "clocks": clocks,
         "gpu_launches": args.steps * launches_per_step,
+        "kernels_per_step": kernel_names,
     }
     # end to end: host buffers through the C ABI, copies inside the timed region
     if not args.no_e2e:

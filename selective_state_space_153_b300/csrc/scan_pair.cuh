@@ -1,0 +1,342 @@
+// Selective scan, channel-pair kernel: each lane walks the sequence for TWO channels and KS
+// of their states, so one shared-memory read of B[t, n..n+3] (and of C) serves two channels
+// and every arithmetic step runs on packed pairs (f32x2): per (channel, state, timestep) one
+// MUFU ex2 and four FP32 operations -- dt*A, dt*u*B, the recurrence FMA and the readout FMA.
+//
+// Source of the computation: the per-timestep loop of section 3.2 of "From RNN to Mamba:
+// state-space model principles and long-sequence modelling in practice" (lmnt.cn):
+// A_bar = exp(dt*A), B_bar = dt*B_t, h = A_bar*h + B_bar*x_t, y_t = sum_n h*C_t, then
+// y + x*D and the SiLU(z) gate; dt = softplus(delta + bias) (sections 3.2-3.3).
+//
+// Work decomposition (one CTA): batch row b, kCh = WARPS*2*(32/GP) consecutive channels,
+// one chunk [l_begin, l_end) of the sequence walked in tiles of T timesteps.
+//   lane (warp w, lane l): pair P = w*(32/GP) + l/GP -> channels 2P and 2P+1 of the block;
+//   state group g = l%GP owns the states n = 4*(GP*q + g) + j (q < KS/4, j < 4), so the GP
+//   groups of a pair read GP adjacent 16-byte pieces of a B/C row (one wavefront per
+//   LDS.128, broadcast to the 32/GP pairs of the warp).
+//   y: per channel each lane keeps its partial sum over its KS states; every GP timesteps
+//   the GP lanes exchange partials with a transposed butterfly (lane g ends with the sum for
+//   timestep tb+g), add D*u, apply the gate and store y.
+// Pipeline per tile: raw io rows (u, delta, z, B, C) arrive by cp.async three tiles deep;
+// one barrier per tile; then tile j+1 is converted (softplus, dt*u per (channel, t); B, C to
+// fp32, transposed to [t][n]) while tile j is scanned from the previous conversion.
+//
+// Modes: FULL computes y (and the final state of the last chunk); AGG computes only the
+// chunk's end state from h = 0 and the chunk's sum of dt, from which chunk_combine_kernel
+// forms each chunk's incoming state (the recurrence is a composition of affine maps --
+// section 2.2 of the lmnt.cn page, section 3.4 of "Mamba architecture principles and
+// industrial long-text practice", jsqmd.com -- so chunk end states compose exactly).
+#pragma once
+#include "common.cuh"
+#include "scan_seq.cuh"
+
+namespace ssm {
+
+template <typename IO, int KS, int GP, int WARPS, int T>
+struct PairCfg {
+    static constexpr int kThreads = WARPS * 32;
+    static constexpr int kPairsW = 32 / GP;            // pairs per warp
+    static constexpr int kPairs = WARPS * kPairsW;     // pairs per CTA
+    static constexpr int kCh = 2 * kPairs;             // channels per CTA
+    static constexpr int kQN = KS / 4;                 // float4 quads of states per lane
+    static constexpr int kNP = 4 * GP * kQN;           // padded state count
+    static constexpr int kEpr = 16 / (int)sizeof(IO);  // io elements per 16-byte piece
+    static constexpr int kRS = T;                      // raw row stride (io elements)
+    static constexpr int kRawRows = 3 * kCh + 2 * kNP;  // u, delta, z rows, then B, C rows
+    static constexpr size_t kRawBytes = (size_t)kRawRows * kRS * sizeof(IO);
+    static constexpr size_t kDxBytes = (size_t)T * kPairs * sizeof(float4);
+    static constexpr size_t kBcBytes = (size_t)T * 2 * kNP * sizeof(float);
+    static constexpr size_t kYsBytes = (size_t)kCh * kRS * sizeof(IO);   // y tile staging, rows like raw
+    static constexpr size_t kOffDx = 3 * kRawBytes;
+    static constexpr size_t kOffBc = kOffDx + 2 * kDxBytes;
+    static constexpr size_t kOffYs = kOffBc + 2 * kBcBytes;
+    static constexpr size_t kOffBias = kOffYs + 2 * kYsBytes;
+    static constexpr size_t kSmem = kOffBias + (size_t)kCh * sizeof(float);
+    static_assert(KS == 4 || KS == 8, "states per lane per channel: 4 or 8");
+    static_assert(GP == 1 || GP == 2 || GP == 4 || GP == 8 || GP == 16, "lanes per pair");
+    static_assert(T % 8 == 0 && T % GP == 0 && T % kEpr == 0, "tile: whole 16-byte pieces and reduce groups");
+    static_assert((kRS * sizeof(IO)) % 16 == 0 && kRawBytes % 16 == 0, "16-byte aligned raw rows");
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+
+// warps per CTA for a lane split: at most 64 channels per CTA (SSM_PAIR_WARPS for GP >= 4)
+#ifndef SSM_PAIR_WARPS
+#define SSM_PAIR_WARPS 4
+#endif
+constexpr int pair_warps(int gp) { return gp >= 4 ? SSM_PAIR_WARPS : gp; }
+
+template <typename IO, int KS, int GP, int WARPS, int T, bool AGG>
+__global__ void __launch_bounds__(WARPS * 32)
+scan_pair_kernel(const SeqParams p) {
+    using Cfg = PairCfg<IO, KS, GP, WARPS, T>;
+    constexpr int kCh = Cfg::kCh, kPairs = Cfg::kPairs, kQN = Cfg::kQN, kNP = Cfg::kNP, kRS = Cfg::kRS;
+    constexpr int kEpr = Cfg::kEpr, kPieces = T / kEpr;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float4 *sDX0 = reinterpret_cast<float4 *>(smem + Cfg::kOffDx);   // [T][kPairs] (dt0, dt0*u0, dt1, dt1*u1)
+    float *sBC0 = reinterpret_cast<float *>(smem + Cfg::kOffBc);     // [T][2*kNP]  B | C
+    IO *sYS0 = reinterpret_cast<IO *>(smem + Cfg::kOffYs);           // [kCh][kRS]  y tile, io type
+    float *sBias = reinterpret_cast<float *>(smem + Cfg::kOffBias);  // [kCh]
+    auto raw_of = [&](int j) { return reinterpret_cast<IO *>(smem + (size_t)(j % 3) * Cfg::kRawBytes); };
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t b = blockIdx.x / p.chan_blocks;
+    const int64_t d0 = (int64_t)(blockIdx.x % p.chan_blocks) * kCh;
+    const int k = blockIdx.y;
+    const int64_t l_begin = (int64_t)k * p.chunk_len;
+    const int64_t l_end = min(p.L, l_begin + p.chunk_len);
+    const int ntiles = (int)((l_end - l_begin + T - 1) / T);
+    const int N = (int)p.N;
+    const int64_t BD = p.Bt * p.Dm;
+
+    const int pr = warp * Cfg::kPairsW + lane / GP;   // pair within the block
+    const int g = lane % GP;
+    const int c0 = 2 * pr;                             // first channel of the pair (block-relative)
+    const int64_t dch[2] = {d0 + c0, d0 + c0 + 1};
+    const bool cv[2] = {dch[0] < p.Dm, dch[1] < p.Dm};
+
+    // A * log2(e) for the lane's states, as (n, n+1) pairs; zero for padded states
+    float2 Ap[2][kQN][2];
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int q = 0; q < kQN; ++q)
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+                const int n = 4 * (GP * q + g) + 2 * pp;
+                const float a0 = (cv[ch] && n < N) ? p.A[dch[ch] * p.N + n] * kLog2e : 0.0f;
+                const float a1 = (cv[ch] && n + 1 < N) ? p.A[dch[ch] * p.N + n + 1] * kLog2e : 0.0f;
+                Ap[ch][q][pp] = make_float2(a0, a1);
+            }
+    float2 h[2][kQN][2];
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int q = 0; q < kQN; ++q) {
+            h[ch][q][0] = make_float2(0.f, 0.f);
+            h[ch][q][1] = make_float2(0.f, 0.f);
+            if (!AGG && p.hin != nullptr && cv[ch]) {
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    p.hin + ((int64_t)k * BD + b * p.Dm + dch[ch]) * p.npad + 4 * (GP * q + g));
+                h[ch][q][0] = make_float2(v.x, v.y);
+                h[ch][q][1] = make_float2(v.z, v.w);
+            }
+        }
+    const float Dd[2] = {(!AGG && p.D != nullptr && cv[0]) ? p.D[dch[0]] : 0.0f,
+                         (!AGG && p.D != nullptr && cv[1]) ? p.D[dch[1]] : 0.0f};
+
+    const IO *gU = reinterpret_cast<const IO *>(p.u);
+    const IO *gDelta = reinterpret_cast<const IO *>(p.delta);
+    const IO *gZ = reinterpret_cast<const IO *>(p.z);
+    const IO *gB = reinterpret_cast<const IO *>(p.B);
+    const IO *gC = reinterpret_cast<const IO *>(p.C);
+    const bool has_z = !AGG && p.z != nullptr;
+
+    // raw rows: [0,kCh) u, [kCh,2kCh) delta, [2kCh,3kCh) z, then kNP B rows, kNP C rows
+    auto issue_tile = [&](int j) {
+        IO *raw = raw_of(j);
+        const int64_t t0 = l_begin + (int64_t)j * T;
+        const int len = (int)min((int64_t)T, l_end - t0);
+        const int nch_rows = has_z ? 3 * kCh : 2 * kCh;
+        const int nn_rows = AGG ? N : 2 * N;
+        const int total = (nch_rows + nn_rows) * kPieces;
+        for (int i = tid; i < total; i += Cfg::kThreads) {
+            const int row = i / kPieces, e0 = (i % kPieces) * kEpr;
+            const IO *src;
+            IO *dst;
+            bool ok;
+            if (row < nch_rows) {
+                const int kind = row / kCh, cc = row % kCh;
+                const IO *base = kind == 0 ? gU : (kind == 1 ? gDelta : gZ);
+                ok = d0 + cc < p.Dm;
+                src = base + ((b * p.Dm + d0 + cc) * p.L + t0 + e0);
+                dst = raw + (size_t)(kind * kCh + cc) * kRS + e0;
+            } else {
+                const int r = row - nch_rows, kind = r / N, n = r % N;
+                ok = true;
+                src = (kind == 0 ? gB : gC) + ((b * p.N + n) * p.L + t0 + e0);
+                dst = raw + (size_t)(3 * kCh + kind * kNP + n) * kRS + e0;
+            }
+            const int avail = ok ? max(0, min(kEpr, len - e0)) : 0;
+            cp_async16(dst, avail > 0 ? (const void *)src : (const void *)gU, avail * (int)sizeof(IO));
+        }
+        cp_async_commit();
+    };
+
+    // tile j's raw rows -> (dt, dt*u) per (channel, t) and fp32 B, C as [t][n]
+    auto convert = [&](int j) {
+        const IO *raw = raw_of(j);
+        float4 *sDX = sDX0 + (size_t)(j & 1) * T * kPairs;
+        float *sBC = sBC0 + (size_t)(j & 1) * T * 2 * kNP;
+        const int64_t t0 = l_begin + (int64_t)j * T;
+        const int len = (int)min((int64_t)T, l_end - t0);
+        for (int i = tid; i < kCh * kPieces; i += Cfg::kThreads) {
+            const int cc = i % kCh, tq = (i / kCh) * kEpr;
+            float uu[kEpr], dl[kEpr];
+            unpack16(*reinterpret_cast<const uint4 *>(raw + (size_t)cc * kRS + tq), uu, IO(0.0f));
+            unpack16(*reinterpret_cast<const uint4 *>(raw + (size_t)(kCh + cc) * kRS + tq), dl, IO(0.0f));
+            const bool ok = d0 + cc < p.Dm;
+            const float bb = sBias[cc];
+            float2 *dst = reinterpret_cast<float2 *>(sDX) + (size_t)tq * kPairs * 2 + cc;
+#pragma unroll
+            for (int e = 0; e < kEpr; ++e) {
+                float dt = 0.0f, x = 0.0f;
+                if (ok && tq + e < len) {
+                    dt = dl[e] + bb;
+                    if (p.softplus) dt = softplus_f(dt);
+                    x = dt * uu[e];
+                }
+                dst[(size_t)e * kPairs * 2] = make_float2(dt, x);
+            }
+        }
+        const int nkind = AGG ? 1 : 2;
+        for (int i = tid; i < nkind * kNP * kPieces; i += Cfg::kThreads) {
+            const int n = i % kNP, r = i / kNP, kind = r % nkind, tq = (r / nkind) * kEpr;
+            float v[kEpr];
+            if (n < N) {
+                unpack16(*reinterpret_cast<const uint4 *>(raw + (size_t)(3 * kCh + kind * kNP + n) * kRS + tq), v, IO(0.0f));
+            } else {
+#pragma unroll
+                for (int e = 0; e < kEpr; ++e) v[e] = 0.0f;
+            }
+            float *dst = sBC + (size_t)tq * 2 * kNP + kind * kNP + n;
+#pragma unroll
+            for (int e = 0; e < kEpr; ++e) dst[(size_t)e * 2 * kNP] = v[e];
+        }
+    };
+
+    float dsum[2] = {0.f, 0.f}, dsum_c[2] = {0.f, 0.f};   // compensated sums of dt (AGG)
+    IO *gY = reinterpret_cast<IO *>(p.y);
+
+    // coalesced store of tile j's staged y rows (16-byte pieces; element-wise on a ragged tail)
+    auto store_y = [&](int j) {
+        const IO *ys = sYS0 + (size_t)(j & 1) * kCh * kRS;
+        const int64_t t0 = l_begin + (int64_t)j * T;
+        const int len = (int)min((int64_t)T, l_end - t0);
+        for (int i = tid; i < kCh * kPieces; i += Cfg::kThreads) {
+            const int cc = i / kPieces, e0 = (i % kPieces) * kEpr;
+            if (d0 + cc >= p.Dm || e0 >= len) continue;
+            IO *dst = gY + (b * p.Dm + d0 + cc) * p.L + t0 + e0;
+            const IO *src = ys + (size_t)cc * kRS + e0;
+            if (e0 + kEpr <= len) {
+                *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+            } else {
+                for (int e = 0; e < len - e0; ++e) dst[e] = src[e];
+            }
+        }
+    };
+
+    for (int i = tid; i < kCh; i += Cfg::kThreads)
+        sBias[i] = (p.bias != nullptr && d0 + i < p.Dm) ? p.bias[d0 + i] : 0.0f;
+    if (ntiles > 0) {
+        issue_tile(0);
+        cp_async_wait<0>();
+        __syncthreads();
+        convert(0);
+        if (ntiles > 1) issue_tile(1);
+    }
+    for (int j = 0; j < ntiles; ++j) {
+        cp_async_wait<0>();   // tile j+1's raw rows (issued one tile ago)
+        __syncthreads();      // conversion of tile j done; scan of tile j-1 done everywhere
+        if (j + 2 < ntiles) issue_tile(j + 2);
+        if (!AGG && j > 0) store_y(j - 1);
+        if (j + 1 < ntiles) convert(j + 1);
+
+        const float4 *sDX = sDX0 + (size_t)(j & 1) * T * kPairs;
+        const float *sBC = sBC0 + (size_t)(j & 1) * T * 2 * kNP;
+        const IO *raw = raw_of(j);
+        IO *ys = sYS0 + (size_t)(j & 1) * kCh * kRS;
+        float tsum[2] = {0.f, 0.f};
+#pragma unroll 1
+        for (int tb = 0; tb < T; tb += GP) {
+            float yp[2][GP];
+#pragma unroll
+            for (int s = 0; s < GP; ++s) {
+                const int t = tb + s;
+                const float4 dx = sDX[(size_t)t * kPairs + pr];
+                const float2 dd[2] = {make_float2(dx.x, dx.x), make_float2(dx.z, dx.z)};
+                const float2 xx[2] = {make_float2(dx.y, dx.y), make_float2(dx.w, dx.w)};
+                if (AGG) { tsum[0] += dx.x; tsum[1] += dx.z; }
+                float2 ya[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int q = 0; q < kQN; ++q) {
+                    const float4 bq = *reinterpret_cast<const float4 *>(sBC + (size_t)t * 2 * kNP + 4 * (GP * q + g));
+                    float4 cq = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (!AGG) cq = *reinterpret_cast<const float4 *>(sBC + (size_t)t * 2 * kNP + kNP + 4 * (GP * q + g));
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const float2 e0 = __fmul2_rn(dd[ch], Ap[ch][q][0]);
+                        const float2 e1 = __fmul2_rn(dd[ch], Ap[ch][q][1]);
+                        const float2 a0 = make_float2(ex2(e0.x), ex2(e0.y));
+                        const float2 a1 = make_float2(ex2(e1.x), ex2(e1.y));
+                        const float2 w0 = __fmul2_rn(xx[ch], make_float2(bq.x, bq.y));
+                        const float2 w1 = __fmul2_rn(xx[ch], make_float2(bq.z, bq.w));
+                        h[ch][q][0] = __ffma2_rn(a0, h[ch][q][0], w0);
+                        h[ch][q][1] = __ffma2_rn(a1, h[ch][q][1], w1);
+                        if (!AGG) {
+                            ya[ch] = __ffma2_rn(make_float2(cq.x, cq.y), h[ch][q][0], ya[ch]);
+                            ya[ch] = __ffma2_rn(make_float2(cq.z, cq.w), h[ch][q][1], ya[ch]);
+                        }
+                    }
+                }
+                if (!AGG) {
+                    yp[0][s] = ya[0].x + ya[0].y;
+                    yp[1][s] = ya[1].x + ya[1].y;
+                }
+            }
+            if (!AGG) {
+                // the timestep this lane finished, for both channels; staged for a coalesced
+                // store after the next barrier (rows past the last channel are never stored)
+                const int t = tb + g;
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    const float ysum = group_reduce_transpose<GP>(yp[ch], lane);
+                    const int cc = c0 + ch;
+                    float yv = fmaf(Dd[ch], io_traits<IO>::to_f(raw[(size_t)cc * kRS + t]), ysum);
+                    if (has_z) yv *= silu_f(io_traits<IO>::to_f(raw[(size_t)(2 * kCh + cc) * kRS + t]));
+                    store_io(ys + (size_t)cc * kRS + t, yv);
+                }
+            }
+        }
+        if (AGG) {
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                const float yk = tsum[ch] - dsum_c[ch];
+                const float tk = dsum[ch] + yk;
+                dsum_c[ch] = (tk - dsum[ch]) - yk;
+                dsum[ch] = tk;
+            }
+        }
+    }
+    cp_async_wait<0>();
+    if (!AGG && ntiles > 0) {
+        __syncthreads();
+        store_y(ntiles - 1);
+    }
+
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        if (!cv[ch]) continue;
+        const int64_t bd = b * p.Dm + dch[ch];
+        if (AGG) {
+            float *dst = p.agg_h + ((int64_t)k * BD + bd) * p.npad;
+#pragma unroll
+            for (int q = 0; q < kQN; ++q)
+                *reinterpret_cast<float4 *>(dst + 4 * (GP * q + g)) =
+                    make_float4(h[ch][q][0].x, h[ch][q][0].y, h[ch][q][1].x, h[ch][q][1].y);
+            if (g == 0) p.agg_s[(int64_t)k * BD + bd] = dsum[ch];
+        } else if (p.last_state != nullptr && k == p.nchunks - 1) {
+            float *dst = p.last_state + bd * p.N;
+#pragma unroll
+            for (int q = 0; q < kQN; ++q) {
+                const float v[4] = {h[ch][q][0].x, h[ch][q][0].y, h[ch][q][1].x, h[ch][q][1].y};
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int n = 4 * (GP * q + g) + jj;
+                    if (n < N) dst[n] = v[jj];
+                }
+            }
+        }
+    }
+}
+
+}  // namespace ssm

@@ -19,6 +19,7 @@
 #include "scan_seq.cuh"
 #include "scan_tc.cuh"
 #include "scan_tp.cuh"
+#include "scan_pair.cuh"
 
 namespace {
 
@@ -363,6 +364,166 @@ ssm_status_t scan_checks(const ssm_dims_t *dims, const void *u, const void *delt
     return SSM_OK;
 }
 
+// ---- channel-pair sequential path (default for 16-byte aligned rows) ----------------------
+#ifndef SSM_PAIR_T
+#define SSM_PAIR_T 16
+#endif
+constexpr int kPairT = SSM_PAIR_T;   // timesteps per tile of the channel-pair kernel
+
+struct PairPlan {
+    bool use = false;
+    int ks = 8, gp = 8;          // states per lane per channel, lanes per channel pair
+    int nchunks = 1;
+    int64_t chunk_len = 0;
+    int chan_blocks = 0;
+    int np = 0;                  // padded states = ks * gp
+    size_t smem = 0;
+};
+
+// smallest power-of-two lane count gp with gp * ks >= N states
+int pair_gp(int64_t N, int ks) {
+    int gp = 1;
+    while ((int64_t)gp * ks < N) gp *= 2;
+    return gp;
+}
+
+template <typename IO, int KS, int GP, bool AGG>
+cudaError_t launch_pair_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
+    using Cfg = PairCfg<IO, KS, GP, pair_warps(GP), kPairT>;
+    auto k = scan_pair_kernel<IO, KS, GP, pair_warps(GP), kPairT, AGG>;
+    static unsigned long long attr_set = 0;  // per instantiation: bit i = set on device i
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set |= 1ull << dev;
+    }
+    dim3 grid((unsigned)(prm.Bt * prm.chan_blocks), (unsigned)grid_y);
+    k<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(prm);
+    return cudaGetLastError();
+}
+
+template <typename IO, int KS, int GP>
+cudaError_t launch_pair_g(const SeqParams &prm, bool agg, int grid_y, cudaStream_t s) {
+    return agg ? launch_pair_t<IO, KS, GP, true>(prm, grid_y, s) : launch_pair_t<IO, KS, GP, false>(prm, grid_y, s);
+}
+
+#define SSM_PAIR_CASES(X) X(4, 1) X(4, 2) X(4, 4) X(8, 1) X(8, 2) X(8, 4) X(8, 8) X(8, 16)
+
+template <typename IO>
+cudaError_t launch_pair(const PairPlan &pl, const SeqParams &prm, bool agg, int grid_y, cudaStream_t s) {
+    switch (pl.ks * 100 + pl.gp) {
+#define SSM_PAIR_LAUNCH(KS, GP) case KS * 100 + GP: return launch_pair_g<IO, KS, GP>(prm, agg, grid_y, s);
+        SSM_PAIR_CASES(SSM_PAIR_LAUNCH)
+#undef SSM_PAIR_LAUNCH
+        default: return cudaErrorInvalidConfiguration;
+    }
+}
+
+size_t pair_smem(ssm_dtype_t io, int ks, int gp) {
+    switch (ks * 100 + gp) {
+#define SSM_PAIR_SMEM(KS, GP) \
+    case KS * 100 + GP: \
+        return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(GP), kPairT>::kSmem \
+                              : PairCfg<float, KS, GP, pair_warps(GP), kPairT>::kSmem;
+        SSM_PAIR_CASES(SSM_PAIR_SMEM)
+#undef SSM_PAIR_SMEM
+        default: return 0;
+    }
+}
+
+PairPlan plan_pair(const ssm_dims_t &d) {
+    PairPlan p;
+    if (env_is("SSM_KERNEL", "seq") || env_is("SSM_KERNEL", "tc") || env_is("SSM_KERNEL", "tp")) return p;
+    const size_t esz = io_size(d.io_dtype);
+    if (((size_t)d.seqlen * esz) % 16 != 0 || d.dstate > 128) return p;   // rows move in 16-byte pieces
+    const int64_t N = d.dstate, BD = d.batch * d.dim, sms = sm_count();
+    // eight states per lane and channel, unless four give the GPU at least one warp per SM
+    // sub-partition where eight do not (few channels with few states)
+    p.ks = 8;
+    p.gp = pair_gp(N, 8);
+    if (N <= 16 && (BD * p.gp + 63) / 64 < 4 * sms) { p.ks = 4; p.gp = pair_gp(N, 4); }
+    p.np = p.ks * p.gp;
+    p.smem = pair_smem(d.io_dtype, p.ks, p.gp);
+    if (p.smem == 0) return p;
+    const int64_t warps = pair_warps(p.gp), kch = warps * 64 / p.gp;
+    p.chan_blocks = (int)((d.dim + kch - 1) / kch);
+    // CTAs resident per SM (228 KB of shared memory with 1 KB reserved per CTA, 2048 threads).
+    // The sequence is cut into chunks (aggregate pass + combine + full pass, about 1.7x the
+    // work) only when the channels alone give fewer than half a warp per SM sub-partition;
+    // the chunk count then fills one wave of resident CTAs.
+    const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>((228 * 1024) / (int64_t)(p.smem + 1024),
+                                                                    2048 / (warps * 32)));
+    const int64_t slots = sms * per_sm, base = d.batch * p.chan_blocks;
+    int64_t nc = 1;
+    if (base * warps < 2 * sms) nc = std::max<int64_t>(1, slots / base);
+    if (const char *env = std::getenv("SSM_PAIR_CHUNKS")) nc = std::max(1, std::atoi(env));   // experiments
+    nc = std::min<int64_t>(nc, std::max<int64_t>(1, d.seqlen / (4 * kPairT)));
+    nc = std::min<int64_t>(nc, 4096);
+    int64_t cl = (d.seqlen + nc - 1) / nc;
+    cl = (cl + kPairT - 1) / kPairT * kPairT;
+    p.chunk_len = std::max<int64_t>(cl, kPairT);
+    p.nchunks = (int)((d.seqlen + p.chunk_len - 1) / p.chunk_len);
+    p.use = true;
+    return p;
+}
+
+size_t pair_workspace_bytes(const ssm_dims_t &d, const PairPlan &p) {
+    if (!p.use || p.nchunks <= 1) return 0;
+    const size_t BD = (size_t)(d.batch * d.dim);
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t agg_h = (size_t)p.nchunks * BD * p.np * 4, agg_s = (size_t)p.nchunks * BD * 4;
+    return up(agg_h) + up(agg_s) + up(agg_h);
+}
+
+ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *u, const void *delta, const float *A,
+                           const void *B, const void *C, const float *D, const void *z, const float *delta_bias,
+                           int delta_softplus, void *y, float *last_state, void *workspace, size_t ws_bytes,
+                           bool own_ws, cudaStream_t s) {
+    const size_t need = pair_workspace_bytes(d, pl);
+    bool allocated = false;
+    if (need > 0) {
+        if (workspace == nullptr || ws_bytes < need) {
+            if (!own_ws) return SSM_ERR_WORKSPACE;
+            if (cudaMallocAsync(&workspace, need, s) != cudaSuccess) return SSM_ERR_CUDA;
+            allocated = true;
+        } else if (!aligned16(workspace)) {
+            return SSM_ERR_ALIGN;
+        }
+    }
+    SeqParams prm{};
+    prm.u = u; prm.delta = delta; prm.z = z; prm.B = B; prm.C = C;
+    prm.A = A; prm.D = D; prm.bias = delta_bias; prm.y = y; prm.last_state = last_state;
+    prm.Bt = d.batch; prm.Dm = d.dim; prm.L = d.seqlen; prm.N = d.dstate;
+    prm.softplus = delta_softplus ? 1 : 0;
+    prm.chunk_len = pl.chunk_len; prm.nchunks = pl.nchunks;
+    prm.chan_blocks = pl.chan_blocks;
+    prm.npad = pl.np;
+    cudaError_t e = cudaSuccess;
+    const bool bf = d.io_dtype == SSM_BF16;
+    if (pl.nchunks > 1) {
+        const size_t BD = (size_t)(d.batch * d.dim), np = (size_t)pl.np;
+        auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+        char *w = static_cast<char *>(workspace);
+        prm.agg_h = reinterpret_cast<float *>(w);
+        prm.agg_s = reinterpret_cast<float *>(w + up((size_t)pl.nchunks * BD * np * 4));
+        float *hin = reinterpret_cast<float *>(w + up((size_t)pl.nchunks * BD * np * 4) + up((size_t)pl.nchunks * BD * 4));
+        e = bf ? launch_pair<bf16>(pl, prm, true, pl.nchunks - 1, s) : launch_pair<float>(pl, prm, true, pl.nchunks - 1, s);
+        if (e == cudaSuccess) {
+            const int64_t total = (int64_t)BD * pl.np;
+            chunk_combine_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+                A, prm.agg_h, prm.agg_s, hin, (int64_t)BD, d.dim, d.dstate, pl.np, pl.nchunks);
+            e = cudaGetLastError();
+        }
+        prm.hin = hin;
+    }
+    if (e == cudaSuccess)
+        e = bf ? launch_pair<bf16>(pl, prm, false, pl.nchunks, s) : launch_pair<float>(pl, prm, false, pl.nchunks, s);
+    if (allocated) cudaFreeAsync(workspace, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, const float *A,
                       const void *B, const void *C, const float *D, const void *z,
                       const float *delta_bias, int delta_softplus, void *y, float *last_state,
@@ -377,6 +538,10 @@ ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, 
         }
         return SSM_OK;
     }
+    const PairPlan pp = plan_pair(d);
+    if (pp.use)
+        return run_scan_pair(d, pp, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
+                             ws_bytes, own_ws, s);
     const TcPlan tp = plan_tc(d);
     if (tp.use) {
         char *w = static_cast<char *>(workspace);
@@ -492,6 +657,8 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_dims_t *dims, const void *u, const
 size_t ssm_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
+    const PairPlan pp = plan_pair(*dims);
+    if (pp.use) return pair_workspace_bytes(*dims, pp);
     const TcPlan tp = plan_tc(*dims);
     if (tp.use) return tp.bytes;
     return seq_workspace_bytes(*dims, plan_scan(*dims));

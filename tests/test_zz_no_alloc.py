@@ -36,8 +36,16 @@ def test_scratch_size_matches_header():
     assert val == ssm.SCRATCH_MAX_BYTES == 16 * 1024 * 1024
 
 
-def test_oversize_shape_rejected_on_host(lib):
-    # 1 x 1536 x 131072 x 64 needs ~65 MiB of scratch: refused with SSM_ERR_WORKSPACE
+@pytest.fixture
+def time_split_plan(monkeypatch):
+    """The persistent time-split kernel keeps fp32 B/C for the whole sequence in its workspace:
+    a plan whose scratch exceeds the fixed size (the default plans stay within a few MiB)."""
+    monkeypatch.setenv("SSM_KERNEL", "tc")
+    yield
+
+
+def test_oversize_shape_rejected_on_host(lib, time_split_plan):
+    # 1 x 1536 x 131072 x 64 on the time-split plan needs ~65 MiB of scratch: SSM_ERR_WORKSPACE
     d = ssm.dims(1, 1536, 131072, 64, ssm.SSM_BF16)
     assert ssm.workspace_bytes(1, 1536, 131072, 64) > ssm.SCRATCH_MAX_BYTES
     rc = lib.ssm_selective_scan_fwd_noalloc(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
@@ -122,7 +130,7 @@ def test_noalloc_back_to_back_different_shapes(lib):
 
 
 @pytest.mark.gpu
-def test_noalloc_oversize_raises_clear_error(lib):
+def test_noalloc_oversize_raises_clear_error(lib, time_split_plan):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     L, N, Dm = 131072, 64, 1536
