@@ -65,6 +65,26 @@ struct PairCfg {
 #endif
 constexpr int pair_warps(int gp) { return gp >= 4 ? SSM_PAIR_WARPS : gp; }
 
+// S (4 or 8) consecutive io elements from shared memory as floats; the source is aligned to
+// S elements (8 or 16 bytes for bf16, 16 or 32 for fp32)
+template <int S>
+__device__ __forceinline__ void load_steps(const __nv_bfloat16 *src, float (&out)[S]) {
+    if constexpr (S == 8) {
+        unpack16(*reinterpret_cast<const uint4 *>(src), out, __nv_bfloat16(0.0f));
+    } else {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        out[0] = bf16lo(v.x); out[1] = bf16hi(v.x); out[2] = bf16lo(v.y); out[3] = bf16hi(v.y);
+    }
+}
+template <int S>
+__device__ __forceinline__ void load_steps(const float *src, float (&out)[S]) {
+#pragma unroll
+    for (int q = 0; q < S / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4 *>(src + 4 * q);
+        out[4 * q] = v.x; out[4 * q + 1] = v.y; out[4 * q + 2] = v.z; out[4 * q + 3] = v.w;
+    }
+}
+
 template <typename IO, int KS, int GP, int WARPS, int T, bool AGG>
 __global__ void __launch_bounds__(WARPS * 32)
 scan_pair_kernel(const SeqParams p) {
@@ -169,16 +189,18 @@ scan_pair_kernel(const SeqParams p) {
         float *sBC = sBC0 + (size_t)(j & 1) * T * 2 * kNP;
         const int64_t t0 = l_begin + (int64_t)j * T;
         const int len = (int)min((int64_t)T, l_end - t0);
-        for (int i = tid; i < kCh * kPieces; i += Cfg::kThreads) {
-            const int cc = i % kCh, tq = (i / kCh) * kEpr;
-            float uu[kEpr], dl[kEpr];
-            unpack16(*reinterpret_cast<const uint4 *>(raw + (size_t)cc * kRS + tq), uu, IO(0.0f));
-            unpack16(*reinterpret_cast<const uint4 *>(raw + (size_t)(kCh + cc) * kRS + tq), dl, IO(0.0f));
+        // eight timesteps per item, or four when eight would leave threads without work
+        constexpr int kSI = (kCh * (T / 8) >= Cfg::kThreads) ? 8 : 4;
+        for (int i = tid; i < kCh * (T / kSI); i += Cfg::kThreads) {
+            const int cc = i % kCh, tq = (i / kCh) * kSI;
+            float uu[kSI], dl[kSI];
+            load_steps<kSI>(raw + (size_t)cc * kRS + tq, uu);
+            load_steps<kSI>(raw + (size_t)(kCh + cc) * kRS + tq, dl);
             const bool ok = d0 + cc < p.Dm;
             const float bb = sBias[cc];
             float2 *dst = reinterpret_cast<float2 *>(sDX) + (size_t)tq * kPairs * 2 + cc;
 #pragma unroll
-            for (int e = 0; e < kEpr; ++e) {
+            for (int e = 0; e < kSI; ++e) {
                 float dt = 0.0f, x = 0.0f;
                 if (ok && tq + e < len) {
                     dt = dl[e] + bb;

@@ -444,20 +444,23 @@ PairPlan plan_pair(const ssm_dims_t &d) {
     p.ks = 8;
     p.gp = pair_gp(N, 8);
     if (N <= 16 && (BD * p.gp + 63) / 64 < 4 * sms) { p.ks = 4; p.gp = pair_gp(N, 4); }
+    if (env_is("SSM_PAIR_KS", "4") && N <= 16) { p.ks = 4; p.gp = pair_gp(N, 4); }   // experiments, tests
+    if (env_is("SSM_PAIR_KS", "8")) { p.ks = 8; p.gp = pair_gp(N, 8); }
     p.np = p.ks * p.gp;
     p.smem = pair_smem(d.io_dtype, p.ks, p.gp);
     if (p.smem == 0) return p;
     const int64_t warps = pair_warps(p.gp), kch = warps * 64 / p.gp;
     p.chan_blocks = (int)((d.dim + kch - 1) / kch);
     // CTAs resident per SM (228 KB of shared memory with 1 KB reserved per CTA, 2048 threads).
-    // The sequence is cut into chunks (aggregate pass + combine + full pass, about 1.7x the
-    // work) only when the channels alone give fewer than half a warp per SM sub-partition;
-    // the chunk count then fills one wave of resident CTAs.
+    // The sequence is cut into chunks (aggregate pass + combine + full pass, up to 1.7x the
+    // work) when the channels alone give fewer than two warps per SM sub-partition: the
+    // latency-bound recurrence gains more from the extra warps than the aggregate pass costs
+    // (measured on B300). The chunk count then fills one wave of resident CTAs.
     const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>((228 * 1024) / (int64_t)(p.smem + 1024),
                                                                     2048 / (warps * 32)));
     const int64_t slots = sms * per_sm, base = d.batch * p.chan_blocks;
     int64_t nc = 1;
-    if (base * warps < 2 * sms) nc = std::max<int64_t>(1, slots / base);
+    if (base * warps < 8 * sms) nc = std::max<int64_t>(1, slots / base);
     if (const char *env = std::getenv("SSM_PAIR_CHUNKS")) nc = std::max(1, std::atoi(env));   // experiments
     nc = std::min<int64_t>(nc, std::max<int64_t>(1, d.seqlen / (4 * kPairT)));
     nc = std::min<int64_t>(nc, 4096);

@@ -83,10 +83,11 @@ def test_state_update_argument_errors(lib):
 
 
 def test_workspace_query(lib):
-    # a long sequence over few channels is cut into chunks whose carries pass through the
-    # workspace; a wide batch fills the GPU with channels alone and needs none
+    # a sequence over too few channels to give every SM sub-partition two warps is cut into
+    # chunks whose carries pass through the workspace; a batch wide enough needs none
     assert ssm.workspace_bytes(1, 1536, 131072, 64) > 0
-    assert ssm.workspace_bytes(8, 1536, 2048, 16) == 0
+    assert ssm.workspace_bytes(8, 1536, 2048, 16) > 0
+    assert ssm.workspace_bytes(16, 2048, 2048, 16) == 0
     assert ssm.workspace_bytes(8, 1536, 2047, 16) == 0
     assert ssm.workspace_bytes(0, 1536, 2048, 16) == 0
     assert lib.ssm_selective_scan_workspace_bytes(None) == 0

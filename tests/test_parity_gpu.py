@@ -74,6 +74,33 @@ def test_shapes(Bt, D, L, N, io, gate, dskip, bias, sp):
     compare_scan(inp, y, h)
 
 
+# ---- the channel-pair kernel: every lane split, ragged tails, partial channel blocks ------
+PAIR_CASES = [
+    # Bt, D, L, N, io, gate, dskip, states per lane (KS), chunks (0 = planner's choice)
+    (1, 3, 200, 4, "f32", False, "ones", "4", 0),        # KS 4, one lane per pair
+    (2, 70, 520, 8, "bf16", True, "normal", "4", 0),     # KS 4, two lanes per pair
+    (1, 100, 1000, 16, "bf16", False, "ones", "4", 3),   # KS 4, four lanes per pair
+    (2, 67, 136, 7, "f32", True, None, "8", 0),          # KS 8, one lane per pair
+    (3, 45, 1000, 16, "bf16", True, "ones", "8", 2),     # KS 8, two lanes per pair
+    (1, 50, 776, 24, "bf16", True, "normal", "8", 0),    # KS 8, four lanes per pair
+    (1, 40, 2000, 64, "bf16", False, "ones", "8", 5),    # KS 8, eight lanes per pair
+    (3, 9, 136, 50, "f32", True, "normal", "8", 0),      # KS 8, eight lanes, padded states
+    (1, 20, 520, 100, "bf16", True, "ones", "8", 4),     # KS 8, sixteen lanes per pair
+    (2, 33, 40, 128, "f32", False, "normal", "8", 1),    # KS 8, sixteen lanes, a short ragged tile
+]
+
+
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,ks,chunks", PAIR_CASES)
+def test_pair_kernel_shapes(Bt, D, L, N, io, gate, dskip, ks, chunks, monkeypatch):
+    monkeypatch.setenv("SSM_PAIR_KS", ks)
+    if chunks:
+        monkeypatch.setenv("SSM_PAIR_CHUNKS", str(chunks))
+    cfg = gen.ScanConfig("pair", Bt, D, L, N, io=io, gate=gate, dskip=dskip, seed=Bt * 1000 + L + N)
+    inp = gen.scan_inputs(cfg)
+    y, h = gpu_scan(inp)
+    compare_scan(inp, y, h)
+
+
 @pytest.mark.parametrize("plan", ["16,4,5", "16,4,1", "4,4,3", "16,8,2", "8,1,7"])
 def test_forced_plans(plan, monkeypatch):
     N = {"16,4,5": 64, "16,4,1": 64, "4,4,3": 16, "16,8,2": 128, "8,1,7": 8}[plan]
