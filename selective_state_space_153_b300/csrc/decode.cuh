@@ -11,6 +11,16 @@
 
 namespace ssm {
 
+// four consecutive io elements (8-byte aligned for bf16, 16 for fp32) as floats
+__device__ __forceinline__ void load_io4(const __nv_bfloat16 *src, float *out) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(src));
+    out[0] = bf16lo(v.x); out[1] = bf16hi(v.x); out[2] = bf16lo(v.y); out[3] = bf16hi(v.y);
+}
+__device__ __forceinline__ void load_io4(const float *src, float *out) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+    out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+}
+
 struct DecodeParams {
     float *state;
     const void *x, *dt, *B, *C, *z;
@@ -18,6 +28,48 @@ struct DecodeParams {
     void *y;
     int64_t Bt, Dm, N;
 };
+
+// Vector path: lane l of a warp owns the 16-byte piece q = l % LPC of channel
+// d = warp*(32/LPC) + l/LPC of batch row b = blockIdx.y (LPC = N/4 lanes per channel), so
+// every warp-wide load or store covers 512 contiguous bytes of the state and the index
+// arithmetic is shifts (no 64-bit division). B and C of the row are read as 4-element
+// vectors (the caller checks their alignment); the y partials are summed across the LPC
+// lanes of a channel.
+template <typename IO, int LPC>
+__global__ void __launch_bounds__(256) decode_wide_kernel(const DecodeParams p) {
+    const int b = blockIdx.y;
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const int q = t % LPC;
+    const int d = t / LPC;
+    const bool valid = d < p.Dm;
+    float acc = 0.0f, xv = 0.0f, zv = 0.0f;
+    if (valid) {
+        const int64_t cl = (int64_t)b * p.Dm + d;
+        float4 *sp = reinterpret_cast<float4 *>(p.state + cl * p.N) + q;
+        float4 v = __ldcs(sp);
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p.A + (int64_t)d * p.N) + q);
+        xv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.x)[cl]);
+        const float dt = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.dt)[cl]);
+        if (p.z != nullptr) zv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.z)[cl]);
+        float bv[4], cv[4];
+        load_io4(reinterpret_cast<const IO *>(p.B) + (int64_t)b * p.N + 4 * q, bv);
+        load_io4(reinterpret_cast<const IO *>(p.C) + (int64_t)b * p.N + 4 * q, cv);
+        const float dx = dt * xv, dl = dt * kLog2e;
+        v.x = fmaf(ex2(dl * a.x), v.x, dx * bv[0]);
+        v.y = fmaf(ex2(dl * a.y), v.y, dx * bv[1]);
+        v.z = fmaf(ex2(dl * a.z), v.z, dx * bv[2]);
+        v.w = fmaf(ex2(dl * a.w), v.w, dx * bv[3]);
+        __stcs(sp, v);
+        acc = fmaf(cv[0], v.x, fmaf(cv[1], v.y, fmaf(cv[2], v.z, cv[3] * v.w)));
+    }
+#pragma unroll
+    for (int o = LPC / 2; o >= 1; o /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (valid && q == 0) {
+        float yv = acc + (p.D != nullptr ? p.D[d] * xv : 0.0f);
+        if (p.z != nullptr) yv *= silu_f(zv);
+        store_io(reinterpret_cast<IO *>(p.y) + (int64_t)b * p.Dm + d, yv);
+    }
+}
 
 template <typename IO, int LPC>  // LPC: lanes per channel = N/4
 __global__ void __launch_bounds__(256) decode_vec_kernel(const DecodeParams p) {

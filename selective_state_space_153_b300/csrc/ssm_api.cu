@@ -719,7 +719,17 @@ ssm_status_t ssm_state_update(const ssm_dims_t *dims, float *state, const void *
     const int64_t N = dims->dstate, chans = dims->batch * dims->dim;
     const bool bf = dims->io_dtype == SSM_BF16;
     const int lpc = (int)(N / 4);
-    if (N % 4 == 0 && lpc >= 1 && lpc <= 32 && (32 % lpc) == 0) {
+    // batch rows on grid.y and 16-byte B/C reads when B and C rows are 4-element aligned;
+    // the row's channels must fit a 32-bit thread index and grid.y (65535 rows)
+    const bool wide = aligned_to(B, 4 * esz) && aligned_to(C, 4 * esz) && dims->batch <= 65535 &&
+                      dims->dim * lpc < (int64_t)1 << 30 && !env_is("SSM_DEC_OLD", "1");
+    if (wide && N % 4 == 0 && lpc >= 1 && lpc <= 32 && (32 % lpc) == 0) {
+        const dim3 grid((unsigned)((dims->dim * lpc + 255) / 256), (unsigned)dims->batch);
+#define SSM_DECW(L) \
+    case L: bf ? decode_wide_kernel<bf16, L><<<grid, 256, 0, s>>>(p) : decode_wide_kernel<float, L><<<grid, 256, 0, s>>>(p); break;
+        switch (lpc) { SSM_DECW(1) SSM_DECW(2) SSM_DECW(4) SSM_DECW(8) SSM_DECW(16) SSM_DECW(32) default: return SSM_ERR_UNSUPPORTED; }
+#undef SSM_DECW
+    } else if (N % 4 == 0 && lpc >= 1 && lpc <= 32 && (32 % lpc) == 0) {
         const int64_t threads = chans * lpc;
         const unsigned grid = (unsigned)((threads + 255) / 256);
 #define SSM_DEC(L) \

@@ -227,6 +227,30 @@ def test_decode_shapes(N, gate, dskip, io):
     assert oracle.rel_err(st.cpu().numpy(), so, sm) <= tol
 
 
+@pytest.mark.parametrize("N", [16, 64])
+def test_decode_unaligned_bc_rows(N):
+    """B and C rows at an odd element offset (allowed: per-token vectors need only element
+    alignment) take the path that reads them element by element; results match the oracle."""
+    inp = gen.decode_inputs(gen.DECODE, Bt=3, D=50, N=N, gate=True, dskip="ones", steps=5)
+    g = to_dev(inp)
+    st = g["state0"].clone()
+    ys = []
+    for s in range(5):
+        bc = []
+        for k in ("B", "C"):
+            big = torch.empty(g[k][s].numel() + 1, dtype=g[k].dtype, device="cuda")
+            view = big[1:].view_as(g[k][s])
+            view.copy_(g[k][s])
+            bc.append(view)
+        assert bc[0].data_ptr() % 8 != 0
+        ys.append(ssm.state_update(st, g["x"][s], g["dt"][s], g["A"], bc[0], bc[1], D=g["D"], z=g["z"][s]))
+    torch.cuda.synchronize()
+    y = torch.stack(ys, -1)
+    yo, so, ym, sm = _decode_oracle(inp, [0, 1, 2], 5)
+    assert oracle.rel_err(y.float().cpu().numpy(), yo, ym) <= TOL["bf16"]
+    assert oracle.rel_err(st.cpu().numpy(), so, sm) <= TOL["bf16"]
+
+
 def test_scan_then_decode_equals_longer_scan():
     """A scan of L steps then k recurrent steps from its final state equals the oracle's
     scan of L+k steps (softplus folded: the decode step takes the final dt)."""
