@@ -36,9 +36,11 @@ SM_COUNT = 148
 EX2_PER_CLK_SM = 32          # measured on B300: MUFU ex2.approx.f32 issue rate per SM per clock
 FALLBACK_HBM_GBS = 6400.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum of the dominant scan kernel per launch from the
-# ncu capture summarised in profiles/ (None until a capture of the current kernel exists).
-TRAFFIC_BYTES_PER_LAUNCH = None
+# dram__bytes_read.sum + dram__bytes_write.sum per scan call of the long-sequence workload
+# (aggregate pass + combine + full pass), from the ncu capture of the same kernels on the
+# 1/8-length case scaled by 8 (traffic grows with L): profiles/scan_pair_long16k_full.md.
+# Valid for the default workload only; None elsewhere.
+TRAFFIC_BYTES_PER_LAUNCH = {"long128k": 8 * (96.36 + 3.08 + 4.80 + 112.57 + 22.51) * 1e6}
 
 
 def count_kernel_launches(fn):
@@ -57,6 +59,12 @@ def count_kernel_launches(fn):
         return None, []
 
 
+def workload_config(args):
+    from dataclasses import replace
+    cfg = gen.SCAN_CONFIGS[args.workload]
+    return replace(cfg, L=args.seqlen) if args.seqlen > 0 else cfg
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -64,6 +72,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long128k", choices=list(gen.SCAN_CONFIGS))
+    ap.add_argument("--seqlen", type=int, default=0,
+                    help="override the workload's sequence length (profiling of a smaller case)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -212,7 +222,7 @@ def bench_ours(args, rank, ws, local):
     from selective_state_space_153_b300 import ssm
     ssm.load()
     dev = torch.device("cuda", torch.cuda.current_device())
-    cfg = gen.SCAN_CONFIGS[args.workload]
+    cfg = workload_config(args)
     inp = gen.scan_inputs(cfg)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     y = torch.empty_like(g["u"])
@@ -256,8 +266,8 @@ def bench_ours(args, rank, ws, local):
     achieved = elems / t_step / 1e9
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     launches_per_step, kernel_names = count_kernel_launches(step)
-    if launches_per_step is None:   # profiler unavailable: the planner's count for this shape
-        launches_per_step = 2 if ssm.workspace_bytes(cfg.Bt, cfg.D, cfg.L, cfg.N,
+    if not launches_per_step:   # profiler unavailable (or held by another tool): the planner's count
+        launches_per_step = 3 if ssm.workspace_bytes(cfg.Bt, cfg.D, cfg.L, cfg.N,
                                                     ssm.SSM_BF16 if cfg.io == "bf16" else ssm.SSM_F32) > 0 else 1
     out = {
         "metric": "scan elements/s (B*D*L*N/s); fraction of the max(HBM, SFU) roofline; decode tok/s",
@@ -271,9 +281,12 @@ def bench_ours(args, rank, ws, local):
                    "l2": "inputs larger than L2 (%.0f MB per step)" % (io_bytes / 1e6)},
         "tokens_per_s": ws * cfg.Bt * cfg.L / t_step,
         "roofline": {"bound": "alu", "achieved": achieved, "peak": ex2_peak, "unit": "Gexp/s",
-                     "frac": achieved / ex2_peak, "traffic": TRAFFIC_BYTES_PER_LAUNCH,
+                     "frac": achieved / ex2_peak,
+                     "traffic": TRAFFIC_BYTES_PER_LAUNCH.get(args.workload) if not args.seqlen else None,
                      "peak_source": f"MUFU ex2 {EX2_PER_CLK_SM}/clk/SM x {SM_COUNT} SMs x {sm_max:.0f} MHz",
-                     "kernel": "whole scan call (%d launch%s)" % (launches_per_step, "es" if launches_per_step > 1 else ""),
+                     "kernel": "whole scan call (%d launch%s: %s)" % (
+                         launches_per_step, "es" if launches_per_step > 1 else "",
+                         ", ".join(k.split("(")[0].replace("void ", "") for k in kernel_names) or "n/a"),
                      "hbm": {"achieved_gbs": io_bytes / t_step / 1e9, "peak_gbs": hbm, "peak_kind": peak_kind,
                              "frac": io_bytes / t_step / 1e9 / hbm},
                      "frac_at_sampled_clock": (achieved / (SM_COUNT * EX2_PER_CLK_SM * clocks["sm_mhz"] * 1e6 / 1e9)
@@ -376,7 +389,7 @@ def bench_reference(args, rank, ws):
     if rank != 0:
         return None
     import oracle
-    cfg = gen.SCAN_CONFIGS[args.workload]
+    cfg = workload_config(args)
     inp = gen.scan_inputs(cfg)
     nthreads = os.cpu_count() or 1
     rate1, _, _, t1 = oracle_rate(inp, 0.0, nthreads)   # one channel, to size the sample

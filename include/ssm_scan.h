@@ -139,9 +139,10 @@ ssm_status_t ssm_selective_scan_fwd_ws(const ssm_dims_t *dims, const void *u,
  *     keep it alive until each call has completed on the stream.
  *
  * Scratch size: returns SSM_ERR_WORKSPACE, before any CUDA work is queued, when
- * ssm_selective_scan_workspace_bytes(dims) exceeds SSM_SCRATCH_MAX_BYTES. For example,
- * 8 x 1536 x 2048 x 16 needs 3.5 MiB and fits; 1 x 1536 x 131072 x 64 needs about 65 MiB
- * and is rejected. Use ssm_selective_scan_fwd_ws for those.
+ * ssm_selective_scan_workspace_bytes(dims) exceeds SSM_SCRATCH_MAX_BYTES. The default plans
+ * keep only chunk carries there (1 x 1536 x 131072 x 64 needs about 9 MiB and fits); a plan
+ * that also keeps the whole sequence's B and C there (the persistent time-split kernel,
+ * about 65 MiB for that shape) is rejected. Use ssm_selective_scan_fwd_ws for those.
  * Zero state: the control words at the start of the scratch (the persistent kernel's
  * work ticket and per-segment carry flags) must be zero when that kernel starts; every
  * call clears them on `stream` (cudaMemsetAsync) before its launch. Everything else in
