@@ -49,6 +49,15 @@ def _bind(lib):
     lib.oracle_state_update.argtypes = [
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _dp, _dp,
         _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
+    lib.oracle_scan_channels_disc.restype = ctypes.c_int
+    lib.oracle_scan_channels_disc.argtypes = [
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        _dp, _dp, _dp, _dp, _dp, _ip, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, _dp,
+        _dp, _dp, _dp, _dp, ctypes.c_int]
+    lib.oracle_state_update_disc.restype = ctypes.c_int
+    lib.oracle_state_update_disc.argtypes = [
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _dp, _dp,
+        _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, _dp, _dp]
     return lib
 
 
@@ -76,8 +85,8 @@ def _ptr(a):
 
 
 def scan_rows(u, delta, A, B, C, bidx, D=None, z=None, delta_bias=None,
-              delta_softplus=False, h0=None, with_mag=False, nthreads=1, lib=None):
-    """Scan channels given as packed rows.
+              delta_softplus=False, h0=None, with_mag=False, nthreads=1, lib=None, zoh=False):
+    """Scan channels given as packed rows (``zoh``: zero-order-hold B_bar instead of dt*B).
 
     u, delta, z: [nchan, L]; A, h0: [nchan, N]; D, delta_bias: [nchan];
     B, C: [nbatch, N, L]; bidx: [nchan] batch row of each channel.
@@ -97,17 +106,17 @@ def scan_rows(u, delta, A, B, C, bidx, D=None, z=None, delta_bias=None,
     hl = np.zeros((nchan, N))
     ym = np.zeros((nchan, L)) if with_mag else None
     hm = np.zeros((nchan, N)) if with_mag else None
-    rc = lib.oracle_scan_channels(
+    rc = lib.oracle_scan_channels_disc(
         nchan, L, N, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
         bidx.ctypes.data_as(_ip), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
-        _ptr(h0), _ptr(y), _ptr(ym), _ptr(hl), _ptr(hm), int(nthreads))
+        int(bool(zoh)), _ptr(h0), _ptr(y), _ptr(ym), _ptr(hl), _ptr(hm), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_scan_channels failed ({rc})")
     return (y, hl, ym, hm) if with_mag else (y, hl)
 
 
 def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=False,
-                   h0=None, with_mag=False, nthreads=1, channels=None, lib=None):
+                   h0=None, with_mag=False, nthreads=1, channels=None, lib=None, zoh=False):
     """Scan full tensors: u, delta, z [Bt, D, L]; A [D, N]; B, C [Bt, N, L]; D, bias [D];
     h0 [Bt, D, N]. ``channels``: optional list of (b, d) pairs; then only those channels are
     computed and the results are packed [len(channels), ...] in that order."""
@@ -127,7 +136,7 @@ def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_sof
                     None if D is None else np.asarray(D)[ds],
                     rows3(z), None if delta_bias is None else np.asarray(delta_bias)[ds],
                     delta_softplus, None if h0 is None else np.asarray(h0)[bs, ds, :],
-                    with_mag, nthreads, lib)
+                    with_mag, nthreads, lib, zoh)
     if channels is not None:
         return out
     shp_y, shp_h = (Bt, Dm, L), (Bt, Dm, N)
@@ -137,7 +146,8 @@ def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_sof
     return tuple(res)
 
 
-def state_update(state, x, dt, A, B, C, D=None, z=None, smag=None, with_mag=False, lib=None):
+def state_update(state, x, dt, A, B, C, D=None, z=None, smag=None, with_mag=False, lib=None,
+                 zoh=False):
     """One recurrent step. state [Bt, D, N] (a new array is returned; the input is not
     modified); x, dt, z [Bt, D]; A [D, N]; B, C [Bt, N]; D [D].
     Returns (y [Bt, D], new_state) or, with ``with_mag``, (y, new_state, ymag, new_smag);
@@ -151,8 +161,8 @@ def state_update(state, x, dt, A, B, C, D=None, z=None, smag=None, with_mag=Fals
         sm = np.abs(st) if smag is None else np.array(smag, dtype=np.float64, order="C", copy=True)
     y = np.zeros((Bt, Dm))
     ym = np.zeros((Bt, Dm)) if with_mag else None
-    rc = lib.oracle_state_update(Bt, Dm, N, _ptr(st), _ptr(sm), _ptr(x), _ptr(dt), _ptr(A),
-                                 _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y), _ptr(ym))
+    rc = lib.oracle_state_update_disc(Bt, Dm, N, _ptr(st), _ptr(sm), _ptr(x), _ptr(dt), _ptr(A),
+                                      _ptr(B), _ptr(C), _ptr(D), _ptr(z), int(bool(zoh)), _ptr(y), _ptr(ym))
     if rc != 0:
         raise RuntimeError(f"oracle_state_update failed ({rc})")
     return (y, st, ym, sm) if with_mag else (y, st)

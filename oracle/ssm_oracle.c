@@ -25,7 +25,11 @@
  *   same recurrence for one step with the (already positive) step given directly.
  *
  * Readings where the pages are silent or disagree (each also listed in the design notes):
- *   - B_bar = dt * B (the page's code), not the exact zero-order-hold (A_bar - 1)/A * B.
+ *   - B_bar = dt * B (the page's code) by default. The exact zero-order-hold variant of
+ *     "Mamba architecture principles and industrial long-text practice" (jsqmd.com, section
+ *     2.3) and of the Mamba paper notes (section 3.2), B_bar = (exp(dt*A) - 1)/A * B, is
+ *     selected with zoh != 0 and computed as dt*B * phi(dt*A), phi(x) = expm1(x)/x, phi(0) = 1
+ *     (the A -> 0 limit is the Euler step).
  *   - softplus is log1p(exp(v)) with the common pass-through for v > 20 (beta = 1).
  *   - y_t reads the state AFTER the update at t (the page's code updates, then reads).
  *   - A is a real diagonal (per channel, per state); B and C are shared by all channels
@@ -46,13 +50,15 @@
 
 static double softplus(double v) { return v > 20.0 ? v : log1p(exp(v)); }
 static double silu(double v) { return v / (1.0 + exp(-v)); }
+/* expm1(x)/x, the factor that turns dt*B into the zero-order-hold B_bar; 1 at x = 0 */
+static double zoh_factor(double x) { return x == 0.0 ? 1.0 : expm1(x) / x; }
 
 /* One channel: the loop of the page, in its order. */
 static void scan_one_channel(int64_t L, int64_t N,
                              const double *u, const double *delta, const double *A,
                              const double *B, const double *C, /* [N][L] of this batch row */
                              int has_D, double Dval, const double *z,
-                             int has_bias, double bias, int use_softplus,
+                             int has_bias, double bias, int use_softplus, int zoh,
                              const double *h0, double *h, double *hm,
                              double *y, double *ymag) {
     for (int64_t n = 0; n < N; ++n) {
@@ -67,6 +73,7 @@ static void scan_one_channel(int64_t L, int64_t N,
         for (int64_t n = 0; n < N; ++n) {
             double A_bar = exp(dt * A[n]);
             double B_bar = dt * B[n * L + t];
+            if (zoh) B_bar *= zoh_factor(dt * A[n]);
             h[n] = A_bar * h[n] + B_bar * x;
             hm[n] = A_bar * hm[n] + fabs(B_bar * x);
             acc += h[n] * C[n * L + t];
@@ -88,7 +95,7 @@ typedef struct {
     int64_t nchan, L, N;
     const double *u, *delta, *A, *B, *C, *Dskip, *z, *dbias, *h0;
     const int64_t *bidx;
-    int softplus;
+    int softplus, zoh;
     double *y, *ymag, *hlast, *hmag;
     int tid, nthreads;
     int status;
@@ -111,7 +118,7 @@ static void *scan_worker(void *arg) {
         scan_one_channel(j->L, j->N, j->u + c * j->L, j->delta + c * j->L, j->A + c * j->N,
                          Bb, Cb, j->Dskip != NULL, j->Dskip ? j->Dskip[c] : 0.0,
                          j->z ? j->z + c * j->L : NULL, j->dbias != NULL,
-                         j->dbias ? j->dbias[c] : 0.0, j->softplus,
+                         j->dbias ? j->dbias[c] : 0.0, j->softplus, j->zoh,
                          j->h0 ? j->h0 + c * j->N : NULL, h, hm, j->y + c * j->L,
                          j->ymag ? j->ymag + c * j->L : NULL);
         for (int64_t n = 0; n < j->N; ++n) {
@@ -134,13 +141,13 @@ static void *scan_worker(void *arg) {
  * Channels are independent; with nthreads > 1 they are dealt out round-robin to threads.
  * Returns 0, or nonzero on bad arguments / allocation failure.
  */
-int oracle_scan_channels(int64_t nchan, int64_t L, int64_t N,
-                         const double *u, const double *delta, const double *A,
-                         const double *B, const double *C, const int64_t *bidx,
-                         const double *Dskip, const double *z, const double *dbias,
-                         int use_softplus, const double *h0,
-                         double *y, double *ymag, double *hlast, double *hmag,
-                         int nthreads) {
+int oracle_scan_channels_disc(int64_t nchan, int64_t L, int64_t N,
+                              const double *u, const double *delta, const double *A,
+                              const double *B, const double *C, const int64_t *bidx,
+                              const double *Dskip, const double *z, const double *dbias,
+                              int use_softplus, int zoh, const double *h0,
+                              double *y, double *ymag, double *hlast, double *hmag,
+                              int nthreads) {
     if (nchan < 0 || L < 0 || N < 1) return 1;
     if (nchan == 0 || L == 0) {
         for (int64_t c = 0; c < nchan; ++c)
@@ -157,7 +164,7 @@ int oracle_scan_channels(int64_t nchan, int64_t L, int64_t N,
     pthread_t th[256];
     for (int i = 0; i < nthreads; ++i) {
         scan_job_t j = {nchan, L, N, u, delta, A, B, C, Dskip, z, dbias, h0, bidx,
-                        use_softplus, y, ymag, hlast, hmag, i, nthreads, 1};
+                        use_softplus, zoh, y, ymag, hlast, hmag, i, nthreads, 1};
         jobs[i] = j;
     }
     if (nthreads == 1) {
@@ -176,16 +183,28 @@ int oracle_scan_channels(int64_t nchan, int64_t L, int64_t N,
     return st;
 }
 
+/* The page's Euler step B_bar = dt * B (zoh = 0). */
+int oracle_scan_channels(int64_t nchan, int64_t L, int64_t N,
+                         const double *u, const double *delta, const double *A,
+                         const double *B, const double *C, const int64_t *bidx,
+                         const double *Dskip, const double *z, const double *dbias,
+                         int use_softplus, const double *h0,
+                         double *y, double *ymag, double *hlast, double *hmag,
+                         int nthreads) {
+    return oracle_scan_channels_disc(nchan, L, N, u, delta, A, B, C, bidx, Dskip, z, dbias,
+                                     use_softplus, 0, h0, y, ymag, hlast, hmag, nthreads);
+}
+
 /*
  * One recurrent inference step for every (b, d): the page's loop body for a single
  * timestep, starting from the given state, with dt already the positive step (no bias,
  * no softplus). Layouts: state, smag [Bt][D][N] (in/out); x, dt, z, y, ymag [Bt][D];
  * A [D][N]; B, C [Bt][N]; Dskip [D]. smag/ymag: magnitude companion (NULL = skip).
  */
-int oracle_state_update(int64_t Bt, int64_t D, int64_t N, double *state, double *smag,
-                        const double *x, const double *dt, const double *A,
-                        const double *B, const double *C, const double *Dskip,
-                        const double *z, double *y, double *ymag) {
+int oracle_state_update_disc(int64_t Bt, int64_t D, int64_t N, double *state, double *smag,
+                             const double *x, const double *dt, const double *A,
+                             const double *B, const double *C, const double *Dskip,
+                             const double *z, int zoh, double *y, double *ymag) {
     if (Bt < 0 || D < 0 || N < 1) return 1;
     if (Bt == 0 || D == 0) return 0;
     if (!state || !x || !dt || !A || !B || !C || !y) return 1;
@@ -198,6 +217,7 @@ int oracle_state_update(int64_t Bt, int64_t D, int64_t N, double *state, double 
             for (int64_t n = 0; n < N; ++n) {
                 double A_bar = exp(dt[bd] * A[d * N + n]);
                 double B_bar = dt[bd] * B[b * N + n];
+                if (zoh) B_bar *= zoh_factor(dt[bd] * A[d * N + n]);
                 h[n] = A_bar * h[n] + B_bar * x[bd];
                 acc += h[n] * C[b * N + n];
                 if (hm) {
@@ -217,4 +237,12 @@ int oracle_state_update(int64_t Bt, int64_t D, int64_t N, double *state, double 
         }
     }
     return 0;
+}
+
+/* The page's Euler step for the recurrent update (zoh = 0). */
+int oracle_state_update(int64_t Bt, int64_t D, int64_t N, double *state, double *smag,
+                        const double *x, const double *dt, const double *A,
+                        const double *B, const double *C, const double *Dskip,
+                        const double *z, double *y, double *ymag) {
+    return oracle_state_update_disc(Bt, D, N, state, smag, x, dt, A, B, C, Dskip, z, 0, y, ymag);
 }

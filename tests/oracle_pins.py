@@ -281,6 +281,86 @@ def pin_magnitude(lib):
     _close(hm2, h2, 1e-13, 0, "companion equals state for non-negative terms")
 
 
-ALL_PINS = [pin_lti_convolution, pin_tiny_step, pin_prefix_sum, pin_softplus, pin_gate,
+# ---- exact zero-order hold (jsqmd.com "Mamba architecture principles ...", section 2.3) ----
+# The ZOH discretisation samples the continuous system dh/dtau = A h + B u, with u and B held
+# constant over each step, exactly at the step ends.
+
+# Constant input from h = 0: h(tau) = (exp(A tau) - 1)/A * B u  (tau * B u for A = 0).
+def pin_zoh_step_response(lib):
+    rng = _rng(21)
+    L, N, dt, uu = 60, 5, 0.13, 0.7
+    A = np.array([-3.0, -0.4, -1e-3, 0.0, 0.5])
+    Bc, Cc = rng.standard_normal(N), rng.standard_normal(N)
+    y, h = oracle.scan_rows(np.full((1, L), uu), np.full((1, L), dt), A[None],
+                            np.repeat(Bc[:, None], L, 1)[None], np.repeat(Cc[:, None], L, 1)[None],
+                            [0], delta_softplus=False, lib=lib, zoh=True)
+    tau = dt * (np.arange(L) + 1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        g = np.where(A[:, None] == 0, tau[None, :], np.expm1(A[:, None] * tau[None, :]) / A[:, None])
+    h_ref = g * (Bc * uu)[:, None]                                # [N, L]
+    _close(y[0], (Cc[:, None] * h_ref).sum(0), 1e-11, 1e-13, "ZOH step response y")
+    _close(h[0], h_ref[:, -1], 1e-11, 1e-13, "ZOH step response state")
+
+
+# Varying steps, inputs and B: each step integrated as an ODE by scipy (no closed form used).
+def pin_zoh_piecewise_ode(lib):
+    from scipy.integrate import solve_ivp
+    rng = _rng(22)
+    L, N = 12, 3
+    A = np.array([-2.0, -0.3, 0.2])
+    dt = rng.uniform(0.05, 0.6, L)
+    u = rng.standard_normal(L)
+    B = rng.standard_normal((N, L))
+    C = rng.standard_normal((N, L))
+    y, h = oracle.scan_rows(u[None], dt[None], A[None], B[None], C[None], [0],
+                            delta_softplus=False, lib=lib, zoh=True)
+    hs = np.zeros(N)
+    for t in range(L):
+        sol = solve_ivp(lambda _tau, x, t=t: A * x + B[:, t] * u[t], (0.0, dt[t]), hs,
+                        rtol=1e-12, atol=1e-14, method="DOP853")
+        hs = sol.y[:, -1]
+        _close(y[0, t], (C[:, t] * hs).sum(), 1e-8, 1e-10, f"ZOH vs ODE y[{t}]")
+    _close(h[0], hs, 1e-8, 1e-10, "ZOH vs ODE state")
+
+
+# As the step goes to zero ZOH and the Euler step agree to first order in dt*A.
+def pin_zoh_small_step_limit(lib):
+    rng = _rng(23)
+    L, N = 50, 4
+    A = -rng.uniform(0.5, 4, N)
+    u = rng.standard_normal(L)
+    B = rng.standard_normal((N, L))
+    C = rng.standard_normal((N, L))
+    dt = np.full(L, 1e-7)
+    yz, hz = oracle.scan_rows(u[None], dt[None], A[None], B[None], C[None], [0], lib=lib, zoh=True)
+    ye, he = oracle.scan_rows(u[None], dt[None], A[None], B[None], C[None], [0], lib=lib, zoh=False)
+    _close(hz, he, 1e-5, 0.0, "ZOH -> Euler as dt -> 0")
+    assert np.max(np.abs(hz - he)) > 0.0, "ZOH flag has no effect"
+
+
+# The recurrent step with ZOH equals the ZOH scan started from the same state.
+def pin_zoh_decode_equals_scan(lib):
+    rng = _rng(24)
+    Bt, Dm, N, S = 2, 3, 4, 40
+    A = -rng.uniform(0.1, 6, size=(Dm, N))
+    st0 = rng.standard_normal((Bt, Dm, N))
+    x = rng.standard_normal((S, Bt, Dm))
+    dt = np.log1p(np.exp(rng.standard_normal((S, Bt, Dm)) - 1))
+    B = rng.standard_normal((S, Bt, N))
+    C = rng.standard_normal((S, Bt, N))
+    st = st0
+    ys = []
+    for s in range(S):
+        y, st = oracle.state_update(st, x[s], dt[s], A, B[s], C[s], lib=lib, zoh=True)
+        ys.append(y)
+    yr, hr = oracle.selective_scan(np.moveaxis(x, 0, -1), np.moveaxis(dt, 0, -1), A,
+                                   np.moveaxis(B, 0, -1), np.moveaxis(C, 0, -1),
+                                   delta_softplus=False, h0=st0, lib=lib, zoh=True)
+    _close(np.stack(ys, -1), yr, 1e-13, 1e-14, "ZOH decode vs scan outputs")
+    _close(st, hr, 1e-13, 1e-14, "ZOH decode vs scan state")
+
+
+ALL_PINS = [pin_zoh_step_response, pin_zoh_piecewise_ode, pin_zoh_small_step_limit,
+            pin_zoh_decode_equals_scan, pin_lti_convolution, pin_tiny_step, pin_prefix_sum, pin_softplus, pin_gate,
             pin_split_resume, pin_tree_bruteforce, pin_linear_causal, pin_hand_case,
             pin_decode_equals_scan, pin_magnitude]

@@ -37,6 +37,10 @@ MUTANTS = [
     ("decode_B_batch", [("double B_bar = dt[bd] * B[b * N + n];", "double B_bar = dt[bd] * B[n];")]),
     ("decode_no_D", [("double yt = acc + (Dskip ? x[bd] * Dskip[d] : 0.0);", "double yt = acc;")]),
     ("h0_ignored", [("h[n] = h0 ? h0[n] : 0.0;", "h[n] = 0.0;")]),
+    ("zoh_factor_exp_not_expm1", [("return x == 0.0 ? 1.0 : expm1(x) / x;", "return x == 0.0 ? 1.0 : exp(x) / x;")]),
+    ("zoh_factor_missing_divide", [("return x == 0.0 ? 1.0 : expm1(x) / x;", "return x == 0.0 ? 1.0 : expm1(x);")]),
+    ("zoh_ignored_in_scan", [("if (zoh) B_bar *= zoh_factor(dt * A[n]);", "(void)zoh;")]),
+    ("zoh_ignored_in_decode", [("if (zoh) B_bar *= zoh_factor(dt[bd] * A[d * N + n]);", "(void)zoh;")]),
 ]
 
 
