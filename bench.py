@@ -75,6 +75,7 @@ def parse():
     ap.add_argument("--seqlen", type=int, default=0,
                     help="override the workload's sequence length (profiling of a smaller case)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-zoh", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -295,6 +296,28 @@ def bench_ours(args, rank, ws, local):
         "gpu_launches": args.steps * launches_per_step,
         "kernels_per_step": kernel_names,
     }
+    # the exact zero-order-hold variant on the same workload, timed the same way
+    if not args.no_zoh:
+        def zstep():
+            ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                                   delta_bias=g["delta_bias"], delta_softplus=cfg.softplus, y=y, last_state=last,
+                                   stream=stream, discretization="zoh")
+        for _ in range(args.warmup):
+            zstep()
+        torch.cuda.synchronize()
+        z0, z1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        z0.record(stream)
+        for _ in range(args.steps):
+            zstep()
+        z1.record(stream)
+        torch.cuda.synchronize()
+        zms = max_over_ranks(z0.elapsed_time(z1), ws) / args.steps
+        assert ssm.stream_status(stream) == ssm.SSM_OK
+        out["zoh"] = {"discretization": "exact zero-order hold (exp(dt*A) - 1)/A * B",
+                      "ms_per_step": zms, "value": weak_scaling_value(elems, ws, zms / 1e3), "unit": "elem/s",
+                      "roofline_frac": elems / (zms / 1e3) / 1e9 / ex2_peak}
+        out["gpu_launches"] += args.steps * launches_per_step
     # end to end: host buffers through the C ABI, copies inside the timed region
     if not args.no_e2e:
         pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}

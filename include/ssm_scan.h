@@ -178,6 +178,41 @@ ssm_status_t ssm_state_update(const ssm_dims_t *dims, float *state, const void *
                               const void *dt, const float *A, const void *B, const void *C,
                               const float *D, const void *z, void *y, void *stream);
 
+/* Discretisation of B (the A_bar = exp(dt*A) step is the same in both). */
+typedef enum {
+    SSM_DISC_EULER = 0, /* B_bar = dt*B: the per-timestep loop of lmnt.cn "From RNN to Mamba"
+                           section 3.2 (what ssm_selective_scan_fwd and ssm_state_update do) */
+    SSM_DISC_ZOH = 1    /* exact zero-order hold B_bar = (exp(dt*A) - 1)/A * B, equal to dt*B
+                           where A = 0: jsqmd.com "Mamba architecture principles and industrial
+                           long-text practice" section 2.3 */
+} ssm_disc_t;
+
+/*
+ * ssm_selective_scan_fwd with the discretisation chosen (ssm_disc_t). `workspace` may be
+ * NULL (the library then allocates stream-ordered, as ssm_selective_scan_fwd), or a
+ * caller-owned buffer as for ssm_selective_scan_fwd_ws. The zero-order hold runs on the
+ * default channel-pair kernel, i.e. for rows whose byte length (seqlen * io size) is a
+ * multiple of 16; other shapes return SSM_ERR_UNSUPPORTED (as does an unknown
+ * `discretization`). B_bar*u is formed as dt*u*B * phi(dt*A), phi(x) = (e^x - 1)/x, with a
+ * cubic polynomial for |x| < 1/8 and (exp(x) - 1)/x otherwise: relative error of phi about
+ * 2e-6 at most, no extra exponential per element. Other arguments and errors: as
+ * ssm_selective_scan_fwd / ssm_selective_scan_fwd_ws.
+ */
+ssm_status_t ssm_selective_scan_fwd_disc(const ssm_dims_t *dims, const void *u,
+                                         const void *delta, const float *A, const void *B,
+                                         const void *C, const float *D, const void *z,
+                                         const float *delta_bias, int delta_softplus,
+                                         int discretization, void *y, float *last_state,
+                                         void *workspace, size_t workspace_bytes,
+                                         void *stream);
+
+/* ssm_state_update with the discretisation chosen (ssm_disc_t); same arguments and errors,
+ * SSM_ERR_UNSUPPORTED for an unknown `discretization`. */
+ssm_status_t ssm_state_update_disc(const ssm_dims_t *dims, float *state, const void *x,
+                                   const void *dt, const float *A, const void *B,
+                                   const void *C, const float *D, const void *z,
+                                   int discretization, void *y, void *stream);
+
 /*
  * Host-buffer scan: the same computation as ssm_selective_scan_fwd, with every array in
  * HOST memory (pinned memory gives the fastest copies). The call copies the inputs to the

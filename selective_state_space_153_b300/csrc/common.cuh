@@ -48,6 +48,17 @@ __device__ __forceinline__ float silu_f(float z) {
     return z * rcp_approx(1.0f + e);
 }
 
+// phi(x) = (e^x - 1)/x, the factor that turns dt*B into the zero-order-hold B_bar
+// ((exp(dt*A) - 1)/A * B); x = dt*A, abar = exp(x) already computed. For |x| < 1/8 a cubic
+// Taylor polynomial (truncation <= 2e-6 relative), else (abar - 1)/x (cancellation in
+// abar - 1 <= 2e-6 relative there). phi(0) = 1: the Euler step.
+__device__ __forceinline__ float zoh_phi(float x, float abar) {
+    float p = fmaf(x, 1.0f / 24.0f, 1.0f / 6.0f);
+    p = fmaf(p, x, 0.5f);
+    p = fmaf(p, x, 1.0f);
+    return fabsf(x) < 0.125f ? p : (abar - 1.0f) * rcp_approx(x);
+}
+
 // --- io conversions ---------------------------------------------------------------------
 template <typename IO> struct io_traits;
 template <> struct io_traits<float> {

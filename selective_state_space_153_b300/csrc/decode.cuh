@@ -27,6 +27,7 @@ struct DecodeParams {
     const float *A, *D;
     void *y;
     int64_t Bt, Dm, N;
+    int zoh;   // nonzero: launch the zero-order-hold variant (B_bar = (exp(dt*A) - 1)/A * B)
 };
 
 // Vector path: lane l of a warp owns the 16-byte piece q = l % LPC of channel
@@ -35,7 +36,7 @@ struct DecodeParams {
 // arithmetic is shifts (no 64-bit division). B and C of the row are read as 4-element
 // vectors (the caller checks their alignment); the y partials are summed across the LPC
 // lanes of a channel.
-template <typename IO, int LPC>
+template <typename IO, int LPC, bool ZOH = false>
 __global__ void __launch_bounds__(256) decode_wide_kernel(const DecodeParams p) {
     const int b = blockIdx.y;
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
@@ -55,10 +56,22 @@ __global__ void __launch_bounds__(256) decode_wide_kernel(const DecodeParams p) 
         load_io4(reinterpret_cast<const IO *>(p.B) + (int64_t)b * p.N + 4 * q, bv);
         load_io4(reinterpret_cast<const IO *>(p.C) + (int64_t)b * p.N + 4 * q, cv);
         const float dx = dt * xv, dl = dt * kLog2e;
-        v.x = fmaf(ex2(dl * a.x), v.x, dx * bv[0]);
-        v.y = fmaf(ex2(dl * a.y), v.y, dx * bv[1]);
-        v.z = fmaf(ex2(dl * a.z), v.z, dx * bv[2]);
-        v.w = fmaf(ex2(dl * a.w), v.w, dx * bv[3]);
+        if constexpr (ZOH) {
+            const float ab[4] = {ex2(dl * a.x), ex2(dl * a.y), ex2(dl * a.z), ex2(dl * a.w)};
+            const float av[4] = {a.x, a.y, a.z, a.w};
+            float wv[4] = {dx * bv[0], dx * bv[1], dx * bv[2], dx * bv[3]};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wv[i] *= zoh_phi(dt * av[i], ab[i]);
+            v.x = fmaf(ab[0], v.x, wv[0]);
+            v.y = fmaf(ab[1], v.y, wv[1]);
+            v.z = fmaf(ab[2], v.z, wv[2]);
+            v.w = fmaf(ab[3], v.w, wv[3]);
+        } else {
+            v.x = fmaf(ex2(dl * a.x), v.x, dx * bv[0]);
+            v.y = fmaf(ex2(dl * a.y), v.y, dx * bv[1]);
+            v.z = fmaf(ex2(dl * a.z), v.z, dx * bv[2]);
+            v.w = fmaf(ex2(dl * a.w), v.w, dx * bv[3]);
+        }
         __stcs(sp, v);
         acc = fmaf(cv[0], v.x, fmaf(cv[1], v.y, fmaf(cv[2], v.z, cv[3] * v.w)));
     }
@@ -71,7 +84,7 @@ __global__ void __launch_bounds__(256) decode_wide_kernel(const DecodeParams p) 
     }
 }
 
-template <typename IO, int LPC>  // LPC: lanes per channel = N/4
+template <typename IO, int LPC, bool ZOH = false>  // LPC: lanes per channel = N/4
 __global__ void __launch_bounds__(256) decode_vec_kernel(const DecodeParams p) {
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t chan = gid / LPC;   // b*Dm + d
@@ -98,10 +111,17 @@ __global__ void __launch_bounds__(256) decode_vec_kernel(const DecodeParams p) {
         const float c0 = io_traits<IO>::to_f(Cm[nb]), c1 = io_traits<IO>::to_f(Cm[nb + 1]);
         const float c2 = io_traits<IO>::to_f(Cm[nb + 2]), c3 = io_traits<IO>::to_f(Cm[nb + 3]);
         const float dx = dt * xv, dl = dt * kLog2e;
-        s.x = fmaf(ex2(dl * a4.x), s.x, dx * b0);
-        s.y = fmaf(ex2(dl * a4.y), s.y, dx * b1);
-        s.z = fmaf(ex2(dl * a4.z), s.z, dx * b2);
-        s.w = fmaf(ex2(dl * a4.w), s.w, dx * b3);
+        const float ab[4] = {ex2(dl * a4.x), ex2(dl * a4.y), ex2(dl * a4.z), ex2(dl * a4.w)};
+        float wv[4] = {dx * b0, dx * b1, dx * b2, dx * b3};
+        if constexpr (ZOH) {
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wv[i] *= zoh_phi(dt * av[i], ab[i]);
+        }
+        s.x = fmaf(ab[0], s.x, wv[0]);
+        s.y = fmaf(ab[1], s.y, wv[1]);
+        s.z = fmaf(ab[2], s.z, wv[2]);
+        s.w = fmaf(ab[3], s.w, wv[3]);
         __stcs(sp, s);
         acc = fmaf(c0, s.x, fmaf(c1, s.y, fmaf(c2, s.z, c3 * s.w)));
     }
@@ -114,7 +134,7 @@ __global__ void __launch_bounds__(256) decode_vec_kernel(const DecodeParams p) {
     }
 }
 
-template <typename IO>
+template <typename IO, bool ZOH = false>
 __global__ void __launch_bounds__(256) decode_scalar_kernel(const DecodeParams p) {
     const int64_t cl = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (cl >= p.Bt * p.Dm) return;
@@ -127,7 +147,10 @@ __global__ void __launch_bounds__(256) decode_scalar_kernel(const DecodeParams p
     float acc = 0.0f;
     for (int64_t n = 0; n < p.N; ++n) {
         float s = p.state[cl * p.N + n];
-        s = fmaf(ex2(dl * p.A[d * p.N + n]), s, dx * io_traits<IO>::to_f(Bm[b * p.N + n]));
+        const float an = p.A[d * p.N + n], ab = ex2(dl * an);
+        float w = dx * io_traits<IO>::to_f(Bm[b * p.N + n]);
+        if constexpr (ZOH) w *= zoh_phi(dt * an, ab);
+        s = fmaf(ab, s, w);
         p.state[cl * p.N + n] = s;
         acc = fmaf(io_traits<IO>::to_f(Cm[b * p.N + n]), s, acc);
     }

@@ -21,6 +21,13 @@
 // one barrier per tile; then tile j+1 is converted (softplus, dt*u per (channel, t); B, C to
 // fp32, transposed to [t][n]) while tile j is scanned from the previous conversion.
 //
+// Discretisation: B_bar*u = dt*u*B (the lmnt.cn loop) or, with ZOH, the exact zero-order
+// hold (exp(dt*A) - 1)/A * B * u of "Mamba architecture principles and industrial long-text
+// practice" (jsqmd.com), section 2.3, computed as dt*u*B * phi(dt*A), phi(x) = (e^x - 1)/x:
+// for |x| < 1/8 a cubic Taylor polynomial (truncation <= 2e-6 relative), else
+// (a - 1) * (1/dt) * (1/A) with a = exp(dt*A) already computed for the recurrence (the
+// cancellation in a - 1 is then <= 2e-6 relative). No extra exponential per element.
+//
 // Modes: FULL computes y (and the final state of the last chunk); AGG computes only the
 // chunk's end state from h = 0 and the chunk's sum of dt, from which chunk_combine_kernel
 // forms each chunk's incoming state (the recurrence is a composition of affine maps --
@@ -85,7 +92,19 @@ __device__ __forceinline__ void load_steps(const float *src, float (&out)[S]) {
     }
 }
 
-template <typename IO, int KS, int GP, int WARPS, int T, bool AGG>
+// phi(x) = (e^x - 1)/x for the pair (x0, x1), x = dt*A given in log2 units (xl2 = x / ln 2),
+// a = exp(x) from the recurrence; inv_dt = 1/dt of the channel, inv_a = 1/A of the states
+__device__ __forceinline__ float2 zoh_phi2(float2 xl2, float2 a, float inv_dt, float2 inv_a) {
+    const float2 x = __fmul2_rn(xl2, make_float2(0.69314718055994531f, 0.69314718055994531f));
+    float2 poly = __ffma2_rn(x, make_float2(1.0f / 24.0f, 1.0f / 24.0f), make_float2(1.0f / 6.0f, 1.0f / 6.0f));
+    poly = __ffma2_rn(poly, x, make_float2(0.5f, 0.5f));
+    poly = __ffma2_rn(poly, x, make_float2(1.0f, 1.0f));
+    const float2 em1 = __fadd2_rn(a, make_float2(-1.0f, -1.0f));
+    const float2 big = __fmul2_rn(__fmul2_rn(em1, make_float2(inv_dt, inv_dt)), inv_a);
+    return make_float2(fabsf(x.x) < 0.125f ? poly.x : big.x, fabsf(x.y) < 0.125f ? poly.y : big.y);
+}
+
+template <typename IO, int KS, int GP, int WARPS, int T, bool AGG, bool ZOH = false>
 __global__ void __launch_bounds__(WARPS * 32)
 scan_pair_kernel(const SeqParams p) {
     using Cfg = PairCfg<IO, KS, GP, WARPS, T>;
@@ -127,6 +146,19 @@ scan_pair_kernel(const SeqParams p) {
                 const float a1 = (cv[ch] && n + 1 < N) ? p.A[dch[ch] * p.N + n + 1] * kLog2e : 0.0f;
                 Ap[ch][q][pp] = make_float2(a0, a1);
             }
+    // 1/A of the lane's states (ZOH; zero where A = 0, where phi's polynomial branch applies)
+    float2 iA[2][kQN][2];
+    if constexpr (ZOH) {
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+            for (int q = 0; q < kQN; ++q)
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    const float a0 = Ap[ch][q][pp].x, a1 = Ap[ch][q][pp].y;   // A*log2(e)
+                    iA[ch][q][pp] = make_float2(a0 != 0.0f ? kLog2e / a0 : 0.0f, a1 != 0.0f ? kLog2e / a1 : 0.0f);
+                }
+    }
     float2 h[2][kQN][2];
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch)
@@ -290,8 +322,15 @@ scan_pair_kernel(const SeqParams p) {
                         const float2 e1 = __fmul2_rn(dd[ch], Ap[ch][q][1]);
                         const float2 a0 = make_float2(ex2(e0.x), ex2(e0.y));
                         const float2 a1 = make_float2(ex2(e1.x), ex2(e1.y));
-                        const float2 w0 = __fmul2_rn(xx[ch], make_float2(bq.x, bq.y));
-                        const float2 w1 = __fmul2_rn(xx[ch], make_float2(bq.z, bq.w));
+                        float2 w0, w1;
+                        if constexpr (ZOH) {
+                            const float idt = rcp_approx(ch ? dx.z : dx.x);
+                            w0 = __fmul2_rn(__fmul2_rn(xx[ch], make_float2(bq.x, bq.y)), zoh_phi2(e0, a0, idt, iA[ch][q][0]));
+                            w1 = __fmul2_rn(__fmul2_rn(xx[ch], make_float2(bq.z, bq.w)), zoh_phi2(e1, a1, idt, iA[ch][q][1]));
+                        } else {
+                            w0 = __fmul2_rn(xx[ch], make_float2(bq.x, bq.y));
+                            w1 = __fmul2_rn(xx[ch], make_float2(bq.z, bq.w));
+                        }
                         h[ch][q][0] = __ffma2_rn(a0, h[ch][q][0], w0);
                         h[ch][q][1] = __ffma2_rn(a1, h[ch][q][1], w1);
                         if (!AGG) {

@@ -46,6 +46,7 @@ struct SeqParams {
     float *agg_s;       // [nchunks][Bt*Dm]          (AGG writes)
     const float *hin;   // [nchunks][Bt*Dm][Npad] or null (FULL reads)
     int npad;           // NPER*G of the launched kernel
+    int zoh;            // channel-pair kernel only: zero-order-hold B_bar (set by the host)
 };
 
 template <typename IO, int NPER, int G, int WARPS, int T>

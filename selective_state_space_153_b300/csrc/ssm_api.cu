@@ -387,10 +387,10 @@ int pair_gp(int64_t N, int ks) {
     return gp;
 }
 
-template <typename IO, int KS, int GP, bool AGG>
+template <typename IO, int KS, int GP, bool AGG, bool ZOH>
 cudaError_t launch_pair_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
     using Cfg = PairCfg<IO, KS, GP, pair_warps(GP), kPairT>;
-    auto k = scan_pair_kernel<IO, KS, GP, pair_warps(GP), kPairT, AGG>;
+    auto k = scan_pair_kernel<IO, KS, GP, pair_warps(GP), kPairT, AGG, ZOH>;
     static unsigned long long attr_set = 0;  // per instantiation: bit i = set on device i
     int dev = 0;
     cudaGetDevice(&dev);
@@ -406,7 +406,11 @@ cudaError_t launch_pair_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
 
 template <typename IO, int KS, int GP>
 cudaError_t launch_pair_g(const SeqParams &prm, bool agg, int grid_y, cudaStream_t s) {
-    return agg ? launch_pair_t<IO, KS, GP, true>(prm, grid_y, s) : launch_pair_t<IO, KS, GP, false>(prm, grid_y, s);
+    if (prm.zoh)
+        return agg ? launch_pair_t<IO, KS, GP, true, true>(prm, grid_y, s)
+                   : launch_pair_t<IO, KS, GP, false, true>(prm, grid_y, s);
+    return agg ? launch_pair_t<IO, KS, GP, true, false>(prm, grid_y, s)
+               : launch_pair_t<IO, KS, GP, false, false>(prm, grid_y, s);
 }
 
 #define SSM_PAIR_CASES(X) X(4, 1) X(4, 2) X(4, 4) X(8, 1) X(8, 2) X(8, 4) X(8, 8) X(8, 16)
@@ -483,7 +487,7 @@ size_t pair_workspace_bytes(const ssm_dims_t &d, const PairPlan &p) {
 ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *u, const void *delta, const float *A,
                            const void *B, const void *C, const float *D, const void *z, const float *delta_bias,
                            int delta_softplus, void *y, float *last_state, void *workspace, size_t ws_bytes,
-                           bool own_ws, cudaStream_t s) {
+                           bool own_ws, cudaStream_t s, int zoh) {
     const size_t need = pair_workspace_bytes(d, pl);
     bool allocated = false;
     if (need > 0) {
@@ -503,6 +507,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
     prm.chunk_len = pl.chunk_len; prm.nchunks = pl.nchunks;
     prm.chan_blocks = pl.chan_blocks;
     prm.npad = pl.np;
+    prm.zoh = zoh ? 1 : 0;
     cudaError_t e = cudaSuccess;
     const bool bf = d.io_dtype == SSM_BF16;
     if (pl.nchunks > 1) {
@@ -530,7 +535,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
 ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, const float *A,
                       const void *B, const void *C, const float *D, const void *z,
                       const float *delta_bias, int delta_softplus, void *y, float *last_state,
-                      void *workspace, size_t ws_bytes, bool own_ws, cudaStream_t s) {
+                      void *workspace, size_t ws_bytes, bool own_ws, cudaStream_t s, int zoh = 0) {
     const ssm_dims_t d = *dims;
     if (d.batch == 0 || d.dim == 0) return SSM_OK;
     if (d.seqlen == 0) {
@@ -544,7 +549,8 @@ ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, 
     const PairPlan pp = plan_pair(d);
     if (pp.use)
         return run_scan_pair(d, pp, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
-                             ws_bytes, own_ws, s);
+                             ws_bytes, own_ws, s, zoh);
+    if (zoh) return SSM_ERR_UNSUPPORTED;   // the zero-order hold runs on the channel-pair kernel only
     const TcPlan tp = plan_tc(d);
     if (tp.use) {
         char *w = static_cast<char *>(workspace);
@@ -699,9 +705,12 @@ ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_dims_t *dims, const void *
                     static_cast<cudaStream_t>(stream));
 }
 
-ssm_status_t ssm_state_update(const ssm_dims_t *dims, float *state, const void *x, const void *dt,
-                              const float *A, const void *B, const void *C, const float *D,
-                              const void *z, void *y, void *stream) {
+}  // extern "C"
+
+namespace {
+ssm_status_t state_update_impl(const ssm_dims_t *dims, float *state, const void *x, const void *dt,
+                               const float *A, const void *B, const void *C, const float *D,
+                               const void *z, void *y, void *stream, int zoh) {
     ssm_status_t st = check_dims(dims, false);
     if (st != SSM_OK) return st;
     if (dims->batch == 0 || dims->dim == 0) return SSM_OK;
@@ -714,7 +723,7 @@ ssm_status_t ssm_state_update(const ssm_dims_t *dims, float *state, const void *
     for (const void *q : tok)
         if (q != nullptr && !aligned_to(q, esz)) return SSM_ERR_ALIGN;
     if (D != nullptr && !aligned_to(D, 4)) return SSM_ERR_ALIGN;
-    DecodeParams p{state, x, dt, B, C, z, A, D, y, dims->batch, dims->dim, dims->dstate};
+    DecodeParams p{state, x, dt, B, C, z, A, D, y, dims->batch, dims->dim, dims->dstate, zoh ? 1 : 0};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t N = dims->dstate, chans = dims->batch * dims->dim;
     const bool bf = dims->io_dtype == SSM_BF16;
@@ -725,23 +734,64 @@ ssm_status_t ssm_state_update(const ssm_dims_t *dims, float *state, const void *
                       dims->dim * lpc < (int64_t)1 << 30 && !env_is("SSM_DEC_OLD", "1");
     if (wide && N % 4 == 0 && lpc >= 1 && lpc <= 32 && (32 % lpc) == 0) {
         const dim3 grid((unsigned)((dims->dim * lpc + 255) / 256), (unsigned)dims->batch);
-#define SSM_DECW(L) \
-    case L: bf ? decode_wide_kernel<bf16, L><<<grid, 256, 0, s>>>(p) : decode_wide_kernel<float, L><<<grid, 256, 0, s>>>(p); break;
+#define SSM_DECW(L)                                                                                    \
+    case L:                                                                                            \
+        if (zoh) bf ? decode_wide_kernel<bf16, L, true><<<grid, 256, 0, s>>>(p) : decode_wide_kernel<float, L, true><<<grid, 256, 0, s>>>(p); \
+        else bf ? decode_wide_kernel<bf16, L><<<grid, 256, 0, s>>>(p) : decode_wide_kernel<float, L><<<grid, 256, 0, s>>>(p);                \
+        break;
         switch (lpc) { SSM_DECW(1) SSM_DECW(2) SSM_DECW(4) SSM_DECW(8) SSM_DECW(16) SSM_DECW(32) default: return SSM_ERR_UNSUPPORTED; }
 #undef SSM_DECW
     } else if (N % 4 == 0 && lpc >= 1 && lpc <= 32 && (32 % lpc) == 0) {
         const int64_t threads = chans * lpc;
         const unsigned grid = (unsigned)((threads + 255) / 256);
-#define SSM_DEC(L) \
-    case L: bf ? decode_vec_kernel<bf16, L><<<grid, 256, 0, s>>>(p) : decode_vec_kernel<float, L><<<grid, 256, 0, s>>>(p); break;
+#define SSM_DEC(L)                                                                                     \
+    case L:                                                                                            \
+        if (zoh) bf ? decode_vec_kernel<bf16, L, true><<<grid, 256, 0, s>>>(p) : decode_vec_kernel<float, L, true><<<grid, 256, 0, s>>>(p); \
+        else bf ? decode_vec_kernel<bf16, L><<<grid, 256, 0, s>>>(p) : decode_vec_kernel<float, L><<<grid, 256, 0, s>>>(p);                \
+        break;
         switch (lpc) { SSM_DEC(1) SSM_DEC(2) SSM_DEC(4) SSM_DEC(8) SSM_DEC(16) SSM_DEC(32) default: return SSM_ERR_UNSUPPORTED; }
 #undef SSM_DEC
     } else {
         const unsigned grid = (unsigned)((chans + 255) / 256);
-        if (bf) decode_scalar_kernel<bf16><<<grid, 256, 0, s>>>(p);
-        else decode_scalar_kernel<float><<<grid, 256, 0, s>>>(p);
+        if (zoh) {
+            if (bf) decode_scalar_kernel<bf16, true><<<grid, 256, 0, s>>>(p);
+            else decode_scalar_kernel<float, true><<<grid, 256, 0, s>>>(p);
+        } else {
+            if (bf) decode_scalar_kernel<bf16><<<grid, 256, 0, s>>>(p);
+            else decode_scalar_kernel<float><<<grid, 256, 0, s>>>(p);
+        }
     }
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+ssm_status_t ssm_state_update(const ssm_dims_t *dims, float *state, const void *x, const void *dt,
+                              const float *A, const void *B, const void *C, const float *D,
+                              const void *z, void *y, void *stream) {
+    return state_update_impl(dims, state, x, dt, A, B, C, D, z, y, stream, 0);
+}
+
+ssm_status_t ssm_state_update_disc(const ssm_dims_t *dims, float *state, const void *x, const void *dt,
+                                   const float *A, const void *B, const void *C, const float *D,
+                                   const void *z, int discretization, void *y, void *stream) {
+    if (discretization != SSM_DISC_EULER && discretization != SSM_DISC_ZOH) return SSM_ERR_UNSUPPORTED;
+    return state_update_impl(dims, state, x, dt, A, B, C, D, z, y, stream, discretization == SSM_DISC_ZOH);
+}
+
+ssm_status_t ssm_selective_scan_fwd_disc(const ssm_dims_t *dims, const void *u, const void *delta,
+                                         const float *A, const void *B, const void *C, const float *D,
+                                         const void *z, const float *delta_bias, int delta_softplus,
+                                         int discretization, void *y, float *last_state, void *workspace,
+                                         size_t workspace_bytes, void *stream) {
+    ssm_status_t st = scan_checks(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
+    if (st != SSM_OK) return st;
+    if (discretization != SSM_DISC_EULER && discretization != SSM_DISC_ZOH) return SSM_ERR_UNSUPPORTED;
+    if (workspace != nullptr && !aligned16(workspace)) return SSM_ERR_ALIGN;
+    return run_scan(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
+                    workspace_bytes, workspace == nullptr, static_cast<cudaStream_t>(stream),
+                    discretization == SSM_DISC_ZOH);
 }
 
 ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, const void *delta,

@@ -19,6 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libssm_scan.so")
 SSM_OK, SSM_ERR_NULL, SSM_ERR_SHAPE, SSM_ERR_DTYPE, SSM_ERR_ALIGN = 0, 1, 2, 3, 4
 SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = 5, 6, 7, 8
 SSM_F32, SSM_BF16 = 0, 1
+SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
+_DISC = {"euler": SSM_DISC_EULER, "zoh": SSM_DISC_ZOH}
 MAX_DSTATE = 128
 SCRATCH_MAX_BYTES = 16 * 1024 * 1024   # SSM_SCRATCH_MAX_BYTES: the no-alloc entry's fixed scratch
 
@@ -26,7 +28,7 @@ SCRATCH_MAX_BYTES = 16 * 1024 * 1024   # SSM_SCRATCH_MAX_BYTES: the no-alloc ent
 EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_workspace_bytes",
            "ssm_selective_scan_fwd_ws", "ssm_state_update", "ssm_selective_scan_fwd_host",
            "ssm_stream_status", "ssm_status_string", "ssm_version",
-           "ssm_selective_scan_fwd_noalloc")
+           "ssm_selective_scan_fwd_noalloc", "ssm_selective_scan_fwd_disc", "ssm_state_update_disc")
 
 
 class SsmDims(ctypes.Structure):
@@ -60,6 +62,10 @@ def load(path: str = LIB_PATH):
     lib.ssm_selective_scan_fwd_ws.argtypes = scan_args + [_vp, ctypes.c_size_t, _vp]
     lib.ssm_selective_scan_fwd_ws.restype = ctypes.c_int
     lib.ssm_selective_scan_fwd_host.argtypes = scan_args + [_vp]
+    lib.ssm_selective_scan_fwd_disc.argtypes = scan_args[:10] + [ctypes.c_int] + scan_args[10:] + [_vp, ctypes.c_size_t, _vp]
+    lib.ssm_selective_scan_fwd_disc.restype = ctypes.c_int
+    lib.ssm_state_update_disc.argtypes = [dp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp]
+    lib.ssm_state_update_disc.restype = ctypes.c_int
     lib.ssm_selective_scan_fwd_noalloc.argtypes = scan_args + [_vp]
     lib.ssm_selective_scan_fwd_noalloc.restype = ctypes.c_int
     lib.ssm_selective_scan_fwd_host.restype = ctypes.c_int
@@ -109,10 +115,11 @@ def dims(batch, dim, seqlen, dstate, io) -> SsmDims:
 
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
                        y=None, last_state=None, return_last_state=False, stream=None,
-                       workspace=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                       workspace=None, discretization="euler") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Device scan. u, delta, z [Bt, D, L]; B, C [Bt, N, L] (io dtype); A [D, N], D, bias [D]
     fp32. Returns (y, last_state or None). ``workspace``: optional uint8 device tensor for
-    ssm_selective_scan_fwd_ws."""
+    ssm_selective_scan_fwd_ws. ``discretization``: "euler" (B_bar = dt*B) or "zoh" (exact
+    zero-order hold, through ssm_selective_scan_fwd_disc)."""
     lib = load()
     Bt, Dm, L = u.shape
     N = A.shape[1]
@@ -124,7 +131,12 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta
     dm = dims(Bt, Dm, L, N, io)
     args = [ctypes.byref(dm), _p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
             int(bool(delta_softplus)), _p(y), _p(last_state)]
-    if workspace is None:
+    if discretization != "euler":
+        ws_p = None if workspace is None else _p(workspace)
+        ws_n = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        rc = lib.ssm_selective_scan_fwd_disc(*args[:10], _DISC[discretization], *args[10:], ws_p, ws_n,
+                                             _stream_ptr(stream))
+    elif workspace is None:
         rc = lib.ssm_selective_scan_fwd(*args, _stream_ptr(stream))
     else:
         rc = lib.ssm_selective_scan_fwd_ws(*args, _p(workspace), workspace.numel() * workspace.element_size(),
@@ -185,17 +197,22 @@ def selective_scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, 
     return y, last_state
 
 
-def state_update(state, x, dt, A, B, C, D=None, z=None, y=None, stream=None) -> torch.Tensor:
+def state_update(state, x, dt, A, B, C, D=None, z=None, y=None, stream=None,
+                 discretization="euler") -> torch.Tensor:
     """In-place recurrent step on ``state`` [Bt, D, N] fp32; x, dt, z [Bt, D]; B, C [Bt, N]
-    (io dtype); A [D, N]; D [D]. Returns y [Bt, D]."""
+    (io dtype); A [D, N]; D [D]. Returns y [Bt, D]. ``discretization``: "euler" or "zoh"."""
     lib = load()
     Bt, Dm, N = state.shape
     io = _io_code(x)
     if y is None:
         y = torch.empty_like(x)
     dm = dims(Bt, Dm, 1, N, io)
-    rc = lib.ssm_state_update(ctypes.byref(dm), _p(state), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D),
-                              _p(z), _p(y), _stream_ptr(stream))
+    if discretization != "euler":
+        rc = lib.ssm_state_update_disc(ctypes.byref(dm), _p(state), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D),
+                                       _p(z), _DISC[discretization], _p(y), _stream_ptr(stream))
+    else:
+        rc = lib.ssm_state_update(ctypes.byref(dm), _p(state), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D),
+                                  _p(z), _p(y), _stream_ptr(stream))
     if rc != SSM_OK:
         raise SsmError(rc, "ssm_state_update")
     return y

@@ -22,22 +22,24 @@ def to_dev(inp, dev="cuda"):
     return out
 
 
-def gpu_scan(inp, stream=None, workspace=None):
+def gpu_scan(inp, stream=None, workspace=None, discretization="euler"):
     g = to_dev(inp)
     y, h = ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
                                   delta_bias=g["delta_bias"], delta_softplus=g["delta_softplus"],
-                                  return_last_state=True, stream=stream, workspace=workspace)
+                                  return_last_state=True, stream=stream, workspace=workspace,
+                                  discretization=discretization)
     torch.cuda.synchronize()
     return y, h
 
 
-def oracle_scan(inp, channels=None, nthreads=8):
+def oracle_scan(inp, channels=None, nthreads=8, zoh=False):
     """Oracle on all channels, or on a list of (b, d) pairs (then packed [nch, ...])."""
     f = gen.as_f64
     if channels is None:
         return oracle.selective_scan(f(inp["u"]), f(inp["delta"]), f(inp["A"]), f(inp["B"]), f(inp["C"]),
                                      D=f(inp["D"]), z=f(inp["z"]), delta_bias=f(inp["delta_bias"]),
-                                     delta_softplus=inp["delta_softplus"], with_mag=True, nthreads=nthreads)
+                                     delta_softplus=inp["delta_softplus"], with_mag=True, nthreads=nthreads,
+                                     zoh=zoh)
     ch = np.asarray(channels, dtype=np.int64).reshape(-1, 2)
     bs, ds = ch[:, 0], ch[:, 1]
 
@@ -51,13 +53,13 @@ def oracle_scan(inp, channels=None, nthreads=8):
     bias = None if inp["delta_bias"] is None else f(inp["delta_bias"])[ds]
     return oracle.scan_rows(rows(inp["u"]), rows(inp["delta"]), A, f(inp["B"]), f(inp["C"]), bs, D=D,
                             z=rows(inp["z"]), delta_bias=bias, delta_softplus=inp["delta_softplus"],
-                            with_mag=True, nthreads=nthreads)
+                            with_mag=True, nthreads=nthreads, zoh=zoh)
 
 
-def compare_scan(inp, y_gpu, h_gpu, channels=None, tol=None, nthreads=8):
+def compare_scan(inp, y_gpu, h_gpu, channels=None, tol=None, nthreads=8, zoh=False):
     io = inp["cfg"].io
     tol = TOL[io] if tol is None else tol
-    yo, ho, ym, hm = oracle_scan(inp, channels, nthreads)
+    yo, ho, ym, hm = oracle_scan(inp, channels, nthreads, zoh=zoh)
     if channels is None:
         yg = y_gpu.float().cpu().double().numpy()
         hg = h_gpu.cpu().double().numpy()

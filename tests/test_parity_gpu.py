@@ -101,6 +101,77 @@ def test_pair_kernel_shapes(Bt, D, L, N, io, gate, dskip, ks, chunks, monkeypatc
     compare_scan(inp, y, h)
 
 
+# ---- exact zero-order hold (jsqmd.com section 2.3), on the channel-pair kernel ----------
+ZOH_CASES = [
+    # Bt, D, L, N, io, gate, dskip, forced chunks (0 = planner)
+    (1, 4, 64, 4, "f32", False, "ones", 0),
+    (2, 37, 1000, 16, "f32", True, "normal", 0),
+    (3, 20, 520, 32, "f32", True, "ones", 3),
+    (1, 40, 2000, 64, "bf16", False, "ones", 5),
+    (2, 33, 136, 128, "bf16", True, "normal", 0),
+]
+
+
+def _zoh_inputs(cfg):
+    inp = gen.scan_inputs(cfg)
+    # a zero and a tiny A column: the polynomial branch of (e^x - 1)/x and the A -> 0 limit
+    inp["A"][:, 0] = 0.0
+    if inp["A"].shape[1] > 1:
+        inp["A"][:, 1] = -1e-4
+    return inp
+
+
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,chunks", ZOH_CASES)
+def test_zoh_shapes(Bt, D, L, N, io, gate, dskip, chunks, monkeypatch):
+    if chunks:
+        monkeypatch.setenv("SSM_PAIR_CHUNKS", str(chunks))
+    cfg = gen.ScanConfig("zoh", Bt, D, L, N, io=io, gate=gate, dskip=dskip, seed=7 * L + N)
+    inp = _zoh_inputs(cfg)
+    y, h = gpu_scan(inp, discretization="zoh")
+    compare_scan(inp, y, h, zoh=True)
+    # the flag matters: Euler differs from the ZOH oracle on these inputs
+    ye, he = gpu_scan(inp)
+    with pytest.raises(AssertionError):
+        compare_scan(inp, ye, he, zoh=True)
+
+
+def test_zoh_long128k_sampled():
+    inp = gen.scan_inputs(gen.LONG128K)
+    y, h = gpu_scan(inp, discretization="zoh")
+    compare_scan(inp, y, h, channels=sample_channels(1, 1536, 8, seed=5), zoh=True)
+
+
+def test_zoh_ragged_rows_unsupported():
+    cfg = gen.ScanConfig("zr", 1, 8, 1001, 16, io="bf16", seed=3)
+    g = to_dev(gen.scan_inputs(cfg))
+    with pytest.raises(ssm.SsmError) as ei:
+        ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], discretization="zoh")
+    assert ei.value.code == ssm.SSM_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("N,io", [(16, "bf16"), (64, "bf16"), (5, "f32")])
+def test_zoh_decode(N, io):
+    inp = gen.decode_inputs(gen.DECODE, Bt=3, D=50, N=N, gate=True, dskip="ones", steps=7)
+    inp["A"][:, 0] = 0.0
+    if io == "f32":
+        for k in ("x", "dt", "B", "C", "z"):
+            inp[k] = inp[k].float()
+    g = to_dev(inp)
+    st = g["state0"].clone()
+    ys = [ssm.state_update(st, g["x"][s], g["dt"][s], g["A"], g["B"][s], g["C"][s], D=g["D"], z=g["z"][s],
+                           discretization="zoh") for s in range(7)]
+    torch.cuda.synchronize()
+    f = gen.as_f64
+    so = f(inp["state0"])
+    sm = np.abs(so)
+    for s in range(7):
+        yo, so, ym, sm = oracle.state_update(so, f(inp["x"][s]), f(inp["dt"][s]), f(inp["A"]), f(inp["B"][s]),
+                                             f(inp["C"][s]), D=f(inp["D"]), z=f(inp["z"][s]), smag=sm,
+                                             with_mag=True, zoh=True)
+        assert oracle.rel_err(ys[s].float().cpu().numpy(), yo, ym) <= TOL[io]
+    assert oracle.rel_err(st.cpu().numpy(), so, sm) <= TOL[io]
+
+
 @pytest.mark.parametrize("plan", ["16,4,5", "16,4,1", "4,4,3", "16,8,2", "8,1,7"])
 def test_forced_plans(plan, monkeypatch):
     N = {"16,4,5": 64, "16,4,1": 64, "4,4,3": 16, "16,8,2": 128, "8,1,7": 8}[plan]
