@@ -49,6 +49,8 @@ def _bind(lib):
     lib.oracle_state_update.argtypes = [
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _dp, _dp,
         _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
+    lib.oracle_conv_silu.restype = ctypes.c_int
+    lib.oracle_conv_silu.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _dp, _dp, _dp, _dp]
     lib.oracle_scan_channels_disc.restype = ctypes.c_int
     lib.oracle_scan_channels_disc.argtypes = [
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -182,3 +184,20 @@ def rel_err(got, ref, mag):
     if not np.all(np.isfinite(got)):
         return float("inf")
     return float(e.max())
+
+
+def conv_silu(x, w, cb=None, lib=None):
+    """Causal depthwise conv + bias + SiLU in front of the scan: x [..., L] rows with
+    w [..., K] and cb [...] per row (leading dims flattened alike). Returns u like x."""
+    lib = lib or load()
+    x = np.asarray(x, dtype=np.float64)
+    shp = x.shape
+    L = shp[-1]
+    xr = np.ascontiguousarray(x.reshape(-1, L))
+    wr = np.ascontiguousarray(np.asarray(w, dtype=np.float64).reshape(xr.shape[0], -1))
+    cr = None if cb is None else np.ascontiguousarray(np.asarray(cb, dtype=np.float64).reshape(-1))
+    u = np.zeros_like(xr)
+    rc = lib.oracle_conv_silu(xr.shape[0], L, wr.shape[1], _ptr(xr), _ptr(wr), _ptr(cr), _ptr(u))
+    if rc != 0:
+        raise RuntimeError(f"oracle_conv_silu failed ({rc})")
+    return u.reshape(shp)

@@ -246,3 +246,29 @@ int oracle_state_update(int64_t Bt, int64_t D, int64_t N, double *state, double 
                         const double *z, double *y, double *ymag) {
     return oracle_state_update_disc(Bt, D, N, state, smag, x, dt, A, B, C, Dskip, z, 0, y, ymag);
 }
+
+/*
+ * The conv-to-gate span in front of the scan (lmnt.cn "From RNN to Mamba", sections 3.1-3.2:
+ * nn.Conv1d(d_inner, d_inner, kernel_size=d_conv, groups=d_inner, padding=d_conv-1), the
+ * output cut to the first L steps, then SiLU), per channel:
+ *     u[t] = SiLU(bias + sum_{k<K} w[k] * x[t - (K-1) + k]),   x[t < 0] = 0
+ * i.e. a causal depthwise correlation. Layouts: x, u [nchan][L]; w [nchan][K]; cb [nchan]
+ * (NULL = no bias). Returns 0, or nonzero on bad arguments.
+ */
+int oracle_conv_silu(int64_t nchan, int64_t L, int64_t K, const double *x, const double *w,
+                     const double *cb, double *u) {
+    if (nchan < 0 || L < 0 || K < 1) return 1;
+    if (nchan == 0 || L == 0) return 0;
+    if (!x || !w || !u) return 1;
+    for (int64_t c = 0; c < nchan; ++c) {
+        for (int64_t t = 0; t < L; ++t) {
+            double acc = cb ? cb[c] : 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const int64_t s = t - (K - 1) + k;
+                if (s >= 0) acc += w[c * K + k] * x[c * L + s];
+            }
+            u[c * L + t] = silu(acc);
+        }
+    }
+    return 0;
+}

@@ -360,7 +360,43 @@ def pin_zoh_decode_equals_scan(lib):
     _close(st, hr, 1e-13, 1e-14, "ZOH decode vs scan state")
 
 
-ALL_PINS = [pin_zoh_step_response, pin_zoh_piecewise_ode, pin_zoh_small_step_limit,
+# ---- conv-to-gate span (lmnt.cn sections 3.1-3.2: depthwise Conv1d, padding d_conv-1,
+# output cut to L, then SiLU) --------------------------------------------------------------
+def _silu(v):
+    return v / (1.0 + np.exp(-v))
+
+
+# The causal correlation equals numpy's full convolution with the reversed kernel, cut to L.
+def pin_conv_numpy(lib):
+    rng = _rng(31)
+    nch, L = 4, 37
+    for K in (1, 2, 4):
+        x = rng.standard_normal((nch, L))
+        w = rng.standard_normal((nch, K))
+        cb = rng.standard_normal(nch)
+        u = oracle.conv_silu(x, w, cb, lib=lib)
+        ref = np.stack([np.convolve(x[c], w[c][::-1])[:L] + cb[c] for c in range(nch)])
+        _close(u, _silu(ref), 1e-13, 1e-15, f"conv K={K} vs numpy")
+
+
+# The page's module itself: torch Conv1d(groups=D, padding=K-1) in fp64, cut to L, SiLU.
+def pin_conv_torch_module(lib):
+    import torch
+    rng = _rng(32)
+    Dm, L, K = 6, 29, 4
+    x = rng.standard_normal((2, Dm, L))
+    conv = torch.nn.Conv1d(Dm, Dm, kernel_size=K, groups=Dm, padding=K - 1, dtype=torch.float64)
+    with torch.no_grad():
+        conv.weight.copy_(torch.from_numpy(rng.standard_normal((Dm, 1, K))))
+        conv.bias.copy_(torch.from_numpy(rng.standard_normal(Dm)))
+        ref = torch.nn.functional.silu(conv(torch.from_numpy(x))[:, :, :L]).numpy()
+    w = conv.weight.detach().numpy()[:, 0, :]
+    cb = conv.bias.detach().numpy()
+    u = oracle.conv_silu(x, np.broadcast_to(w, (2, Dm, K)), np.broadcast_to(cb, (2, Dm)), lib=lib)
+    _close(u, ref, 1e-13, 1e-15, "conv vs torch Conv1d module")
+
+
+ALL_PINS = [pin_conv_numpy, pin_conv_torch_module, pin_zoh_step_response, pin_zoh_piecewise_ode, pin_zoh_small_step_limit,
             pin_zoh_decode_equals_scan, pin_lti_convolution, pin_tiny_step, pin_prefix_sum, pin_softplus, pin_gate,
             pin_split_resume, pin_tree_bruteforce, pin_linear_causal, pin_hand_case,
             pin_decode_equals_scan, pin_magnitude]

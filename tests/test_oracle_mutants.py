@@ -40,6 +40,10 @@ MUTANTS = [
     ("zoh_factor_exp_not_expm1", [("return x == 0.0 ? 1.0 : expm1(x) / x;", "return x == 0.0 ? 1.0 : exp(x) / x;")]),
     ("zoh_factor_missing_divide", [("return x == 0.0 ? 1.0 : expm1(x) / x;", "return x == 0.0 ? 1.0 : expm1(x);")]),
     ("zoh_ignored_in_scan", [("if (zoh) B_bar *= zoh_factor(dt * A[n]);", "(void)zoh;")]),
+    ("conv_kernel_reversed", [("if (s >= 0) acc += w[c * K + k] * x[c * L + s];",
+                               "if (s >= 0) acc += w[c * K + (K - 1 - k)] * x[c * L + s];")]),
+    ("conv_padding_off_by_one", [("const int64_t s = t - (K - 1) + k;", "const int64_t s = t - K + k;")]),
+    ("conv_bias_dropped", [("double acc = cb ? cb[c] : 0.0;", "double acc = 0.0;")]),
     ("zoh_ignored_in_decode", [("if (zoh) B_bar *= zoh_factor(dt[bd] * A[d * N + n]);", "(void)zoh;")]),
 ]
 
