@@ -76,6 +76,7 @@ def parse():
                     help="override the workload's sequence length (profiling of a smaller case)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-zoh", action="store_true")
+    ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -317,6 +318,32 @@ def bench_ours(args, rank, ws, local):
         out["zoh"] = {"discretization": "exact zero-order hold (exp(dt*A) - 1)/A * B",
                       "ms_per_step": zms, "value": weak_scaling_value(elems, ws, zms / 1e3), "unit": "elem/s",
                       "roofline_frac": elems / (zms / 1e3) / 1e9 / ex2_peak}
+        out["gpu_launches"] += args.steps * launches_per_step
+    # the conv1d (K = 4) + SiLU front fused in the scan, on the same workload, timed the same way
+    if not args.no_conv:
+        gw = torch.Generator().manual_seed(11)
+        cw = (torch.randn(cfg.D, 4, generator=gw) * 0.5).to(dev)
+        cbias = (torch.randn(cfg.D, generator=gw) * 0.2).to(dev)
+
+        def cstep():
+            ssm.conv_selective_scan_fwd(g["u"], cw, cbias, g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                                        delta_bias=g["delta_bias"], delta_softplus=cfg.softplus, y=y,
+                                        last_state=last, stream=stream)
+        for _ in range(args.warmup):
+            cstep()
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        c0.record(stream)
+        for _ in range(args.steps):
+            cstep()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        cms = max_over_ranks(c0.elapsed_time(c1), ws) / args.steps
+        assert ssm.stream_status(stream) == ssm.SSM_OK
+        out["conv_front"] = {"fused": "causal depthwise conv1d (K=4) + bias + SiLU in front of the scan",
+                             "ms_per_step": cms, "value": weak_scaling_value(elems, ws, cms / 1e3), "unit": "elem/s",
+                             "roofline_frac": elems / (cms / 1e3) / 1e9 / ex2_peak}
         out["gpu_launches"] += args.steps * launches_per_step
     # end to end: host buffers through the C ABI, copies inside the timed region
     if not args.no_e2e:

@@ -17,7 +17,8 @@
  * ssm_state_update.
  *
  * Readings the library fixes where the pages are silent:
- *   - B_bar*u = dt*B*u (the page's code), not the exact zero-order hold (A_bar-1)/A*B.
+ *   - B_bar*u = dt*B*u (the page's code); the exact zero-order hold (A_bar-1)/A*B is
+ *     available through ssm_selective_scan_fwd_disc / ssm_state_update_disc.
  *   - softplus(v) = v for v > 20, else log(1 + exp(v)) (beta = 1).
  *   - y at t uses the state after the update at t.
  *   - B and C are shared by all channels of a batch row: [batch][dstate][seqlen].
@@ -212,6 +213,34 @@ ssm_status_t ssm_state_update_disc(const ssm_dims_t *dims, float *state, const v
                                    const void *dt, const float *A, const void *B,
                                    const void *C, const float *D, const void *z,
                                    int discretization, void *y, void *stream);
+
+/*
+ * The conv-to-gate span of the Mamba block fused in front of the scan (lmnt.cn "From RNN to
+ * Mamba", sections 3.1-3.2: a depthwise Conv1d with kernel size K and padding K-1, its
+ * output cut to the first seqlen steps, then SiLU), per channel:
+ *     u[b,d,t] = SiLU(conv_b[d] + sum_{k<K} conv_w[d][k] * x[b,d,t-(K-1)+k]),  x[t < 0] = 0
+ * and then exactly ssm_selective_scan_fwd with this u (also in the D skip term). u is formed
+ * tile by tile in shared memory and never written to HBM.
+ *   x           device, [batch][dim][seqlen] io dtype: the input of the convolution.
+ *   conv_w      device, [dim][conv_width] fp32 (the Conv1d weight [dim][1][K] squeezed).
+ *   conv_b      device, [dim] fp32, or NULL for no conv bias.
+ *   conv_width  K, 1..4 (SSM_ERR_UNSUPPORTED otherwise).
+ *   workspace   NULL (stream-ordered allocation by the library) or a caller buffer of at
+ *               least ssm_conv_selective_scan_workspace_bytes(dims) bytes.
+ * Runs on the channel-pair kernel: rows whose byte length is not a multiple of 16 return
+ * SSM_ERR_UNSUPPORTED. Other arguments, layouts and errors: as ssm_selective_scan_fwd.
+ */
+ssm_status_t ssm_conv_selective_scan_fwd(const ssm_dims_t *dims, const void *x,
+                                         const float *conv_w, const float *conv_b,
+                                         int conv_width, const void *delta, const float *A,
+                                         const void *B, const void *C, const float *D,
+                                         const void *z, const float *delta_bias,
+                                         int delta_softplus, void *y, float *last_state,
+                                         void *workspace, size_t workspace_bytes,
+                                         void *stream);
+
+/* Bytes of device workspace ssm_conv_selective_scan_fwd needs for `dims` (0 if none). */
+size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims);
 
 /*
  * Host-buffer scan: the same computation as ssm_selective_scan_fwd, with every array in

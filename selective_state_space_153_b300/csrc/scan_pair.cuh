@@ -39,7 +39,7 @@
 
 namespace ssm {
 
-template <typename IO, int KS, int GP, int WARPS, int T>
+template <typename IO, int KS, int GP, int WARPS, int T, bool CONV = false>
 struct PairCfg {
     static constexpr int kThreads = WARPS * 32;
     static constexpr int kPairsW = 32 / GP;            // pairs per warp
@@ -58,7 +58,13 @@ struct PairCfg {
     static constexpr size_t kOffBc = kOffDx + 2 * kDxBytes;
     static constexpr size_t kOffYs = kOffBc + 2 * kBcBytes;
     static constexpr size_t kOffBias = kOffYs + 2 * kYsBytes;
-    static constexpr size_t kSmem = kOffBias + (size_t)kCh * sizeof(float);
+    // conv front: the conv + SiLU output u [2][kCh][T] fp32, the right-aligned taps [kCh][4],
+    // the conv bias [kCh] and the chunk's first-tile halo [kCh][4] (three steps used)
+    static constexpr size_t kOffSu = kOffBias + (size_t)kCh * sizeof(float);
+    static constexpr size_t kSuBytes = CONV ? (size_t)2 * kCh * T * sizeof(float) : 0;
+    static constexpr size_t kOffCw = kOffSu + kSuBytes;
+    static constexpr size_t kCwBytes = CONV ? (size_t)kCh * 9 * sizeof(float) : 0;
+    static constexpr size_t kSmem = kOffCw + kCwBytes;
     static_assert(KS == 4 || KS == 8, "states per lane per channel: 4 or 8");
     static_assert(GP == 1 || GP == 2 || GP == 4 || GP == 8 || GP == 16, "lanes per pair");
     static_assert(T % 8 == 0 && T % GP == 0 && T % kEpr == 0, "tile: whole 16-byte pieces and reduce groups");
@@ -104,10 +110,10 @@ __device__ __forceinline__ float2 zoh_phi2(float2 xl2, float2 a, float inv_dt, f
     return make_float2(fabsf(x.x) < 0.125f ? poly.x : big.x, fabsf(x.y) < 0.125f ? poly.y : big.y);
 }
 
-template <typename IO, int KS, int GP, int WARPS, int T, bool AGG, bool ZOH = false>
+template <typename IO, int KS, int GP, int WARPS, int T, bool AGG, bool ZOH = false, bool CONV = false>
 __global__ void __launch_bounds__(WARPS * 32)
 scan_pair_kernel(const SeqParams p) {
-    using Cfg = PairCfg<IO, KS, GP, WARPS, T>;
+    using Cfg = PairCfg<IO, KS, GP, WARPS, T, CONV>;
     constexpr int kCh = Cfg::kCh, kPairs = Cfg::kPairs, kQN = Cfg::kQN, kNP = Cfg::kNP, kRS = Cfg::kRS;
     constexpr int kEpr = Cfg::kEpr, kPieces = T / kEpr;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -115,6 +121,10 @@ scan_pair_kernel(const SeqParams p) {
     float *sBC0 = reinterpret_cast<float *>(smem + Cfg::kOffBc);     // [T][2*kNP]  B | C
     IO *sYS0 = reinterpret_cast<IO *>(smem + Cfg::kOffYs);           // [kCh][kRS]  y tile, io type
     float *sBias = reinterpret_cast<float *>(smem + Cfg::kOffBias);  // [kCh]
+    float *sSu0 = reinterpret_cast<float *>(smem + Cfg::kOffSu);     // conv front: [2][kCh][T] u
+    float *sCw = reinterpret_cast<float *>(smem + Cfg::kOffCw);      // conv front: [kCh][4] taps
+    float *sCb = sCw + 4 * kCh;                                      // [kCh] conv bias
+    float *sHalo = sCb + kCh;                                        // [kCh][4] steps before the chunk
     auto raw_of = [&](int j) { return reinterpret_cast<IO *>(smem + (size_t)(j % 3) * Cfg::kRawBytes); };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -228,6 +238,29 @@ scan_pair_kernel(const SeqParams p) {
             float uu[kSI], dl[kSI];
             load_steps<kSI>(raw + (size_t)cc * kRS + tq, uu);
             load_steps<kSI>(raw + (size_t)(kCh + cc) * kRS + tq, dl);
+            if constexpr (CONV) {
+                // u = SiLU(bias + sum_k w[k] x[t-3+k]) over the window x[tq-3 .. tq+kSI-1]; the
+                // three steps before the tile come from this tile's row, the previous tile's
+                // raw row (still resident) or, for the chunk's first tile, the halo
+                float xw[kSI + 3];
+#pragma unroll
+                for (int e = 0; e < kSI; ++e) xw[3 + e] = uu[e];
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    if (tq > 0) xw[i] = io_traits<IO>::to_f(raw[(size_t)cc * kRS + tq - 3 + i]);
+                    else if (j > 0) xw[i] = io_traits<IO>::to_f(raw_of(j - 1)[(size_t)cc * kRS + T - 3 + i]);
+                    else xw[i] = sHalo[cc * 4 + i];
+                }
+                float *su = sSu0 + (size_t)(j & 1) * kCh * T + (size_t)cc * T + tq;
+#pragma unroll
+                for (int e = 0; e < kSI; ++e) {
+                    float acc = sCb[cc];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc = fmaf(sCw[cc * 4 + k], xw[e + k], acc);
+                    uu[e] = silu_f(acc);
+                    su[e] = uu[e];
+                }
+            }
             const bool ok = d0 + cc < p.Dm;
             const float bb = sBias[cc];
             float2 *dst = reinterpret_cast<float2 *>(sDX) + (size_t)tq * kPairs * 2 + cc;
@@ -281,6 +314,20 @@ scan_pair_kernel(const SeqParams p) {
 
     for (int i = tid; i < kCh; i += Cfg::kThreads)
         sBias[i] = (p.bias != nullptr && d0 + i < p.Dm) ? p.bias[d0 + i] : 0.0f;
+    if constexpr (CONV) {
+        for (int i = tid; i < kCh; i += Cfg::kThreads) {
+            const bool okc = d0 + i < p.Dm;
+            for (int k = 0; k < 4; ++k) {   // taps right-aligned: the last tap meets x[t]
+                const int kk = k - (4 - p.conv_k);
+                sCw[i * 4 + k] = (okc && kk >= 0) ? p.conv_w[(d0 + i) * p.conv_k + kk] : 0.0f;
+            }
+            sCb[i] = (okc && p.conv_b != nullptr) ? p.conv_b[d0 + i] : 0.0f;
+            for (int k = 0; k < 3; ++k) {
+                const int64_t s = l_begin - 3 + k;
+                sHalo[i * 4 + k] = (okc && s >= 0) ? io_traits<IO>::to_f(gU[(b * p.Dm + d0 + i) * p.L + s]) : 0.0f;
+            }
+        }
+    }
     if (ntiles > 0) {
         issue_tile(0);
         cp_async_wait<0>();
@@ -352,7 +399,9 @@ scan_pair_kernel(const SeqParams p) {
                 for (int ch = 0; ch < 2; ++ch) {
                     const float ysum = group_reduce_transpose<GP>(yp[ch], lane);
                     const int cc = c0 + ch;
-                    float yv = fmaf(Dd[ch], io_traits<IO>::to_f(raw[(size_t)cc * kRS + t]), ysum);
+                    const float uv = CONV ? sSu0[(size_t)(j & 1) * kCh * T + (size_t)cc * T + t]
+                                          : io_traits<IO>::to_f(raw[(size_t)cc * kRS + t]);
+                    float yv = fmaf(Dd[ch], uv, ysum);
                     if (has_z) yv *= silu_f(io_traits<IO>::to_f(raw[(size_t)(2 * kCh + cc) * kRS + t]));
                     store_io(ys + (size_t)cc * kRS + t, yv);
                 }

@@ -47,6 +47,9 @@ struct SeqParams {
     const float *hin;   // [nchunks][Bt*Dm][Npad] or null (FULL reads)
     int npad;           // NPER*G of the launched kernel
     int zoh;            // channel-pair kernel only: zero-order-hold B_bar (set by the host)
+    const float *conv_w;   // channel-pair kernel with the conv front: [Dm][conv_k] fp32
+    const float *conv_b;   // [Dm] fp32 or null
+    int conv_k;            // 1..4
 };
 
 template <typename IO, int NPER, int G, int WARPS, int T>

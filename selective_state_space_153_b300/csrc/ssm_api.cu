@@ -387,10 +387,10 @@ int pair_gp(int64_t N, int ks) {
     return gp;
 }
 
-template <typename IO, int KS, int GP, bool AGG, bool ZOH>
+template <typename IO, int KS, int GP, bool AGG, bool ZOH, bool CONV = false>
 cudaError_t launch_pair_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
-    using Cfg = PairCfg<IO, KS, GP, pair_warps(GP), kPairT>;
-    auto k = scan_pair_kernel<IO, KS, GP, pair_warps(GP), kPairT, AGG, ZOH>;
+    using Cfg = PairCfg<IO, KS, GP, pair_warps(GP), kPairT, CONV>;
+    auto k = scan_pair_kernel<IO, KS, GP, pair_warps(GP), kPairT, AGG, ZOH, CONV>;
     static unsigned long long attr_set = 0;  // per instantiation: bit i = set on device i
     int dev = 0;
     cudaGetDevice(&dev);
@@ -406,6 +406,9 @@ cudaError_t launch_pair_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
 
 template <typename IO, int KS, int GP>
 cudaError_t launch_pair_g(const SeqParams &prm, bool agg, int grid_y, cudaStream_t s) {
+    if (prm.conv_w != nullptr)   // conv front (Euler discretisation)
+        return agg ? launch_pair_t<IO, KS, GP, true, false, true>(prm, grid_y, s)
+                   : launch_pair_t<IO, KS, GP, false, false, true>(prm, grid_y, s);
     if (prm.zoh)
         return agg ? launch_pair_t<IO, KS, GP, true, true>(prm, grid_y, s)
                    : launch_pair_t<IO, KS, GP, false, true>(prm, grid_y, s);
@@ -425,10 +428,12 @@ cudaError_t launch_pair(const PairPlan &pl, const SeqParams &prm, bool agg, int 
     }
 }
 
-size_t pair_smem(ssm_dtype_t io, int ks, int gp) {
+size_t pair_smem(ssm_dtype_t io, int ks, int gp, bool conv) {
     switch (ks * 100 + gp) {
 #define SSM_PAIR_SMEM(KS, GP) \
     case KS * 100 + GP: \
+        if (conv) return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(GP), kPairT, true>::kSmem \
+                                        : PairCfg<float, KS, GP, pair_warps(GP), kPairT, true>::kSmem; \
         return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(GP), kPairT>::kSmem \
                               : PairCfg<float, KS, GP, pair_warps(GP), kPairT>::kSmem;
         SSM_PAIR_CASES(SSM_PAIR_SMEM)
@@ -437,7 +442,7 @@ size_t pair_smem(ssm_dtype_t io, int ks, int gp) {
     }
 }
 
-PairPlan plan_pair(const ssm_dims_t &d) {
+PairPlan plan_pair(const ssm_dims_t &d, bool conv = false) {
     PairPlan p;
     if (env_is("SSM_KERNEL", "seq") || env_is("SSM_KERNEL", "tc") || env_is("SSM_KERNEL", "tp")) return p;
     const size_t esz = io_size(d.io_dtype);
@@ -451,7 +456,7 @@ PairPlan plan_pair(const ssm_dims_t &d) {
     if (env_is("SSM_PAIR_KS", "4") && N <= 16) { p.ks = 4; p.gp = pair_gp(N, 4); }   // experiments, tests
     if (env_is("SSM_PAIR_KS", "8")) { p.ks = 8; p.gp = pair_gp(N, 8); }
     p.np = p.ks * p.gp;
-    p.smem = pair_smem(d.io_dtype, p.ks, p.gp);
+    p.smem = pair_smem(d.io_dtype, p.ks, p.gp, conv);
     if (p.smem == 0) return p;
     const int64_t warps = pair_warps(p.gp), kch = warps * 64 / p.gp;
     p.chan_blocks = (int)((d.dim + kch - 1) / kch);
@@ -487,7 +492,8 @@ size_t pair_workspace_bytes(const ssm_dims_t &d, const PairPlan &p) {
 ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *u, const void *delta, const float *A,
                            const void *B, const void *C, const float *D, const void *z, const float *delta_bias,
                            int delta_softplus, void *y, float *last_state, void *workspace, size_t ws_bytes,
-                           bool own_ws, cudaStream_t s, int zoh) {
+                           bool own_ws, cudaStream_t s, int zoh, const float *conv_w = nullptr,
+                           const float *conv_b = nullptr, int conv_k = 0) {
     const size_t need = pair_workspace_bytes(d, pl);
     bool allocated = false;
     if (need > 0) {
@@ -508,6 +514,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
     prm.chan_blocks = pl.chan_blocks;
     prm.npad = pl.np;
     prm.zoh = zoh ? 1 : 0;
+    prm.conv_w = conv_w; prm.conv_b = conv_b; prm.conv_k = conv_k;
     cudaError_t e = cudaSuccess;
     const bool bf = d.io_dtype == SSM_BF16;
     if (pl.nchunks > 1) {
@@ -792,6 +799,35 @@ ssm_status_t ssm_selective_scan_fwd_disc(const ssm_dims_t *dims, const void *u, 
     return run_scan(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
                     workspace_bytes, workspace == nullptr, static_cast<cudaStream_t>(stream),
                     discretization == SSM_DISC_ZOH);
+}
+
+ssm_status_t ssm_conv_selective_scan_fwd(const ssm_dims_t *dims, const void *x, const float *conv_w,
+                                         const float *conv_b, int conv_width, const void *delta, const float *A,
+                                         const void *B, const void *C, const float *D, const void *z,
+                                         const float *delta_bias, int delta_softplus, void *y, float *last_state,
+                                         void *workspace, size_t workspace_bytes, void *stream) {
+    ssm_status_t st = scan_checks(dims, x, delta, A, B, C, D, z, delta_bias, y, last_state);
+    if (st != SSM_OK) return st;
+    if (conv_width < 1 || conv_width > 4) return SSM_ERR_UNSUPPORTED;
+    if (conv_b != nullptr && !aligned_to(conv_b, 4)) return SSM_ERR_ALIGN;
+    if (workspace != nullptr && !aligned16(workspace)) return SSM_ERR_ALIGN;
+    const ssm_dims_t d = *dims;
+    if (d.batch == 0 || d.dim == 0 || d.seqlen == 0)
+        return run_scan(dims, x, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
+                        workspace_bytes, workspace == nullptr, static_cast<cudaStream_t>(stream));
+    if (conv_w == nullptr) return SSM_ERR_NULL;
+    if (!aligned_to(conv_w, 4)) return SSM_ERR_ALIGN;
+    const PairPlan pp = plan_pair(d, true);
+    if (!pp.use) return SSM_ERR_UNSUPPORTED;   // the conv front runs on the channel-pair kernel only
+    return run_scan_pair(d, pp, x, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
+                         workspace_bytes, workspace == nullptr, static_cast<cudaStream_t>(stream), 0, conv_w, conv_b,
+                         conv_width);
+}
+
+size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
+    if (check_dims(dims, true) != SSM_OK) return 0;
+    if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
+    return pair_workspace_bytes(*dims, plan_pair(*dims, true));
 }
 
 ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, const void *delta,

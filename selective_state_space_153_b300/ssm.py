@@ -28,7 +28,8 @@ SCRATCH_MAX_BYTES = 16 * 1024 * 1024   # SSM_SCRATCH_MAX_BYTES: the no-alloc ent
 EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_workspace_bytes",
            "ssm_selective_scan_fwd_ws", "ssm_state_update", "ssm_selective_scan_fwd_host",
            "ssm_stream_status", "ssm_status_string", "ssm_version",
-           "ssm_selective_scan_fwd_noalloc", "ssm_selective_scan_fwd_disc", "ssm_state_update_disc")
+           "ssm_selective_scan_fwd_noalloc", "ssm_selective_scan_fwd_disc", "ssm_state_update_disc",
+           "ssm_conv_selective_scan_fwd", "ssm_conv_selective_scan_workspace_bytes")
 
 
 class SsmDims(ctypes.Structure):
@@ -66,6 +67,10 @@ def load(path: str = LIB_PATH):
     lib.ssm_selective_scan_fwd_disc.restype = ctypes.c_int
     lib.ssm_state_update_disc.argtypes = [dp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp]
     lib.ssm_state_update_disc.restype = ctypes.c_int
+    lib.ssm_conv_selective_scan_fwd.argtypes = [dp, _vp, _vp, _vp, ctypes.c_int] + scan_args[2:] + [_vp, ctypes.c_size_t, _vp]
+    lib.ssm_conv_selective_scan_fwd.restype = ctypes.c_int
+    lib.ssm_conv_selective_scan_workspace_bytes.argtypes = [dp]
+    lib.ssm_conv_selective_scan_workspace_bytes.restype = ctypes.c_size_t
     lib.ssm_selective_scan_fwd_noalloc.argtypes = scan_args + [_vp]
     lib.ssm_selective_scan_fwd_noalloc.restype = ctypes.c_int
     lib.ssm_selective_scan_fwd_host.restype = ctypes.c_int
@@ -169,6 +174,32 @@ def selective_scan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=Non
         need = workspace_bytes(Bt, Dm, L, N, io)
         raise SsmError(rc, f"ssm_selective_scan_fwd_noalloc (scratch needed {need} B, "
                            f"fixed size {SCRATCH_MAX_BYTES} B)")
+    return y, last_state
+
+
+def conv_selective_scan_fwd(x, conv_w, conv_b, delta, A, B, C, D=None, z=None, delta_bias=None,
+                            delta_softplus=True, y=None, last_state=None, return_last_state=False,
+                            stream=None, workspace=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Causal depthwise conv (conv_w [D, K] fp32, K <= 4; conv_b [D] or None) + SiLU fused in
+    front of the scan, through ssm_conv_selective_scan_fwd. x: [Bt, D, L] io dtype (the conv
+    input); other tensors as selective_scan_fwd."""
+    lib = load()
+    Bt, Dm, L = x.shape
+    N = A.shape[1]
+    io = _io_code(x)
+    if y is None:
+        y = torch.empty_like(x)
+    if return_last_state and last_state is None:
+        last_state = torch.empty((Bt, Dm, N), dtype=torch.float32, device=x.device)
+    dm = dims(Bt, Dm, L, N, io)
+    ws_p = None if workspace is None else _p(workspace)
+    ws_n = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.ssm_conv_selective_scan_fwd(ctypes.byref(dm), _p(x), _p(conv_w), _p(conv_b), int(conv_w.shape[1]),
+                                         _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                                         int(bool(delta_softplus)), _p(y), _p(last_state), ws_p, ws_n,
+                                         _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SsmError(rc, "ssm_conv_selective_scan_fwd")
     return y, last_state
 
 

@@ -101,6 +101,53 @@ def test_pair_kernel_shapes(Bt, D, L, N, io, gate, dskip, ks, chunks, monkeypatc
     compare_scan(inp, y, h)
 
 
+# ---- conv1d + SiLU front fused in the scan (lmnt.cn sections 3.1-3.2) --------------------
+CONV_CASES = [
+    # Bt, D, L, N, io, gate, dskip, K, forced chunks (0 = planner)
+    (1, 4, 64, 4, "f32", False, "ones", 4, 0),
+    (2, 37, 1000, 16, "bf16", True, "normal", 4, 0),
+    (1, 50, 2000, 64, "bf16", False, "ones", 4, 5),
+    (3, 20, 520, 32, "f32", True, "ones", 3, 3),
+    (2, 33, 136, 16, "f32", True, None, 2, 4),
+    (1, 16, 96, 8, "bf16", False, "ones", 1, 2),
+]
+
+
+def _conv_case(Bt, D, L, N, io, gate, dskip, K, seed):
+    cfg = gen.ScanConfig("conv", Bt, D, L, N, io=io, gate=gate, dskip=dskip, seed=seed)
+    inp = gen.scan_inputs(cfg)
+    rng = np.random.default_rng(seed + 1)
+    w = torch.from_numpy(rng.standard_normal((D, K)).astype(np.float32) * 0.5)
+    cb = torch.from_numpy(rng.standard_normal(D).astype(np.float32) * 0.2)
+    return inp, w, cb
+
+
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,K,chunks", CONV_CASES)
+def test_conv_front_shapes(Bt, D, L, N, io, gate, dskip, K, chunks, monkeypatch):
+    if chunks:
+        monkeypatch.setenv("SSM_PAIR_CHUNKS", str(chunks))
+    inp, w, cb = _conv_case(Bt, D, L, N, io, gate, dskip, K, 13 * L + N + K)
+    g = to_dev(inp)
+    y, h = ssm.conv_selective_scan_fwd(g["u"], w.cuda(), cb.cuda(), g["delta"], g["A"], g["B"], g["C"], D=g["D"],
+                                       z=g["z"], delta_bias=g["delta_bias"], delta_softplus=True,
+                                       return_last_state=True)
+    torch.cuda.synchronize()
+    # oracle: the conv + SiLU span, then the scan on its output (same rows in double)
+    u = oracle.conv_silu(gen.as_f64(inp["u"]), np.broadcast_to(w.double().numpy(), (Bt, D, K)),
+                         np.broadcast_to(cb.double().numpy(), (Bt, D)))
+    ref = dict(inp)
+    ref["u"] = torch.from_numpy(u)
+    compare_scan(ref, y, h)
+
+
+def test_conv_front_ragged_rows_unsupported():
+    inp, w, cb = _conv_case(1, 8, 1001, 16, "bf16", False, "ones", 4, 3)
+    g = to_dev(inp)
+    with pytest.raises(ssm.SsmError) as ei:
+        ssm.conv_selective_scan_fwd(g["u"], w.cuda(), cb.cuda(), g["delta"], g["A"], g["B"], g["C"])
+    assert ei.value.code == ssm.SSM_ERR_UNSUPPORTED
+
+
 # ---- exact zero-order hold (jsqmd.com section 2.3), on the channel-pair kernel ----------
 ZOH_CASES = [
     # Bt, D, L, N, io, gate, dskip, forced chunks (0 = planner)
