@@ -396,7 +396,47 @@ def pin_conv_torch_module(lib):
     _close(u, ref, 1e-13, 1e-15, "conv vs torch Conv1d module")
 
 
-ALL_PINS = [pin_conv_numpy, pin_conv_torch_module, pin_zoh_step_response, pin_zoh_piecewise_ode, pin_zoh_small_step_limit,
+# ---- backward (gradients of the loop, by PyTorch autograd in float64) ----------------------
+# The autograd forward equals the C oracle, and every gradient equals a central finite
+# difference of the C oracle's forward (an independent derivative of the pinned loop).
+def pin_backward_finite_differences(lib):
+    import torch
+
+    from oracle import backward as bwd
+    rng = _rng(41)
+    Bt, Dm, L, N = 1, 2, 9, 3
+    ins = {"u": rng.standard_normal((Bt, Dm, L)), "delta": rng.standard_normal((Bt, Dm, L)) * 0.5,
+           "A": -rng.uniform(0.3, 2.0, (Dm, N)), "B": rng.standard_normal((Bt, N, L)),
+           "C": rng.standard_normal((Bt, N, L)), "D": rng.standard_normal(Dm),
+           "z": rng.standard_normal((Bt, Dm, L)), "delta_bias": rng.standard_normal(Dm) * 0.3}
+    dy = rng.standard_normal((Bt, Dm, L))
+    dlast = rng.standard_normal((Bt, Dm, N))
+
+    def f(x):
+        y, h = oracle.selective_scan(x["u"], x["delta"], x["A"], x["B"], x["C"], D=x["D"], z=x["z"],
+                                     delta_bias=x["delta_bias"], delta_softplus=True, lib=lib)
+        return float((y * dy).sum() + (h * dlast).sum())
+
+    tt = {k: torch.tensor(v) for k, v in ins.items()}
+    yt, ht = bwd.scan_forward_torch(tt["u"], tt["delta"], tt["A"], tt["B"], tt["C"], D=tt["D"], z=tt["z"],
+                                    delta_bias=tt["delta_bias"])
+    yo, ho = oracle.selective_scan(ins["u"], ins["delta"], ins["A"], ins["B"], ins["C"], D=ins["D"], z=ins["z"],
+                                   delta_bias=ins["delta_bias"], delta_softplus=True, lib=lib)
+    _close(yt.detach().numpy(), yo, 1e-12, 1e-13, "autograd forward vs C oracle")
+    g = bwd.scan_backward(**ins, delta_softplus=True, dy=dy, dlast=dlast)
+    eps = 1e-6
+    for k, arr in ins.items():
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            xp = {kk: vv.copy() for kk, vv in ins.items()}
+            xm = {kk: vv.copy() for kk, vv in ins.items()}
+            xp[k][idx] += eps
+            xm[k][idx] -= eps
+            fd[idx] = (f(xp) - f(xm)) / (2 * eps)
+        _close(g[k], fd, 1e-6, 1e-7, f"d/d{k}: autograd vs finite differences")
+
+
+ALL_PINS = [pin_backward_finite_differences, pin_conv_numpy, pin_conv_torch_module, pin_zoh_step_response, pin_zoh_piecewise_ode, pin_zoh_small_step_limit,
             pin_zoh_decode_equals_scan, pin_lti_convolution, pin_tiny_step, pin_prefix_sum, pin_softplus, pin_gate,
             pin_split_resume, pin_tree_bruteforce, pin_linear_causal, pin_hand_case,
             pin_decode_equals_scan, pin_magnitude]
