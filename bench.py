@@ -77,6 +77,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-zoh", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -369,6 +370,9 @@ def bench_ours(args, rank, ws, local):
                       "d2h_bytes_per_step": d2h, "ms_per_step": te / ke * 1e3,
                       "entry": "ssm_selective_scan_fwd_host (pinned host buffers)"}
         del pin, yh
+    if not args.no_bwd:
+        out["backward"] = bench_backward(dev, ws)
+        out["gpu_launches"] += out["backward"]["launches"]
     if not args.no_decode:
         out["decode"] = bench_decode(dev)
         out["gpu_launches"] += out["decode"]["launches"]
@@ -379,6 +383,47 @@ def bench_ours(args, rank, ws, local):
                                "sample": f"{nch} of {cfg.Bt * cfg.D} channels, full L={cfg.L}, N={cfg.N}, "
                                          f"fp64 sequential C, {cores} threads, {secs:.1f} s"}
     return out
+
+
+def bench_backward(dev, ws):
+    """Gradients of the scan (ssm_selective_scan_bwd) on the batch-8 workload (8 x 1536 x 2048
+    x 16, bf16, gate and bias): checkpointed forward + reverse adjoint, fp32 gradients."""
+    from selective_state_space_153_b300 import ssm
+    cfg = gen.M130
+    inp = gen.scan_inputs(cfg)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    dy = torch.randn(g["u"].shape, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).to(dev)
+    wsb = torch.empty(ssm.load().ssm_selective_scan_bwd_workspace_bytes(
+        ctypes_dims(cfg.Bt, cfg.D, cfg.L, cfg.N)), dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+
+    def step():
+        ssm.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, D=g["D"], z=g["z"],
+                               delta_bias=g["delta_bias"], delta_softplus=True, workspace=wsb, stream=s)
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    k = 5
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    e0.record(s)
+    for _ in range(k):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), ws) / k
+    elems = cfg.elements
+    return {"workload": f"backward of {cfg.name}: Bt={cfg.Bt} D={cfg.D} L={cfg.L} N={cfg.N} bf16 io, fp32 gradients",
+            "ms_per_step": ms, "value": ws * elems / (ms / 1e3), "unit": "elem/s",
+            "exps_per_element": 3,
+            "roofline_frac_of_ex2_peak": 3 * elems / (ms / 1e3) / (SM_COUNT * EX2_PER_CLK_SM * 2032.0e6),
+            "launches": 2 * k + 2 * 2}
+
+
+def ctypes_dims(Bt, Dm, L, N):
+    import ctypes
+    from selective_state_space_153_b300 import ssm
+    return ctypes.byref(ssm.dims(Bt, Dm, L, N, ssm.SSM_BF16))
 
 
 def bench_decode(dev):

@@ -243,6 +243,39 @@ ssm_status_t ssm_conv_selective_scan_fwd(const ssm_dims_t *dims, const void *x,
 size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims);
 
 /*
+ * Selective scan backward (training differentiates through the recurrence: lmnt.cn "From RNN
+ * to Mamba" section 2.2; the loop is section 3.2): gradients of
+ *     sum_{b,d,t} y[b,d,t] * dy[b,d,t]  +  sum_{b,d,n} last_state[b,d,n] * dlast_state[b,d,n]
+ * with respect to every input of ssm_selective_scan_fwd (Euler discretisation). The forward
+ * states are recomputed from checkpoints taken every 16 steps (workspace) and the adjoint
+ * recurrence lambda_t = dyhat_t C_t + exp(dt_{t+1} A) lambda_{t+1} is run backwards.
+ *   u, delta, A, B, C, D, z, delta_bias, delta_softplus: as ssm_selective_scan_fwd.
+ *   dy           device, [batch][dim][seqlen] io dtype (gradient of y).
+ *   dlast_state  device, [batch][dim][dstate] fp32 gradient of the final state, or NULL.
+ *   du, ddelta   device, [batch][dim][seqlen] fp32, written (ddelta: of the raw delta).
+ *   dA           device, [dim][dstate] fp32, written (summed over batch and time).
+ *   dB, dC       device, [batch][dstate][seqlen] fp32, written (summed over channels).
+ *   dD           device, [dim] fp32, or NULL if not wanted.
+ *   dz           device, [batch][dim][seqlen] fp32, or NULL (zeros when z is NULL).
+ *   ddelta_bias  device, [dim] fp32, or NULL if not wanted.
+ *   workspace    NULL (stream-ordered allocation by the library) or a caller buffer of at
+ *                least ssm_selective_scan_bwd_workspace_bytes(dims) bytes, 16-byte aligned.
+ * Pointers need only their element alignment. Sums over channels, batch rows and time use
+ * fp32 atomic additions, so results may differ in the last bits between runs.
+ */
+ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const void *delta,
+                                    const float *A, const void *B, const void *C,
+                                    const float *D, const void *z, const float *delta_bias,
+                                    int delta_softplus, const void *dy,
+                                    const float *dlast_state, float *du, float *ddelta,
+                                    float *dA, float *dB, float *dC, float *dD, float *dz,
+                                    float *ddelta_bias, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace ssm_selective_scan_bwd needs for `dims` (0 if none). */
+size_t ssm_selective_scan_bwd_workspace_bytes(const ssm_dims_t *dims);
+
+/*
  * Host-buffer scan: the same computation as ssm_selective_scan_fwd, with every array in
  * HOST memory (pinned memory gives the fastest copies). The call copies the inputs to the
  * device, scans, copies y (and last_state) back, and returns when the results are in the

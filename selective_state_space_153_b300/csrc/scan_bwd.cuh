@@ -1,0 +1,206 @@
+// Selective scan backward: gradients of sum(y*dy) (+ sum(h_last*dlast)) with respect to u,
+// delta, A, B, C, D, z and the dt bias, for the per-timestep loop of section 3.2 of
+// "From RNN to Mamba: state-space model principles and long-sequence modelling in practice"
+// (lmnt.cn). Training differentiates through the recurrence (section 2.2 of that page); the
+// adjoint of h_t = a_t*h_{t-1} + dt_t*u_t*B_t, y_t = (sum_n C_t*h_t + D*u_t)*SiLU(z_t) is the
+// reverse recurrence
+//     lambda_t = dyhat_t * C_t + c_t,   c_{t-1} = a_t * lambda_t,   c_{L-1} = dlast,
+// with dyhat_t = dy_t * SiLU(z_t), from which (per channel d, state n, step t)
+//     dB_t += lambda_t dt_t u_t         dC_t += dyhat_t h_t          (summed over channels)
+//     du_t  = sum_n lambda_t dt_t B_t + dyhat_t D
+//     ddt_t = sum_n lambda_t (u_t B_t + A a_t h_{t-1}),   ddelta_t = ddt_t * sigmoid(v_t)
+//     dA   += lambda_t dt_t a_t h_{t-1}   dD += dyhat_t u_t   dz_t = dy_t yhat_t SiLU'(z_t)
+// (v = delta + bias; sigmoid is the softplus derivative; without softplus ddelta = ddt).
+//
+// Work decomposition: a thread owns Q states n = g + G*q of one channel (G lanes per
+// channel, a power of two <= 32; the batch row is grid.y so a warp never spans two rows).
+// Pass 1 (scan_bwd_ckpt_kernel) runs the recurrence forward and stores h at the start of
+// every S-step segment. Pass 2 (scan_bwd_kernel) walks the segments backwards: it recomputes
+// the segment's S states into registers from the checkpoint, then runs the adjoint over the
+// segment in reverse. Sums over the states of a channel use shuffles across its G lanes; sums
+// over channels (dB, dC) are pre-reduced across the warp's channels with shuffles and then
+// added with fp32 atomics, as are dA, dD and the dt bias (summed over the sequence in the
+// thread first).
+#pragma once
+#include "common.cuh"
+
+namespace ssm {
+
+constexpr int kBwdS = 16;        // steps per checkpoint segment
+constexpr int kBwdThreads = 128;
+
+struct BwdParams {
+    const void *u, *delta, *z, *B, *C, *dy;
+    const float *A, *D, *bias, *dlast;
+    float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *dbias;
+    float *ckpt;                  // [Bt*Dm][nseg][G*Q]: h before each segment's first step
+    int64_t Bt, Dm, L, N;
+    int softplus, nseg;
+};
+
+__device__ __forceinline__ float bwd_dt(float v, int softplus) { return softplus ? softplus_f(v) : v; }
+
+// sum over the G lanes of a channel (lanes g = lane % G are consecutive)
+template <int G>
+__device__ __forceinline__ float sum_lanes(float v) {
+#pragma unroll
+    for (int o = G / 2; o >= 1; o /= 2) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+// sum over the 32/G channels of a warp (lanes with the same g)
+template <int G>
+__device__ __forceinline__ float sum_channels(float v) {
+#pragma unroll
+    for (int o = G; o < 32; o *= 2) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <typename IO, int G, int Q>
+__global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdParams p) {
+    constexpr int kCpb = kBwdThreads / G;
+    const int tid = threadIdx.x, g = tid % G;
+    const int64_t b = blockIdx.y, d = (int64_t)blockIdx.x * kCpb + tid / G;
+    if (d >= p.Dm) return;
+    const int64_t bd = b * p.Dm + d;
+    const IO *U = reinterpret_cast<const IO *>(p.u) + bd * p.L;
+    const IO *DL = reinterpret_cast<const IO *>(p.delta) + bd * p.L;
+    const IO *Bm = reinterpret_cast<const IO *>(p.B) + b * p.N * p.L;
+    const float bias = p.bias ? p.bias[d] : 0.0f;
+    float Ap[Q], h[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int n = g + G * q;
+        Ap[q] = n < p.N ? p.A[d * p.N + n] * kLog2e : 0.0f;
+        h[q] = 0.0f;
+    }
+    float *ck = p.ckpt + bd * (int64_t)p.nseg * (G * Q);
+    for (int64_t t = 0; t < p.L; ++t) {
+        if (t % kBwdS == 0) {
+#pragma unroll
+            for (int q = 0; q < Q; ++q) ck[(t / kBwdS) * (G * Q) + g + G * q] = h[q];
+        }
+        const float dt = bwd_dt(io_traits<IO>::to_f(DL[t]) + bias, p.softplus);
+        const float x = dt * io_traits<IO>::to_f(U[t]);
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const int n = g + G * q;
+            const float bn = n < p.N ? io_traits<IO>::to_f(Bm[n * p.L + t]) : 0.0f;
+            h[q] = fmaf(ex2(dt * Ap[q]), h[q], x * bn);
+        }
+    }
+}
+
+template <typename IO, int G, int Q>
+__global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p) {
+    constexpr int kCpb = kBwdThreads / G;
+    const int tid = threadIdx.x, g = tid % G;
+    const int64_t b = blockIdx.y, d = (int64_t)blockIdx.x * kCpb + tid / G;
+    const bool valid = d < p.Dm;                // invalid lanes still take part in the shuffles
+    const int64_t dd = valid ? d : 0;
+    const int64_t bd = b * p.Dm + dd;
+    const IO *U = reinterpret_cast<const IO *>(p.u) + bd * p.L;
+    const IO *DL = reinterpret_cast<const IO *>(p.delta) + bd * p.L;
+    const IO *Z = p.z ? reinterpret_cast<const IO *>(p.z) + bd * p.L : nullptr;
+    const IO *DY = reinterpret_cast<const IO *>(p.dy) + bd * p.L;
+    const IO *Bm = reinterpret_cast<const IO *>(p.B) + b * p.N * p.L;
+    const IO *Cm = reinterpret_cast<const IO *>(p.C) + b * p.N * p.L;
+    const float bias = (valid && p.bias) ? p.bias[dd] : 0.0f;
+    const float Dv = (valid && p.D) ? p.D[dd] : 0.0f;
+    float An[Q], Ap[Q], c[Q], dA[Q];
+    bool nv[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int n = g + G * q;
+        nv[q] = valid && n < p.N;
+        An[q] = nv[q] ? p.A[dd * p.N + n] : 0.0f;
+        Ap[q] = An[q] * kLog2e;
+        c[q] = (nv[q] && p.dlast) ? p.dlast[bd * p.N + n] : 0.0f;
+        dA[q] = 0.0f;
+    }
+    float dD = 0.0f, dbias = 0.0f;
+    const float *ck = p.ckpt + bd * (int64_t)p.nseg * (G * Q);
+    for (int seg = p.nseg - 1; seg >= 0; --seg) {
+        const int64_t t0 = (int64_t)seg * kBwdS;
+        float hs[Q][kBwdS + 1];                 // hs[q][0]: h before the segment; hs[q][i+1]: after step t0+i
+#pragma unroll
+        for (int q = 0; q < Q; ++q) hs[q][0] = valid ? ck[(int64_t)seg * (G * Q) + g + G * q] : 0.0f;
+#pragma unroll
+        for (int i = 0; i < kBwdS; ++i) {
+            const int64_t t = t0 + i;
+            const bool in = t < p.L;
+            const float dt = in ? bwd_dt(io_traits<IO>::to_f(DL[t]) + bias, p.softplus) : 0.0f;
+            const float x = in ? dt * io_traits<IO>::to_f(U[t]) : 0.0f;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int n = g + G * q;
+                const float bn = (in && nv[q]) ? io_traits<IO>::to_f(Bm[n * p.L + t]) : 0.0f;
+                hs[q][i + 1] = fmaf(ex2(dt * Ap[q]), hs[q][i], x * bn);
+            }
+        }
+#pragma unroll
+        for (int i = kBwdS - 1; i >= 0; --i) {
+            const int64_t t = t0 + i;
+            if (t >= p.L) continue;             // uniform across the block (same t everywhere)
+            const float v = io_traits<IO>::to_f(DL[t]) + bias;
+            const float dt = bwd_dt(v, p.softplus);
+            const float uu = io_traits<IO>::to_f(U[t]);
+            float bq[Q], cq[Q], yh = 0.0f;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int n = g + G * q;
+                bq[q] = nv[q] ? io_traits<IO>::to_f(Bm[n * p.L + t]) : 0.0f;
+                cq[q] = nv[q] ? io_traits<IO>::to_f(Cm[n * p.L + t]) : 0.0f;
+                yh = fmaf(cq[q], hs[q][i + 1], yh);
+            }
+            yh = sum_lanes<G>(yh) + Dv * uu;    // yhat_t, before the gate
+            const float dyv = valid ? io_traits<IO>::to_f(DY[t]) : 0.0f;
+            float dyh = dyv, dzv = 0.0f;
+            if (Z) {
+                const float zz = io_traits<IO>::to_f(Z[t]);
+                const float sg = 1.0f / (1.0f + ex2(-zz * kLog2e));
+                dyh = dyv * zz * sg;            // dy * SiLU(z)
+                dzv = dyv * yh * sg * (1.0f + zz * (1.0f - sg));
+            }
+            float du = 0.0f, ddt = 0.0f;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int n = g + G * q;
+                const float a = ex2(dt * Ap[q]);
+                const float lam = fmaf(dyh, cq[q], c[q]);
+                const float hp = hs[q][i];
+                du = fmaf(lam * dt, bq[q], du);
+                ddt = fmaf(lam, fmaf(uu, bq[q], An[q] * a * hp), ddt);
+                dA[q] = fmaf(lam * dt * a, hp, dA[q]);
+                c[q] = a * lam;
+                // sums over the warp's channels, then one atomic per (state, step) and warp
+                const float gb = sum_channels<G>(nv[q] ? lam * dt * uu : 0.0f);
+                const float gc = sum_channels<G>(nv[q] ? dyh * hs[q][i + 1] : 0.0f);
+                if ((threadIdx.x & 31) < G && n < p.N) {
+                    atomicAdd(p.dB + (b * p.N + n) * p.L + t, gb);
+                    atomicAdd(p.dC + (b * p.N + n) * p.L + t, gc);
+                }
+            }
+            du = sum_lanes<G>(du);
+            ddt = sum_lanes<G>(ddt);
+            if (valid && g == 0) {
+                const float sg = p.softplus ? 1.0f / (1.0f + ex2(-v * kLog2e)) : 1.0f;
+                const float ddl = ddt * sg;
+                p.du[bd * p.L + t] = fmaf(dyh, Dv, du);
+                p.ddelta[bd * p.L + t] = ddl;
+                if (p.dz) p.dz[bd * p.L + t] = dzv;
+                dD = fmaf(dyh, uu, dD);
+                dbias += ddl;
+            }
+        }
+    }
+    if (!valid) return;
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+        if (nv[q]) atomicAdd(p.dA + dd * p.N + g + G * q, dA[q]);
+    if (g == 0) {
+        if (p.dD) atomicAdd(p.dD + dd, dD);
+        if (p.dbias) atomicAdd(p.dbias + dd, dbias);
+    }
+}
+
+}  // namespace ssm

@@ -20,6 +20,7 @@
 #include "scan_tc.cuh"
 #include "scan_tp.cuh"
 #include "scan_pair.cuh"
+#include "scan_bwd.cuh"
 
 namespace {
 
@@ -828,6 +829,90 @@ size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
     return pair_workspace_bytes(*dims, plan_pair(*dims, true));
+}
+
+size_t ssm_selective_scan_bwd_workspace_bytes(const ssm_dims_t *dims) {
+    if (check_dims(dims, true) != SSM_OK) return 0;
+    if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
+    const int64_t N = dims->dstate;
+    int G = 1;
+    while (G < 32 && G < N) G *= 2;
+    const int64_t Q = (N + G - 1) / G <= 1 ? 1 : ((N + G - 1) / G <= 2 ? 2 : 4);
+    const int64_t nseg = (dims->seqlen + kBwdS - 1) / kBwdS;
+    return (size_t)(dims->batch * dims->dim) * (size_t)nseg * (size_t)(G * Q) * sizeof(float);
+}
+
+ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const void *delta, const float *A,
+                                    const void *B, const void *C, const float *D, const void *z,
+                                    const float *delta_bias, int delta_softplus, const void *dy,
+                                    const float *dlast_state, float *du, float *ddelta, float *dA, float *dB,
+                                    float *dC, float *dD, float *dz, float *ddelta_bias, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    ssm_status_t st = check_dims(dims, true);
+    if (st != SSM_OK) return st;
+    const ssm_dims_t d = *dims;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d.batch == 0 || d.dim == 0) return SSM_OK;
+    if (!A || !dA) return SSM_ERR_NULL;
+    const bool empty = d.seqlen == 0;
+    if (!empty && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC)) return SSM_ERR_NULL;
+    const size_t esz = io_size(d.io_dtype);
+    const void *io_ptrs[] = {u, delta, B, C, z, dy};
+    for (const void *q : io_ptrs)
+        if (q != nullptr && !aligned_to(q, esz)) return SSM_ERR_ALIGN;
+    const void *f_ptrs[] = {A, D, delta_bias, dlast_state, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias};
+    for (const void *q : f_ptrs)
+        if (q != nullptr && !aligned_to(q, 4)) return SSM_ERR_ALIGN;
+    if (d.batch > 65535) return SSM_ERR_UNSUPPORTED;
+    // gradients summed over the sequence, the batch or the channels start at zero
+    const size_t BD = (size_t)(d.batch * d.dim), NL = (size_t)(d.dstate * d.seqlen);
+    if (cudaMemsetAsync(dA, 0, (size_t)(d.dim * d.dstate) * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
+    if (dD && cudaMemsetAsync(dD, 0, (size_t)d.dim * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
+    if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)d.dim * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
+    if (empty) return SSM_OK;
+    if (cudaMemsetAsync(dB, 0, (size_t)d.batch * NL * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaMemsetAsync(dC, 0, (size_t)d.batch * NL * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
+    if (dz && !z && cudaMemsetAsync(dz, 0, BD * (size_t)d.seqlen * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
+    const size_t need = ssm_selective_scan_bwd_workspace_bytes(dims);
+    bool allocated = false;
+    if (workspace == nullptr) {
+        if (cudaMallocAsync(&workspace, need, s) != cudaSuccess) return SSM_ERR_CUDA;
+        allocated = true;
+    } else if (workspace_bytes < need) {
+        return SSM_ERR_WORKSPACE;
+    } else if (!aligned16(workspace)) {
+        return SSM_ERR_ALIGN;
+    }
+    BwdParams p{u, delta, z, B, C, dy, A, D, delta_bias, dlast_state, du, ddelta, dA, dB, dC, dD,
+                z ? dz : nullptr, ddelta_bias, static_cast<float *>(workspace), d.batch, d.dim, d.seqlen,
+                d.dstate, delta_softplus ? 1 : 0, (int)((d.seqlen + kBwdS - 1) / kBwdS)};
+    const int64_t N = d.dstate;
+    int G = 1;
+    while (G < 32 && G < N) G *= 2;
+    const int Q = (N + G - 1) / G <= 1 ? 1 : ((N + G - 1) / G <= 2 ? 2 : 4);
+    const dim3 grid((unsigned)((d.dim + kBwdThreads / G - 1) / (kBwdThreads / G)), (unsigned)d.batch);
+    const bool bf = d.io_dtype == SSM_BF16;
+#define SSM_BWD(GG, QQ)                                                                                \
+    case GG * 10 + QQ:                                                                                 \
+        if (bf) {                                                                                      \
+            scan_bwd_ckpt_kernel<bf16, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                       \
+            scan_bwd_kernel<bf16, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                            \
+        } else {                                                                                       \
+            scan_bwd_ckpt_kernel<float, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                      \
+            scan_bwd_kernel<float, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                           \
+        }                                                                                              \
+        break;
+    switch (G * 10 + Q) {
+        SSM_BWD(1, 1) SSM_BWD(2, 1) SSM_BWD(4, 1) SSM_BWD(8, 1) SSM_BWD(16, 1) SSM_BWD(32, 1)
+        SSM_BWD(32, 2) SSM_BWD(32, 4)
+        default:
+            if (allocated) cudaFreeAsync(workspace, s);
+            return SSM_ERR_UNSUPPORTED;
+    }
+#undef SSM_BWD
+    const cudaError_t e = cudaGetLastError();
+    if (allocated) cudaFreeAsync(workspace, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, const void *delta,

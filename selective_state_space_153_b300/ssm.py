@@ -29,7 +29,8 @@ EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_workspace_bytes",
            "ssm_selective_scan_fwd_ws", "ssm_state_update", "ssm_selective_scan_fwd_host",
            "ssm_stream_status", "ssm_status_string", "ssm_version",
            "ssm_selective_scan_fwd_noalloc", "ssm_selective_scan_fwd_disc", "ssm_state_update_disc",
-           "ssm_conv_selective_scan_fwd", "ssm_conv_selective_scan_workspace_bytes")
+           "ssm_conv_selective_scan_fwd", "ssm_conv_selective_scan_workspace_bytes",
+           "ssm_selective_scan_bwd", "ssm_selective_scan_bwd_workspace_bytes")
 
 
 class SsmDims(ctypes.Structure):
@@ -71,6 +72,10 @@ def load(path: str = LIB_PATH):
     lib.ssm_conv_selective_scan_fwd.restype = ctypes.c_int
     lib.ssm_conv_selective_scan_workspace_bytes.argtypes = [dp]
     lib.ssm_conv_selective_scan_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssm_selective_scan_bwd.argtypes = scan_args[:10] + [_vp] * 10 + [_vp, ctypes.c_size_t, _vp]
+    lib.ssm_selective_scan_bwd.restype = ctypes.c_int
+    lib.ssm_selective_scan_bwd_workspace_bytes.argtypes = [dp]
+    lib.ssm_selective_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.ssm_selective_scan_fwd_noalloc.argtypes = scan_args + [_vp]
     lib.ssm_selective_scan_fwd_noalloc.restype = ctypes.c_int
     lib.ssm_selective_scan_fwd_host.restype = ctypes.c_int
@@ -201,6 +206,33 @@ def conv_selective_scan_fwd(x, conv_w, conv_b, delta, A, B, C, D=None, z=None, d
     if rc != SSM_OK:
         raise SsmError(rc, "ssm_conv_selective_scan_fwd")
     return y, last_state
+
+
+def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=True,
+                       dlast_state=None, stream=None, workspace=None):
+    """Gradients of sum(y*dy) (+ sum(last_state*dlast_state)) through the device scan, via
+    ssm_selective_scan_bwd. Returns a dict of fp32 device tensors: u, delta, A, B, C, and
+    D / z / delta_bias when those inputs are given."""
+    lib = load()
+    Bt, Dm, L = u.shape
+    N = A.shape[1]
+    io = _io_code(u)
+    f32 = dict(dtype=torch.float32, device=u.device)
+    g = {"u": torch.empty((Bt, Dm, L), **f32), "delta": torch.empty((Bt, Dm, L), **f32),
+         "A": torch.empty((Dm, N), **f32), "B": torch.empty((Bt, N, L), **f32), "C": torch.empty((Bt, N, L), **f32),
+         "D": torch.empty((Dm,), **f32) if D is not None else None,
+         "z": torch.empty((Bt, Dm, L), **f32) if z is not None else None,
+         "delta_bias": torch.empty((Dm,), **f32) if delta_bias is not None else None}
+    dm = dims(Bt, Dm, L, N, io)
+    ws_p = None if workspace is None else _p(workspace)
+    ws_n = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.ssm_selective_scan_bwd(ctypes.byref(dm), _p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z),
+                                    _p(delta_bias), int(bool(delta_softplus)), _p(dy), _p(dlast_state),
+                                    _p(g["u"]), _p(g["delta"]), _p(g["A"]), _p(g["B"]), _p(g["C"]), _p(g["D"]),
+                                    _p(g["z"]), _p(g["delta_bias"]), ws_p, ws_n, _stream_ptr(stream))
+    if rc != SSM_OK:
+        raise SsmError(rc, "ssm_selective_scan_bwd")
+    return g
 
 
 def workspace_bytes(Bt, Dm, L, N, io=SSM_BF16) -> int:

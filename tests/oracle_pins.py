@@ -425,15 +425,17 @@ def pin_backward_finite_differences(lib):
     _close(yt.detach().numpy(), yo, 1e-12, 1e-13, "autograd forward vs C oracle")
     g = bwd.scan_backward(**ins, delta_softplus=True, dy=dy, dlast=dlast)
     eps = 1e-6
+    pick = _rng(42)
     for k, arr in ins.items():
-        fd = np.zeros_like(arr)
-        for idx in np.ndindex(arr.shape):
+        flat = list(np.ndindex(arr.shape))
+        for j in pick.choice(len(flat), size=min(6, len(flat)), replace=False):
+            idx = flat[j]
             xp = {kk: vv.copy() for kk, vv in ins.items()}
             xm = {kk: vv.copy() for kk, vv in ins.items()}
             xp[k][idx] += eps
             xm[k][idx] -= eps
-            fd[idx] = (f(xp) - f(xm)) / (2 * eps)
-        _close(g[k], fd, 1e-6, 1e-7, f"d/d{k}: autograd vs finite differences")
+            fd = (f(xp) - f(xm)) / (2 * eps)
+            _close(g[k][idx], fd, 1e-6, 1e-7, f"d/d{k}{idx}: autograd vs finite differences")
 
 
 ALL_PINS = [pin_backward_finite_differences, pin_conv_numpy, pin_conv_torch_module, pin_zoh_step_response, pin_zoh_piecewise_ode, pin_zoh_small_step_limit,

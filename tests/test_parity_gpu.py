@@ -101,6 +101,48 @@ def test_pair_kernel_shapes(Bt, D, L, N, io, gate, dskip, ks, chunks, monkeypatc
     compare_scan(inp, y, h)
 
 
+# ---- backward: gradients against float64 autograd of the loop (oracle/backward.py) --------
+BWD_CASES = [
+    # Bt, D, L, N, io, gate, dskip, bias, dlast
+    (1, 4, 64, 4, "f32", False, "ones", True, False),
+    (2, 7, 100, 16, "f32", True, "normal", True, True),
+    (1, 5, 40, 64, "f32", True, "ones", False, False),
+    (1, 3, 33, 100, "f32", False, None, True, True),
+    (2, 9, 70, 16, "bf16", True, "normal", True, False),
+    (1, 40, 48, 8, "f32", False, "ones", True, False),
+]
+
+
+def _rel_max(got, ref):
+    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,bias,dlast", BWD_CASES)
+def test_backward_gradients(Bt, D, L, N, io, gate, dskip, bias, dlast):
+    from oracle import backward as obwd
+    cfg = gen.ScanConfig("bwd", Bt, D, L, N, io=io, gate=gate, dskip=dskip, bias=bias, seed=3 * L + N)
+    inp = gen.scan_inputs(cfg)
+    rng = np.random.default_rng(L + N)
+    dy = torch.from_numpy(rng.standard_normal((Bt, D, L)).astype(np.float32)).to(inp["u"].dtype)
+    dl = torch.from_numpy(rng.standard_normal((Bt, D, N)).astype(np.float32)) if dlast else None
+    g = to_dev(inp)
+    got = ssm.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.cuda(), D=g["D"], z=g["z"],
+                                 delta_bias=g["delta_bias"], delta_softplus=True,
+                                 dlast_state=None if dl is None else dl.cuda())
+    torch.cuda.synchronize()
+    f = gen.as_f64
+    ref = obwd.scan_backward(f(inp["u"]), f(inp["delta"]), f(inp["A"]), f(inp["B"]), f(inp["C"]), D=f(inp["D"]),
+                             z=f(inp["z"]), delta_bias=f(inp["delta_bias"]), delta_softplus=True, dy=f(dy),
+                             dlast=None if dl is None else f(dl))
+    tol = 1e-4 if io == "f32" else 2e-2
+    for k, r in ref.items():
+        if r is None:
+            assert got[k] is None
+            continue
+        err = _rel_max(got[k].double().cpu().numpy(), r)
+        assert err <= tol, f"d{k}: max error {err:.3e} of max |grad| (tol {tol})"
+
+
 # ---- conv1d + SiLU front fused in the scan (lmnt.cn sections 3.1-3.2) --------------------
 CONV_CASES = [
     # Bt, D, L, N, io, gate, dskip, K, forced chunks (0 = planner)
