@@ -18,9 +18,10 @@
 // every S-step segment. Pass 2 (scan_bwd_kernel) walks the segments backwards: it recomputes
 // the segment's S states into registers from the checkpoint, then runs the adjoint over the
 // segment in reverse. Sums over the states of a channel use shuffles across its G lanes; sums
-// over channels (dB, dC) are pre-reduced across the warp's channels with shuffles and then
-// added with fp32 atomics, as are dA, dD and the dt bias (summed over the sequence in the
-// thread first).
+// over channels (dB, dC) are pre-reduced across the warp's channels with shuffles, staged
+// per warp for the whole segment in shared memory, summed over the CTA's warps after the
+// segment and added with one fp32 atomic per (CTA, state, step); dA, dD and the dt bias are
+// summed over the sequence in the thread and added once at the end.
 #pragma once
 #include "common.cuh"
 
@@ -28,6 +29,8 @@ namespace ssm {
 
 constexpr int kBwdS = 16;        // steps per checkpoint segment
 constexpr int kBwdThreads = 128;
+// dynamic shared memory of scan_bwd_kernel<., G, Q>: [2][warps][kBwdS][G*Q] floats
+constexpr size_t bwd_smem_bytes(int G, int Q) { return (size_t)2 * (kBwdThreads / 32) * kBwdS * G * Q * sizeof(float); }
 
 struct BwdParams {
     const void *u, *delta, *z, *B, *C, *dy;
@@ -93,7 +96,14 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
 template <typename IO, int G, int Q>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p) {
     constexpr int kCpb = kBwdThreads / G;
-    const int tid = threadIdx.x, g = tid % G;
+    constexpr int kWarps = kBwdThreads / 32;
+    // per warp and step of the segment: its channel-summed dB and dC for the G*Q states,
+    // [2][kWarps][kBwdS][G*Q]
+    extern __shared__ float sPartBuf[];
+    auto sPart = [&](int which, int w, int i, int n) -> float & {
+        return sPartBuf[(((size_t)which * kWarps + w) * kBwdS + i) * (G * Q) + n];
+    };
+    const int tid = threadIdx.x, g = tid % G, warp = tid >> 5;
     const int64_t b = blockIdx.y, d = (int64_t)blockIdx.x * kCpb + tid / G;
     const bool valid = d < p.Dm;                // invalid lanes still take part in the shuffles
     const int64_t dd = valid ? d : 0;
@@ -140,7 +150,13 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p
 #pragma unroll
         for (int i = kBwdS - 1; i >= 0; --i) {
             const int64_t t = t0 + i;
-            if (t >= p.L) continue;             // uniform across the block (same t everywhere)
+            if (t >= p.L) {                     // uniform across the block (same t everywhere)
+                if ((threadIdx.x & 31) < G) {
+#pragma unroll
+                    for (int q = 0; q < Q; ++q) sPart(0, warp, i, g + G * q) = sPart(1, warp, i, g + G * q) = 0.0f;
+                }
+                continue;
+            }
             const float v = io_traits<IO>::to_f(DL[t]) + bias;
             const float dt = bwd_dt(v, p.softplus);
             const float uu = io_traits<IO>::to_f(U[t]);
@@ -172,12 +188,12 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p
                 ddt = fmaf(lam, fmaf(uu, bq[q], An[q] * a * hp), ddt);
                 dA[q] = fmaf(lam * dt * a, hp, dA[q]);
                 c[q] = a * lam;
-                // sums over the warp's channels, then one atomic per (state, step) and warp
+                // sums over the warp's channels, staged for the CTA-wide sum after the segment
                 const float gb = sum_channels<G>(nv[q] ? lam * dt * uu : 0.0f);
                 const float gc = sum_channels<G>(nv[q] ? dyh * hs[q][i + 1] : 0.0f);
-                if ((threadIdx.x & 31) < G && n < p.N) {
-                    atomicAdd(p.dB + (b * p.N + n) * p.L + t, gb);
-                    atomicAdd(p.dC + (b * p.N + n) * p.L + t, gc);
+                if ((threadIdx.x & 31) < G) {
+                    sPart(0, warp, i, g + G * q) = gb;
+                    sPart(1, warp, i, g + G * q) = gc;
                 }
             }
             du = sum_lanes<G>(du);
@@ -192,6 +208,19 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p
                 dbias += ddl;
             }
         }
+        // dB, dC of the segment: sum the warps' partials, one atomic per (state, step)
+        __syncthreads();
+        for (int e = tid; e < 2 * kBwdS * G * Q; e += kBwdThreads) {
+            const int which = e / (kBwdS * G * Q), r = e % (kBwdS * G * Q);
+            const int i = r / (G * Q), n = r % (G * Q);
+            const int64_t t = t0 + i;
+            if (n >= p.N || t >= p.L) continue;
+            float acc = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) acc += sPart(which, w, i, n);
+            atomicAdd((which ? p.dC : p.dB) + (b * p.N + n) * p.L + t, acc);
+        }
+        __syncthreads();
     }
     if (!valid) return;
 #pragma unroll

@@ -893,15 +893,19 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     const dim3 grid((unsigned)((d.dim + kBwdThreads / G - 1) / (kBwdThreads / G)), (unsigned)d.batch);
     const bool bf = d.io_dtype == SSM_BF16;
 #define SSM_BWD(GG, QQ)                                                                                \
-    case GG * 10 + QQ:                                                                                 \
+    case GG * 10 + QQ: {                                                                               \
+        constexpr size_t sm = bwd_smem_bytes(GG, QQ);                                                  \
         if (bf) {                                                                                      \
+            cudaFuncSetAttribute(scan_bwd_kernel<bf16, GG, QQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
             scan_bwd_ckpt_kernel<bf16, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                       \
-            scan_bwd_kernel<bf16, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                            \
+            scan_bwd_kernel<bf16, GG, QQ><<<grid, kBwdThreads, sm, s>>>(p);                           \
         } else {                                                                                       \
+            cudaFuncSetAttribute(scan_bwd_kernel<float, GG, QQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
             scan_bwd_ckpt_kernel<float, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                      \
-            scan_bwd_kernel<float, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                           \
+            scan_bwd_kernel<float, GG, QQ><<<grid, kBwdThreads, sm, s>>>(p);                          \
         }                                                                                              \
-        break;
+        break;                                                                                         \
+    }
     switch (G * 10 + Q) {
         SSM_BWD(1, 1) SSM_BWD(2, 1) SSM_BWD(4, 1) SSM_BWD(8, 1) SSM_BWD(16, 1) SSM_BWD(32, 1)
         SSM_BWD(32, 2) SSM_BWD(32, 4)
