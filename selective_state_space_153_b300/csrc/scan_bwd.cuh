@@ -29,7 +29,8 @@ namespace ssm {
 
 constexpr int kBwdS = 16;        // steps per checkpoint segment
 constexpr int kBwdThreads = 128;
-// dynamic shared memory of scan_bwd_kernel<., G, Q>: [2][warps][kBwdS][G*Q] floats
+// dynamic shared memory of scan_bwd_kernel<., G, Q> beyond its input tile: the dB/dC
+// partials [2][warps][kBwdS][G*Q] floats
 constexpr size_t bwd_smem_bytes(int G, int Q) { return (size_t)2 * (kBwdThreads / 32) * kBwdS * G * Q * sizeof(float); }
 
 struct BwdParams {
@@ -58,37 +59,86 @@ __device__ __forceinline__ float sum_channels(float v) {
     return v;
 }
 
+// Inputs of one S-step segment, staged by the whole CTA with coalesced loads: B and C rows of
+// the batch row ([G*Q][S], zero beyond N or L) and, per channel of the CTA, dt, the softplus
+// derivative, u, dy and z ([kCpb][S]); dt = softplus(delta + bias) is formed once per
+// (channel, step) here rather than in every lane.
+template <typename IO, int G, int Q>
+struct BwdTile {
+    static constexpr int kCpb = kBwdThreads / G;
+    static constexpr int kFloats = 2 * G * Q * kBwdS + 5 * kCpb * kBwdS;
+    float *B, *C, *dt, *sg, *u, *dy, *z;
+    __device__ BwdTile(float *base) {
+        B = base; C = B + G * Q * kBwdS; dt = C + G * Q * kBwdS; sg = dt + kCpb * kBwdS;
+        u = sg + kCpb * kBwdS; dy = u + kCpb * kBwdS; z = dy + kCpb * kBwdS;
+    }
+    // full = false: only what the forward recompute needs (B, dt, u)
+    __device__ void load(const BwdParams &p, int64_t b, int64_t t0, bool full) {
+        const int tid = threadIdx.x;
+        const IO *Bm = reinterpret_cast<const IO *>(p.B) + b * p.N * p.L;
+        const IO *Cm = reinterpret_cast<const IO *>(p.C) + b * p.N * p.L;
+        for (int e = tid; e < (full ? 2 : 1) * G * Q * kBwdS; e += kBwdThreads) {
+            const int which = e / (G * Q * kBwdS), r = e % (G * Q * kBwdS), n = r / kBwdS, i = r % kBwdS;
+            const int64_t t = t0 + i;
+            float v = 0.0f;
+            if (n < p.N && t < p.L) v = io_traits<IO>::to_f((which ? Cm : Bm)[n * p.L + t]);
+            (which ? C : B)[r] = v;
+        }
+        for (int e = tid; e < kCpb * kBwdS; e += kBwdThreads) {
+            const int cc = e / kBwdS, i = e % kBwdS;
+            const int64_t d = (int64_t)blockIdx.x * kCpb + cc, t = t0 + i;
+            float dtv = 0.0f, sgv = 0.0f, uv = 0.0f, dyv = 0.0f, zv = 0.0f;
+            if (d < p.Dm && t < p.L) {
+                const int64_t idx = (b * p.Dm + d) * p.L + t;
+                const float v = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.delta)[idx]) +
+                                (p.bias ? p.bias[d] : 0.0f);
+                dtv = bwd_dt(v, p.softplus);
+                sgv = p.softplus ? 1.0f / (1.0f + ex2(-v * kLog2e)) : 1.0f;
+                uv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.u)[idx]);
+                if (full) {
+                    dyv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.dy)[idx]);
+                    if (p.z) zv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.z)[idx]);
+                }
+            }
+            dt[e] = dtv; sg[e] = sgv; u[e] = uv; dy[e] = dyv; z[e] = zv;
+        }
+    }
+};
+
+template <int G, int Q>
+constexpr size_t bwd_tile_bytes() { return (size_t)BwdTile<float, G, Q>::kFloats * sizeof(float); }
+
 template <typename IO, int G, int Q>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdParams p) {
     constexpr int kCpb = kBwdThreads / G;
-    const int tid = threadIdx.x, g = tid % G;
-    const int64_t b = blockIdx.y, d = (int64_t)blockIdx.x * kCpb + tid / G;
-    if (d >= p.Dm) return;
-    const int64_t bd = b * p.Dm + d;
-    const IO *U = reinterpret_cast<const IO *>(p.u) + bd * p.L;
-    const IO *DL = reinterpret_cast<const IO *>(p.delta) + bd * p.L;
-    const IO *Bm = reinterpret_cast<const IO *>(p.B) + b * p.N * p.L;
-    const float bias = p.bias ? p.bias[d] : 0.0f;
+    extern __shared__ float smemf[];
+    BwdTile<IO, G, Q> tile(smemf);
+    const int tid = threadIdx.x, g = tid % G, cc = tid / G;
+    const int64_t b = blockIdx.y, d = (int64_t)blockIdx.x * kCpb + cc;
+    const bool valid = d < p.Dm;                 // every thread takes part in the tile loads
+    const int64_t bd = b * p.Dm + (valid ? d : 0);
     float Ap[Q], h[Q];
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
         const int n = g + G * q;
-        Ap[q] = n < p.N ? p.A[d * p.N + n] * kLog2e : 0.0f;
+        Ap[q] = (valid && n < p.N) ? p.A[(valid ? d : 0) * p.N + n] * kLog2e : 0.0f;
         h[q] = 0.0f;
     }
     float *ck = p.ckpt + bd * (int64_t)p.nseg * (G * Q);
-    for (int64_t t = 0; t < p.L; ++t) {
-        if (t % kBwdS == 0) {
+    for (int seg = 0; seg < p.nseg; ++seg) {
+        if (valid) {
 #pragma unroll
-            for (int q = 0; q < Q; ++q) ck[(t / kBwdS) * (G * Q) + g + G * q] = h[q];
+            for (int q = 0; q < Q; ++q) ck[(int64_t)seg * (G * Q) + g + G * q] = h[q];
         }
-        const float dt = bwd_dt(io_traits<IO>::to_f(DL[t]) + bias, p.softplus);
-        const float x = dt * io_traits<IO>::to_f(U[t]);
+        __syncthreads();
+        tile.load(p, b, (int64_t)seg * kBwdS, false);
+        __syncthreads();
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const int n = g + G * q;
-            const float bn = n < p.N ? io_traits<IO>::to_f(Bm[n * p.L + t]) : 0.0f;
-            h[q] = fmaf(ex2(dt * Ap[q]), h[q], x * bn);
+        for (int i = 0; i < kBwdS; ++i) {
+            const float dt = tile.dt[cc * kBwdS + i];
+            const float x = dt * tile.u[cc * kBwdS + i];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) h[q] = fmaf(ex2(dt * Ap[q]), h[q], x * tile.B[(g + G * q) * kBwdS + i]);
         }
     }
 }
@@ -97,24 +147,19 @@ template <typename IO, int G, int Q>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p) {
     constexpr int kCpb = kBwdThreads / G;
     constexpr int kWarps = kBwdThreads / 32;
-    // per warp and step of the segment: its channel-summed dB and dC for the G*Q states,
-    // [2][kWarps][kBwdS][G*Q]
-    extern __shared__ float sPartBuf[];
+    // staged segment inputs, then per warp and step the channel-summed dB and dC partials
+    // for the G*Q states ([2][kWarps][kBwdS][G*Q])
+    extern __shared__ float smemf[];
+    BwdTile<IO, G, Q> tile(smemf);
+    float *sPartBuf = smemf + BwdTile<IO, G, Q>::kFloats;
     auto sPart = [&](int which, int w, int i, int n) -> float & {
         return sPartBuf[(((size_t)which * kWarps + w) * kBwdS + i) * (G * Q) + n];
     };
-    const int tid = threadIdx.x, g = tid % G, warp = tid >> 5;
-    const int64_t b = blockIdx.y, d = (int64_t)blockIdx.x * kCpb + tid / G;
+    const int tid = threadIdx.x, g = tid % G, warp = tid >> 5, cc = tid / G;
+    const int64_t b = blockIdx.y, d = (int64_t)blockIdx.x * kCpb + cc;
     const bool valid = d < p.Dm;                // invalid lanes still take part in the shuffles
     const int64_t dd = valid ? d : 0;
     const int64_t bd = b * p.Dm + dd;
-    const IO *U = reinterpret_cast<const IO *>(p.u) + bd * p.L;
-    const IO *DL = reinterpret_cast<const IO *>(p.delta) + bd * p.L;
-    const IO *Z = p.z ? reinterpret_cast<const IO *>(p.z) + bd * p.L : nullptr;
-    const IO *DY = reinterpret_cast<const IO *>(p.dy) + bd * p.L;
-    const IO *Bm = reinterpret_cast<const IO *>(p.B) + b * p.N * p.L;
-    const IO *Cm = reinterpret_cast<const IO *>(p.C) + b * p.N * p.L;
-    const float bias = (valid && p.bias) ? p.bias[dd] : 0.0f;
     const float Dv = (valid && p.D) ? p.D[dd] : 0.0f;
     float An[Q], Ap[Q], c[Q], dA[Q];
     bool nv[Q];
@@ -131,21 +176,19 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p
     const float *ck = p.ckpt + bd * (int64_t)p.nseg * (G * Q);
     for (int seg = p.nseg - 1; seg >= 0; --seg) {
         const int64_t t0 = (int64_t)seg * kBwdS;
+        __syncthreads();                        // the previous segment is done with the tile
+        tile.load(p, b, t0, true);
+        __syncthreads();
         float hs[Q][kBwdS + 1];                 // hs[q][0]: h before the segment; hs[q][i+1]: after step t0+i
 #pragma unroll
         for (int q = 0; q < Q; ++q) hs[q][0] = valid ? ck[(int64_t)seg * (G * Q) + g + G * q] : 0.0f;
 #pragma unroll
         for (int i = 0; i < kBwdS; ++i) {
-            const int64_t t = t0 + i;
-            const bool in = t < p.L;
-            const float dt = in ? bwd_dt(io_traits<IO>::to_f(DL[t]) + bias, p.softplus) : 0.0f;
-            const float x = in ? dt * io_traits<IO>::to_f(U[t]) : 0.0f;
+            const float dt = tile.dt[cc * kBwdS + i];
+            const float x = dt * tile.u[cc * kBwdS + i];
 #pragma unroll
-            for (int q = 0; q < Q; ++q) {
-                const int n = g + G * q;
-                const float bn = (in && nv[q]) ? io_traits<IO>::to_f(Bm[n * p.L + t]) : 0.0f;
-                hs[q][i + 1] = fmaf(ex2(dt * Ap[q]), hs[q][i], x * bn);
-            }
+            for (int q = 0; q < Q; ++q)
+                hs[q][i + 1] = fmaf(ex2(dt * Ap[q]), hs[q][i], x * tile.B[(g + G * q) * kBwdS + i]);
         }
 #pragma unroll
         for (int i = kBwdS - 1; i >= 0; --i) {
@@ -157,22 +200,20 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p
                 }
                 continue;
             }
-            const float v = io_traits<IO>::to_f(DL[t]) + bias;
-            const float dt = bwd_dt(v, p.softplus);
-            const float uu = io_traits<IO>::to_f(U[t]);
+            const float dt = tile.dt[cc * kBwdS + i];
+            const float uu = tile.u[cc * kBwdS + i];
             float bq[Q], cq[Q], yh = 0.0f;
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
-                const int n = g + G * q;
-                bq[q] = nv[q] ? io_traits<IO>::to_f(Bm[n * p.L + t]) : 0.0f;
-                cq[q] = nv[q] ? io_traits<IO>::to_f(Cm[n * p.L + t]) : 0.0f;
+                bq[q] = tile.B[(g + G * q) * kBwdS + i];
+                cq[q] = tile.C[(g + G * q) * kBwdS + i];
                 yh = fmaf(cq[q], hs[q][i + 1], yh);
             }
             yh = sum_lanes<G>(yh) + Dv * uu;    // yhat_t, before the gate
-            const float dyv = valid ? io_traits<IO>::to_f(DY[t]) : 0.0f;
+            const float dyv = tile.dy[cc * kBwdS + i];
             float dyh = dyv, dzv = 0.0f;
-            if (Z) {
-                const float zz = io_traits<IO>::to_f(Z[t]);
+            if (p.z) {
+                const float zz = tile.z[cc * kBwdS + i];
                 const float sg = 1.0f / (1.0f + ex2(-zz * kLog2e));
                 dyh = dyv * zz * sg;            // dy * SiLU(z)
                 dzv = dyv * yh * sg * (1.0f + zz * (1.0f - sg));
@@ -180,7 +221,6 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p
             float du = 0.0f, ddt = 0.0f;
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
-                const int n = g + G * q;
                 const float a = ex2(dt * Ap[q]);
                 const float lam = fmaf(dyh, cq[q], c[q]);
                 const float hp = hs[q][i];
@@ -199,8 +239,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p
             du = sum_lanes<G>(du);
             ddt = sum_lanes<G>(ddt);
             if (valid && g == 0) {
-                const float sg = p.softplus ? 1.0f / (1.0f + ex2(-v * kLog2e)) : 1.0f;
-                const float ddl = ddt * sg;
+                const float ddl = ddt * tile.sg[cc * kBwdS + i];
                 p.du[bd * p.L + t] = fmaf(dyh, Dv, du);
                 p.ddelta[bd * p.L + t] = ddl;
                 if (p.dz) p.dz[bd * p.L + t] = dzv;
@@ -220,7 +259,6 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p
             for (int w = 0; w < kWarps; ++w) acc += sPart(which, w, i, n);
             atomicAdd((which ? p.dC : p.dB) + (b * p.N + n) * p.L + t, acc);
         }
-        __syncthreads();
     }
     if (!valid) return;
 #pragma unroll

@@ -831,13 +831,25 @@ size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
     return pair_workspace_bytes(*dims, plan_pair(*dims, true));
 }
 
+}  // extern "C"
+
+namespace {
+// backward lane split: Q <= 4 states per lane, G lanes per channel (a power of two, <= 32)
+void bwd_split(int64_t N, int *G, int *Q) {
+    *Q = N <= 1 ? 1 : (N <= 2 ? 2 : 4);
+    int g = 1;
+    while (g < 32 && (int64_t)g * *Q < N) g *= 2;
+    *G = g;
+}
+}  // namespace
+
+extern "C" {
+
 size_t ssm_selective_scan_bwd_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
-    const int64_t N = dims->dstate;
-    int G = 1;
-    while (G < 32 && G < N) G *= 2;
-    const int64_t Q = (N + G - 1) / G <= 1 ? 1 : ((N + G - 1) / G <= 2 ? 2 : 4);
+    int G, Q;
+    bwd_split(dims->dstate, &G, &Q);
     const int64_t nseg = (dims->seqlen + kBwdS - 1) / kBwdS;
     return (size_t)(dims->batch * dims->dim) * (size_t)nseg * (size_t)(G * Q) * sizeof(float);
 }
@@ -886,29 +898,27 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     BwdParams p{u, delta, z, B, C, dy, A, D, delta_bias, dlast_state, du, ddelta, dA, dB, dC, dD,
                 z ? dz : nullptr, ddelta_bias, static_cast<float *>(workspace), d.batch, d.dim, d.seqlen,
                 d.dstate, delta_softplus ? 1 : 0, (int)((d.seqlen + kBwdS - 1) / kBwdS)};
-    const int64_t N = d.dstate;
-    int G = 1;
-    while (G < 32 && G < N) G *= 2;
-    const int Q = (N + G - 1) / G <= 1 ? 1 : ((N + G - 1) / G <= 2 ? 2 : 4);
+    int G, Q;
+    bwd_split(d.dstate, &G, &Q);
     const dim3 grid((unsigned)((d.dim + kBwdThreads / G - 1) / (kBwdThreads / G)), (unsigned)d.batch);
     const bool bf = d.io_dtype == SSM_BF16;
 #define SSM_BWD(GG, QQ)                                                                                \
     case GG * 10 + QQ: {                                                                               \
-        constexpr size_t sm = bwd_smem_bytes(GG, QQ);                                                  \
+        constexpr size_t tb = bwd_tile_bytes<GG, QQ>(), sm = tb + bwd_smem_bytes(GG, QQ);             \
         if (bf) {                                                                                      \
             cudaFuncSetAttribute(scan_bwd_kernel<bf16, GG, QQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
-            scan_bwd_ckpt_kernel<bf16, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                       \
+            scan_bwd_ckpt_kernel<bf16, GG, QQ><<<grid, kBwdThreads, tb, s>>>(p);                      \
             scan_bwd_kernel<bf16, GG, QQ><<<grid, kBwdThreads, sm, s>>>(p);                           \
         } else {                                                                                       \
             cudaFuncSetAttribute(scan_bwd_kernel<float, GG, QQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
-            scan_bwd_ckpt_kernel<float, GG, QQ><<<grid, kBwdThreads, 0, s>>>(p);                      \
+            scan_bwd_ckpt_kernel<float, GG, QQ><<<grid, kBwdThreads, tb, s>>>(p);                     \
             scan_bwd_kernel<float, GG, QQ><<<grid, kBwdThreads, sm, s>>>(p);                          \
         }                                                                                              \
         break;                                                                                         \
     }
     switch (G * 10 + Q) {
-        SSM_BWD(1, 1) SSM_BWD(2, 1) SSM_BWD(4, 1) SSM_BWD(8, 1) SSM_BWD(16, 1) SSM_BWD(32, 1)
-        SSM_BWD(32, 2) SSM_BWD(32, 4)
+        SSM_BWD(1, 1) SSM_BWD(1, 2) SSM_BWD(1, 4) SSM_BWD(2, 4) SSM_BWD(4, 4) SSM_BWD(8, 4)
+        SSM_BWD(16, 4) SSM_BWD(32, 4)
         default:
             if (allocated) cudaFreeAsync(workspace, s);
             return SSM_ERR_UNSUPPORTED;
