@@ -8,6 +8,9 @@ namespace ssm {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// compile-time bool tag (selects a code variant inside a generic lambda)
+template <bool V> struct BoolC { static constexpr bool value = V; };
+
 // 2^x on the MUFU unit (ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -107,6 +110,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)),
                  "l"(gmem), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void *gmem, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr), "l"(gmem), "r"(src_bytes)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }

@@ -28,6 +28,13 @@
 // (a - 1) * (1/dt) * (1/A) with a = exp(dt*A) already computed for the recurrence (the
 // cancellation in a - 1 is then <= 2e-6 relative). No extra exponential per element.
 //
+// Structured A: where every state of a warp's channels has A[d, n] = (n + 1) * A[d, 0] (the
+// S4D-real initialisation A_log = log(1..N) of section 3.3 of the lmnt.cn page, before
+// training moves it), exp(dt*A[d, n]) = r^(n+1) with r = exp(dt*A[d, 0]). Such a warp
+// (detected at run time with a warp vote, unless the host switches detection off) takes
+// the decays of a quad of states n0..n0+3 as e, e*r, e*r^2, e*r^3 with e = exp(dt*A[d, n0]):
+// one ex2 per quad and one per channel for r instead of one per state.
+//
 // Modes: FULL computes y (and the final state of the last chunk); AGG computes only the
 // chunk's end state from h = 0 and the chunk's sum of dt, from which chunk_combine_kernel
 // forms each chunk's incoming state (the recurrence is a composition of affine maps --
@@ -156,6 +163,23 @@ scan_pair_kernel(const SeqParams p) {
                 const float a1 = (cv[ch] && n + 1 < N) ? p.A[dch[ch] * p.N + n + 1] * kLog2e : 0.0f;
                 Ap[ch][q][pp] = make_float2(a0, a1);
             }
+    // structured-A test for the lane's states; padded states (n >= N) never qualify
+    float Ap0[2];
+    bool lane_st = p.structured != 0;
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        const float A0 = cv[ch] ? p.A[dch[ch] * p.N] : 0.0f;
+        Ap0[ch] = A0 * kLog2e;
+#pragma unroll
+        for (int q = 0; q < kQN; ++q)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int n = 4 * (GP * q + g) + jj;
+                if (n >= N) lane_st = false;
+                else if (cv[ch] && p.A[dch[ch] * p.N + n] != (float)(n + 1) * A0) lane_st = false;
+            }
+    }
+    const bool st = __all_sync(0xffffffffu, lane_st);
     // 1/A of the lane's states (ZOH; zero where A = 0, where phi's polynomial branch applies)
     float2 iA[2][kQN][2];
     if constexpr (ZOH) {
@@ -193,33 +217,56 @@ scan_pair_kernel(const SeqParams p) {
     const IO *gC = reinterpret_cast<const IO *>(p.C);
     const bool has_z = !AGG && p.z != nullptr;
 
-    // raw rows: [0,kCh) u, [kCh,2kCh) delta, [2kCh,3kCh) z, then kNP B rows, kNP C rows
+    // raw rows: [0,kCh) u, [kCh,2kCh) delta, then (full pass) [2kCh,3kCh) z, then kNP B rows
+    // and (full pass) kNP C rows; padded state rows are never copied (converted as zeros).
+    // Copy item i of a tile is row i / kPieces, piece i % kPieces. A thread's items are the
+    // same in every tile, so where it has few of them their global sources (at the chunk's
+    // first step; null for an item with nothing to copy) are computed once and a tile adds
+    // its time offset; the shared destinations are a fixed stride apart.
+    constexpr int kRowB = AGG ? 2 * kCh : 3 * kCh;
+    constexpr int kRows = AGG ? 2 * kCh + kNP : 3 * kCh + 2 * kNP;
+    constexpr int kItems = (kRows * kPieces + Cfg::kThreads - 1) / Cfg::kThreads;
+    constexpr bool kPre = kItems <= 6;
+    constexpr uint32_t kItemStride = (uint32_t)((Cfg::kThreads / kPieces) * kRS * sizeof(IO));
+    const int e0_me = (tid % kPieces) * kEpr;   // the thread's piece: kThreads is a multiple of kPieces
+    const uint32_t idst0 = (uint32_t)(((tid / kPieces) * kRS + e0_me) * sizeof(IO));
+    auto item_src = [&](int row) -> const IO * {   // source at the chunk's first step, or null
+        if (row < kRowB) {
+            const int kind = row / kCh, cc = row % kCh;
+            if (d0 + cc >= p.Dm || (kind == 2 && !has_z)) return nullptr;
+            const IO *base = kind == 0 ? gU : (kind == 1 ? gDelta : gZ);
+            return base + ((b * p.Dm + d0 + cc) * p.L + l_begin + e0_me);
+        }
+        if (row >= kRows) return nullptr;
+        const int r = row - kRowB, kind = r / kNP, n = r % kNP;
+        if (n >= N) return nullptr;
+        return (kind == 0 ? gB : gC) + ((b * p.N + n) * p.L + l_begin + e0_me);
+    };
+    const IO *isrc[kPre ? kItems : 1];
+    if constexpr (kPre) {
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) isrc[k] = item_src((tid + k * Cfg::kThreads) / kPieces);
+    }
     auto issue_tile = [&](int j) {
-        IO *raw = raw_of(j);
-        const int64_t t0 = l_begin + (int64_t)j * T;
-        const int len = (int)min((int64_t)T, l_end - t0);
-        const int nch_rows = has_z ? 3 * kCh : 2 * kCh;
-        const int nn_rows = AGG ? N : 2 * N;
-        const int total = (nch_rows + nn_rows) * kPieces;
-        for (int i = tid; i < total; i += Cfg::kThreads) {
-            const int row = i / kPieces, e0 = (i % kPieces) * kEpr;
-            const IO *src;
-            IO *dst;
-            bool ok;
-            if (row < nch_rows) {
-                const int kind = row / kCh, cc = row % kCh;
-                const IO *base = kind == 0 ? gU : (kind == 1 ? gDelta : gZ);
-                ok = d0 + cc < p.Dm;
-                src = base + ((b * p.Dm + d0 + cc) * p.L + t0 + e0);
-                dst = raw + (size_t)(kind * kCh + cc) * kRS + e0;
-            } else {
-                const int r = row - nch_rows, kind = r / N, n = r % N;
-                ok = true;
-                src = (kind == 0 ? gB : gC) + ((b * p.N + n) * p.L + t0 + e0);
-                dst = raw + (size_t)(3 * kCh + kind * kNP + n) * kRS + e0;
+        const uint32_t raw_s = smem_u32(raw_of(j));
+        const int64_t toff = (int64_t)j * T;
+        const int len = (int)min((int64_t)T, l_end - l_begin - toff);
+        const int avail = max(0, min(kEpr, len - e0_me));
+        if constexpr (kPre) {
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                if (isrc[k] != nullptr)
+                    cp_async16(raw_s + idst0 + k * kItemStride,
+                               avail > 0 ? (const void *)(isrc[k] + toff) : (const void *)gU,
+                               avail * (int)sizeof(IO));
             }
-            const int avail = ok ? max(0, min(kEpr, len - e0)) : 0;
-            cp_async16(dst, avail > 0 ? (const void *)src : (const void *)gU, avail * (int)sizeof(IO));
+        } else {
+            for (int i = tid; i < kRows * kPieces; i += Cfg::kThreads) {
+                const IO *src = item_src(i / kPieces);
+                if (src != nullptr)
+                    cp_async16(raw_s + (uint32_t)(((i / kPieces) * kRS + e0_me) * sizeof(IO)),
+                               avail > 0 ? (const void *)(src + toff) : (const void *)gU, avail * (int)sizeof(IO));
+            }
         }
         cp_async_commit();
     };
@@ -275,12 +322,12 @@ scan_pair_kernel(const SeqParams p) {
                 dst[(size_t)e * kPairs * 2] = make_float2(dt, x);
             }
         }
-        const int nkind = AGG ? 1 : 2;
+        constexpr int nkind = AGG ? 1 : 2;
         for (int i = tid; i < nkind * kNP * kPieces; i += Cfg::kThreads) {
             const int n = i % kNP, r = i / kNP, kind = r % nkind, tq = (r / nkind) * kEpr;
             float v[kEpr];
             if (n < N) {
-                unpack16(*reinterpret_cast<const uint4 *>(raw + (size_t)(3 * kCh + kind * kNP + n) * kRS + tq), v, IO(0.0f));
+                unpack16(*reinterpret_cast<const uint4 *>(raw + (size_t)(kRowB + kind * kNP + n) * kRS + tq), v, IO(0.0f));
             } else {
 #pragma unroll
                 for (int e = 0; e < kEpr; ++e) v[e] = 0.0f;
@@ -294,20 +341,42 @@ scan_pair_kernel(const SeqParams p) {
     float dsum[2] = {0.f, 0.f}, dsum_c[2] = {0.f, 0.f};   // compensated sums of dt (AGG)
     IO *gY = reinterpret_cast<IO *>(p.y);
 
-    // coalesced store of tile j's staged y rows (16-byte pieces; element-wise on a ragged tail)
+    // coalesced store of tile j's staged y rows (16-byte pieces; element-wise on a ragged
+    // tail); the thread's pieces are fixed, with their global destination at the chunk's
+    // first step computed once (null past the last channel)
+    constexpr int kYItems = (kCh * kPieces + Cfg::kThreads - 1) / Cfg::kThreads;
+    IO *ydst[kYItems <= 2 ? kYItems : 1];
+    if constexpr (kYItems <= 2) {
+#pragma unroll
+        for (int k = 0; k < kYItems; ++k) {
+            const int i = tid + k * Cfg::kThreads, cc = i / kPieces;
+            ydst[k] = (!AGG && i < kCh * kPieces && d0 + cc < p.Dm)
+                          ? gY + ((b * p.Dm + d0 + cc) * p.L + l_begin + e0_me) : nullptr;
+        }
+    }
     auto store_y = [&](int j) {
         const IO *ys = sYS0 + (size_t)(j & 1) * kCh * kRS;
-        const int64_t t0 = l_begin + (int64_t)j * T;
-        const int len = (int)min((int64_t)T, l_end - t0);
-        for (int i = tid; i < kCh * kPieces; i += Cfg::kThreads) {
-            const int cc = i / kPieces, e0 = (i % kPieces) * kEpr;
-            if (d0 + cc >= p.Dm || e0 >= len) continue;
-            IO *dst = gY + (b * p.Dm + d0 + cc) * p.L + t0 + e0;
-            const IO *src = ys + (size_t)cc * kRS + e0;
-            if (e0 + kEpr <= len) {
+        const int64_t toff = (int64_t)j * T;
+        const int len = (int)min((int64_t)T, l_end - l_begin - toff);
+        if (e0_me >= len) return;
+        auto put = [&](IO *dst, const IO *src) {
+            if (e0_me + kEpr <= len) {
                 *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
             } else {
-                for (int e = 0; e < len - e0; ++e) dst[e] = src[e];
+                for (int e = 0; e < len - e0_me; ++e) dst[e] = src[e];
+            }
+        };
+        if constexpr (kYItems <= 2) {
+#pragma unroll
+            for (int k = 0; k < kYItems; ++k) {
+                const int cc = (tid + k * Cfg::kThreads) / kPieces;
+                if (ydst[k] != nullptr) put(ydst[k] + toff, ys + (size_t)cc * kRS + e0_me);
+            }
+        } else {
+            for (int i = tid; i < kCh * kPieces; i += Cfg::kThreads) {
+                const int cc = i / kPieces;
+                if (d0 + cc >= p.Dm) continue;
+                put(gY + ((b * p.Dm + d0 + cc) * p.L + l_begin + e0_me) + toff, ys + (size_t)cc * kRS + e0_me);
             }
         }
     };
@@ -347,66 +416,92 @@ scan_pair_kernel(const SeqParams p) {
         const IO *raw = raw_of(j);
         IO *ys = sYS0 + (size_t)(j & 1) * kCh * kRS;
         float tsum[2] = {0.f, 0.f};
+        auto scan_tile = [&](auto st_c) {
+            constexpr bool ST = decltype(st_c)::value;
 #pragma unroll 1
-        for (int tb = 0; tb < T; tb += GP) {
-            float yp[2][GP];
+            for (int tb = 0; tb < T; tb += GP) {
+                float yp[2][GP];
 #pragma unroll
-            for (int s = 0; s < GP; ++s) {
-                const int t = tb + s;
-                const float4 dx = sDX[(size_t)t * kPairs + pr];
-                const float2 dd[2] = {make_float2(dx.x, dx.x), make_float2(dx.z, dx.z)};
-                const float2 xx[2] = {make_float2(dx.y, dx.y), make_float2(dx.w, dx.w)};
-                if (AGG) { tsum[0] += dx.x; tsum[1] += dx.z; }
-                float2 ya[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                for (int s = 0; s < GP; ++s) {
+                    const int t = tb + s;
+                    const float4 dx = sDX[(size_t)t * kPairs + pr];
+                    const float2 dd[2] = {make_float2(dx.x, dx.x), make_float2(dx.z, dx.z)};
+                    const float2 xx[2] = {make_float2(dx.y, dx.y), make_float2(dx.w, dx.w)};
+                    if (AGG) { tsum[0] += dx.x; tsum[1] += dx.z; }
+                    // structured A: r = exp(dt*A[d, 0]) and (r^2, r^2) per channel
+                    float r[2] = {1.0f, 1.0f};
+                    float2 r2[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
+                    if constexpr (ST) {
 #pragma unroll
-                for (int q = 0; q < kQN; ++q) {
-                    const float4 bq = *reinterpret_cast<const float4 *>(sBC + (size_t)t * 2 * kNP + 4 * (GP * q + g));
-                    float4 cq = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (!AGG) cq = *reinterpret_cast<const float4 *>(sBC + (size_t)t * 2 * kNP + kNP + 4 * (GP * q + g));
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch) {
-                        const float2 e0 = __fmul2_rn(dd[ch], Ap[ch][q][0]);
-                        const float2 e1 = __fmul2_rn(dd[ch], Ap[ch][q][1]);
-                        const float2 a0 = make_float2(ex2(e0.x), ex2(e0.y));
-                        const float2 a1 = make_float2(ex2(e1.x), ex2(e1.y));
-                        float2 w0, w1;
-                        if constexpr (ZOH) {
-                            const float idt = rcp_approx(ch ? dx.z : dx.x);
-                            w0 = __fmul2_rn(__fmul2_rn(xx[ch], make_float2(bq.x, bq.y)), zoh_phi2(e0, a0, idt, iA[ch][q][0]));
-                            w1 = __fmul2_rn(__fmul2_rn(xx[ch], make_float2(bq.z, bq.w)), zoh_phi2(e1, a1, idt, iA[ch][q][1]));
-                        } else {
-                            w0 = __fmul2_rn(xx[ch], make_float2(bq.x, bq.y));
-                            w1 = __fmul2_rn(xx[ch], make_float2(bq.z, bq.w));
+                        for (int ch = 0; ch < 2; ++ch) {
+                            r[ch] = ex2(dd[ch].x * Ap0[ch]);
+                            r2[ch] = __fmul2_rn(make_float2(r[ch], r[ch]), make_float2(r[ch], r[ch]));
                         }
-                        h[ch][q][0] = __ffma2_rn(a0, h[ch][q][0], w0);
-                        h[ch][q][1] = __ffma2_rn(a1, h[ch][q][1], w1);
-                        if (!AGG) {
-                            ya[ch] = __ffma2_rn(make_float2(cq.x, cq.y), h[ch][q][0], ya[ch]);
-                            ya[ch] = __ffma2_rn(make_float2(cq.z, cq.w), h[ch][q][1], ya[ch]);
+                    }
+                    float2 ya[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int q = 0; q < kQN; ++q) {
+                        const float4 bq = *reinterpret_cast<const float4 *>(sBC + (size_t)t * 2 * kNP + 4 * (GP * q + g));
+                        float4 cq = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (!AGG) cq = *reinterpret_cast<const float4 *>(sBC + (size_t)t * 2 * kNP + kNP + 4 * (GP * q + g));
+#pragma unroll
+                        for (int ch = 0; ch < 2; ++ch) {
+                            float2 e0, e1, a0, a1;
+                            if constexpr (ST) {
+                                const float e = ex2(dd[ch].x * Ap[ch][q][0].x);   // first state of the quad
+                                a0 = make_float2(e, e * r[ch]);
+                                a1 = __fmul2_rn(a0, r2[ch]);
+                                if constexpr (ZOH) {
+                                    e0 = __fmul2_rn(dd[ch], Ap[ch][q][0]);
+                                    e1 = __fmul2_rn(dd[ch], Ap[ch][q][1]);
+                                }
+                            } else {
+                                e0 = __fmul2_rn(dd[ch], Ap[ch][q][0]);
+                                e1 = __fmul2_rn(dd[ch], Ap[ch][q][1]);
+                                a0 = make_float2(ex2(e0.x), ex2(e0.y));
+                                a1 = make_float2(ex2(e1.x), ex2(e1.y));
+                            }
+                            float2 w0, w1;
+                            if constexpr (ZOH) {
+                                const float idt = rcp_approx(ch ? dx.z : dx.x);
+                                w0 = __fmul2_rn(__fmul2_rn(xx[ch], make_float2(bq.x, bq.y)), zoh_phi2(e0, a0, idt, iA[ch][q][0]));
+                                w1 = __fmul2_rn(__fmul2_rn(xx[ch], make_float2(bq.z, bq.w)), zoh_phi2(e1, a1, idt, iA[ch][q][1]));
+                            } else {
+                                w0 = __fmul2_rn(xx[ch], make_float2(bq.x, bq.y));
+                                w1 = __fmul2_rn(xx[ch], make_float2(bq.z, bq.w));
+                            }
+                            h[ch][q][0] = __ffma2_rn(a0, h[ch][q][0], w0);
+                            h[ch][q][1] = __ffma2_rn(a1, h[ch][q][1], w1);
+                            if (!AGG) {
+                                ya[ch] = __ffma2_rn(make_float2(cq.x, cq.y), h[ch][q][0], ya[ch]);
+                                ya[ch] = __ffma2_rn(make_float2(cq.z, cq.w), h[ch][q][1], ya[ch]);
+                            }
                         }
+                    }
+                    if (!AGG) {
+                        yp[0][s] = ya[0].x + ya[0].y;
+                        yp[1][s] = ya[1].x + ya[1].y;
                     }
                 }
                 if (!AGG) {
-                    yp[0][s] = ya[0].x + ya[0].y;
-                    yp[1][s] = ya[1].x + ya[1].y;
-                }
-            }
-            if (!AGG) {
-                // the timestep this lane finished, for both channels; staged for a coalesced
-                // store after the next barrier (rows past the last channel are never stored)
-                const int t = tb + g;
+                    // the timestep this lane finished, for both channels; staged for a coalesced
+                    // store after the next barrier (rows past the last channel are never stored)
+                    const int t = tb + g;
 #pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    const float ysum = group_reduce_transpose<GP>(yp[ch], lane);
-                    const int cc = c0 + ch;
-                    const float uv = CONV ? sSu0[(size_t)(j & 1) * kCh * T + (size_t)cc * T + t]
-                                          : io_traits<IO>::to_f(raw[(size_t)cc * kRS + t]);
-                    float yv = fmaf(Dd[ch], uv, ysum);
-                    if (has_z) yv *= silu_f(io_traits<IO>::to_f(raw[(size_t)(2 * kCh + cc) * kRS + t]));
-                    store_io(ys + (size_t)cc * kRS + t, yv);
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const float ysum = group_reduce_transpose<GP>(yp[ch], lane);
+                        const int cc = c0 + ch;
+                        const float uv = CONV ? sSu0[(size_t)(j & 1) * kCh * T + (size_t)cc * T + t]
+                                              : io_traits<IO>::to_f(raw[(size_t)cc * kRS + t]);
+                        float yv = fmaf(Dd[ch], uv, ysum);
+                        if (has_z) yv *= silu_f(io_traits<IO>::to_f(raw[(size_t)(2 * kCh + cc) * kRS + t]));
+                        store_io(ys + (size_t)cc * kRS + t, yv);
+                    }
                 }
             }
-        }
+        };
+        if (st) scan_tile(BoolC<true>{});
+        else scan_tile(BoolC<false>{});
         if (AGG) {
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {

@@ -50,6 +50,7 @@ struct SeqParams {
     const float *conv_w;   // channel-pair kernel with the conv front: [Dm][conv_k] fp32
     const float *conv_b;   // [Dm] fp32 or null
     int conv_k;            // 1..4
+    int structured;        // channel-pair kernel: 1 = detect structured A per warp, 0 = never
 };
 
 template <typename IO, int NPER, int G, int WARPS, int T>

@@ -10,6 +10,7 @@
 #include <cstring>
 
 #include <cuda.h>
+#include <atomic>
 #include <mutex>
 
 #include "ssm_scan.h"
@@ -29,6 +30,9 @@ using namespace ssm;
 
 constexpr int kTile = 32;
 constexpr int kWarps = 4;
+
+// structured-A detection in the forward scans (ssm_set_structured_a): 1 = on, 0 = off
+std::atomic<int> g_structured_a{0};
 
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -516,6 +520,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
     prm.npad = pl.np;
     prm.zoh = zoh ? 1 : 0;
     prm.conv_w = conv_w; prm.conv_b = conv_b; prm.conv_k = conv_k;
+    prm.structured = g_structured_a.load();
     cudaError_t e = cudaSuccess;
     const bool bf = d.io_dtype == SSM_BF16;
     if (pl.nchunks > 1) {
@@ -1053,6 +1058,8 @@ const char *ssm_status_string(ssm_status_t status) {
         default: return "SSM_ERR_UNKNOWN";
     }
 }
+
+int ssm_set_structured_a(int enable) { return g_structured_a.exchange(enable ? 1 : 0); }
 
 int ssm_version(void) { return (1 << 16) | 0; }
 

@@ -30,7 +30,8 @@ EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_workspace_bytes",
            "ssm_stream_status", "ssm_status_string", "ssm_version",
            "ssm_selective_scan_fwd_noalloc", "ssm_selective_scan_fwd_disc", "ssm_state_update_disc",
            "ssm_conv_selective_scan_fwd", "ssm_conv_selective_scan_workspace_bytes",
-           "ssm_selective_scan_bwd", "ssm_selective_scan_bwd_workspace_bytes")
+           "ssm_selective_scan_bwd", "ssm_selective_scan_bwd_workspace_bytes",
+           "ssm_set_structured_a")
 
 
 class SsmDims(ctypes.Structure):
@@ -89,6 +90,8 @@ def load(path: str = LIB_PATH):
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_version.argtypes = []
     lib.ssm_version.restype = ctypes.c_int
+    lib.ssm_set_structured_a.argtypes = [ctypes.c_int]
+    lib.ssm_set_structured_a.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -283,6 +286,13 @@ def state_update(state, x, dt, A, B, C, D=None, z=None, y=None, stream=None,
 
 def stream_status(stream=None) -> int:
     return int(load().ssm_stream_status(_stream_ptr(stream)))
+
+
+def set_structured_a(enable: bool) -> bool:
+    """Switch the forward scans' run-time structured-A test (A[d, n] == (n + 1) * A[d, 0]
+    for every state of a warp's channels; such warps form the decays from powers of
+    exp(dt * A[d, 0])). Off by default; returns the previous setting. Process-wide."""
+    return bool(load().ssm_set_structured_a(1 if enable else 0))
 
 
 def version() -> Tuple[int, int]:
