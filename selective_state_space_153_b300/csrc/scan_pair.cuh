@@ -79,11 +79,24 @@ struct PairCfg {
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
-// warps per CTA for a lane split: at most 64 channels per CTA (SSM_PAIR_WARPS for GP >= 4)
+// Warps per CTA for a lane split and pass: SSM_PAIR_WARPS (at most 64 channels per CTA) for
+// four or more lanes per pair, fewer for GP < 4; the full pass of the 8-states x 8-lanes
+// split (dstate 33..64) runs SSM_PAIR_WARPS_WIDE warps, so a CTA's B/C conversion and copies
+// serve twice the channels (measured faster for that pass only; narrower CTAs win for the
+// aggregate pass and for the other splits).
 #ifndef SSM_PAIR_WARPS
 #define SSM_PAIR_WARPS 4
 #endif
-constexpr int pair_warps(int gp) { return gp >= 4 ? SSM_PAIR_WARPS : gp; }
+#ifndef SSM_PAIR_WARPS_WIDE
+#define SSM_PAIR_WARPS_WIDE 8
+#endif
+constexpr int pair_warps(int ks, int gp, bool agg) {
+    return gp >= 4 ? ((!agg && ks == 8 && gp == 8) ? SSM_PAIR_WARPS_WIDE : SSM_PAIR_WARPS) : gp;
+}
+// Registers per thread the kernels are held to (launch bounds), so that residency per SM
+// follows from the block size alone: 128, or 168 for sixteen lanes per pair.
+constexpr int pair_reg_budget(int gp) { return gp >= 16 ? 168 : 128; }
+constexpr int pair_min_blocks(int warps, int gp) { return 65536 / (warps * 32 * pair_reg_budget(gp)); }
 
 // S (4 or 8) consecutive io elements from shared memory as floats; the source is aligned to
 // S elements (8 or 16 bytes for bf16, 16 or 32 for fp32)
@@ -118,7 +131,7 @@ __device__ __forceinline__ float2 zoh_phi2(float2 xl2, float2 a, float inv_dt, f
 }
 
 template <typename IO, int KS, int GP, int WARPS, int T, bool AGG, bool ZOH = false, bool CONV = false>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, pair_min_blocks(WARPS, GP))
 scan_pair_kernel(const SeqParams p) {
     using Cfg = PairCfg<IO, KS, GP, WARPS, T, CONV>;
     constexpr int kCh = Cfg::kCh, kPairs = Cfg::kPairs, kQN = Cfg::kQN, kNP = Cfg::kNP, kRS = Cfg::kRS;

@@ -380,9 +380,9 @@ struct PairPlan {
     int ks = 8, gp = 8;          // states per lane per channel, lanes per channel pair
     int nchunks = 1;
     int64_t chunk_len = 0;
-    int chan_blocks = 0;
+    int cb_agg = 0, cb_full = 0;         // channel blocks per batch row, aggregate / full pass
     int np = 0;                  // padded states = ks * gp
-    size_t smem = 0;
+    size_t smem_agg = 0, smem_full = 0;  // dynamic shared memory per CTA of each pass
 };
 
 // smallest power-of-two lane count gp with gp * ks >= N states
@@ -394,8 +394,9 @@ int pair_gp(int64_t N, int ks) {
 
 template <typename IO, int KS, int GP, bool AGG, bool ZOH, bool CONV = false>
 cudaError_t launch_pair_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
-    using Cfg = PairCfg<IO, KS, GP, pair_warps(GP), kPairT, CONV>;
-    auto k = scan_pair_kernel<IO, KS, GP, pair_warps(GP), kPairT, AGG, ZOH, CONV>;
+    constexpr int W = pair_warps(KS, GP, AGG);
+    using Cfg = PairCfg<IO, KS, GP, W, kPairT, CONV>;
+    auto k = scan_pair_kernel<IO, KS, GP, W, kPairT, AGG, ZOH, CONV>;
     static unsigned long long attr_set = 0;  // per instantiation: bit i = set on device i
     int dev = 0;
     cudaGetDevice(&dev);
@@ -433,14 +434,20 @@ cudaError_t launch_pair(const PairPlan &pl, const SeqParams &prm, bool agg, int 
     }
 }
 
-size_t pair_smem(ssm_dtype_t io, int ks, int gp, bool conv) {
+size_t pair_smem(ssm_dtype_t io, int ks, int gp, bool conv, bool agg) {
     switch (ks * 100 + gp) {
 #define SSM_PAIR_SMEM(KS, GP) \
     case KS * 100 + GP: \
-        if (conv) return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(GP), kPairT, true>::kSmem \
-                                        : PairCfg<float, KS, GP, pair_warps(GP), kPairT, true>::kSmem; \
-        return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(GP), kPairT>::kSmem \
-                              : PairCfg<float, KS, GP, pair_warps(GP), kPairT>::kSmem;
+        if (agg) { \
+            if (conv) return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(KS, GP, true), kPairT, true>::kSmem \
+                                            : PairCfg<float, KS, GP, pair_warps(KS, GP, true), kPairT, true>::kSmem; \
+            return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(KS, GP, true), kPairT>::kSmem \
+                                  : PairCfg<float, KS, GP, pair_warps(KS, GP, true), kPairT>::kSmem; \
+        } \
+        if (conv) return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(KS, GP, false), kPairT, true>::kSmem \
+                                        : PairCfg<float, KS, GP, pair_warps(KS, GP, false), kPairT, true>::kSmem; \
+        return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(KS, GP, false), kPairT>::kSmem \
+                              : PairCfg<float, KS, GP, pair_warps(KS, GP, false), kPairT>::kSmem;
         SSM_PAIR_CASES(SSM_PAIR_SMEM)
 #undef SSM_PAIR_SMEM
         default: return 0;
@@ -461,20 +468,31 @@ PairPlan plan_pair(const ssm_dims_t &d, bool conv = false) {
     if (env_is("SSM_PAIR_KS", "4") && N <= 16) { p.ks = 4; p.gp = pair_gp(N, 4); }   // experiments, tests
     if (env_is("SSM_PAIR_KS", "8")) { p.ks = 8; p.gp = pair_gp(N, 8); }
     p.np = p.ks * p.gp;
-    p.smem = pair_smem(d.io_dtype, p.ks, p.gp, conv);
-    if (p.smem == 0) return p;
-    const int64_t warps = pair_warps(p.gp), kch = warps * 64 / p.gp;
-    p.chan_blocks = (int)((d.dim + kch - 1) / kch);
-    // CTAs resident per SM (228 KB of shared memory with 1 KB reserved per CTA, 2048 threads).
-    // The sequence is cut into chunks (aggregate pass + combine + full pass, up to 1.7x the
-    // work) when the channels alone give fewer than two warps per SM sub-partition: the
-    // latency-bound recurrence gains more from the extra warps than the aggregate pass costs
-    // (measured on B300). The chunk count then fills one wave of resident CTAs.
-    const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>((228 * 1024) / (int64_t)(p.smem + 1024),
-                                                                    2048 / (warps * 32)));
-    const int64_t slots = sms * per_sm, base = d.batch * p.chan_blocks;
+    p.smem_agg = pair_smem(d.io_dtype, p.ks, p.gp, conv, true);
+    p.smem_full = pair_smem(d.io_dtype, p.ks, p.gp, conv, false);
+    if (p.smem_agg == 0 || p.smem_full == 0) return p;
+    const int64_t wa = pair_warps(p.ks, p.gp, true), wf = pair_warps(p.ks, p.gp, false);
+    p.cb_agg = (int)((d.dim + wa * 64 / p.gp - 1) / (wa * 64 / p.gp));
+    p.cb_full = (int)((d.dim + wf * 64 / p.gp - 1) / (wf * 64 / p.gp));
+    // CTAs of the full pass resident per SM: shared memory (228 KB, 1 KB reserved per CTA),
+    // threads (2048) and the registers the launch bounds allow.
+    const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(
+        std::min<int64_t>((228 * 1024) / (int64_t)(p.smem_full + 1024), 2048 / (wf * 32)),
+        pair_min_blocks((int)wf, p.gp)));
+    // The sequence is cut into chunks (aggregate pass + combine + full pass) when the channels
+    // alone give fewer than two warps per SM sub-partition: the latency-bound recurrence gains
+    // more from the extra warps than the aggregate pass (up to 1.9x the work) costs. The chunk
+    // count is up to four waves of resident CTAs, as long as a chunk keeps 2048 steps: more
+    // waves even out the tails of the waves (measured on B300 for 1 x 1536 x 131072 x 64);
+    // chunks of a few hundred steps lose to their fixed costs.
+    const int64_t slots = sms * per_sm, base = d.batch * p.cb_full;
     int64_t nc = 1;
-    if (base * warps < 8 * sms) nc = std::max<int64_t>(1, slots / base);
+    if (base * wf < 8 * sms) {
+        const int64_t wave = std::max<int64_t>(1, slots / base);
+        int64_t w = 4;
+        while (w > 1 && d.seqlen < wave * w * 2048) --w;
+        nc = wave * w;
+    }
     if (const char *env = std::getenv("SSM_PAIR_CHUNKS")) nc = std::max(1, std::atoi(env));   // experiments
     nc = std::min<int64_t>(nc, std::max<int64_t>(1, d.seqlen / (4 * kPairT)));
     nc = std::min<int64_t>(nc, 4096);
@@ -516,7 +534,6 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
     prm.Bt = d.batch; prm.Dm = d.dim; prm.L = d.seqlen; prm.N = d.dstate;
     prm.softplus = delta_softplus ? 1 : 0;
     prm.chunk_len = pl.chunk_len; prm.nchunks = pl.nchunks;
-    prm.chan_blocks = pl.chan_blocks;
     prm.npad = pl.np;
     prm.zoh = zoh ? 1 : 0;
     prm.conv_w = conv_w; prm.conv_b = conv_b; prm.conv_k = conv_k;
@@ -530,6 +547,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
         prm.agg_h = reinterpret_cast<float *>(w);
         prm.agg_s = reinterpret_cast<float *>(w + up((size_t)pl.nchunks * BD * np * 4));
         float *hin = reinterpret_cast<float *>(w + up((size_t)pl.nchunks * BD * np * 4) + up((size_t)pl.nchunks * BD * 4));
+        prm.chan_blocks = pl.cb_agg;
         e = bf ? launch_pair<bf16>(pl, prm, true, pl.nchunks - 1, s) : launch_pair<float>(pl, prm, true, pl.nchunks - 1, s);
         if (e == cudaSuccess) {
             const int64_t total = (int64_t)BD * pl.np;
@@ -539,6 +557,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
         }
         prm.hin = hin;
     }
+    prm.chan_blocks = pl.cb_full;
     if (e == cudaSuccess)
         e = bf ? launch_pair<bf16>(pl, prm, false, pl.nchunks, s) : launch_pair<float>(pl, prm, false, pl.nchunks, s);
     if (allocated) cudaFreeAsync(workspace, s);

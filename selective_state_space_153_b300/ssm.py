@@ -22,7 +22,7 @@ SSM_F32, SSM_BF16 = 0, 1
 SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
 _DISC = {"euler": SSM_DISC_EULER, "zoh": SSM_DISC_ZOH}
 MAX_DSTATE = 128
-SCRATCH_MAX_BYTES = 16 * 1024 * 1024   # SSM_SCRATCH_MAX_BYTES: the no-alloc entry's fixed scratch
+SCRATCH_MAX_BYTES = 48 * 1024 * 1024   # SSM_SCRATCH_MAX_BYTES: the no-alloc entry's fixed scratch
 
 # every symbol include/ssm_scan.h declares
 EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_workspace_bytes",

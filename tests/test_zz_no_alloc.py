@@ -33,7 +33,7 @@ def test_scratch_size_matches_header():
     val = 1
     for f in m.group(1).split("*"):
         val *= int(f)
-    assert val == ssm.SCRATCH_MAX_BYTES == 16 * 1024 * 1024
+    assert val == ssm.SCRATCH_MAX_BYTES == 48 * 1024 * 1024
 
 
 @pytest.fixture
