@@ -16,6 +16,7 @@ during the timed region.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -37,10 +38,9 @@ EX2_PER_CLK_SM = 32          # measured on B300: MUFU ex2.approx.f32 issue rate 
 FALLBACK_HBM_GBS = 6400.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per scan call of the long-sequence workload
-# (aggregate pass + combine + full pass), from the ncu capture of the same kernels on the
-# 1/8-length case scaled by 8 (traffic grows with L): profiles/scan_pair_long16k_full.md.
-# Valid for the default workload only; None elsewhere.
-TRAFFIC_BYTES_PER_LAUNCH = {"long128k": 8 * (96.36 + 3.08 + 4.80 + 112.57 + 22.51) * 1e6}
+# (aggregate pass + combine + full pass), from a one-pass ncu capture of the full-size call:
+# profiles/scan_pair_long128k_traffic.md. Valid for the default workload only; None elsewhere.
+TRAFFIC_BYTES_PER_LAUNCH = {"long128k": (822594048 + 18120192) + 19176448 + (881697280 + 377892864)}
 
 
 def count_kernel_launches(fn):
@@ -236,11 +236,17 @@ def bench_ours(args, rank, ws, local):
     # exponential per element, the SFU roofline's premise; the library's default). The
     # structured-A path, which the generator's A = -(n+1) would pass, is timed separately.
     ssm.set_structured_a(False)
+    # The chunk-carry workspace is allocated once, outside the timed region, and passed in
+    # (ssm_selective_scan_fwd_ws), so that the device times hold the scan kernels and not the
+    # stream-ordered allocator; the end-to-end line keeps the allocating host entry point.
+    io_code = ssm.SSM_BF16 if cfg.io == "bf16" else ssm.SSM_F32
+    scan_ws = torch.empty(max(1, ssm.workspace_bytes(cfg.Bt, cfg.D, cfg.L, cfg.N, io_code)), dtype=torch.uint8,
+                          device=dev)
 
     def step():
         ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
                                delta_bias=g["delta_bias"], delta_softplus=cfg.softplus, y=y, last_state=last,
-                               stream=stream)
+                               stream=stream, workspace=scan_ws)
 
     def timed(fn):
         """ms per call of fn: warm-up, then args.steps calls between events on `stream`."""
@@ -324,7 +330,7 @@ def bench_ours(args, rank, ws, local):
         def zstep():
             ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
                                    delta_bias=g["delta_bias"], delta_softplus=cfg.softplus, y=y, last_state=last,
-                                   stream=stream, discretization="zoh")
+                                   stream=stream, workspace=scan_ws, discretization="zoh")
         zms = timed(zstep)
         out["zoh"] = {"discretization": "exact zero-order hold (exp(dt*A) - 1)/A * B",
                       "ms_per_step": zms, "value": weak_scaling_value(elems, ws, zms / 1e3), "unit": "elem/s",
@@ -336,10 +342,13 @@ def bench_ours(args, rank, ws, local):
         cw = (torch.randn(cfg.D, 4, generator=gw) * 0.5).to(dev)
         cbias = (torch.randn(cfg.D, generator=gw) * 0.2).to(dev)
 
+        cws = torch.empty(max(1, int(ssm.load().ssm_conv_selective_scan_workspace_bytes(
+            ctypes.byref(ssm.dims(cfg.Bt, cfg.D, cfg.L, cfg.N, io_code))))), dtype=torch.uint8, device=dev)
+
         def cstep():
             ssm.conv_selective_scan_fwd(g["u"], cw, cbias, g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
                                         delta_bias=g["delta_bias"], delta_softplus=cfg.softplus, y=y,
-                                        last_state=last, stream=stream)
+                                        last_state=last, stream=stream, workspace=cws)
         cms = timed(cstep)
         out["conv_front"] = {"fused": "causal depthwise conv1d (K=4) + bias + SiLU in front of the scan",
                              "ms_per_step": cms, "value": weak_scaling_value(elems, ws, cms / 1e3), "unit": "elem/s",
