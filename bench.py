@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6400.0
 # dram__bytes_read.sum + dram__bytes_write.sum per scan call of the long-sequence workload
 # (aggregate pass + combine + full pass), from a one-pass ncu capture of the full-size call:
 # profiles/scan_pair_long128k_traffic.md. Valid for the default workload only; None elsewhere.
-TRAFFIC_BYTES_PER_LAUNCH = {"long128k": (822594048 + 18120192) + 19176448 + (881697280 + 377892864)}
+TRAFFIC_BYTES_PER_LAUNCH = {"long128k": (811089408 + 19332864) + 21572608 + (865208320 + 374617344)}
 
 
 def count_kernel_launches(fn):

@@ -141,7 +141,7 @@ ssm_status_t ssm_selective_scan_fwd_ws(const ssm_dims_t *dims, const void *u,
  *
  * Scratch size: returns SSM_ERR_WORKSPACE, before any CUDA work is queued, when
  * ssm_selective_scan_workspace_bytes(dims) exceeds SSM_SCRATCH_MAX_BYTES. The default plans
- * keep only chunk carries there (1 x 1536 x 131072 x 64 needs about 36 MiB and fits); a plan
+ * keep only chunk carries there (1 x 1536 x 131072 x 64 needs about 41 MiB and fits); a plan
  * that also keeps the whole sequence's B and C there (the persistent time-split kernel,
  * about 65 MiB for that shape) is rejected. Use ssm_selective_scan_fwd_ws for those.
  * Zero state: the control words at the start of the scratch (the persistent kernel's

@@ -72,7 +72,7 @@ struct PairCfg {
     static constexpr size_t kOffCw = kOffSu + kSuBytes;
     static constexpr size_t kCwBytes = CONV ? (size_t)kCh * 9 * sizeof(float) : 0;
     static constexpr size_t kSmem = kOffCw + kCwBytes;
-    static_assert(KS == 4 || KS == 8, "states per lane per channel: 4 or 8");
+    static_assert(KS == 4 || KS == 8 || KS == 16, "states per lane per channel: 4, 8 or 16");
     static_assert(GP == 1 || GP == 2 || GP == 4 || GP == 8 || GP == 16, "lanes per pair");
     static_assert(T % 8 == 0 && T % GP == 0 && T % kEpr == 0, "tile: whole 16-byte pieces and reduce groups");
     static_assert((kRS * sizeof(IO)) % 16 == 0 && kRawBytes % 16 == 0, "16-byte aligned raw rows");
@@ -94,9 +94,10 @@ constexpr int pair_warps(int ks, int gp, bool agg) {
     return gp >= 4 ? ((!agg && ks == 8 && gp == 8) ? SSM_PAIR_WARPS_WIDE : SSM_PAIR_WARPS) : gp;
 }
 // Registers per thread the kernels are held to (launch bounds), so that residency per SM
-// follows from the block size alone: 128, or 168 for sixteen lanes per pair.
-constexpr int pair_reg_budget(int gp) { return gp >= 16 ? 168 : 128; }
-constexpr int pair_min_blocks(int warps, int gp) { return 65536 / (warps * 32 * pair_reg_budget(gp)); }
+// follows from the block size alone: 128, or 168 for sixteen lanes per pair and for sixteen
+// states per lane (whose 32 states and 32 decay factors per lane spill under 128).
+constexpr int pair_reg_budget(int ks, int gp) { return (gp >= 16 || ks >= 16) ? 168 : 128; }
+constexpr int pair_min_blocks(int warps, int ks, int gp) { return 65536 / (warps * 32 * pair_reg_budget(ks, gp)); }
 
 // S (4 or 8) consecutive io elements from shared memory as floats; the source is aligned to
 // S elements (8 or 16 bytes for bf16, 16 or 32 for fp32)
@@ -131,7 +132,7 @@ __device__ __forceinline__ float2 zoh_phi2(float2 xl2, float2 a, float inv_dt, f
 }
 
 template <typename IO, int KS, int GP, int WARPS, int T, bool AGG, bool ZOH = false, bool CONV = false>
-__global__ void __launch_bounds__(WARPS * 32, pair_min_blocks(WARPS, GP))
+__global__ void __launch_bounds__(WARPS * 32, pair_min_blocks(WARPS, KS, GP))
 scan_pair_kernel(const SeqParams p) {
     using Cfg = PairCfg<IO, KS, GP, WARPS, T, CONV>;
     constexpr int kCh = Cfg::kCh, kPairs = Cfg::kPairs, kQN = Cfg::kQN, kNP = Cfg::kNP, kRS = Cfg::kRS;

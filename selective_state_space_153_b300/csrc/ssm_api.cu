@@ -422,7 +422,7 @@ cudaError_t launch_pair_g(const SeqParams &prm, bool agg, int grid_y, cudaStream
                : launch_pair_t<IO, KS, GP, false, false>(prm, grid_y, s);
 }
 
-#define SSM_PAIR_CASES(X) X(4, 1) X(4, 2) X(4, 4) X(8, 1) X(8, 2) X(8, 4) X(8, 8) X(8, 16)
+#define SSM_PAIR_CASES(X) X(4, 1) X(4, 2) X(4, 4) X(8, 1) X(8, 2) X(8, 4) X(8, 8) X(8, 16) X(16, 4)
 
 template <typename IO>
 cudaError_t launch_pair(const PairPlan &pl, const SeqParams &prm, bool agg, int grid_y, cudaStream_t s) {
@@ -465,8 +465,15 @@ PairPlan plan_pair(const ssm_dims_t &d, bool conv = false) {
     p.ks = 8;
     p.gp = pair_gp(N, 8);
     if (N <= 16 && (BD * p.gp + 63) / 64 < 4 * sms) { p.ks = 4; p.gp = pair_gp(N, 4); }
+    // sixteen states per lane for 33..64 states where the sequence will be chunked (eight
+    // states per lane give fewer than two warps per SM sub-partition): the y reduction and the
+    // per-step dt loads are shared by twice the states (measured on B300 for
+    // 1 x 1536 x 131072 x 64: full pass 2.85 -> 2.73 ms at 3 CTAs per SM). Not with the conv
+    // front, whose per-channel window work does not shrink with it (5.34 -> 5.63 ms there).
+    if (!conv && N > 32 && N <= 64 && BD * p.gp / 64 < 8 * sms) { p.ks = 16; p.gp = pair_gp(N, 16); }
     if (env_is("SSM_PAIR_KS", "4") && N <= 16) { p.ks = 4; p.gp = pair_gp(N, 4); }   // experiments, tests
     if (env_is("SSM_PAIR_KS", "8")) { p.ks = 8; p.gp = pair_gp(N, 8); }
+    if (env_is("SSM_PAIR_KS", "16") && N > 32 && N <= 64) { p.ks = 16; p.gp = pair_gp(N, 16); }
     p.np = p.ks * p.gp;
     p.smem_agg = pair_smem(d.io_dtype, p.ks, p.gp, conv, true);
     p.smem_full = pair_smem(d.io_dtype, p.ks, p.gp, conv, false);
@@ -478,7 +485,7 @@ PairPlan plan_pair(const ssm_dims_t &d, bool conv = false) {
     // threads (2048) and the registers the launch bounds allow.
     const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(
         std::min<int64_t>((228 * 1024) / (int64_t)(p.smem_full + 1024), 2048 / (wf * 32)),
-        pair_min_blocks((int)wf, p.gp)));
+        pair_min_blocks((int)wf, p.ks, p.gp)));
     // The sequence is cut into chunks (aggregate pass + combine + full pass) when the channels
     // alone give fewer than two warps per SM sub-partition: the latency-bound recurrence gains
     // more from the extra warps than the aggregate pass (up to 1.9x the work) costs. The chunk

@@ -57,6 +57,7 @@ CASES = [
     (1, 40, 2000, 64, "f32", False, "ones", "8", 5),     # the long-sequence lane split, chunked
     (1, 20, 520, 128, "bf16", True, "ones", "8", 4),
     (2, 33, 40, 128, "f32", False, "normal", "8", 1),    # a short ragged tile
+    (1, 40, 2000, 64, "f32", False, "ones", "16", 5),    # sixteen states per lane
 ]
 
 
