@@ -65,6 +65,22 @@ def workload_config(args):
     return replace(cfg, L=args.seqlen) if args.seqlen > 0 else cfg
 
 
+def scan_io_bytes(cfg) -> int:
+    """Algorithmic HBM bytes of one scan call: every input read once, every output written once."""
+    esz = 2 if cfg.io == "bf16" else 4
+    return (cfg.Bt * cfg.D * cfg.L * esz * (3 + (1 if cfg.gate else 0))      # u, delta, (z), y
+            + 2 * cfg.Bt * cfg.N * cfg.L * esz + cfg.D * cfg.N * 4 + 2 * cfg.D * 4
+            + (cfg.Bt * cfg.D * cfg.N * 4 if cfg.last_state else 0))
+
+
+def config_json(cfg) -> dict:
+    """The bench line's `config`, identical for both arms."""
+    return {"workload": f"{cfg.name}: selective scan Bt={cfg.Bt} D={cfg.D} L={cfg.L} N={cfg.N} "
+                        f"io={cfg.io} gate={cfg.gate} last_state={cfg.last_state}",
+            "batch": cfg.Bt, "dim": cfg.D, "seqlen": cfg.L, "dstate": cfg.N, "io": cfg.io,
+            "l2": "inputs larger than L2 (%.0f MB per step)" % (scan_io_bytes(cfg) / 1e6)}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -284,10 +300,7 @@ def bench_ours(args, rank, ws, local):
     assert ssm.stream_status(stream) == ssm.SSM_OK
 
     elems = cfg.elements
-    esz = 2 if cfg.io == "bf16" else 4
-    io_bytes = (cfg.Bt * cfg.D * cfg.L * esz * (3 + (1 if cfg.gate else 0))      # u, delta, (z), y
-                + 2 * cfg.Bt * cfg.N * cfg.L * esz + cfg.D * cfg.N * 4 + 2 * cfg.D * 4
-                + (cfg.Bt * cfg.D * cfg.N * 4 if cfg.last_state else 0))
+    io_bytes = scan_io_bytes(cfg)
     t_step = ms_max / args.steps / 1e3
     peaks, peak_kind = measured_peaks()
     clocks = sampler.summary()
@@ -303,12 +316,9 @@ def bench_ours(args, rank, ws, local):
         "metric": "scan elements/s (B*D*L*N/s); fraction of the max(HBM, SFU) roofline; decode tok/s",
         "value": weak_scaling_value(elems, ws, t_step), "unit": "elem/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 compute, bf16 io" if cfg.io == "bf16" else "f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded generator, PCG64)",
-        "config": {"workload": f"{cfg.name}: selective scan Bt={cfg.Bt} D={cfg.D} L={cfg.L} N={cfg.N} "
-                               f"io={cfg.io} gate={cfg.gate} last_state={cfg.last_state}",
-                   "batch": cfg.Bt, "dim": cfg.D, "seqlen": cfg.L, "dstate": cfg.N,
-                   "l2": "inputs larger than L2 (%.0f MB per step)" % (io_bytes / 1e6)},
+        "config": config_json(cfg),
         "tokens_per_s": ws * cfg.Bt * cfg.L / t_step,
         "roofline": {"bound": "alu", "achieved": achieved, "peak": ex2_peak, "unit": "Gexp/s",
                      "frac": achieved / ex2_peak,
@@ -535,8 +545,7 @@ def bench_reference(args, rank, ws):
             "value": v, "unit": "elem/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded generator, PCG64)",
-            "config": {"workload": f"{cfg.name}: selective scan Bt={cfg.Bt} D={cfg.D} L={cfg.L} N={cfg.N} io={cfg.io}",
-                       "batch": cfg.Bt, "dim": cfg.D, "seqlen": cfg.L, "dstate": cfg.N},
+            "config": config_json(cfg),
             "cpu_baseline": {"value": v, "unit": "elem/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
