@@ -465,12 +465,18 @@ PairPlan plan_pair(const ssm_dims_t &d, bool conv = false) {
     p.ks = 8;
     p.gp = pair_gp(N, 8);
     if (N <= 16 && (BD * p.gp + 63) / 64 < 4 * sms) { p.ks = 4; p.gp = pair_gp(N, 4); }
-    // sixteen states per lane for 33..64 states where the sequence will be chunked (eight
-    // states per lane give fewer than two warps per SM sub-partition): the y reduction and the
-    // per-step dt loads are shared by twice the states (measured on B300 for
-    // 1 x 1536 x 131072 x 64: full pass 2.85 -> 2.73 ms at 3 CTAs per SM). Not with the conv
-    // front, whose per-channel window work does not shrink with it (5.34 -> 5.63 ms there).
-    if (!conv && N > 32 && N <= 64 && BD * p.gp / 64 < 8 * sms) { p.ks = 16; p.gp = pair_gp(N, 16); }
+    // sixteen states per lane for 33..64 states where a long sequence (>= 65536 steps) will
+    // be chunked (eight states per lane give fewer than two warps per SM sub-partition): the y
+    // reduction and the per-step dt loads are shared by twice the states, at 3 CTAs per SM
+    // instead of 16 warps. Measured on B300 against eight states per lane: 1 x 1536 x 131072
+    // x 64 4.77 vs 4.89 ms, 1 x 768 x 131072 2.41 vs 2.50, 1 x 2560 x 65536 3.95 vs 4.09,
+    // 2 x 1536 x 65536 equal; shorter sequences lost (4 x 1536 x 16384 2.54 vs 2.37 ms,
+    // 1 x 5120 x 32768 4.08 vs 4.04). Not with the conv front, whose per-channel window work
+    // does not shrink with it (5.34 -> 5.63 ms on the first shape).
+    if (!conv && N > 32 && N <= 64 && d.seqlen >= 65536 && BD * p.gp / 64 < 8 * sms) {
+        p.ks = 16;
+        p.gp = pair_gp(N, 16);
+    }
     if (env_is("SSM_PAIR_KS", "4") && N <= 16) { p.ks = 4; p.gp = pair_gp(N, 4); }   // experiments, tests
     if (env_is("SSM_PAIR_KS", "8")) { p.ks = 8; p.gp = pair_gp(N, 8); }
     if (env_is("SSM_PAIR_KS", "16") && N > 32 && N <= 64) { p.ks = 16; p.gp = pair_gp(N, 16); }
