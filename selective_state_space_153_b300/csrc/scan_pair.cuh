@@ -9,7 +9,8 @@
 // y + x*D and the SiLU(z) gate; dt = softplus(delta + bias) (sections 3.2-3.3).
 //
 // Work decomposition (one CTA): batch row b, kCh = WARPS*2*(32/GP) consecutive channels,
-// one chunk [l_begin, l_end) of the sequence walked in tiles of T timesteps.
+// one chunk [l_begin, l_end) of the sequence walked in tiles of T timesteps. KS is 4, 8 or
+// 16 states per lane and channel; the planner picks it and the CTA width per pass.
 //   lane (warp w, lane l): pair P = w*(32/GP) + l/GP -> channels 2P and 2P+1 of the block;
 //   state group g = l%GP owns the states n = 4*(GP*q + g) + j (q < KS/4, j < 4), so the GP
 //   groups of a pair read GP adjacent 16-byte pieces of a B/C row (one wavefront per
