@@ -93,6 +93,34 @@ def test_workspace_query(lib):
     assert lib.ssm_selective_scan_workspace_bytes(None) == 0
 
 
+def _chunks_from_workspace(Bt, Dm, L, N):
+    """Chunk count of the pair kernel's plan, read back from its workspace size: two
+    [chunks][Bt*Dm][64] fp32 carry arrays and one [chunks][Bt*Dm] fp32 dt-sum array, each
+    rounded up to 256 bytes (64 padded states at N = 64)."""
+    ws = ssm.workspace_bytes(Bt, Dm, L, N)
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for nc in range(1, 4097):
+        bd = Bt * Dm
+        if 2 * up(nc * bd * 64 * 4) + up(nc * bd * 4) == ws:
+            return nc
+    raise AssertionError(f"workspace {ws} matches no chunk count")
+
+
+@pytest.mark.parametrize("shape,chunks", [
+    # sixteen states per lane, 3 CTAs per SM: 18 CTAs of 64 channels per wave, three waves
+    # of chunks while a chunk keeps >= 2048 steps
+    ((1, 1536, 131072, 64), 54),
+    ((1, 768, 131072, 64), 37),
+    # shorter sequences keep eight states per lane (8-warp full-pass CTAs, 2 per SM)
+    ((1, 1536, 16384, 64), 12),
+    ((4, 1536, 16384, 64), 6),
+])
+def test_planner_chunk_counts(lib, shape, chunks):
+    """The long-sequence plans the bench and the parity tests run (148 SMs, the B300 count,
+    is also the planner's fallback when no GPU is present)."""
+    assert _chunks_from_workspace(*shape) == chunks
+
+
 def test_ws_entry_rejects_small_workspace(lib):
     d = ssm.dims(1, 1536, 131072, 64, ssm.SSM_BF16)
     need = ssm.workspace_bytes(1, 1536, 131072, 64)
