@@ -97,9 +97,11 @@ typedef struct {
  *                   or NULL.
  *   stream          cudaStream_t the work is queued on.
  * Sequences are split into chunks processed in parallel when batch*dim alone cannot fill
- * the GPU; the chunk states then pass through a workspace that the library allocates
- * stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`) unless one was given with
- * ssm_selective_scan_fwd_ws.
+ * the GPU; the chunk states then pass through a workspace: the one registered for the
+ * current device with ssm_set_workspace if there is one (SSM_ERR_WORKSPACE if it is too
+ * small; nothing is allocated then), else one the library allocates stream-ordered
+ * (cudaMallocAsync / cudaFreeAsync on `stream`). ssm_selective_scan_fwd_ws takes a
+ * workspace per call instead.
  */
 ssm_status_t ssm_selective_scan_fwd(const ssm_dims_t *dims, const void *u, const void *delta,
                                     const float *A, const void *B, const void *C,
@@ -120,6 +122,31 @@ ssm_status_t ssm_selective_scan_fwd_ws(const ssm_dims_t *dims, const void *u,
                                        const float *delta_bias, int delta_softplus, void *y,
                                        float *last_state, void *workspace,
                                        size_t workspace_bytes, void *stream);
+
+/*
+ * Registers a process-wide default workspace for the current CUDA device (the workspace of
+ * the split-sequence carries: "Mamba architecture principles and industrial long-text
+ * practice", jsqmd.com, section 3.4, a long sequence cut into chunks whose states are passed
+ * on; lmnt.cn "From RNN to Mamba" section 5.3 keeps the recurrent state in a fixed buffer).
+ *   dev_ptr  device memory of the current device, 16-byte aligned, or NULL to unregister
+ *            (the library then allocates stream-ordered again).
+ *   bytes    its size; 0 with dev_ptr NULL.
+ * Used by ssm_selective_scan_fwd, and by ssm_selective_scan_fwd_disc,
+ * ssm_conv_selective_scan_fwd and ssm_selective_scan_bwd when they are given a NULL
+ * workspace, for calls on this device: a call that needs more than `bytes` returns
+ * SSM_ERR_WORKSPACE before queuing any work, and nothing is allocated while a workspace is
+ * registered. ssm_selective_scan_workspace_bytes (and the _conv_ / _bwd_ variants) give
+ * the size a call needs.
+ * Ownership: the caller keeps the memory; it must stay valid until every call that used it
+ * has completed on its stream. The library never frees it.
+ * Concurrency: calls that use the registered workspace and overlap on the GPU race on it,
+ * whichever streams or host threads issue them: queue them on one stream or order them
+ * with events. ssm_selective_scan_fwd_host never uses it.
+ * Returns SSM_OK; SSM_ERR_NULL (dev_ptr NULL, bytes > 0); SSM_ERR_WORKSPACE (bytes 0 with a
+ * pointer); SSM_ERR_ALIGN; SSM_ERR_CUDA (no current device); SSM_ERR_UNSUPPORTED (device
+ * index >= 64). Takes effect for calls made after it returns.
+ */
+ssm_status_t ssm_set_workspace(void *dev_ptr, size_t bytes);
 
 /* Size of the library's fixed device scratch used by ssm_selective_scan_fwd_noalloc. */
 #define SSM_SCRATCH_MAX_BYTES ((size_t)48 * 1024 * 1024)
@@ -311,6 +338,54 @@ ssm_status_t ssm_stream_status(void *stream);
  * setting (0 or 1). Never fails.
  */
 int ssm_set_structured_a(int enable);
+
+/*
+ * Launch-plan override: a test and tuning hook, not needed for normal use. The library reads
+ * no environment variables; tests and tuning runs that want a particular kernel, lane split
+ * or chunk count set it here. Every field 0 means the planner's own choice. Process-wide;
+ * takes effect for calls made after it returns (and for ssm_*_workspace_bytes).
+ *   kernel                  SSM_KERNEL_AUTO (the planner), SSM_KERNEL_PAIR (the channel-pair
+ *                           kernel where the rows allow it), SSM_KERNEL_SEQ (the sequential-
+ *                           lane kernel), SSM_KERNEL_TC / SSM_KERNEL_TP (the persistent
+ *                           time-split kernels, barrier-phased / pipelined: they keep a
+ *                           stretch's decays in tensor memory and chain segment carries
+ *                           through release/acquire flags with a bounded wait).
+ *   pair_states_per_lane    channel-pair kernel: 4 (dstate <= 16), 8, or 16 (33..64 states).
+ *   chunks                  the number of sequence chunks of the channel-pair or sequential-
+ *                           lane kernel (clamped to what the sequence length allows).
+ *   seq_states_per_lane, seq_lanes_per_channel
+ *                           sequential-lane split; both 0, or one of the built pairs (4,1),
+ *                           (8,1), (16,1), (4,4), (16,2), (16,4), (16,8).
+ *   decode_elementwise      1: the recurrent step reads B and C element by element.
+ *   force_timeout           1: the persistent kernels' carry wait watches a flag that nothing
+ *                           sets, with a short limit, so that it gives up and records
+ *                           SSM_ERR_TIMEOUT (read by ssm_stream_status); tests the failure
+ *                           path without faulting anything.
+ * ssm_set_plan_override(NULL) restores the planner. Returns SSM_ERR_UNSUPPORTED for an
+ * unknown kernel, lane split or states-per-lane value and SSM_ERR_SHAPE for a negative count;
+ * the previous override then stays in force.
+ */
+typedef enum {
+    SSM_KERNEL_AUTO = 0,
+    SSM_KERNEL_PAIR = 1,
+    SSM_KERNEL_SEQ = 2,
+    SSM_KERNEL_TC = 3,
+    SSM_KERNEL_TP = 4
+} ssm_kernel_t;
+
+typedef struct {
+    int kernel;
+    int pair_states_per_lane;
+    int chunks;
+    int seq_states_per_lane;
+    int seq_lanes_per_channel;
+    int decode_elementwise;
+    int force_timeout;
+} ssm_plan_override_t;
+
+ssm_status_t ssm_set_plan_override(const ssm_plan_override_t *ov);
+/* The override in force (all zero when none); SSM_ERR_NULL for a NULL `out`. */
+ssm_status_t ssm_get_plan_override(ssm_plan_override_t *out);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char *ssm_status_string(ssm_status_t status);

@@ -6,23 +6,24 @@
  * baseline may load this file's library. It shares no code, header, table or helper with
  * the CUDA path, and the CUDA path never calls it.
  *
- * What it computes, restated from the source pages (no blocking, no reordering, no
- * parallel algorithm; every quantity in double):
+ * What it computes: the definition of the discretised selective state-space model, in
+ * double, one timestep after another (no blocking, no reordering, no parallel algorithm).
+ * The equations, per batch row b, channel d and state n, for t = 0, 1, ..., L-1:
  *
- *   "From RNN to Mamba: state-space model principles and long-sequence modelling in
- *   practice" (lmnt.cn/news/271401), section 3.2 ("implementation details of the
- *   selective scan"), the naive per-timestep loop over t:
- *       dt_t   = softplus(raw step)                      (the step is input-dependent)
- *       A_bar  = exp(dt_t * A)                           (A diagonal, so elementwise)
- *       B_bar  = dt_t * B_t
- *       h      = A_bar * h + B_bar * x_t
- *       y_t    = sum_n h[n] * C_t[n]
- *   and after the loop  y = y + x * D  and  out = y * SiLU(z).
- *   Section 2.2 of the same page: A is diagonal, so the state update is elementwise.
- *   Section 3.3: a dt bias added before the softplus sets the step range.
- *   Section 5.3: recurrent inference keeps one fixed-size fp32 state per channel and
- *   advances it one token at a time -- that is oracle_state_update below, which is the
- *   same recurrence for one step with the (already positive) step given directly.
+ *   (1) step        dt_t = softplus(delta_t + bias)        input-dependent step; bias added
+ *                                                           before the softplus (lmnt.cn
+ *                                                           "From RNN to Mamba", section 3.3)
+ *   (2) discretise  A_bar_t[n] = exp(dt_t * A[n])           A diagonal, so the matrix
+ *                   B_bar_t[n] = dt_t * B_t[n]              exponential is elementwise
+ *                                                           (same page, sections 2.2, 3.2)
+ *   (3) recurrence  h_t[n] = A_bar_t[n] h_{t-1}[n] + B_bar_t[n] u_t,   h_{-1} = 0
+ *   (4) readout     y_t = sum_n C_t[n] h_t[n] + D u_t,  then y_t * SiLU(z_t)
+ *                                                           (section 3.2: output C h plus
+ *                                                           the D skip term, gated by z)
+ *
+ * Section 5.3 of the same page: recurrent inference keeps one fixed-size fp32 state per
+ * channel and advances it one token at a time -- that is oracle_state_update below, the
+ * same equations (2)-(4) for one step with the (already positive) step given directly.
  *
  * Readings where the pages are silent or disagree (each also listed in the design notes):
  *   - B_bar = dt * B (the page's code) by default. The exact zero-order-hold variant of
@@ -53,7 +54,7 @@ static double silu(double v) { return v / (1.0 + exp(-v)); }
 /* expm1(x)/x, the factor that turns dt*B into the zero-order-hold B_bar; 1 at x = 0 */
 static double zoh_factor(double x) { return x == 0.0 ? 1.0 : expm1(x) / x; }
 
-/* One channel: the loop of the page, in its order. */
+/* One channel: equations (1)-(4) above, one timestep after another. */
 static void scan_one_channel(int64_t L, int64_t N,
                              const double *u, const double *delta, const double *A,
                              const double *B, const double *C, /* [N][L] of this batch row */

@@ -1,9 +1,14 @@
 """Build the CUDA library libssm_scan.so in-tree (sm_103a only).
 
-    python -m selective_state_space_153_b300.build
+    python -m selective_state_space_153_b300.build [--force]
+
+Every kernel family is its own translation unit (csrc/k_*.cu, plus the host logic in
+csrc/ssm_api.cu), compiled as relocatable device code in parallel and linked into one shared
+library (the device status word is defined once, in ssm_api.cu).
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import os
 import subprocess
 import sys
@@ -13,9 +18,13 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libssm_scan.so")
-SOURCES = ["ssm_api.cu"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-              "-Xcompiler", "-fPIC", "-shared", "--expt-relaxed-constexpr"]
+OBJ = os.path.join(PKG, "_build")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
+
+
+def sources():
+    return sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
 def _nvcc() -> str:
@@ -24,27 +33,54 @@ def _nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _deps():
+    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "ssm_scan.h"),
+                                                                 os.path.abspath(__file__)]
+
+
+def _stale(target: str, deps) -> bool:
+    if not os.path.exists(target):
         return True
-    t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "ssm_scan.h")]
+    t = os.path.getmtime(target)
     return any(os.path.getmtime(f) > t for f in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and not _stale():
-        return LIB
-    tmp = LIB + ".tmp"
-    cmd = [_nvcc(), *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-o", tmp,
-           *[os.path.join(CSRC, s) for s in SOURCES]]
+def build(force: bool = False, verbose: bool = False, extra=(), lib: str = LIB, objdir: str = OBJ,
+          jobs: int = 0) -> str:
+    """Compile every csrc/*.cu (in parallel) and link ``lib``. ``extra``: additional nvcc
+    flags (e.g. ``-DSSM_CHECK``; a build with extra flags should name its own ``lib`` and
+    ``objdir``)."""
+    deps = _deps()
+    if not force and not _stale(lib, deps):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
+    nvcc = _nvcc()
+    objs = []
+
+    def compile_one(src):
+        obj = os.path.join(objdir, src[:-3] + ".o")
+        cmd = [nvcc, *NVCC_FLAGS, *extra, "-dc", "-I", INCLUDE, "-I", CSRC, "-o", obj + ".tmp",
+               os.path.join(CSRC, src)]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src} ({r.returncode}):\n{r.stderr[-8000:]}")
+        os.replace(obj + ".tmp", obj)
+        return obj
+
+    srcs = sources()
+    with cf.ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, srcs))
+    tmp = lib + ".tmp"
+    cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed ({r.returncode}):\n{r.stderr[-8000:]}")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link failed ({r.returncode}):\n{r.stderr[-8000:]}")
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

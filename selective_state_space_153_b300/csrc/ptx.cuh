@@ -8,8 +8,9 @@
 
 namespace ssm {
 
-// device status word read by ssm_stream_status (0 = OK); set by bounded waits that gave up
-__device__ int g_ssm_status = 0;
+// device status word read by ssm_stream_status (0 = OK); set by bounded waits that gave up.
+// Defined once in ssm_api.cu (the library is built with relocatable device code).
+extern __device__ int g_ssm_status;
 
 __device__ __forceinline__ void set_status(int code) { atomicCAS(&g_ssm_status, 0, code); }
 

@@ -1,43 +1,83 @@
 // Host side of the C ABI declared in include/ssm_scan.h: argument checks, launch planning,
-// kernel dispatch, workspace handling and the host-buffer pipeline.
+// kernel dispatch (launch.h; the kernels live in the k_*.cu translation units), workspace
+// handling and the host-buffer pipeline.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
-
-#include <cuda.h>
-#include <atomic>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "ssm_scan.h"
-#include "common.cuh"
-#include "ptx.cuh"
-#include "decode.cuh"
-#include "scan_seq.cuh"
-#include "scan_tc.cuh"
+#include "launch.h"
 #include "scan_tp.cuh"
-#include "scan_pair.cuh"
-#include "scan_bwd.cuh"
+
+namespace ssm {
+// the device status word that bounded waits set (declared in ptx.cuh)
+__device__ int g_ssm_status = 0;
+}  // namespace ssm
 
 namespace {
 
 using bf16 = __nv_bfloat16;
 using namespace ssm;
 
-constexpr int kTile = 32;
-constexpr int kWarps = 4;
-
 // structured-A detection in the forward scans (ssm_set_structured_a): 1 = on, 0 = off
 std::atomic<int> g_structured_a{0};
 
+// ---- launch-plan override (ssm_set_plan_override): process-wide, all zero = the planner ----
+std::mutex g_override_mu;
+ssm_plan_override_t g_override{};
+
+ssm_plan_override_t plan_override() {
+    std::lock_guard<std::mutex> lock(g_override_mu);
+    return g_override;
+}
+
+// ---- registered default workspace (ssm_set_workspace), one per device --------------------
+constexpr int kMaxDevices = 64;
+std::mutex g_ws_mu;
+void *g_ws_ptr[kMaxDevices] = {};
+size_t g_ws_bytes[kMaxDevices] = {};
+
+// The current device's registered workspace, or {nullptr, 0}.
+void registered_workspace(void **ptr, size_t *bytes) {
+    *ptr = nullptr;
+    *bytes = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return;
+    }
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    *ptr = g_ws_ptr[dev];
+    *bytes = g_ws_bytes[dev];
+}
+
+// How an entry point without a workspace argument (or given NULL) gets its workspace:
+// the registered one if there is one (then it must be large enough: no allocation), else a
+// stream-ordered allocation by the library.
+struct WsChoice {
+    void *ptr;
+    size_t bytes;
+    bool may_alloc;
+};
+WsChoice default_workspace() {
+    WsChoice c{nullptr, 0, true};
+    registered_workspace(&c.ptr, &c.bytes);
+    if (c.ptr != nullptr) c.may_alloc = false;
+    return c;
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t io_size(ssm_dtype_t t) { return t == SSM_BF16 ? 2 : 4; }
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 ssm_status_t check_dims(const ssm_dims_t *dims, bool need_L) {
     if (dims == nullptr) return SSM_ERR_NULL;
@@ -46,19 +86,12 @@ ssm_status_t check_dims(const ssm_dims_t *dims, bool need_L) {
     if (dims->dstate > SSM_MAX_DSTATE) return SSM_ERR_UNSUPPORTED;
     // overflow guard: every tensor must have < 2^62 bytes
     const double lim = 4.0e18;
-    const double bdl = (double)dims->batch * (double)dims->dim * (double)(need_L ? std::max<int64_t>(dims->seqlen, 1) : 1);
-    if (bdl * 4.0 > lim || (double)dims->batch * dims->dstate * (need_L ? std::max<int64_t>(dims->seqlen, 1) : 1) * 4.0 > lim ||
+    const double Lf = (double)(need_L ? std::max<int64_t>(dims->seqlen, 1) : 1);
+    if ((double)dims->batch * dims->dim * Lf * 4.0 > lim || (double)dims->batch * dims->dstate * Lf * 4.0 > lim ||
         (double)dims->batch * dims->dim * dims->dstate * 4.0 > lim)
         return SSM_ERR_SHAPE;
     return SSM_OK;
 }
-
-// ---- launch plan for the scan ------------------------------------------------------------
-struct ScanPlan {
-    int nper, g;   // states per lane, lanes per channel
-    int nchunks;
-    int64_t chunk_len;
-};
 
 int sm_count() {
     int dev = 0, n = 148;
@@ -66,7 +99,14 @@ int sm_count() {
     return n;
 }
 
-ScanPlan plan_scan(const ssm_dims_t &d) {
+// ---- sequential-lane kernel plan (rows that are not 16-byte multiples) ---------------------
+struct ScanPlan {
+    int nper, g;   // states per lane, lanes per channel
+    int nchunks;
+    int64_t chunk_len;
+};
+
+ScanPlan plan_scan(const ssm_dims_t &d, const ssm_plan_override_t &ov) {
     ScanPlan p{16, 1, 1, d.seqlen};
     const int64_t N = d.dstate, chans = d.batch * d.dim;
     const int64_t sms = sm_count();
@@ -80,22 +120,21 @@ ScanPlan plan_scan(const ssm_dims_t &d) {
     else { p.nper = 16; p.g = 8; }
     const int64_t warps = (chans * p.g + 31) / 32;
     const int64_t want = sms * 12;
-    if (warps < sms * 8 && d.seqlen >= 4 * kTile) {
+    if (warps < sms * 8 && d.seqlen >= 4 * kSeqTile) {
         int64_t nc = (want + warps - 1) / warps;
-        nc = std::min<int64_t>(nc, d.seqlen / (4 * kTile));
+        nc = std::min<int64_t>(nc, d.seqlen / (4 * kSeqTile));
         nc = std::max<int64_t>(std::min<int64_t>(nc, 4096), 1);
         p.nchunks = (int)nc;
     }
-    if (const char *env = std::getenv("SSM_PLAN")) {  // "nper,g,nchunks" (experiments)
-        int a = 0, b = 0, c = 0;
-        if (std::sscanf(env, "%d,%d,%d", &a, &b, &c) == 3 && a > 0 && b > 0 && c > 0) {
-            p.nper = a; p.g = b; p.nchunks = std::min(c, 4096);
-        }
+    if (ov.seq_states_per_lane > 0 && ov.seq_lanes_per_channel > 0) {
+        p.nper = ov.seq_states_per_lane;
+        p.g = ov.seq_lanes_per_channel;
     }
+    if (ov.chunks > 0) p.nchunks = std::min(ov.chunks, 4096);
     if (p.nper * p.g < N) p.nper = (int)((N + p.g - 1) / p.g + 3) / 4 * 4;
     int64_t cl = (d.seqlen + p.nchunks - 1) / p.nchunks;
-    cl = (cl + kTile - 1) / kTile * kTile;
-    p.chunk_len = std::max<int64_t>(cl, kTile);
+    cl = (cl + kSeqTile - 1) / kSeqTile * kSeqTile;
+    p.chunk_len = std::max<int64_t>(cl, kSeqTile);
     p.nchunks = (int)((d.seqlen + p.chunk_len - 1) / p.chunk_len);
     if (p.nchunks < 1) p.nchunks = 1;
     return p;
@@ -105,63 +144,13 @@ size_t seq_workspace_bytes(const ssm_dims_t &d, const ScanPlan &p) {
     if (p.nchunks <= 1) return 0;
     const size_t BD = (size_t)(d.batch * d.dim), npad = (size_t)(p.nper * p.g);
     const size_t agg_h = (size_t)p.nchunks * BD * npad * 4, agg_s = (size_t)p.nchunks * BD * 4;
-    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    return up(agg_h) + up(agg_s) + up(agg_h);
+    return up256(agg_h) + up256(agg_s) + up256(agg_h);
 }
 
-// ---- kernel dispatch -------------------------------------------------------------------
-template <typename IO, int NPER, int G, bool AGG, bool AL>
-cudaError_t launch_seq_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
-    using Cfg = SeqCfg<IO, NPER, G, kWarps, kTile>;
-    auto k = scan_seq_kernel<IO, NPER, G, kWarps, kTile, AGG, AL>;
-    static unsigned long long attr_set = 0;  // per instantiation: bit i = set on device i
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= 1ull << dev;
-    }
-    dim3 grid((unsigned)(prm.Bt * prm.chan_blocks), (unsigned)grid_y);
-    k<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(prm);
-    return cudaGetLastError();
-}
-
-template <typename IO, int NPER, int G>
-cudaError_t launch_seq_g(const SeqParams &prm, bool agg, bool aligned, int grid_y, cudaStream_t s) {
-    if (agg) return aligned ? launch_seq_t<IO, NPER, G, true, true>(prm, grid_y, s)
-                            : launch_seq_t<IO, NPER, G, true, false>(prm, grid_y, s);
-    return aligned ? launch_seq_t<IO, NPER, G, false, true>(prm, grid_y, s)
-                   : launch_seq_t<IO, NPER, G, false, false>(prm, grid_y, s);
-}
-
-template <typename IO>
-cudaError_t launch_seq(const ScanPlan &pl, const SeqParams &prm, bool agg, bool aligned, int grid_y, cudaStream_t s) {
-    switch (pl.nper * 100 + pl.g) {
-        case 401: return launch_seq_g<IO, 4, 1>(prm, agg, aligned, grid_y, s);
-        case 801: return launch_seq_g<IO, 8, 1>(prm, agg, aligned, grid_y, s);
-        case 1601: return launch_seq_g<IO, 16, 1>(prm, agg, aligned, grid_y, s);
-        case 404: return launch_seq_g<IO, 4, 4>(prm, agg, aligned, grid_y, s);
-        case 1602: return launch_seq_g<IO, 16, 2>(prm, agg, aligned, grid_y, s);
-        case 1604: return launch_seq_g<IO, 16, 4>(prm, agg, aligned, grid_y, s);
-        case 1608: return launch_seq_g<IO, 16, 8>(prm, agg, aligned, grid_y, s);
-        default: return cudaErrorInvalidConfiguration;
-    }
-}
-
-int channels_per_cta(const ScanPlan &pl) { return kWarps * 32 / pl.g; }
-
-bool plan_supported(const ScanPlan &pl) {
-    switch (pl.nper * 100 + pl.g) {
-        case 401: case 801: case 1601: case 404: case 1602: case 1604: case 1608: return true;
-        default: return false;
-    }
-}
-
-// ---- persistent TMEM-replay path ---------------------------------------------------------
+// ---- persistent time-split kernels (selected only through the plan override) --------------
 struct TcPlan {
     bool use = false;
-    bool pipelined = true;   // scan_tp_kernel (default, dstate <= 64) or scan_tc_kernel
+    bool pipelined = true;   // scan_tp_kernel (dstate <= 64) or scan_tc_kernel
     int T = kTpT;
     int cpw = 8, np = 64;    // channels per group, padded states
     int G = 4, NG = 0, groups_per_b = 0, nseg = 1, seg_tiles = 1, ntiles = 0;
@@ -169,14 +158,9 @@ struct TcPlan {
     size_t off_carry = 0, off_bc = 0, bytes = 0, ctrl_bytes = 0;
 };
 
-bool env_is(const char *name, const char *val) {
-    const char *e = std::getenv(name);
-    return e != nullptr && std::strcmp(e, val) == 0;
-}
-
-TcPlan plan_tc(const ssm_dims_t &d) {
+TcPlan plan_tc(const ssm_dims_t &d, const ssm_plan_override_t &ov) {
     TcPlan t;
-    if (env_is("SSM_KERNEL", "seq")) return t;
+    if (ov.kernel != SSM_KERNEL_TC && ov.kernel != SSM_KERNEL_TP) return t;
     const size_t esz = io_size(d.io_dtype);
     if (((size_t)d.seqlen * esz) % 16 != 0) return t;                       // TMA row strides
     if (d.seqlen >= (int64_t)1 << 30 || d.dim >= (int64_t)1 << 30 || d.batch >= (int64_t)1 << 30) return t;
@@ -184,7 +168,7 @@ TcPlan plan_tc(const ssm_dims_t &d) {
     // pipelined kernel: GP = 8-state groups per channel pair (N <= 64), 64/GP channels per group;
     // otherwise the barrier-phased kernel: G = 16-state groups per channel, 32/G channels
     // (fp32 with N <= 8 would need 64-channel groups whose tiles do not fit shared memory)
-    t.pipelined = !env_is("SSM_KERNEL", "tc") && N <= 64 && !(N <= 8 && d.io_dtype == SSM_F32);
+    t.pipelined = ov.kernel == SSM_KERNEL_TP && N <= 64 && !(N <= 8 && d.io_dtype == SSM_F32);
     if (t.pipelined) {
         t.G = N <= 8 ? 1 : (N <= 16 ? 2 : (N <= 32 ? 4 : 8));
         t.cpw = 64 / t.G;
@@ -200,20 +184,17 @@ TcPlan plan_tc(const ssm_dims_t &d) {
     t.T = t.pipelined ? kTpT : kTcT;
     t.ntiles = (int)((d.seqlen + t.T - 1) / t.T);
     const int64_t sms = sm_count();
-    const bool forced = env_is("SSM_KERNEL", "tc") || env_is("SSM_KERNEL", "tp");
     if (ng >= (int64_t)1 << 24) return t;
-    if (!forced && (ng < sms || t.ntiles < 4)) return t;
     t.NG = (int)ng;
     int64_t nseg = (16 * sms + ng - 1) / ng;
     nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, t.ntiles));
     t.seg_tiles = (int)((t.ntiles + nseg - 1) / nseg);
     t.nseg = (t.ntiles + t.seg_tiles - 1) / t.seg_tiles;
     t.Lp = (int64_t)t.ntiles * t.T;
-    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    t.ctrl_bytes = up((size_t)(1 + t.NG) * 4);
+    t.ctrl_bytes = up256((size_t)(1 + t.NG) * 4);
     t.off_carry = t.ctrl_bytes;
-    t.off_bc = t.off_carry + up((size_t)t.NG * 2 * 512 * 4);
-    t.bytes = t.off_bc + up((size_t)d.batch * t.Lp * 2 * t.np * 4);
+    t.off_bc = t.off_carry + up256((size_t)t.NG * 2 * 512 * 4);
+    t.bytes = t.off_bc + up256((size_t)d.batch * t.Lp * 2 * t.np * 4);
     t.use = true;
     return t;
 }
@@ -252,67 +233,10 @@ bool make_map(CUtensorMap *m, const void *base, const ssm_dims_t &d, int cpw, in
     return r == CUDA_SUCCESS;
 }
 
-template <typename IO, int G>
-cudaError_t launch_tc_t(const TcParams &prm, cudaStream_t s) {
-    using Cfg = TcCfg<IO, G>;
-    auto k = scan_tc_kernel<IO, G>;
-    static unsigned long long attr_set = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= 1ull << dev;
-    }
-    k<<<(unsigned)sm_count(), Cfg::W * 32, Cfg::SMEM, s>>>(prm);
-    return cudaGetLastError();
-}
-
-template <typename IO, int G>
-cudaError_t launch_tp_t(const TcParams &prm, cudaStream_t s) {
-    using Cfg = TpCfg<IO, G>;
-    auto k = scan_tp_kernel<IO, G>;
-    static unsigned long long attr_set = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= 1ull << dev;
-    }
-    k<<<(unsigned)sm_count(), Cfg::W * 32, Cfg::SMEM, s>>>(prm);
-    return cudaGetLastError();
-}
-
-template <typename IO>
-cudaError_t launch_tc(bool pipelined, int G, const TcParams &prm, cudaStream_t s) {
-    if (pipelined) {
-        switch (G) {
-            case 1:
-                if constexpr (tp_bytes<IO, 1>(2) <= kSmemLimit) return launch_tp_t<IO, 1>(prm, s);
-                return cudaErrorInvalidConfiguration;
-            case 2: return launch_tp_t<IO, 2>(prm, s);
-            case 4: return launch_tp_t<IO, 4>(prm, s);
-            case 8: return launch_tp_t<IO, 8>(prm, s);
-            default: return cudaErrorInvalidConfiguration;
-        }
-    }
-    switch (G) {
-        case 1: return launch_tc_t<IO, 1>(prm, s);
-        case 2: return launch_tc_t<IO, 2>(prm, s);
-        case 4: return launch_tc_t<IO, 4>(prm, s);
-        case 8: return launch_tc_t<IO, 8>(prm, s);
-        default: return cudaErrorInvalidConfiguration;
-    }
-}
-
-ssm_status_t run_scan_tc(const ssm_dims_t &d, const TcPlan &t, const void *u, const void *delta, const float *A,
-                         const void *B, const void *C, const float *D, const void *z, const float *delta_bias,
-                         int delta_softplus, void *y, float *last_state, char *ws, cudaStream_t s) {
+ssm_status_t run_scan_tc(const ssm_dims_t &d, const TcPlan &t, const ssm_plan_override_t &ov, const void *u,
+                         const void *delta, const float *A, const void *B, const void *C, const float *D,
+                         const void *z, const float *delta_bias, int delta_softplus, void *y, float *last_state,
+                         char *ws, cudaStream_t s) {
     TcParams prm;
     std::memset(&prm, 0, sizeof(prm));
     const int cpw = t.cpw;
@@ -331,26 +255,12 @@ ssm_status_t run_scan_tc(const ssm_dims_t &d, const TcPlan &t, const void *u, co
     prm.np = t.np;
     prm.spin_limit = 1u << 24;
     prm.force_timeout = 0;
-    if (env_is("SSM_TEST_FORCE_TIMEOUT", "1")) { prm.force_timeout = 1; prm.spin_limit = 256; }
+    if (ov.force_timeout) { prm.force_timeout = 1; prm.spin_limit = 256; }
     if (cudaMemsetAsync(ws, 0, t.ctrl_bytes, s) != cudaSuccess) return SSM_ERR_CUDA;
-    const int NP = t.np;
-    float *bc = reinterpret_cast<float *>(ws + t.off_bc);
-    const dim3 pg((unsigned)(t.Lp / 32), (unsigned)d.batch);
-    const size_t psm = (size_t)2 * NP * 33 * 4;
-    if (d.io_dtype == SSM_BF16)
-        bc_prep_kernel<bf16><<<pg, 256, psm, s>>>(static_cast<const bf16 *>(B), static_cast<const bf16 *>(C), bc,
-                                                  d.dstate, d.seqlen, t.Lp, NP);
-    else
-        bc_prep_kernel<float><<<pg, 256, psm, s>>>(static_cast<const float *>(B), static_cast<const float *>(C), bc,
-                                                   d.dstate, d.seqlen, t.Lp, NP);
-    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-    const cudaError_t e = d.io_dtype == SSM_BF16 ? launch_tc<bf16>(t.pipelined, t.G, prm, s)
-                                                 : launch_tc<float>(t.pipelined, t.G, prm, s);
-    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
-}
-
-__global__ void zero_f32_kernel(float *p, int64_t n) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) p[i] = 0.0f;
+    if (launch_bc_prep(d.io_dtype, B, C, reinterpret_cast<float *>(ws + t.off_bc), d.dstate, d.seqlen, t.Lp, t.np,
+                       d.batch, s) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return launch_tc(d.io_dtype, t.pipelined, t.G, prm, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status_t scan_checks(const ssm_dims_t *dims, const void *u, const void *delta, const float *A,
@@ -370,11 +280,6 @@ ssm_status_t scan_checks(const ssm_dims_t *dims, const void *u, const void *delt
 }
 
 // ---- channel-pair sequential path (default for 16-byte aligned rows) ----------------------
-#ifndef SSM_PAIR_T
-#define SSM_PAIR_T 16
-#endif
-constexpr int kPairT = SSM_PAIR_T;   // timesteps per tile of the channel-pair kernel
-
 struct PairPlan {
     bool use = false;
     int ks = 8, gp = 8;          // states per lane per channel, lanes per channel pair
@@ -392,71 +297,9 @@ int pair_gp(int64_t N, int ks) {
     return gp;
 }
 
-template <typename IO, int KS, int GP, bool AGG, bool ZOH, bool CONV = false>
-cudaError_t launch_pair_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
-    constexpr int W = pair_warps(KS, GP, AGG);
-    using Cfg = PairCfg<IO, KS, GP, W, kPairT, CONV>;
-    auto k = scan_pair_kernel<IO, KS, GP, W, kPairT, AGG, ZOH, CONV>;
-    static unsigned long long attr_set = 0;  // per instantiation: bit i = set on device i
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= 1ull << dev;
-    }
-    dim3 grid((unsigned)(prm.Bt * prm.chan_blocks), (unsigned)grid_y);
-    k<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(prm);
-    return cudaGetLastError();
-}
-
-template <typename IO, int KS, int GP>
-cudaError_t launch_pair_g(const SeqParams &prm, bool agg, int grid_y, cudaStream_t s) {
-    if (prm.conv_w != nullptr)   // conv front (Euler discretisation)
-        return agg ? launch_pair_t<IO, KS, GP, true, false, true>(prm, grid_y, s)
-                   : launch_pair_t<IO, KS, GP, false, false, true>(prm, grid_y, s);
-    if (prm.zoh)
-        return agg ? launch_pair_t<IO, KS, GP, true, true>(prm, grid_y, s)
-                   : launch_pair_t<IO, KS, GP, false, true>(prm, grid_y, s);
-    return agg ? launch_pair_t<IO, KS, GP, true, false>(prm, grid_y, s)
-               : launch_pair_t<IO, KS, GP, false, false>(prm, grid_y, s);
-}
-
-#define SSM_PAIR_CASES(X) X(4, 1) X(4, 2) X(4, 4) X(8, 1) X(8, 2) X(8, 4) X(8, 8) X(8, 16) X(16, 4)
-
-template <typename IO>
-cudaError_t launch_pair(const PairPlan &pl, const SeqParams &prm, bool agg, int grid_y, cudaStream_t s) {
-    switch (pl.ks * 100 + pl.gp) {
-#define SSM_PAIR_LAUNCH(KS, GP) case KS * 100 + GP: return launch_pair_g<IO, KS, GP>(prm, agg, grid_y, s);
-        SSM_PAIR_CASES(SSM_PAIR_LAUNCH)
-#undef SSM_PAIR_LAUNCH
-        default: return cudaErrorInvalidConfiguration;
-    }
-}
-
-size_t pair_smem(ssm_dtype_t io, int ks, int gp, bool conv, bool agg) {
-    switch (ks * 100 + gp) {
-#define SSM_PAIR_SMEM(KS, GP) \
-    case KS * 100 + GP: \
-        if (agg) { \
-            if (conv) return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(KS, GP, true), kPairT, true>::kSmem \
-                                            : PairCfg<float, KS, GP, pair_warps(KS, GP, true), kPairT, true>::kSmem; \
-            return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(KS, GP, true), kPairT>::kSmem \
-                                  : PairCfg<float, KS, GP, pair_warps(KS, GP, true), kPairT>::kSmem; \
-        } \
-        if (conv) return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(KS, GP, false), kPairT, true>::kSmem \
-                                        : PairCfg<float, KS, GP, pair_warps(KS, GP, false), kPairT, true>::kSmem; \
-        return io == SSM_BF16 ? PairCfg<bf16, KS, GP, pair_warps(KS, GP, false), kPairT>::kSmem \
-                              : PairCfg<float, KS, GP, pair_warps(KS, GP, false), kPairT>::kSmem;
-        SSM_PAIR_CASES(SSM_PAIR_SMEM)
-#undef SSM_PAIR_SMEM
-        default: return 0;
-    }
-}
-
-PairPlan plan_pair(const ssm_dims_t &d, bool conv = false) {
+PairPlan plan_pair(const ssm_dims_t &d, const ssm_plan_override_t &ov, bool conv = false) {
     PairPlan p;
-    if (env_is("SSM_KERNEL", "seq") || env_is("SSM_KERNEL", "tc") || env_is("SSM_KERNEL", "tp")) return p;
+    if (ov.kernel == SSM_KERNEL_SEQ || ov.kernel == SSM_KERNEL_TC || ov.kernel == SSM_KERNEL_TP) return p;
     const size_t esz = io_size(d.io_dtype);
     if (((size_t)d.seqlen * esz) % 16 != 0 || d.dstate > 128) return p;   // rows move in 16-byte pieces
     const int64_t N = d.dstate, BD = d.batch * d.dim, sms = sm_count();
@@ -477,21 +320,21 @@ PairPlan plan_pair(const ssm_dims_t &d, bool conv = false) {
         p.ks = 16;
         p.gp = pair_gp(N, 16);
     }
-    if (env_is("SSM_PAIR_KS", "4") && N <= 16) { p.ks = 4; p.gp = pair_gp(N, 4); }   // experiments, tests
-    if (env_is("SSM_PAIR_KS", "8")) { p.ks = 8; p.gp = pair_gp(N, 8); }
-    if (env_is("SSM_PAIR_KS", "16") && N > 32 && N <= 64) { p.ks = 16; p.gp = pair_gp(N, 16); }
+    if (ov.pair_states_per_lane == 4 && N <= 16) { p.ks = 4; p.gp = pair_gp(N, 4); }
+    if (ov.pair_states_per_lane == 8) { p.ks = 8; p.gp = pair_gp(N, 8); }
+    if (ov.pair_states_per_lane == 16 && N > 32 && N <= 64) { p.ks = 16; p.gp = pair_gp(N, 16); }
     p.np = p.ks * p.gp;
     p.smem_agg = pair_smem(d.io_dtype, p.ks, p.gp, conv, true);
     p.smem_full = pair_smem(d.io_dtype, p.ks, p.gp, conv, false);
     if (p.smem_agg == 0 || p.smem_full == 0) return p;
-    const int64_t wa = pair_warps(p.ks, p.gp, true), wf = pair_warps(p.ks, p.gp, false);
+    const int64_t wa = pair_warps_of(p.ks, p.gp, true), wf = pair_warps_of(p.ks, p.gp, false);
     p.cb_agg = (int)((d.dim + wa * 64 / p.gp - 1) / (wa * 64 / p.gp));
     p.cb_full = (int)((d.dim + wf * 64 / p.gp - 1) / (wf * 64 / p.gp));
     // CTAs of the full pass resident per SM: shared memory (228 KB, 1 KB reserved per CTA),
     // threads (2048) and the registers the launch bounds allow.
     const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(
         std::min<int64_t>((228 * 1024) / (int64_t)(p.smem_full + 1024), 2048 / (wf * 32)),
-        pair_min_blocks((int)wf, p.ks, p.gp)));
+        pair_min_blocks_of(p.ks, p.gp, false)));
     // The sequence is cut into chunks (aggregate pass + combine + full pass) when the channels
     // alone give fewer than two warps per SM sub-partition: the latency-bound recurrence gains
     // more from the extra warps than the aggregate pass (up to 1.9x the work) costs. The chunk
@@ -506,7 +349,7 @@ PairPlan plan_pair(const ssm_dims_t &d, bool conv = false) {
         while (w > 1 && d.seqlen < wave * w * 2048) --w;
         nc = wave * w;
     }
-    if (const char *env = std::getenv("SSM_PAIR_CHUNKS")) nc = std::max(1, std::atoi(env));   // experiments
+    if (ov.chunks > 0) nc = ov.chunks;
     nc = std::min<int64_t>(nc, std::max<int64_t>(1, d.seqlen / (4 * kPairT)));
     nc = std::min<int64_t>(nc, 4096);
     int64_t cl = (d.seqlen + nc - 1) / nc;
@@ -520,27 +363,37 @@ PairPlan plan_pair(const ssm_dims_t &d, bool conv = false) {
 size_t pair_workspace_bytes(const ssm_dims_t &d, const PairPlan &p) {
     if (!p.use || p.nchunks <= 1) return 0;
     const size_t BD = (size_t)(d.batch * d.dim);
-    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t agg_h = (size_t)p.nchunks * BD * p.np * 4, agg_s = (size_t)p.nchunks * BD * 4;
-    return up(agg_h) + up(agg_s) + up(agg_h);
+    return up256(agg_h) + up256(agg_s) + up256(agg_h);
+}
+
+// A workspace of at least `need` bytes for one call: the caller's, or a stream-ordered
+// allocation when allowed. `allocated` tells the caller to free it stream-ordered.
+ssm_status_t acquire_workspace(void **ws, size_t ws_bytes, size_t need, bool may_alloc, cudaStream_t s,
+                               bool *allocated) {
+    *allocated = false;
+    if (need == 0) return SSM_OK;
+    if (*ws == nullptr || ws_bytes < need) {
+        if (!may_alloc) return SSM_ERR_WORKSPACE;
+        if (cudaMallocAsync(ws, need, s) != cudaSuccess) {
+            cudaGetLastError();
+            return SSM_ERR_CUDA;
+        }
+        *allocated = true;
+    } else if (!aligned16(*ws)) {
+        return SSM_ERR_ALIGN;
+    }
+    return SSM_OK;
 }
 
 ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *u, const void *delta, const float *A,
                            const void *B, const void *C, const float *D, const void *z, const float *delta_bias,
                            int delta_softplus, void *y, float *last_state, void *workspace, size_t ws_bytes,
-                           bool own_ws, cudaStream_t s, int zoh, const float *conv_w = nullptr,
+                           bool may_alloc, cudaStream_t s, int zoh, const float *conv_w = nullptr,
                            const float *conv_b = nullptr, int conv_k = 0) {
-    const size_t need = pair_workspace_bytes(d, pl);
     bool allocated = false;
-    if (need > 0) {
-        if (workspace == nullptr || ws_bytes < need) {
-            if (!own_ws) return SSM_ERR_WORKSPACE;
-            if (cudaMallocAsync(&workspace, need, s) != cudaSuccess) return SSM_ERR_CUDA;
-            allocated = true;
-        } else if (!aligned16(workspace)) {
-            return SSM_ERR_ALIGN;
-        }
-    }
+    ssm_status_t st = acquire_workspace(&workspace, ws_bytes, pair_workspace_bytes(d, pl), may_alloc, s, &allocated);
+    if (st != SSM_OK) return st;
     SeqParams prm{};
     prm.u = u; prm.delta = delta; prm.z = z; prm.B = B; prm.C = C;
     prm.A = A; prm.D = D; prm.bias = delta_bias; prm.y = y; prm.last_state = last_state;
@@ -551,109 +404,95 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
     prm.zoh = zoh ? 1 : 0;
     prm.conv_w = conv_w; prm.conv_b = conv_b; prm.conv_k = conv_k;
     prm.structured = g_structured_a.load();
+    const int variant = conv_w != nullptr ? kPairConv : (zoh ? kPairZoh : kPairEuler);
     cudaError_t e = cudaSuccess;
-    const bool bf = d.io_dtype == SSM_BF16;
     if (pl.nchunks > 1) {
         const size_t BD = (size_t)(d.batch * d.dim), np = (size_t)pl.np;
-        auto up = [](size_t x) { return (x + 255) / 256 * 256; };
         char *w = static_cast<char *>(workspace);
         prm.agg_h = reinterpret_cast<float *>(w);
-        prm.agg_s = reinterpret_cast<float *>(w + up((size_t)pl.nchunks * BD * np * 4));
-        float *hin = reinterpret_cast<float *>(w + up((size_t)pl.nchunks * BD * np * 4) + up((size_t)pl.nchunks * BD * 4));
+        prm.agg_s = reinterpret_cast<float *>(w + up256((size_t)pl.nchunks * BD * np * 4));
+        float *hin = reinterpret_cast<float *>(w + up256((size_t)pl.nchunks * BD * np * 4) +
+                                               up256((size_t)pl.nchunks * BD * 4));
         prm.chan_blocks = pl.cb_agg;
-        e = bf ? launch_pair<bf16>(pl, prm, true, pl.nchunks - 1, s) : launch_pair<float>(pl, prm, true, pl.nchunks - 1, s);
-        if (e == cudaSuccess) {
-            const int64_t total = (int64_t)BD * pl.np;
-            chunk_combine_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-                A, prm.agg_h, prm.agg_s, hin, (int64_t)BD, d.dim, d.dstate, pl.np, pl.nchunks);
-            e = cudaGetLastError();
-        }
+        e = launch_pair(d.io_dtype, variant, pl.ks, pl.gp, true, prm, pl.nchunks - 1, s);
+        if (e == cudaSuccess)
+            e = launch_chunk_combine(A, prm.agg_h, prm.agg_s, hin, (int64_t)BD, d.dim, d.dstate, pl.np, pl.nchunks, s);
         prm.hin = hin;
     }
     prm.chan_blocks = pl.cb_full;
-    if (e == cudaSuccess)
-        e = bf ? launch_pair<bf16>(pl, prm, false, pl.nchunks, s) : launch_pair<float>(pl, prm, false, pl.nchunks, s);
+    if (e == cudaSuccess) e = launch_pair(d.io_dtype, variant, pl.ks, pl.gp, false, prm, pl.nchunks, s);
     if (allocated) cudaFreeAsync(workspace, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+// Workspace bytes the scan of `d` needs under the current plan (0 if none).
+size_t scan_workspace_bytes(const ssm_dims_t &d) {
+    if (d.batch == 0 || d.dim == 0 || d.seqlen == 0) return 0;
+    const ssm_plan_override_t ov = plan_override();
+    const PairPlan pp = plan_pair(d, ov);
+    if (pp.use) return pair_workspace_bytes(d, pp);
+    const TcPlan tp = plan_tc(d, ov);
+    if (tp.use) return tp.bytes;
+    return seq_workspace_bytes(d, plan_scan(d, ov));
 }
 
 ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, const float *A,
                       const void *B, const void *C, const float *D, const void *z,
                       const float *delta_bias, int delta_softplus, void *y, float *last_state,
-                      void *workspace, size_t ws_bytes, bool own_ws, cudaStream_t s, int zoh = 0) {
+                      void *workspace, size_t ws_bytes, bool may_alloc, cudaStream_t s, int zoh = 0) {
     const ssm_dims_t d = *dims;
     if (d.batch == 0 || d.dim == 0) return SSM_OK;
     if (d.seqlen == 0) {
-        if (last_state) {
-            const int64_t n = d.batch * d.dim * d.dstate;
-            zero_f32_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, s>>>(last_state, n);
-            if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-        }
+        if (last_state && launch_zero_f32(last_state, d.batch * d.dim * d.dstate, s) != cudaSuccess)
+            return SSM_ERR_CUDA;
         return SSM_OK;
     }
-    const PairPlan pp = plan_pair(d);
+    const ssm_plan_override_t ov = plan_override();
+    const PairPlan pp = plan_pair(d, ov);
     if (pp.use)
         return run_scan_pair(d, pp, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
-                             ws_bytes, own_ws, s, zoh);
+                             ws_bytes, may_alloc, s, zoh);
     if (zoh) return SSM_ERR_UNSUPPORTED;   // the zero-order hold runs on the channel-pair kernel only
-    const TcPlan tp = plan_tc(d);
+    const TcPlan tp = plan_tc(d, ov);
     if (tp.use) {
-        char *w = static_cast<char *>(workspace);
         bool alloc = false;
-        if (w == nullptr || ws_bytes < tp.bytes) {
-            if (!own_ws) return SSM_ERR_WORKSPACE;
-            if (cudaMallocAsync(reinterpret_cast<void **>(&w), tp.bytes, s) != cudaSuccess) return SSM_ERR_CUDA;
-            alloc = true;
-        }
-        const ssm_status_t r = run_scan_tc(d, tp, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, w, s);
-        if (alloc) cudaFreeAsync(w, s);
-        return r;
+        ssm_status_t st = acquire_workspace(&workspace, ws_bytes, tp.bytes, may_alloc, s, &alloc);
+        if (st != SSM_OK) return st;
+        st = run_scan_tc(d, tp, ov, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
+                         static_cast<char *>(workspace), s);
+        if (alloc) cudaFreeAsync(workspace, s);
+        return st;
     }
-    const ScanPlan pl = plan_scan(d);
-    if (!plan_supported(pl)) return SSM_ERR_UNSUPPORTED;
-    const size_t need = seq_workspace_bytes(d, pl);
+    const ScanPlan pl = plan_scan(d, ov);
+    if (!seq_plan_supported(pl.nper, pl.g)) return SSM_ERR_UNSUPPORTED;
     bool allocated = false;
-    if (need > 0) {
-        if (workspace == nullptr || ws_bytes < need) {
-            if (!own_ws) return SSM_ERR_WORKSPACE;
-            if (cudaMallocAsync(&workspace, need, s) != cudaSuccess) return SSM_ERR_CUDA;
-            allocated = true;
-        } else if (!aligned16(workspace)) {
-            return SSM_ERR_ALIGN;
-        }
-    }
+    ssm_status_t st = acquire_workspace(&workspace, ws_bytes, seq_workspace_bytes(d, pl), may_alloc, s, &allocated);
+    if (st != SSM_OK) return st;
     SeqParams prm{};
     prm.u = u; prm.delta = delta; prm.z = z; prm.B = B; prm.C = C;
     prm.A = A; prm.D = D; prm.bias = delta_bias; prm.y = y; prm.last_state = last_state;
     prm.Bt = d.batch; prm.Dm = d.dim; prm.L = d.seqlen; prm.N = d.dstate;
     prm.softplus = delta_softplus ? 1 : 0;
     prm.chunk_len = pl.chunk_len; prm.nchunks = pl.nchunks;
-    const int cpc = channels_per_cta(pl);
+    const int cpc = kSeqWarps * 32 / pl.g;
     prm.chan_blocks = (int)((d.dim + cpc - 1) / cpc);
     prm.npad = pl.nper * pl.g;
-    const size_t esz = io_size(d.io_dtype);
-    const bool aligned = ((size_t)d.seqlen * esz) % 16 == 0;
+    const bool aligned = ((size_t)d.seqlen * io_size(d.io_dtype)) % 16 == 0;
     cudaError_t e = cudaSuccess;
     if (pl.nchunks > 1) {
         const size_t BD = (size_t)(d.batch * d.dim), npad = (size_t)prm.npad;
-        auto up = [](size_t x) { return (x + 255) / 256 * 256; };
         char *w = static_cast<char *>(workspace);
         prm.agg_h = reinterpret_cast<float *>(w);
-        prm.agg_s = reinterpret_cast<float *>(w + up((size_t)pl.nchunks * BD * npad * 4));
-        float *hin = reinterpret_cast<float *>(w + up((size_t)pl.nchunks * BD * npad * 4) + up((size_t)pl.nchunks * BD * 4));
-        e = d.io_dtype == SSM_BF16 ? launch_seq<bf16>(pl, prm, true, aligned, pl.nchunks - 1, s)
-                                   : launch_seq<float>(pl, prm, true, aligned, pl.nchunks - 1, s);
-        if (e == cudaSuccess) {
-            const int64_t total = (int64_t)BD * prm.npad;
-            chunk_combine_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-                A, prm.agg_h, prm.agg_s, hin, (int64_t)BD, d.dim, d.dstate, prm.npad, pl.nchunks);
-            e = cudaGetLastError();
-        }
+        prm.agg_s = reinterpret_cast<float *>(w + up256((size_t)pl.nchunks * BD * npad * 4));
+        float *hin = reinterpret_cast<float *>(w + up256((size_t)pl.nchunks * BD * npad * 4) +
+                                               up256((size_t)pl.nchunks * BD * 4));
+        e = launch_seq(d.io_dtype, pl.nper, pl.g, true, aligned, prm, pl.nchunks - 1, s);
+        if (e == cudaSuccess)
+            e = launch_chunk_combine(A, prm.agg_h, prm.agg_s, hin, (int64_t)BD, d.dim, d.dstate, prm.npad,
+                                     pl.nchunks, s);
         prm.hin = hin;
     }
-    if (e == cudaSuccess)
-        e = d.io_dtype == SSM_BF16 ? launch_seq<bf16>(pl, prm, false, aligned, pl.nchunks, s)
-                                   : launch_seq<float>(pl, prm, false, aligned, pl.nchunks, s);
+    if (e == cudaSuccess) e = launch_seq(d.io_dtype, pl.nper, pl.g, false, aligned, prm, pl.nchunks, s);
     if (allocated) cudaFreeAsync(workspace, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
@@ -666,21 +505,55 @@ ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, 
 // ever passed to run_scan as a caller workspace, so no code path allocates on its behalf.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_SCRATCH_MAX_BYTES];
 
-constexpr int kScratchDevices = 64;   // devices whose scratch address is cached
-std::mutex g_scratch_mu;
-void *g_scratch_addr[kScratchDevices] = {};
+// Identity of the current context (cuCtxGetId), so that a scratch address cached for a
+// device is re-resolved after the device's primary context was torn down and re-created
+// (cudaDeviceReset), when the module and its array move. 0 when the query is unavailable.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_cur = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_cur == nullptr || get_id == nullptr || get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
-// Device address of the current device's scratch, resolved with cudaGetSymbolAddress at
-// first use on that device (which may load the module: outside any stream capture).
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
+
+// Device address of the current device's scratch, resolved with cudaGetSymbolAddress on the
+// first use in each context of the device (which may load the module: outside any stream
+// capture) and cached for the later calls in the same context.
 ssm_status_t scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SSM_ERR_CUDA;
     }
-    const bool cached = dev >= 0 && dev < kScratchDevices;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    // establishes the primary context if the call is the first CUDA work of this thread
+    if (cudaFree(nullptr) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (cached && g_scratch_addr[dev] != nullptr) {
+    if (cached && ctx != 0 && g_scratch_addr[dev] != nullptr && g_scratch_ctx[dev] == ctx) {
         *out = g_scratch_addr[dev];
         return SSM_OK;
     }
@@ -689,7 +562,10 @@ ssm_status_t scratch_address(void **out) {
         cudaGetLastError();   // do not leave the error for the next launch check to find
         return SSM_ERR_CUDA;
     }
-    if (cached) g_scratch_addr[dev] = p;
+    if (cached) {
+        g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
+    }
     *out = p;
     return SSM_OK;
 }
@@ -704,18 +580,14 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_dims_t *dims, const void *u, const
                                     void *y, float *last_state, void *stream) {
     ssm_status_t st = scan_checks(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
     if (st != SSM_OK) return st;
-    return run_scan(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
-                    nullptr, 0, true, static_cast<cudaStream_t>(stream));
+    const WsChoice w = default_workspace();
+    return run_scan(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, w.ptr, w.bytes,
+                    w.may_alloc, static_cast<cudaStream_t>(stream));
 }
 
 size_t ssm_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
-    if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
-    const PairPlan pp = plan_pair(*dims);
-    if (pp.use) return pair_workspace_bytes(*dims, pp);
-    const TcPlan tp = plan_tc(*dims);
-    if (tp.use) return tp.bytes;
-    return seq_workspace_bytes(*dims, plan_scan(*dims));
+    return scan_workspace_bytes(*dims);
 }
 
 ssm_status_t ssm_selective_scan_fwd_ws(const ssm_dims_t *dims, const void *u, const void *delta,
@@ -730,6 +602,22 @@ ssm_status_t ssm_selective_scan_fwd_ws(const ssm_dims_t *dims, const void *u, co
                     workspace, workspace_bytes, false, static_cast<cudaStream_t>(stream));
 }
 
+ssm_status_t ssm_set_workspace(void *dev_ptr, size_t bytes) {
+    if (dev_ptr == nullptr && bytes != 0) return SSM_ERR_NULL;
+    if (dev_ptr != nullptr && bytes == 0) return SSM_ERR_WORKSPACE;
+    if (dev_ptr != nullptr && !aligned16(dev_ptr)) return SSM_ERR_ALIGN;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return SSM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    g_ws_ptr[dev] = dev_ptr;
+    g_ws_bytes[dev] = dev_ptr != nullptr ? bytes : 0;
+    return SSM_OK;
+}
+
 ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_dims_t *dims, const void *u, const void *delta,
                                             const float *A, const void *B, const void *C,
                                             const float *D, const void *z, const float *delta_bias,
@@ -737,14 +625,14 @@ ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_dims_t *dims, const void *
                                             void *stream) {
     ssm_status_t st = scan_checks(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
     if (st != SSM_OK) return st;
-    const size_t need = ssm_selective_scan_workspace_bytes(dims);
+    const size_t need = scan_workspace_bytes(*dims);
     if (need > SSM_SCRATCH_MAX_BYTES) return SSM_ERR_WORKSPACE;
     void *scratch = nullptr;
     if (need > 0) {
         st = scratch_address(&scratch);
         if (st != SSM_OK) return st;
     }
-    // own_ws = false: run_scan may only use the scratch, never allocate a replacement
+    // may_alloc = false: run_scan may only use the scratch, never allocate a replacement
     return run_scan(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
                     scratch, need > 0 ? SSM_SCRATCH_MAX_BYTES : 0, false,
                     static_cast<cudaStream_t>(stream));
@@ -769,44 +657,17 @@ ssm_status_t state_update_impl(const ssm_dims_t *dims, float *state, const void 
         if (q != nullptr && !aligned_to(q, esz)) return SSM_ERR_ALIGN;
     if (D != nullptr && !aligned_to(D, 4)) return SSM_ERR_ALIGN;
     DecodeParams p{state, x, dt, B, C, z, A, D, y, dims->batch, dims->dim, dims->dstate, zoh ? 1 : 0};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t N = dims->dstate, chans = dims->batch * dims->dim;
-    const bool bf = dims->io_dtype == SSM_BF16;
+    const int64_t N = dims->dstate;
     const int lpc = (int)(N / 4);
+    const bool vec = N % 4 == 0 && lpc >= 1 && lpc <= 32 && (32 % lpc) == 0;
     // batch rows on grid.y and 16-byte B/C reads when B and C rows are 4-element aligned;
     // the row's channels must fit a 32-bit thread index and grid.y (65535 rows)
     const bool wide = aligned_to(B, 4 * esz) && aligned_to(C, 4 * esz) && dims->batch <= 65535 &&
-                      dims->dim * lpc < (int64_t)1 << 30 && !env_is("SSM_DEC_OLD", "1");
-    if (wide && N % 4 == 0 && lpc >= 1 && lpc <= 32 && (32 % lpc) == 0) {
-        const dim3 grid((unsigned)((dims->dim * lpc + 255) / 256), (unsigned)dims->batch);
-#define SSM_DECW(L)                                                                                    \
-    case L:                                                                                            \
-        if (zoh) bf ? decode_wide_kernel<bf16, L, true><<<grid, 256, 0, s>>>(p) : decode_wide_kernel<float, L, true><<<grid, 256, 0, s>>>(p); \
-        else bf ? decode_wide_kernel<bf16, L><<<grid, 256, 0, s>>>(p) : decode_wide_kernel<float, L><<<grid, 256, 0, s>>>(p);                \
-        break;
-        switch (lpc) { SSM_DECW(1) SSM_DECW(2) SSM_DECW(4) SSM_DECW(8) SSM_DECW(16) SSM_DECW(32) default: return SSM_ERR_UNSUPPORTED; }
-#undef SSM_DECW
-    } else if (N % 4 == 0 && lpc >= 1 && lpc <= 32 && (32 % lpc) == 0) {
-        const int64_t threads = chans * lpc;
-        const unsigned grid = (unsigned)((threads + 255) / 256);
-#define SSM_DEC(L)                                                                                     \
-    case L:                                                                                            \
-        if (zoh) bf ? decode_vec_kernel<bf16, L, true><<<grid, 256, 0, s>>>(p) : decode_vec_kernel<float, L, true><<<grid, 256, 0, s>>>(p); \
-        else bf ? decode_vec_kernel<bf16, L><<<grid, 256, 0, s>>>(p) : decode_vec_kernel<float, L><<<grid, 256, 0, s>>>(p);                \
-        break;
-        switch (lpc) { SSM_DEC(1) SSM_DEC(2) SSM_DEC(4) SSM_DEC(8) SSM_DEC(16) SSM_DEC(32) default: return SSM_ERR_UNSUPPORTED; }
-#undef SSM_DEC
-    } else {
-        const unsigned grid = (unsigned)((chans + 255) / 256);
-        if (zoh) {
-            if (bf) decode_scalar_kernel<bf16, true><<<grid, 256, 0, s>>>(p);
-            else decode_scalar_kernel<float, true><<<grid, 256, 0, s>>>(p);
-        } else {
-            if (bf) decode_scalar_kernel<bf16><<<grid, 256, 0, s>>>(p);
-            else decode_scalar_kernel<float><<<grid, 256, 0, s>>>(p);
-        }
-    }
-    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+                      dims->dim * lpc < (int64_t)1 << 30 && !plan_override().decode_elementwise;
+    const int kind = vec ? (wide ? 0 : 1) : 2;
+    const cudaError_t e = launch_decode(dims->io_dtype, kind, lpc, zoh != 0, p, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidConfiguration) return SSM_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 }  // namespace
 
@@ -834,9 +695,10 @@ ssm_status_t ssm_selective_scan_fwd_disc(const ssm_dims_t *dims, const void *u, 
     if (st != SSM_OK) return st;
     if (discretization != SSM_DISC_EULER && discretization != SSM_DISC_ZOH) return SSM_ERR_UNSUPPORTED;
     if (workspace != nullptr && !aligned16(workspace)) return SSM_ERR_ALIGN;
-    return run_scan(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
-                    workspace_bytes, workspace == nullptr, static_cast<cudaStream_t>(stream),
-                    discretization == SSM_DISC_ZOH);
+    WsChoice w{workspace, workspace_bytes, false};
+    if (workspace == nullptr) w = default_workspace();
+    return run_scan(dims, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, w.ptr, w.bytes,
+                    w.may_alloc, static_cast<cudaStream_t>(stream), discretization == SSM_DISC_ZOH);
 }
 
 ssm_status_t ssm_conv_selective_scan_fwd(const ssm_dims_t *dims, const void *x, const float *conv_w,
@@ -849,32 +711,33 @@ ssm_status_t ssm_conv_selective_scan_fwd(const ssm_dims_t *dims, const void *x, 
     if (conv_width < 1 || conv_width > 4) return SSM_ERR_UNSUPPORTED;
     if (conv_b != nullptr && !aligned_to(conv_b, 4)) return SSM_ERR_ALIGN;
     if (workspace != nullptr && !aligned16(workspace)) return SSM_ERR_ALIGN;
+    WsChoice w{workspace, workspace_bytes, false};
+    if (workspace == nullptr) w = default_workspace();
     const ssm_dims_t d = *dims;
     if (d.batch == 0 || d.dim == 0 || d.seqlen == 0)
-        return run_scan(dims, x, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
-                        workspace_bytes, workspace == nullptr, static_cast<cudaStream_t>(stream));
+        return run_scan(dims, x, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, w.ptr, w.bytes,
+                        w.may_alloc, static_cast<cudaStream_t>(stream));
     if (conv_w == nullptr) return SSM_ERR_NULL;
     if (!aligned_to(conv_w, 4)) return SSM_ERR_ALIGN;
-    const PairPlan pp = plan_pair(d, true);
+    const PairPlan pp = plan_pair(d, plan_override(), true);
     if (!pp.use) return SSM_ERR_UNSUPPORTED;   // the conv front runs on the channel-pair kernel only
-    return run_scan_pair(d, pp, x, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
-                         workspace_bytes, workspace == nullptr, static_cast<cudaStream_t>(stream), 0, conv_w, conv_b,
-                         conv_width);
+    return run_scan_pair(d, pp, x, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, w.ptr, w.bytes,
+                         w.may_alloc, static_cast<cudaStream_t>(stream), 0, conv_w, conv_b, conv_width);
 }
 
 size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
-    return pair_workspace_bytes(*dims, plan_pair(*dims, true));
+    return pair_workspace_bytes(*dims, plan_pair(*dims, plan_override(), true));
 }
 
 }  // extern "C"
 
 namespace {
-// backward lane split: Q <= 4 states per lane, G lanes per channel (a power of two, <= 32)
-// Q states per thread, G lanes per channel (G * Q >= N). Two states per thread up to 64
-// states: the 16-step state history then fits in registers with 4 CTAs per SM (measured on
-// 8 x 1536 x 2048 x 16: 3.86 ms at four states per thread, 3.23 ms at two).
+// backward lane split: Q states per thread, G lanes per channel (a power of two, <= 32,
+// G * Q >= N). Two states per thread up to 64 states: the 16-step state history then fits in
+// registers with 4 CTAs per SM (measured on 8 x 1536 x 2048 x 16: 3.86 ms at four states per
+// thread, 3.23 ms at two).
 void bwd_split(int64_t N, int *G, int *Q) {
     *Q = N <= 1 ? 1 : (N <= 64 ? 2 : 4);
     int g = 1;
@@ -915,7 +778,12 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     const void *f_ptrs[] = {A, D, delta_bias, dlast_state, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias};
     for (const void *q : f_ptrs)
         if (q != nullptr && !aligned_to(q, 4)) return SSM_ERR_ALIGN;
+    if (workspace != nullptr && !aligned16(workspace)) return SSM_ERR_ALIGN;
     if (d.batch > 65535) return SSM_ERR_UNSUPPORTED;
+    const size_t need = ssm_selective_scan_bwd_workspace_bytes(dims);
+    WsChoice w{workspace, workspace_bytes, false};
+    if (workspace == nullptr) w = default_workspace();
+    if (!empty && need > 0 && !w.may_alloc && (w.ptr == nullptr || w.bytes < need)) return SSM_ERR_WORKSPACE;
     // gradients summed over the sequence, the batch or the channels start at zero
     const size_t BD = (size_t)(d.batch * d.dim), NL = (size_t)(d.dstate * d.seqlen);
     if (cudaMemsetAsync(dA, 0, (size_t)(d.dim * d.dstate) * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
@@ -925,47 +793,18 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     if (cudaMemsetAsync(dB, 0, (size_t)d.batch * NL * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
     if (cudaMemsetAsync(dC, 0, (size_t)d.batch * NL * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
     if (dz && !z && cudaMemsetAsync(dz, 0, BD * (size_t)d.seqlen * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
-    const size_t need = ssm_selective_scan_bwd_workspace_bytes(dims);
+    void *ws = w.ptr;
     bool allocated = false;
-    if (workspace == nullptr) {
-        if (cudaMallocAsync(&workspace, need, s) != cudaSuccess) return SSM_ERR_CUDA;
-        allocated = true;
-    } else if (workspace_bytes < need) {
-        return SSM_ERR_WORKSPACE;
-    } else if (!aligned16(workspace)) {
-        return SSM_ERR_ALIGN;
-    }
+    st = acquire_workspace(&ws, w.bytes, need, w.may_alloc, s, &allocated);
+    if (st != SSM_OK) return st;
     BwdParams p{u, delta, z, B, C, dy, A, D, delta_bias, dlast_state, du, ddelta, dA, dB, dC, dD,
-                z ? dz : nullptr, ddelta_bias, static_cast<float *>(workspace), d.batch, d.dim, d.seqlen,
+                z ? dz : nullptr, ddelta_bias, static_cast<float *>(ws), d.batch, d.dim, d.seqlen,
                 d.dstate, delta_softplus ? 1 : 0, (int)((d.seqlen + kBwdS - 1) / kBwdS)};
     int G, Q;
     bwd_split(d.dstate, &G, &Q);
-    const dim3 grid((unsigned)((d.dim + kBwdThreads / G - 1) / (kBwdThreads / G)), (unsigned)d.batch);
-    const bool bf = d.io_dtype == SSM_BF16;
-#define SSM_BWD(GG, QQ)                                                                                \
-    case GG * 10 + QQ: {                                                                               \
-        constexpr size_t tb = bwd_tile_bytes<GG, QQ>(), sm = tb + bwd_smem_bytes(GG, QQ);             \
-        if (bf) {                                                                                      \
-            cudaFuncSetAttribute(scan_bwd_kernel<bf16, GG, QQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
-            scan_bwd_ckpt_kernel<bf16, GG, QQ><<<grid, kBwdThreads, tb, s>>>(p);                      \
-            scan_bwd_kernel<bf16, GG, QQ><<<grid, kBwdThreads, sm, s>>>(p);                           \
-        } else {                                                                                       \
-            cudaFuncSetAttribute(scan_bwd_kernel<float, GG, QQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
-            scan_bwd_ckpt_kernel<float, GG, QQ><<<grid, kBwdThreads, tb, s>>>(p);                     \
-            scan_bwd_kernel<float, GG, QQ><<<grid, kBwdThreads, sm, s>>>(p);                          \
-        }                                                                                              \
-        break;                                                                                         \
-    }
-    switch (G * 10 + Q) {
-        SSM_BWD(1, 1) SSM_BWD(1, 2) SSM_BWD(2, 2) SSM_BWD(4, 2) SSM_BWD(8, 2) SSM_BWD(16, 2)
-        SSM_BWD(32, 2) SSM_BWD(32, 4)
-        default:
-            if (allocated) cudaFreeAsync(workspace, s);
-            return SSM_ERR_UNSUPPORTED;
-    }
-#undef SSM_BWD
-    const cudaError_t e = cudaGetLastError();
-    if (allocated) cudaFreeAsync(workspace, s);
+    const cudaError_t e = launch_bwd(d.io_dtype, G, Q, p, s);
+    if (allocated) cudaFreeAsync(ws, s);
+    if (e == cudaErrorInvalidConfiguration) return SSM_ERR_UNSUPPORTED;
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -991,7 +830,7 @@ ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, 
     // blocks start on multiples of 4 channels so that A + d0*N, D + d0 and bias + d0 stay
     // 16-byte aligned; each batch row of B and C gets its own 256-byte aligned slot
     const size_t blk = ((Dm + nblk_per_row - 1) / nblk_per_row + 3) / 4 * 4;
-    const size_t bc_row = (N * L * esz + 255) / 256 * 256;
+    const size_t bc_row = up256(N * L * esz);
     cudaStream_t ss[2] = {nullptr, nullptr};
     cudaEvent_t ev_in = nullptr;
     ssm_status_t rc = SSM_OK;
@@ -1043,11 +882,13 @@ ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, 
             if (z) CK(cudaMemcpyAsync(bz[k], static_cast<const char *>(z) + off, nd * L * esz, cudaMemcpyHostToDevice, s));
             ssm_dims_t sub{1, (int64_t)nd, d.seqlen, d.dstate, d.io_dtype};
             const size_t boff = (size_t)b * bc_row;
-            ssm_status_t r = ssm_selective_scan_fwd(
+            // the two pipelines overlap on the GPU: each block's chunk carries get a stream-ordered
+            // allocation of its own, never the registered workspace (which they would share)
+            ssm_status_t r = run_scan(
                 &sub, bu[k], bdl[k], static_cast<float *>(dA) + d0 * N, static_cast<char *>(dB) + boff,
                 static_cast<char *>(dC) + boff, D ? static_cast<float *>(dD) + d0 : nullptr, z ? bz[k] : nullptr,
                 delta_bias ? static_cast<float *>(dbias) + d0 : nullptr, delta_softplus, by[k],
-                last_state ? static_cast<float *>(bst[k]) : nullptr, s);
+                last_state ? static_cast<float *>(bst[k]) : nullptr, nullptr, 0, true, s);
             if (r != SSM_OK) { rc = r; break; }
             CK(cudaMemcpyAsync(static_cast<char *>(y) + off, by[k], nd * L * esz, cudaMemcpyDeviceToHost, s));
             if (last_state)
@@ -1096,6 +937,30 @@ const char *ssm_status_string(ssm_status_t status) {
 
 int ssm_set_structured_a(int enable) { return g_structured_a.exchange(enable ? 1 : 0); }
 
-int ssm_version(void) { return (1 << 16) | 0; }
+ssm_status_t ssm_set_plan_override(const ssm_plan_override_t *ov) {
+    ssm_plan_override_t v{};
+    if (ov != nullptr) {
+        v = *ov;
+        if (v.kernel < SSM_KERNEL_AUTO || v.kernel > SSM_KERNEL_TP) return SSM_ERR_UNSUPPORTED;
+        if (v.pair_states_per_lane != 0 && v.pair_states_per_lane != 4 && v.pair_states_per_lane != 8 &&
+            v.pair_states_per_lane != 16)
+            return SSM_ERR_UNSUPPORTED;
+        if (v.chunks < 0 || v.seq_states_per_lane < 0 || v.seq_lanes_per_channel < 0) return SSM_ERR_SHAPE;
+        if ((v.seq_states_per_lane != 0 || v.seq_lanes_per_channel != 0) &&
+            !seq_plan_supported(v.seq_states_per_lane, v.seq_lanes_per_channel))
+            return SSM_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lock(g_override_mu);
+    g_override = v;
+    return SSM_OK;
+}
+
+ssm_status_t ssm_get_plan_override(ssm_plan_override_t *out) {
+    if (out == nullptr) return SSM_ERR_NULL;
+    *out = plan_override();
+    return SSM_OK;
+}
+
+int ssm_version(void) { return (1 << 16) | 1; }
 
 }  // extern "C"

@@ -23,8 +23,8 @@ Workloads (Bt = batch, D = channels "d_inner", L = sequence length, N = state si
                 fp32 state (d_inner of the 2.8B row, 2 x 2560).
 
 In every scan workload A[d, n] = -(n+1) (the S4D-real initialisation, A_log = log(1..N),
-of "From RNN to Mamba", section 3.3); u, B, C ~ N(0,1) unless stated; the raw step
-``delta`` ~ N(0, 0.5^2) (0.5 is the standard deviation); the per-channel step bias is
+of "From RNN to Mamba", section 3.3; the tests also draw per-channel A, see ``make_A``);
+u, B, C ~ N(0,1) unless stated; the raw step ``delta`` ~ N(0, 0.5^2) (0.5 is the standard deviation); the per-channel step bias is
 log(expm1(x)) with x = exp(U[ln 1e-3, ln 1e-1]), i.e. the bias whose softplus lands
 log-uniformly in [1e-3, 1e-1] (same page, section 3.3; range from "Mamba model analysis",
 intelliparadigm.com, section 3.2). For the decode workload the step ``dt`` is handed to
@@ -40,8 +40,9 @@ from typing import Dict, Optional
 import numpy as np
 import torch
 
-# child-stream roles
-_R_BIAS, _R_DELTA, _R_U, _R_B, _R_C, _R_D, _R_Z, _R_STATE = range(8)
+# child-stream roles (SeedSequence children are fixed by their index, so adding a role at
+# the end leaves the streams of the earlier roles unchanged)
+_R_BIAS, _R_DELTA, _R_U, _R_B, _R_C, _R_D, _R_Z, _R_STATE, _R_A = range(9)
 
 
 @dataclass(frozen=True)
@@ -59,6 +60,7 @@ class ScanConfig:
     softplus: bool = True
     last_state: bool = False
     seed: int = 0
+    a_kind: str = "s4d"          # "s4d", "scaled" or "random" (see make_A)
 
     @property
     def elements(self) -> int:
@@ -75,6 +77,7 @@ class DecodeConfig:
     gate: bool = True
     dskip: Optional[str] = "ones"
     seed: int = 4
+    a_kind: str = "s4d"
 
 
 TINY = ScanConfig("tiny", 1, 4, 64, 4, io="f32", gate=False, dskip="ones", seed=0)
@@ -88,7 +91,7 @@ SCAN_CONFIGS: Dict[str, ScanConfig] = {c.name: c for c in (TINY, BLOCK512, M130,
 
 
 def _streams(seed: int):
-    return [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(8)]
+    return [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(9)]
 
 
 def _to_io(a32: np.ndarray, io: str) -> torch.Tensor:
@@ -105,6 +108,25 @@ def _bias(rng, D: int) -> np.ndarray:
 def s4d_real_A(D: int, N: int) -> torch.Tensor:
     """A[d, n] = -(n + 1)."""
     return -torch.arange(1, N + 1, dtype=torch.float32).repeat(D, 1).contiguous()
+
+
+def make_A(kind: str, D: int, N: int, rng) -> torch.Tensor:
+    """The state matrix diagonal A [D, N] fp32 for a recipe:
+
+    * ``s4d``:    A[d, n] = -(n + 1) for every channel (the workloads' recipe);
+    * ``scaled``: A[d, n] = -(n + 1) * a_d with a per-channel a_d = exp(U[ln 0.3, ln 3]), so
+                  that no two channels share a row (a kernel that read A[n] instead of
+                  A[d, n] would fail);
+    * ``random``: A[d, n] = -U(0.1, 5) independently per channel and state (no structure
+                  across states either: the general path of every kernel)."""
+    if kind == "s4d":
+        return s4d_real_A(D, N)
+    if kind == "scaled":
+        a = np.exp(rng.uniform(math.log(0.3), math.log(3.0), size=(D, 1)))
+        return torch.from_numpy((-np.arange(1, N + 1)[None, :] * a).astype(np.float32))
+    if kind == "random":
+        return torch.from_numpy((-rng.uniform(0.1, 5.0, size=(D, N))).astype(np.float32))
+    raise ValueError(f"unknown A recipe {kind!r}")
 
 
 def _ar1(rng, rows: int, L: int, rho: float = 0.9) -> np.ndarray:
@@ -130,7 +152,7 @@ def scan_inputs(cfg: ScanConfig, seed: Optional[int] = None, **overrides) -> Dic
     s = _streams(seed)
     Bt, D, L, N = cfg.Bt, cfg.D, cfg.L, cfg.N
     out: Dict[str, object] = {"cfg": cfg, "seed": seed}
-    out["A"] = s4d_real_A(D, N)
+    out["A"] = make_A(cfg.a_kind, D, N, s[_R_A])
     out["delta_bias"] = torch.from_numpy(_bias(s[_R_BIAS], D)) if cfg.bias else None
     out["delta"] = _to_io(0.5 * s[_R_DELTA].standard_normal((Bt, D, L), dtype=np.float32), cfg.io)
     if cfg.u_kind == "ar1":
@@ -168,7 +190,7 @@ def decode_inputs(cfg: DecodeConfig = DECODE, seed: Optional[int] = None, steps:
     raw = 0.5 * s[_R_DELTA].standard_normal((S, Bt, D), dtype=np.float32).astype(np.float64)
     dt = np.logaddexp(0.0, raw + bias[None, None, :]).astype(np.float32)
     out: Dict[str, object] = {"cfg": cfg, "seed": seed, "steps": S}
-    out["A"] = s4d_real_A(D, N)
+    out["A"] = make_A(cfg.a_kind, D, N, s[_R_A])
     out["state0"] = torch.from_numpy(s[_R_STATE].standard_normal((Bt, D, N), dtype=np.float32))
     out["x"] = _to_io(s[_R_U].standard_normal((S, Bt, D), dtype=np.float32), "bf16")
     out["dt"] = _to_io(dt, "bf16")

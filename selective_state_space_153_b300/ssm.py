@@ -7,6 +7,7 @@ There is no CPU fallback: if the library is missing, loading raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional, Tuple
@@ -31,12 +32,25 @@ EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_workspace_bytes",
            "ssm_selective_scan_fwd_noalloc", "ssm_selective_scan_fwd_disc", "ssm_state_update_disc",
            "ssm_conv_selective_scan_fwd", "ssm_conv_selective_scan_workspace_bytes",
            "ssm_selective_scan_bwd", "ssm_selective_scan_bwd_workspace_bytes",
-           "ssm_set_structured_a")
+           "ssm_set_structured_a", "ssm_set_workspace", "ssm_set_plan_override",
+           "ssm_get_plan_override")
+
+# ssm_kernel_t
+SSM_KERNEL_AUTO, SSM_KERNEL_PAIR, SSM_KERNEL_SEQ, SSM_KERNEL_TC, SSM_KERNEL_TP = range(5)
+_KERNELS = {"auto": SSM_KERNEL_AUTO, "pair": SSM_KERNEL_PAIR, "seq": SSM_KERNEL_SEQ, "tc": SSM_KERNEL_TC,
+            "tp": SSM_KERNEL_TP}
 
 
 class SsmDims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("seqlen", ctypes.c_int64),
                 ("dstate", ctypes.c_int64), ("io_dtype", ctypes.c_int)]
+
+
+class PlanOverride(ctypes.Structure):
+    """ssm_plan_override_t: every field 0 = the planner's choice."""
+    _fields_ = [("kernel", ctypes.c_int), ("pair_states_per_lane", ctypes.c_int), ("chunks", ctypes.c_int),
+                ("seq_states_per_lane", ctypes.c_int), ("seq_lanes_per_channel", ctypes.c_int),
+                ("decode_elementwise", ctypes.c_int), ("force_timeout", ctypes.c_int)]
 
 
 class SsmError(RuntimeError):
@@ -92,6 +106,12 @@ def load(path: str = LIB_PATH):
     lib.ssm_version.restype = ctypes.c_int
     lib.ssm_set_structured_a.argtypes = [ctypes.c_int]
     lib.ssm_set_structured_a.restype = ctypes.c_int
+    lib.ssm_set_workspace.argtypes = [_vp, ctypes.c_size_t]
+    lib.ssm_set_workspace.restype = ctypes.c_int
+    lib.ssm_set_plan_override.argtypes = [ctypes.POINTER(PlanOverride)]
+    lib.ssm_set_plan_override.restype = ctypes.c_int
+    lib.ssm_get_plan_override.argtypes = [ctypes.POINTER(PlanOverride)]
+    lib.ssm_get_plan_override.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -293,6 +313,51 @@ def set_structured_a(enable: bool) -> bool:
     for every state of a warp's channels; such warps form the decays from powers of
     exp(dt * A[d, 0])). Off by default; returns the previous setting. Process-wide."""
     return bool(load().ssm_set_structured_a(1 if enable else 0))
+
+
+def set_workspace(workspace: Optional[torch.Tensor]) -> None:
+    """Register ``workspace`` (a device tensor, any dtype, 16-byte aligned) as the current
+    device's default scan workspace (ssm_set_workspace), or unregister it with None. While one
+    is registered, scans without a workspace of their own use it and never allocate; keep the
+    tensor alive until those calls have completed."""
+    lib = load()
+    if workspace is None:
+        rc = lib.ssm_set_workspace(None, 0)
+    else:
+        rc = lib.ssm_set_workspace(_p(workspace), workspace.numel() * workspace.element_size())
+    if rc != SSM_OK:
+        raise SsmError(rc, "ssm_set_workspace")
+
+
+def get_plan_override() -> PlanOverride:
+    ov = PlanOverride()
+    rc = load().ssm_get_plan_override(ctypes.byref(ov))
+    if rc != SSM_OK:
+        raise SsmError(rc, "ssm_get_plan_override")
+    return ov
+
+
+def set_plan_override(ov: Optional[PlanOverride]) -> None:
+    rc = load().ssm_set_plan_override(None if ov is None else ctypes.byref(ov))
+    if rc != SSM_OK:
+        raise SsmError(rc, "ssm_set_plan_override")
+
+
+@contextlib.contextmanager
+def plan_override(kernel: str = "auto", pair_states_per_lane: int = 0, chunks: int = 0,
+                  seq_split: Optional[Tuple[int, int]] = None, decode_elementwise: bool = False,
+                  force_timeout: bool = False):
+    """Force a launch plan for the calls inside the block (ssm_set_plan_override; a test and
+    tuning hook), then restore the override that was in force before."""
+    prev = get_plan_override()
+    ov = PlanOverride(_KERNELS[kernel], int(pair_states_per_lane), int(chunks),
+                      int(seq_split[0]) if seq_split else 0, int(seq_split[1]) if seq_split else 0,
+                      int(bool(decode_elementwise)), int(bool(force_timeout)))
+    set_plan_override(ov)
+    try:
+        yield ov
+    finally:
+        set_plan_override(prev)
 
 
 def version() -> Tuple[int, int]:

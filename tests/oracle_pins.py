@@ -425,11 +425,10 @@ def pin_backward_finite_differences(lib):
     _close(yt.detach().numpy(), yo, 1e-12, 1e-13, "autograd forward vs C oracle")
     g = bwd.scan_backward(**ins, delta_softplus=True, dy=dy, dlast=dlast)
     eps = 1e-6
-    pick = _rng(42)
+    # every index of every input (118 on this shape): a gradient that is wrong at a single
+    # position -- one state, one timestep, the last step's D term -- cannot slip through
     for k, arr in ins.items():
-        flat = list(np.ndindex(arr.shape))
-        for j in pick.choice(len(flat), size=min(6, len(flat)), replace=False):
-            idx = flat[j]
+        for idx in np.ndindex(arr.shape):
             xp = {kk: vv.copy() for kk, vv in ins.items()}
             xm = {kk: vv.copy() for kk, vv in ins.items()}
             xp[k][idx] += eps

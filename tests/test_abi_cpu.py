@@ -39,7 +39,7 @@ def test_status_strings_and_version(lib):
         s = ssm.status_string(code)
         assert s.startswith("SSM_")
     assert ssm.status_string(99) == "SSM_ERR_UNKNOWN"
-    assert ssm.version() == (1, 0)
+    assert ssm.version() == (1, 1)   # 1.1: ssm_set_workspace and the plan override
 
 
 A = ctypes.c_void_p(0x1000)      # fake, 16-byte aligned "device" pointers: never dereferenced
@@ -128,3 +128,50 @@ def test_ws_entry_rejects_small_workspace(lib):
     rc = lib.ssm_selective_scan_fwd_ws(ctypes.byref(d), A, A, A, A, A, None, None, None, 1, A, None,
                                        MIS, need, None)
     assert rc == ssm.SSM_ERR_ALIGN
+
+
+def test_set_workspace_argument_errors(lib):
+    """ssm_set_workspace rejects bad arguments on the host (these checks run before any CUDA
+    call); without a GPU, a valid registration fails only at the device query."""
+    assert lib.ssm_set_workspace(None, 64) == ssm.SSM_ERR_NULL
+    assert lib.ssm_set_workspace(ctypes.c_void_p(0x1000), 0) == ssm.SSM_ERR_WORKSPACE
+    assert lib.ssm_set_workspace(ctypes.c_void_p(0x1001), 4096) == ssm.SSM_ERR_ALIGN
+    rc = lib.ssm_set_workspace(None, 0)   # unregister: needs the current device only
+    assert rc in (ssm.SSM_OK, ssm.SSM_ERR_CUDA)
+
+
+def test_plan_override_roundtrip_and_errors(lib):
+    """The override is read back as set, bad values leave the previous one in force, NULL
+    clears it, and it changes what the planner reports (the workspace a shape needs)."""
+    base = ssm.workspace_bytes(1, 1536, 131072, 64)
+    assert ssm.get_plan_override().kernel == ssm.SSM_KERNEL_AUTO
+    with ssm.plan_override(chunks=7) as ov:
+        got = ssm.get_plan_override()
+        assert got.chunks == 7 and got.kernel == 0
+        assert _chunks_from_workspace(1, 1536, 131072, 64) == 7
+        bad = ssm.PlanOverride(9, 0, 0, 0, 0, 0, 0)
+        assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
+        bad = ssm.PlanOverride(0, 5, 0, 0, 0, 0, 0)
+        assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
+        bad = ssm.PlanOverride(0, 0, -1, 0, 0, 0, 0)
+        assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_SHAPE
+        bad = ssm.PlanOverride(0, 0, 0, 16, 3, 0, 0)   # a lane split that is not built
+        assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
+        assert ssm.get_plan_override().chunks == 7
+        assert ov.chunks == 7
+    assert ssm.get_plan_override().chunks == 0
+    assert ssm.workspace_bytes(1, 1536, 131072, 64) == base
+    assert lib.ssm_get_plan_override(None) == ssm.SSM_ERR_NULL
+    with ssm.plan_override(kernel="tc"):
+        # the time-split plan keeps fp32 B/C of the whole sequence in its workspace
+        assert ssm.workspace_bytes(1, 1536, 131072, 64) > 2 * 64 * 131072 * 4
+    assert lib.ssm_set_plan_override(None) == ssm.SSM_OK
+
+
+def test_library_reads_no_environment(lib, monkeypatch):
+    """The experiment switches of earlier builds are gone: an environment variable of that
+    name changes nothing the planner reports."""
+    base = ssm.workspace_bytes(1, 1536, 131072, 64)
+    for k, v in (("SSM_KERNEL", "tc"), ("SSM_PAIR_CHUNKS", "3"), ("SSM_PAIR_KS", "8"), ("SSM_PLAN", "4,4,3")):
+        monkeypatch.setenv(k, v)
+    assert ssm.workspace_bytes(1, 1536, 131072, 64) == base

@@ -48,3 +48,22 @@ def test_decode_inputs():
     assert d["x"].shape == (3, 4, 16) and d["B"].shape == (3, 4, 16)
     assert d["state0"].dtype == torch.float32 and d["dt"].dtype == torch.bfloat16
     assert float(d["dt"].float().min()) > 0
+
+
+def test_per_channel_A_recipes():
+    """``scaled`` and ``random`` give every channel its own row of A (so that a kernel reading
+    A[n] for A[d, n] fails parity), negative, and leave every other array unchanged."""
+    base = gen.scan_inputs(gen.BLOCK512)
+    for kind in ("scaled", "random"):
+        x = gen.scan_inputs(gen.BLOCK512, a_kind=kind)
+        A = x["A"].double().numpy()
+        assert A.shape == (512, 16) and x["A"].dtype == torch.float32
+        assert (A < 0).all()
+        assert len({tuple(r) for r in A}) == 512, "rows must differ between channels"
+        for k in ("u", "delta", "B", "C", "z", "D", "delta_bias"):
+            assert torch.equal(x[k], base[k]), k
+    sc = gen.scan_inputs(gen.BLOCK512, a_kind="scaled")["A"].double().numpy()
+    ratio = sc / sc[:, :1]
+    assert np.allclose(ratio, np.arange(1, 17)[None, :], rtol=1e-6)   # (n+1) * a_d
+    d = gen.decode_inputs(Bt=2, D=8, steps=1, a_kind="random")
+    assert len({tuple(r) for r in d["A"].numpy()}) == 8

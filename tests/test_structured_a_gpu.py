@@ -62,13 +62,11 @@ CASES = [
 
 
 @pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,ks,chunks", CASES)
-def test_structured_shapes(Bt, D, L, N, io, gate, dskip, ks, chunks, monkeypatch):
-    monkeypatch.setenv("SSM_PAIR_KS", ks)
-    if chunks:
-        monkeypatch.setenv("SSM_PAIR_CHUNKS", str(chunks))
+def test_structured_shapes(Bt, D, L, N, io, gate, dskip, ks, chunks):
     cfg = gen.ScanConfig("st", Bt, D, L, N, io=io, gate=gate, dskip=dskip, seed=31 * L + N)
     inp = gen.scan_inputs(cfg)
-    (y, h), (y0, h0) = _both(inp)
+    with ssm.plan_override(pair_states_per_lane=int(ks), chunks=chunks):
+        (y, h), (y0, h0) = _both(inp)
     compare_scan(inp, y, h)
     # the fast path ran: the fp32 final state differs from the general path's in rounding
     assert not torch.equal(h, h0)
@@ -108,12 +106,12 @@ def test_one_broken_channel_falls_back_alone():
     compare_scan(inp, y, h)
 
 
-def test_padded_states_take_general_path(monkeypatch):
+def test_padded_states_take_general_path():
     """dstate 24 with eight states per lane pads the lane's states to 32: no warp qualifies."""
-    monkeypatch.setenv("SSM_PAIR_KS", "8")
     cfg = gen.ScanConfig("pd", 2, 30, 400, 24, io="f32", gate=True, dskip="normal", seed=4)
     inp = gen.scan_inputs(cfg)
-    (y, h), (y0, h0) = _both(inp)
+    with ssm.plan_override(pair_states_per_lane=8):
+        (y, h), (y0, h0) = _both(inp)
     assert torch.equal(y, y0) and torch.equal(h, h0)
     compare_scan(inp, y, h)
 
@@ -128,12 +126,11 @@ def test_zero_a_is_structured_prefix_sum():
 
 
 @pytest.mark.parametrize("N,io,chunks", [(16, "f32", 0), (64, "bf16", 3)])
-def test_structured_zoh(N, io, chunks, monkeypatch):
-    if chunks:
-        monkeypatch.setenv("SSM_PAIR_CHUNKS", str(chunks))
+def test_structured_zoh(N, io, chunks):
     cfg = gen.ScanConfig("sz", 2, 40, 720, N, io=io, gate=True, dskip="ones", seed=N + 1)
     inp = gen.scan_inputs(cfg)
-    (y, h), (y0, h0) = _both(inp, discretization="zoh")
+    with ssm.plan_override(chunks=chunks):
+        (y, h), (y0, h0) = _both(inp, discretization="zoh")
     compare_scan(inp, y, h, zoh=True)
     assert not torch.equal(h, h0)
 

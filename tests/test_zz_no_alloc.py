@@ -37,11 +37,21 @@ def test_scratch_size_matches_header():
 
 
 @pytest.fixture
-def time_split_plan(monkeypatch):
+def time_split_plan(lib):
     """The persistent time-split kernel keeps fp32 B/C for the whole sequence in its workspace:
-    a plan whose scratch exceeds the fixed size (the default plans stay within a few MiB)."""
-    monkeypatch.setenv("SSM_KERNEL", "tc")
-    yield
+    on the long-sequence shape that exceeds the fixed size, which the default plan (chunk
+    carries only, about 41 MiB there) fits."""
+    with ssm.plan_override(kernel="tc"):
+        yield
+
+
+def test_default_long_sequence_plan_fits_scratch(lib):
+    """The default plan of the long-sequence shape keeps its chunk carries within the fixed
+    scratch: a planner change that outgrew it would make that shape fail here first."""
+    need = ssm.workspace_bytes(1, 1536, 131072, 64, ssm.SSM_BF16)
+    assert 0 < need <= ssm.SCRATCH_MAX_BYTES
+    for shape in ((8, 1536, 2048, 16), (1, 512, 1024, 16), (1, 2560, 65536, 64), (2, 1536, 65536, 64)):
+        assert ssm.workspace_bytes(*shape, ssm.SSM_BF16) <= ssm.SCRATCH_MAX_BYTES, shape
 
 
 def test_oversize_shape_rejected_on_host(lib, time_split_plan):
@@ -65,8 +75,8 @@ def test_empty_problem_needs_no_gpu(lib):
                                               None, 1, None, None, None) == ssm.SSM_OK
 
 
-# the persistent kernel with channel pairs (N=16 and N=64), the chunked lane kernel, and a
-# shape that needs no scratch at all
+# default plans: the chunked channel-pair kernel at 16 and 64 states (whose scratch holds the
+# chunk carries), and shapes that need no scratch at all
 CASES = [
     gen.M130,
     gen.ScanConfig("n64_l16k", 1, 1536, 16384, 64, gate=False, dskip="ones", u_kind="ar1", seed=11),
@@ -125,6 +135,30 @@ def test_noalloc_back_to_back_different_shapes(lib):
     torch.cuda.synchronize()
     assert ssm.stream_status() == ssm.SSM_OK
     for (y, h), (yr, hr) in zip(outs, (refs[0], refs[1], refs[0])):
+        assert torch.equal(y, yr)
+        assert torch.equal(h, hr)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kernel", ["tp", "tc"])
+def test_noalloc_persistent_kernels_clear_their_control_words(lib, kernel):
+    """The persistent time-split kernels keep a work ticket and per-segment carry flags at the
+    head of the scratch. Each call clears them: two calls in a row, then a call of another
+    shape, then the first shape again, all equal the allocating entry point bit for bit (stale
+    tickets or flags would show as a mismatch or as a timeout in the status word)."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    small = gen.ScanConfig("tcs", 2, 40, 1000, 16, gate=True, dskip="normal", seed=7, a_kind="random")
+    gs = [_dev(gen.scan_inputs(c)) for c in (gen.M130, small)]
+    with ssm.plan_override(kernel=kernel):
+        for c in (gen.M130, small):
+            need = ssm.workspace_bytes(c.Bt, c.D, c.L, c.N, ssm.SSM_BF16)
+            assert 0 < need <= ssm.SCRATCH_MAX_BYTES
+        refs = [_existing(g) for g in gs]
+        outs = [_noalloc(g) for g in (gs[0], gs[0], gs[1], gs[0])]
+        torch.cuda.synchronize()
+        assert ssm.stream_status() == ssm.SSM_OK
+    for (y, h), (yr, hr) in zip(outs, (refs[0], refs[0], refs[1], refs[0])):
         assert torch.equal(y, yr)
         assert torch.equal(h, hr)
 
