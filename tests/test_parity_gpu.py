@@ -378,6 +378,33 @@ def test_caller_workspace_and_stream():
     assert ssm.stream_status(s) == ssm.SSM_OK
 
 
+def test_registered_workspace():
+    """ssm_set_workspace: with a workspace registered, the scans take their chunk carries
+    from it (results match the oracle), a registration smaller than a call needs makes that
+    call return SSM_ERR_WORKSPACE, and unregistering restores the library's allocation."""
+    inp = gen.scan_inputs(gen.BLOCK512, a_kind="scaled")
+    need = ssm.workspace_bytes(1, 512, 1024, 16)
+    assert need > 0
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")   # stale bytes: must not matter
+    try:
+        ssm.set_workspace(ws)
+        y, h = gpu_scan(inp)
+        compare_scan(inp, y, h)
+        ssm.set_workspace(ws[: need // 2])
+        with pytest.raises(ssm.SsmError) as e:
+            gpu_scan(inp)
+        assert e.value.code == ssm.SSM_ERR_WORKSPACE
+        # a shape that needs no workspace still runs with the small registration
+        small = gen.scan_inputs(gen.ScanConfig("nows", 16, 2048, 64, 16, seed=2))
+        assert ssm.workspace_bytes(16, 2048, 64, 16) == 0
+        y2, h2 = gpu_scan(small)
+        compare_scan(small, y2, h2, channels=sample_channels(16, 2048, 16))
+    finally:
+        ssm.set_workspace(None)
+    y3, h3 = gpu_scan(inp)
+    assert torch.equal(y3, y) and torch.equal(h3, h)
+
+
 @pytest.mark.parametrize("cfg", [gen.BLOCK512, gen.ScanConfig("h", 3, 70, 333, 16, io="f32", gate=True, seed=8)],
                          ids=["block512", "ragged_f32"])
 def test_host_buffer_entry(cfg):
