@@ -5,6 +5,28 @@
 
 namespace ssm {
 
+// Incoming state of every chunk from the chunk aggregates, sequentially over chunks:
+//   hin[0] = 0,  hin[k+1] = exp(A * sum_dt[k]) * hin[k] + hlocal_end[k].
+// One thread per (channel, state).
+__global__ void chunk_combine_kernel(const float *__restrict__ A, const float *__restrict__ agg_h,
+                                     const float *__restrict__ agg_s, float *__restrict__ hin,
+                                     int64_t BD, int64_t Dm, int64_t N, int npad, int nchunks) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= BD * npad) return;
+    const int64_t bd = i / npad;
+    const int n = (int)(i % npad);
+    const int64_t d = bd % Dm;
+    const float Ap = n < N ? A[d * N + n] * kLog2e : 0.0f;
+    float h = 0.0f;
+    for (int k = 0; k < nchunks; ++k) {
+        hin[((int64_t)k * BD + bd) * npad + n] = h;
+        if (k + 1 < nchunks) {
+            const float P = ex2(Ap * agg_s[(int64_t)k * BD + bd]);
+            h = fmaf(P, h, agg_h[((int64_t)k * BD + bd) * npad + n]);
+        }
+    }
+}
+
 namespace {
 using bf16 = __nv_bfloat16;
 
@@ -42,28 +64,6 @@ cudaError_t launch_seq_io(int nper, int g, bool agg, bool aligned, const SeqPara
         SSM_SEQ_CASES(SSM_SEQ_LAUNCH)
 #undef SSM_SEQ_LAUNCH
         default: return cudaErrorInvalidConfiguration;
-    }
-}
-
-// Incoming state of every chunk from the chunk aggregates, sequentially over chunks:
-//   hin[0] = 0,  hin[k+1] = exp(A * sum_dt[k]) * hin[k] + hlocal_end[k].
-// One thread per (channel, state).
-__global__ void chunk_combine_kernel(const float *__restrict__ A, const float *__restrict__ agg_h,
-                                     const float *__restrict__ agg_s, float *__restrict__ hin,
-                                     int64_t BD, int64_t Dm, int64_t N, int npad, int nchunks) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= BD * npad) return;
-    const int64_t bd = i / npad;
-    const int n = (int)(i % npad);
-    const int64_t d = bd % Dm;
-    const float Ap = n < N ? A[d * N + n] * kLog2e : 0.0f;
-    float h = 0.0f;
-    for (int k = 0; k < nchunks; ++k) {
-        hin[((int64_t)k * BD + bd) * npad + n] = h;
-        if (k + 1 < nchunks) {
-            const float P = ex2(Ap * agg_s[(int64_t)k * BD + bd]);
-            h = fmaf(P, h, agg_h[((int64_t)k * BD + bd) * npad + n]);
-        }
     }
 }
 

@@ -66,9 +66,14 @@ struct PairCfg {
     static constexpr size_t kOffBc = kOffDx + 2 * kDxBytes;
     static constexpr size_t kOffYs = kOffBc + 2 * kBcBytes;
     static constexpr size_t kOffBias = kOffYs + 2 * kYsBytes;
+    // steps per conversion item (8, or 4 when 8 would leave threads idle) and the aggregate
+    // pass's per-item sums of dt, [2][kCh][T / kSI]
+    static constexpr int kSI = (kCh * (T / 8) >= kThreads) ? 8 : 4;
+    static constexpr size_t kOffTs = kOffBias + (size_t)kCh * sizeof(float);
+    static constexpr size_t kTsBytes = (size_t)2 * kCh * (T / kSI) * sizeof(float);
     // conv front: the conv + SiLU output u [2][kCh][T] fp32, the right-aligned taps [kCh][4],
     // the conv bias [kCh] and the chunk's first-tile halo [kCh][4] (three steps used)
-    static constexpr size_t kOffSu = kOffBias + (size_t)kCh * sizeof(float);
+    static constexpr size_t kOffSu = kOffTs + kTsBytes;
     static constexpr size_t kSuBytes = CONV ? (size_t)2 * kCh * T * sizeof(float) : 0;
     static constexpr size_t kOffCw = kOffSu + kSuBytes;
     static constexpr size_t kCwBytes = CONV ? (size_t)kCh * 9 * sizeof(float) : 0;
@@ -97,6 +102,8 @@ constexpr int pair_warps(int ks, int gp, bool agg) {
 // Registers per thread the kernels are held to (launch bounds), so that residency per SM
 // follows from the block size alone: 128, or 168 for sixteen lanes per pair and for sixteen
 // states per lane (whose 32 states and 32 decay factors per lane spill under 128).
+// (Measured alternatives on B300 for 1 x 1536 x 131072 x 64: the full pass at 255 registers,
+// 2 CTAs per SM, took 2.99 ms against 2.69 ms at 168 registers, 3 CTAs per SM.)
 constexpr int pair_reg_budget(int ks, int gp) { return (gp >= 16 || ks >= 16) ? 168 : 128; }
 constexpr int pair_min_blocks(int warps, int ks, int gp) { return 65536 / (warps * 32 * pair_reg_budget(ks, gp)); }
 
@@ -143,6 +150,7 @@ scan_pair_kernel(const SeqParams p) {
     float *sBC0 = reinterpret_cast<float *>(smem + Cfg::kOffBc);     // [T][2*kNP]  B | C
     IO *sYS0 = reinterpret_cast<IO *>(smem + Cfg::kOffYs);           // [kCh][kRS]  y tile, io type
     float *sBias = reinterpret_cast<float *>(smem + Cfg::kOffBias);  // [kCh]
+    float *sTS0 = reinterpret_cast<float *>(smem + Cfg::kOffTs);     // [2][kCh][T/kSI] sums of dt
     float *sSu0 = reinterpret_cast<float *>(smem + Cfg::kOffSu);     // conv front: [2][kCh][T] u
     float *sCw = reinterpret_cast<float *>(smem + Cfg::kOffCw);      // conv front: [kCh][4] taps
     float *sCb = sCw + 4 * kCh;                                      // [kCh] conv bias
@@ -286,16 +294,26 @@ scan_pair_kernel(const SeqParams p) {
         cp_async_commit();
     };
 
-    // tile j's raw rows -> (dt, dt*u) per (channel, t) and fp32 B, C as [t][n]
-    auto convert = [&](int j) {
+    // tile j's raw rows -> (dt, dt*u) per (channel, t), fp32 B, C as [t][n] and (aggregate
+    // pass) the sums of dt over each item's steps. Items and their per-thread counts are
+    // compile-time; a FULL tile has all T steps, so only the last tile checks its length.
+    // Eight timesteps per item, or four when eight would leave threads without work.
+    constexpr int kSI = Cfg::kSI;
+    constexpr int kDXItems = kCh * (T / kSI);
+    constexpr int kDXIter = (kDXItems + Cfg::kThreads - 1) / Cfg::kThreads;
+    constexpr int kBCKinds = AGG ? 1 : 2;
+    constexpr int kBCItems = kBCKinds * kNP * kPieces;
+    constexpr int kBCIter = (kBCItems + Cfg::kThreads - 1) / Cfg::kThreads;
+    auto convert = [&](int j, auto full_c) {
+        constexpr bool FULL = decltype(full_c)::value;
         const IO *raw = raw_of(j);
         float4 *sDX = sDX0 + (size_t)(j & 1) * T * kPairs;
         float *sBC = sBC0 + (size_t)(j & 1) * T * 2 * kNP;
-        const int64_t t0 = l_begin + (int64_t)j * T;
-        const int len = (int)min((int64_t)T, l_end - t0);
-        // eight timesteps per item, or four when eight would leave threads without work
-        constexpr int kSI = (kCh * (T / 8) >= Cfg::kThreads) ? 8 : 4;
-        for (int i = tid; i < kCh * (T / kSI); i += Cfg::kThreads) {
+        const int len = FULL ? T : (int)min((int64_t)T, l_end - (l_begin + (int64_t)j * T));
+#pragma unroll
+        for (int it = 0; it < kDXIter; ++it) {
+            const int i = tid + it * Cfg::kThreads;
+            if (kDXItems % Cfg::kThreads != 0 && i >= kDXItems) break;
             const int cc = i % kCh, tq = (i / kCh) * kSI;
             float uu[kSI], dl[kSI];
             load_steps<kSI>(raw + (size_t)cc * kRS + tq, uu);
@@ -325,21 +343,29 @@ scan_pair_kernel(const SeqParams p) {
             }
             const bool ok = d0 + cc < p.Dm;
             const float bb = sBias[cc];
+            float dt[kSI];
+#pragma unroll
+            for (int e = 0; e < kSI; ++e) dt[e] = dl[e] + bb;
+            if (p.softplus) {
+#pragma unroll
+                for (int e = 0; e < kSI; ++e) dt[e] = softplus_f(dt[e]);
+            }
             float2 *dst = reinterpret_cast<float2 *>(sDX) + (size_t)tq * kPairs * 2 + cc;
+            float ts = 0.0f;
 #pragma unroll
             for (int e = 0; e < kSI; ++e) {
-                float dt = 0.0f, x = 0.0f;
-                if (ok && tq + e < len) {
-                    dt = dl[e] + bb;
-                    if (p.softplus) dt = softplus_f(dt);
-                    x = dt * uu[e];
-                }
-                dst[(size_t)e * kPairs * 2] = make_float2(dt, x);
+                const bool in = ok && (FULL || tq + e < len);
+                const float d = in ? dt[e] : 0.0f;
+                ts += d;
+                dst[(size_t)e * kPairs * 2] = make_float2(d, in ? d * uu[e] : 0.0f);
             }
+            if constexpr (AGG) sTS0[(j & 1) * kDXItems + cc * (T / kSI) + tq / kSI] = ts;
         }
-        constexpr int nkind = AGG ? 1 : 2;
-        for (int i = tid; i < nkind * kNP * kPieces; i += Cfg::kThreads) {
-            const int n = i % kNP, r = i / kNP, kind = r % nkind, tq = (r / nkind) * kEpr;
+#pragma unroll
+        for (int it = 0; it < kBCIter; ++it) {
+            const int i = tid + it * Cfg::kThreads;
+            if (kBCItems % Cfg::kThreads != 0 && i >= kBCItems) break;
+            const int n = i % kNP, r = i / kNP, kind = r % kBCKinds, tq = (r / kBCKinds) * kEpr;
             float v[kEpr];
             if (n < N) {
                 unpack16(*reinterpret_cast<const uint4 *>(raw + (size_t)(kRowB + kind * kNP + n) * kRS + tq), v, IO(0.0f));
@@ -351,6 +377,10 @@ scan_pair_kernel(const SeqParams p) {
 #pragma unroll
             for (int e = 0; e < kEpr; ++e) dst[(size_t)e * 2 * kNP] = v[e];
         }
+    };
+    auto convert_tile = [&](int j) {
+        if (l_end - (l_begin + (int64_t)j * T) >= T) convert(j, BoolC<true>{});
+        else convert(j, BoolC<false>{});
     };
 
     float dsum[2] = {0.f, 0.f}, dsum_c[2] = {0.f, 0.f};   // compensated sums of dt (AGG)
@@ -416,7 +446,7 @@ scan_pair_kernel(const SeqParams p) {
         issue_tile(0);
         cp_async_wait<0>();
         __syncthreads();
-        convert(0);
+        convert_tile(0);
         if (ntiles > 1) issue_tile(1);
     }
     for (int j = 0; j < ntiles; ++j) {
@@ -424,25 +454,42 @@ scan_pair_kernel(const SeqParams p) {
         __syncthreads();      // conversion of tile j done; scan of tile j-1 done everywhere
         if (j + 2 < ntiles) issue_tile(j + 2);
         if (!AGG && j > 0) store_y(j - 1);
-        if (j + 1 < ntiles) convert(j + 1);
+        if (j + 1 < ntiles) convert_tile(j + 1);
 
         const float4 *sDX = sDX0 + (size_t)(j & 1) * T * kPairs;
         const float *sBC = sBC0 + (size_t)(j & 1) * T * 2 * kNP;
         const IO *raw = raw_of(j);
         IO *ys = sYS0 + (size_t)(j & 1) * kCh * kRS;
-        float tsum[2] = {0.f, 0.f};
+        // per-lane bases: with the tile fully unrolled every step's offset is a constant
+        const float4 *dxl = sDX + pr;
+        const float *bcl = sBC + 4 * g;
+        // y of the GP steps tb..tb+GP-1: the GP lanes of a pair exchange their partials (lane g
+        // ends with timestep tb+g, both channels), add D*u, apply the gate and stage y for a
+        // coalesced store after the next barrier (rows past the last channel are never stored)
+        auto finish_group = [&](int tb, float (&yp)[2][GP]) {
+            const int t = tb + g;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                const float ysum = group_reduce_transpose<GP>(yp[ch], lane);
+                const int cc = c0 + ch;
+                const float uv = CONV ? sSu0[(size_t)(j & 1) * kCh * T + (size_t)cc * T + t]
+                                      : io_traits<IO>::to_f(raw[(size_t)cc * kRS + t]);
+                float yv = fmaf(Dd[ch], uv, ysum);
+                if (has_z) yv *= silu_f(io_traits<IO>::to_f(raw[(size_t)(2 * kCh + cc) * kRS + t]));
+                store_io(ys + (size_t)cc * kRS + t, yv);
+            }
+        };
         auto scan_tile = [&](auto st_c) {
             constexpr bool ST = decltype(st_c)::value;
-#pragma unroll 1
+#pragma unroll
             for (int tb = 0; tb < T; tb += GP) {
                 float yp[2][GP];
 #pragma unroll
                 for (int s = 0; s < GP; ++s) {
                     const int t = tb + s;
-                    const float4 dx = sDX[(size_t)t * kPairs + pr];
+                    const float4 dx = dxl[t * kPairs];
                     const float2 dd[2] = {make_float2(dx.x, dx.x), make_float2(dx.z, dx.z)};
                     const float2 xx[2] = {make_float2(dx.y, dx.y), make_float2(dx.w, dx.w)};
-                    if (AGG) { tsum[0] += dx.x; tsum[1] += dx.z; }
                     // structured A: r = exp(dt*A[d, 0]) and (r^2, r^2) per channel
                     float r[2] = {1.0f, 1.0f};
                     float2 r2[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
@@ -456,9 +503,9 @@ scan_pair_kernel(const SeqParams p) {
                     float2 ya[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                     for (int q = 0; q < kQN; ++q) {
-                        const float4 bq = *reinterpret_cast<const float4 *>(sBC + (size_t)t * 2 * kNP + 4 * (GP * q + g));
+                        const float4 bq = *reinterpret_cast<const float4 *>(bcl + t * 2 * kNP + 4 * GP * q);
                         float4 cq = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (!AGG) cq = *reinterpret_cast<const float4 *>(sBC + (size_t)t * 2 * kNP + kNP + 4 * (GP * q + g));
+                        if (!AGG) cq = *reinterpret_cast<const float4 *>(bcl + t * 2 * kNP + kNP + 4 * GP * q);
 #pragma unroll
                         for (int ch = 0; ch < 2; ++ch) {
                             float2 e0, e1, a0, a1;
@@ -498,29 +545,20 @@ scan_pair_kernel(const SeqParams p) {
                         yp[1][s] = ya[1].x + ya[1].y;
                     }
                 }
-                if (!AGG) {
-                    // the timestep this lane finished, for both channels; staged for a coalesced
-                    // store after the next barrier (rows past the last channel are never stored)
-                    const int t = tb + g;
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch) {
-                        const float ysum = group_reduce_transpose<GP>(yp[ch], lane);
-                        const int cc = c0 + ch;
-                        const float uv = CONV ? sSu0[(size_t)(j & 1) * kCh * T + (size_t)cc * T + t]
-                                              : io_traits<IO>::to_f(raw[(size_t)cc * kRS + t]);
-                        float yv = fmaf(Dd[ch], uv, ysum);
-                        if (has_z) yv *= silu_f(io_traits<IO>::to_f(raw[(size_t)(2 * kCh + cc) * kRS + t]));
-                        store_io(ys + (size_t)cc * kRS + t, yv);
-                    }
-                }
+                if (!AGG) finish_group(tb, yp);
             }
         };
         if (st) scan_tile(BoolC<true>{});
         else scan_tile(BoolC<false>{});
         if (AGG) {
+            // this tile's sum of dt per channel, from the conversion's per-item sums
+            const float *ts = sTS0 + (j & 1) * kDXItems;
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
-                const float yk = tsum[ch] - dsum_c[ch];
+                float tsum = 0.0f;
+#pragma unroll
+                for (int r = 0; r < T / kSI; ++r) tsum += ts[(c0 + ch) * (T / kSI) + r];
+                const float yk = tsum - dsum_c[ch];
                 const float tk = dsum[ch] + yk;
                 dsum_c[ch] = (tk - dsum[ch]) - yk;
                 dsum[ch] = tk;
