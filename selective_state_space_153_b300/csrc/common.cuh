@@ -62,6 +62,16 @@ __device__ __forceinline__ float zoh_phi(float x, float abar) {
     return fabsf(x) < 0.125f ? p : (abar - 1.0f) * rcp_approx(x);
 }
 
+// a - b on packed pairs (f32x2, round to nearest)
+__device__ __forceinline__ float2 fsub2_rn(float2 a, float2 b) {
+    float2 r;
+    asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
+        " sub.rn.f32x2 pd, pa, pb;\n mov.b64 {%0, %1}, pd;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
 // --- io conversions ---------------------------------------------------------------------
 template <typename IO> struct io_traits;
 template <> struct io_traits<float> {
