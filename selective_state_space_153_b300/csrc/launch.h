@@ -47,7 +47,7 @@ cudaError_t launch_tc(ssm_dtype_t io, bool pipelined, int G, const TcParams &prm
 // 2 = scalar (N % 4 != 0)
 cudaError_t launch_decode(ssm_dtype_t io, int kind, int lpc, bool zoh, const DecodeParams &p, cudaStream_t s);
 
-// backward (scan_bwd.cuh): checkpoint pass then adjoint pass
-cudaError_t launch_bwd(ssm_dtype_t io, int G, int Q, const BwdParams &p, cudaStream_t s);
+// backward (scan_bwd.cuh): checkpoint pass then adjoint pass; G lanes per channel
+cudaError_t launch_bwd(ssm_dtype_t io, int G, const BwdParams &p, cudaStream_t s);
 
 }  // namespace ssm

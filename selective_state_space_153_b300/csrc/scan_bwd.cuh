@@ -7,262 +7,402 @@
 //     lambda_t = dyhat_t * C_t + c_t,   c_{t-1} = a_t * lambda_t,   c_{L-1} = dlast,
 // with dyhat_t = dy_t * SiLU(z_t), from which (per channel d, state n, step t)
 //     dB_t += lambda_t dt_t u_t         dC_t += dyhat_t h_t          (summed over channels)
-//     du_t  = sum_n lambda_t dt_t B_t + dyhat_t D
-//     ddt_t = sum_n lambda_t (u_t B_t + A a_t h_{t-1}),   ddelta_t = ddt_t * sigmoid(v_t)
+//     du_t  = dt_t sum_n lambda_t B_t + dyhat_t D
+//     ddt_t = u_t sum_n lambda_t B_t + sum_n lambda_t A a_t h_{t-1},   ddelta_t = ddt_t sigmoid(v_t)
 //     dA   += lambda_t dt_t a_t h_{t-1}   dD += dyhat_t u_t   dz_t = dy_t yhat_t SiLU'(z_t)
 // (v = delta + bias; sigmoid is the softplus derivative; without softplus ddelta = ddt).
 //
-// Work decomposition: a thread owns Q states n = g + G*q of one channel (G lanes per
-// channel, a power of two <= 32; the batch row is grid.y so a warp never spans two rows).
-// Pass 1 (scan_bwd_ckpt_kernel) runs the recurrence forward and stores h at the start of
-// every S-step segment. Pass 2 (scan_bwd_kernel) walks the segments backwards: it recomputes
-// the segment's S states into registers from the checkpoint, then runs the adjoint over the
-// segment in reverse. Sums over the states of a channel use shuffles across its G lanes; sums
-// over channels (dB, dC) are pre-reduced across the warp's channels with shuffles, staged
-// per warp for the whole segment in shared memory, summed over the CTA's warps after the
-// segment and added with one fp32 atomic per (CTA, state, step); dA, dD and the dt bias are
-// summed over the sequence in the thread and added once at the end.
+// Work decomposition: a thread owns four states n = g + G*q (q < 4) of one channel, G lanes
+// per channel (a power of two, 4G >= N), 32/G channels per warp, 128/G per CTA; the batch
+// row is grid.y. Pass 1 (scan_bwd_ckpt_kernel) runs the recurrence forward and stores h at
+// the start of every S-step segment. Pass 2 (scan_bwd_kernel) walks the segments backwards:
+//   * the CTA stages the segment's B, C rows (as [t][g][q], so a lane's four states are one
+//     16-byte read) and, once per (channel, step), dt, the softplus derivative, u,
+//     dyhat = dy*SiLU(z) and the gate derivative factor dy*SiLU'(z); the raw inputs of the
+//     next segment are fetched into registers while the current one computes;
+//   * each lane recomputes its states' S steps from the checkpoint, then runs the adjoint in
+//     reverse;
+//   * sums over the states of a channel (yhat, sum lambda*B, sum lambda*A*a*h) are kept per
+//     step and combined over the G lanes with a transposed butterfly every G steps, after
+//     which lane g holds (and writes) step g of the group: one exchange per lane and step
+//     instead of a butterfly per value and step;
+//   * the per-element dB and dC terms are collected per state as 4-step vectors in shared
+//     memory, summed over the CTA's channels after the segment and added with one vector
+//     atomic per (state, 4 steps);
+//   * dA, dD and the dt bias are summed in registers and added once at the end.
 #pragma once
 #include "common.cuh"
 
 namespace ssm {
 
-constexpr int kBwdS = 16;        // steps per checkpoint segment
+constexpr int kBwdS = 8;         // steps per checkpoint segment
 constexpr int kBwdThreads = 128;
-// dynamic shared memory of scan_bwd_kernel<., G, Q> beyond its input tile: the dB/dC
-// partials [2][warps][kBwdS][G*Q] floats
-constexpr size_t bwd_smem_bytes(int G, int Q) { return (size_t)2 * (kBwdThreads / 32) * kBwdS * G * Q * sizeof(float); }
+constexpr int kBwdQ = 4;         // states per thread
 
 struct BwdParams {
     const void *u, *delta, *z, *B, *C, *dy;
     const float *A, *D, *bias, *dlast;
     float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *dbias;
-    float *ckpt;                  // [Bt*Dm][nseg][G*Q]: h before each segment's first step
+    float *ckpt;                  // [Bt*Dm][nseg][4G]: h before each segment's first step
     int64_t Bt, Dm, L, N;
     int softplus, nseg;
 };
 
-__device__ __forceinline__ float bwd_dt(float v, int softplus) { return softplus ? softplus_f(v) : v; }
-
-// sum over the G lanes of a channel (lanes g = lane % G are consecutive)
+// Shared-memory layout (floats) of the backward kernels for G lanes per channel.
 template <int G>
-__device__ __forceinline__ float sum_lanes(float v) {
-#pragma unroll
-    for (int o = G / 2; o >= 1; o /= 2) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-// sum over the 32/G channels of a warp (lanes with the same g)
+struct BwdCfg {
+    static constexpr int kQ = kBwdQ, kNP = G * kQ, kS = kBwdS;
+    static constexpr int kCpb = kBwdThreads / G;          // channels per CTA
+    static constexpr int kTileBC = kS * kNP;              // B or C: [S][G][Q]
+    static constexpr int kChan = kCpb * kS;               // per-channel arrays [kCpb][S]
+    // dB/dC partials: per kind and channel, one row of S steps per state, padded so that the
+    // 16-byte stores of a warp's lanes fall into distinct banks
+    static constexpr int kRow = kS + 4;
+    static constexpr int kPartCh = kNP * kRow + 16;
+    static constexpr int kOffB = 0, kOffC = kTileBC, kOffDt = 2 * kTileBC;
+    static constexpr int kOffSg = kOffDt + kChan, kOffU = kOffSg + kChan, kOffDyh = kOffU + kChan;
+    static constexpr int kOffGz = kOffDyh + kChan, kOffPart = kOffGz + kChan;
+    static constexpr int kFloats = kOffPart + 2 * kCpb * kPartCh;
+    static_assert(kS % 4 == 0 && (kOffPart % 4) == 0 && (kPartCh % 4) == 0 && (kRow % 4) == 0, "16-byte rows");
+};
 template <int G>
-__device__ __forceinline__ float sum_channels(float v) {
-#pragma unroll
-    for (int o = G; o < 32; o *= 2) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
+constexpr size_t bwd_smem_bytes() { return (size_t)BwdCfg<G>::kFloats * sizeof(float); }
 
-// Inputs of one S-step segment, staged by the whole CTA with coalesced loads: B and C rows of
-// the batch row ([G*Q][S], zero beyond N or L) and, per channel of the CTA, dt, the softplus
-// derivative, u, dy and z ([kCpb][S]); dt = softplus(delta + bias) is formed once per
-// (channel, step) here rather than in every lane.
-template <typename IO, int G, int Q>
-struct BwdTile {
-    static constexpr int kCpb = kBwdThreads / G;
-    static constexpr int kFloats = 2 * G * Q * kBwdS + 5 * kCpb * kBwdS;
-    float *B, *C, *dt, *sg, *u, *dy, *z;
-    __device__ BwdTile(float *base) {
-        B = base; C = B + G * Q * kBwdS; dt = C + G * Q * kBwdS; sg = dt + kCpb * kBwdS;
-        u = sg + kCpb * kBwdS; dy = u + kCpb * kBwdS; z = dy + kCpb * kBwdS;
-    }
-    // full = false: only what the forward recompute needs (B, dt, u)
-    __device__ void load(const BwdParams &p, int64_t b, int64_t t0, bool full) {
+// Raw inputs of one segment [t0, t0+S) of batch row b for the CTA's channels d0 .. d0+kCpb-1,
+// fetched into registers one segment ahead (the loads are in flight while the previous
+// segment computes) and then staged into shared memory (stage). FULL = false: only B, dt
+// and u (the checkpoint pass).
+template <typename IO, int G, bool FULL>
+struct BwdFetch {
+    using Cfg = BwdCfg<G>;
+    static constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kCpb = Cfg::kCpb;
+    static constexpr int kBC = (FULL ? 2 : 1) * kNP * kS, kBCI = (kBC + kBwdThreads - 1) / kBwdThreads;
+    static constexpr int kCH = kCpb * kS, kCHI = (kCH + kBwdThreads - 1) / kBwdThreads;
+    float bc[kBCI];
+    float dl[kCHI], uu[kCHI], dy[kCHI], zz[kCHI];
+
+    __device__ __forceinline__ void fetch(const BwdParams &p, int64_t b, int64_t t0, int64_t d0) {
         const int tid = threadIdx.x;
         const IO *Bm = reinterpret_cast<const IO *>(p.B) + b * p.N * p.L;
         const IO *Cm = reinterpret_cast<const IO *>(p.C) + b * p.N * p.L;
-        for (int e = tid; e < (full ? 2 : 1) * G * Q * kBwdS; e += kBwdThreads) {
-            const int which = e / (G * Q * kBwdS), r = e % (G * Q * kBwdS), n = r / kBwdS, i = r % kBwdS;
+#pragma unroll
+        for (int k = 0; k < kBCI; ++k) {   // consecutive e: consecutive steps of one row
+            const int e = tid + k * kBwdThreads;
+            const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
             const int64_t t = t0 + i;
-            float v = 0.0f;
-            if (n < p.N && t < p.L) v = io_traits<IO>::to_f((which ? Cm : Bm)[n * p.L + t]);
-            (which ? C : B)[r] = v;
+            bc[k] = (e < kBC && n < p.N && t < p.L) ? io_traits<IO>::to_f((kind ? Cm : Bm)[n * p.L + t]) : 0.0f;
         }
-        for (int e = tid; e < kCpb * kBwdS; e += kBwdThreads) {
-            const int cc = e / kBwdS, i = e % kBwdS;
-            const int64_t d = (int64_t)blockIdx.x * kCpb + cc, t = t0 + i;
-            float dtv = 0.0f, sgv = 0.0f, uv = 0.0f, dyv = 0.0f, zv = 0.0f;
-            if (d < p.Dm && t < p.L) {
+#pragma unroll
+        for (int k = 0; k < kCHI; ++k) {
+            const int e = tid + k * kBwdThreads;
+            const int cc = e / kS, i = e % kS;
+            const int64_t d = d0 + cc, t = t0 + i;
+            dl[k] = uu[k] = dy[k] = zz[k] = 0.0f;
+            if (e < kCH && d < p.Dm && t < p.L) {
                 const int64_t idx = (b * p.Dm + d) * p.L + t;
-                const float v = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.delta)[idx]) +
-                                (p.bias ? p.bias[d] : 0.0f);
-                dtv = bwd_dt(v, p.softplus);
-                sgv = p.softplus ? 1.0f / (1.0f + ex2(-v * kLog2e)) : 1.0f;
-                uv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.u)[idx]);
-                if (full) {
-                    dyv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.dy)[idx]);
-                    if (p.z) zv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.z)[idx]);
+                dl[k] = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.delta)[idx]);
+                uu[k] = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.u)[idx]);
+                if (FULL) {
+                    dy[k] = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.dy)[idx]);
+                    if (p.z) zz[k] = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.z)[idx]);
                 }
             }
-            dt[e] = dtv; sg[e] = sgv; u[e] = uv; dy[e] = dyv; z[e] = zv;
+        }
+    }
+
+    // dt, the softplus derivative, u and (FULL) dyhat = dy*SiLU(z), dy*SiLU'(z) once per
+    // (channel, step); B, C as [t][g][q] (state n = g + G*q), zeros beyond N, L or Dm
+    __device__ __forceinline__ void stage(const BwdParams &p, float *sm, int64_t t0, int64_t d0) const {
+        const int tid = threadIdx.x;
+#pragma unroll
+        for (int k = 0; k < kBCI; ++k) {
+            const int e = tid + k * kBwdThreads;
+            if (e >= kBC) break;
+            const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
+            sm[(kind ? Cfg::kOffC : Cfg::kOffB) + (i * G + n % G) * Cfg::kQ + n / G] = bc[k];
+        }
+#pragma unroll
+        for (int k = 0; k < kCHI; ++k) {
+            const int e = tid + k * kBwdThreads;
+            if (e >= kCH) break;
+            const int cc = e / kS, i = e % kS;
+            const int64_t d = d0 + cc, t = t0 + i;
+            float dtv = 0.0f, sgv = 0.0f, dyh = 0.0f, gz = 0.0f;
+            if (d < p.Dm && t < p.L) {
+                const float v = dl[k] + (p.bias ? p.bias[d] : 0.0f);
+                dtv = p.softplus ? softplus_f(v) : v;
+                sgv = p.softplus ? rcp_approx(1.0f + ex2(-v * kLog2e)) : 1.0f;
+                if (FULL) {
+                    if (p.z) {
+                        const float sz = rcp_approx(1.0f + ex2(-zz[k] * kLog2e));
+                        dyh = dy[k] * zz[k] * sz;                            // dy * SiLU(z)
+                        gz = dy[k] * sz * (1.0f + zz[k] * (1.0f - sz));      // dy * SiLU'(z)
+                    } else {
+                        dyh = dy[k];
+                    }
+                }
+            }
+            sm[Cfg::kOffDt + e] = dtv;
+            sm[Cfg::kOffU + e] = uu[k];
+            if (FULL) {
+                sm[Cfg::kOffSg + e] = sgv;
+                sm[Cfg::kOffDyh + e] = dyh;
+                sm[Cfg::kOffGz + e] = gz;
+            }
         }
     }
 };
 
-template <int G, int Q>
-constexpr size_t bwd_tile_bytes() { return (size_t)BwdTile<float, G, Q>::kFloats * sizeof(float); }
+// Checkpoint pass: the forward recurrence, h stored before every S-step segment; the next
+// segment's raw inputs are fetched into registers while the current one computes.
+template <int G>
+constexpr size_t bwd_ckpt_smem_bytes() { return (size_t)(BwdCfg<G>::kOffU + BwdCfg<G>::kChan) * sizeof(float); }
 
-template <typename IO, int G, int Q>
+template <typename IO, int G>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdParams p) {
-    constexpr int kCpb = kBwdThreads / G;
-    extern __shared__ float smemf[];
-    BwdTile<IO, G, Q> tile(smemf);
+    using Cfg = BwdCfg<G>;
+    constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb;
+    extern __shared__ float4 smem_bwd4[];
+    float *sm = reinterpret_cast<float *>(smem_bwd4);
     const int tid = threadIdx.x, g = tid % G, cc = tid / G;
-    const int64_t b = blockIdx.y, d = (int64_t)blockIdx.x * kCpb + cc;
-    const bool valid = d < p.Dm;                 // every thread takes part in the tile loads
+    const int64_t b = blockIdx.y, d0 = (int64_t)blockIdx.x * kCpb, d = d0 + cc;
+    const bool valid = d < p.Dm;                 // every thread takes part in the staging
     const int64_t bd = b * p.Dm + (valid ? d : 0);
-    float Ap[Q], h[Q];
+    float2 Ap2[2], h2[2];
 #pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        const int n = g + G * q;
-        Ap[q] = (valid && n < p.N) ? p.A[(valid ? d : 0) * p.N + n] * kLog2e : 0.0f;
-        h[q] = 0.0f;
+    for (int k = 0; k < 2; ++k) {
+        const int n0 = g + G * 2 * k, n1 = n0 + G;
+        Ap2[k] = make_float2((valid && n0 < p.N) ? p.A[(valid ? d : 0) * p.N + n0] * kLog2e : 0.0f,
+                             (valid && n1 < p.N) ? p.A[(valid ? d : 0) * p.N + n1] * kLog2e : 0.0f);
+        h2[k] = make_float2(0.f, 0.f);
     }
-    float *ck = p.ckpt + bd * (int64_t)p.nseg * (G * Q);
+    float *ck = p.ckpt + bd * (int64_t)p.nseg * kNP;
+    BwdFetch<IO, G, false> f;
+    f.fetch(p, b, 0, d0);
     for (int seg = 0; seg < p.nseg; ++seg) {
         if (valid) {
 #pragma unroll
-            for (int q = 0; q < Q; ++q) ck[(int64_t)seg * (G * Q) + g + G * q] = h[q];
+            for (int k = 0; k < 2; ++k) {
+                ck[(int64_t)seg * kNP + g + G * 2 * k] = h2[k].x;
+                ck[(int64_t)seg * kNP + g + G * (2 * k + 1)] = h2[k].y;
+            }
         }
         __syncthreads();
-        tile.load(p, b, (int64_t)seg * kBwdS, false);
+        f.stage(p, sm, (int64_t)seg * kS, d0);
         __syncthreads();
+        if (seg + 1 < p.nseg) f.fetch(p, b, (int64_t)(seg + 1) * kS, d0);   // in flight during this segment
 #pragma unroll
-        for (int i = 0; i < kBwdS; ++i) {
-            const float dt = tile.dt[cc * kBwdS + i];
-            const float x = dt * tile.u[cc * kBwdS + i];
+        for (int i = 0; i < kS; ++i) {
+            const float dt = sm[Cfg::kOffDt + cc * kS + i];
+            const float x = dt * sm[Cfg::kOffU + cc * kS + i];
+            const float4 bq = *reinterpret_cast<const float4 *>(sm + Cfg::kOffB + (i * G + g) * kQ);
+            const float2 bv[2] = {make_float2(bq.x, bq.y), make_float2(bq.z, bq.w)};
 #pragma unroll
-            for (int q = 0; q < Q; ++q) h[q] = fmaf(ex2(dt * Ap[q]), h[q], x * tile.B[(g + G * q) * kBwdS + i]);
+            for (int k = 0; k < 2; ++k) {
+                const float2 e = __fmul2_rn(make_float2(dt, dt), Ap2[k]);
+                h2[k] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), h2[k], __fmul2_rn(make_float2(x, x), bv[k]));
+            }
         }
     }
 }
 
-template <typename IO, int G, int Q>
-__global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdParams p) {
-    constexpr int kCpb = kBwdThreads / G;
-    constexpr int kWarps = kBwdThreads / 32;
-    // staged segment inputs, then per warp and step the channel-summed dB and dC partials
-    // for the G*Q states ([2][kWarps][kBwdS][G*Q])
-    extern __shared__ float smemf[];
-    BwdTile<IO, G, Q> tile(smemf);
-    float *sPartBuf = smemf + BwdTile<IO, G, Q>::kFloats;
-    auto sPart = [&](int which, int w, int i, int n) -> float & {
-        return sPartBuf[(((size_t)which * kWarps + w) * kBwdS + i) * (G * Q) + n];
-    };
-    const int tid = threadIdx.x, g = tid % G, warp = tid >> 5, cc = tid / G;
-    const int64_t b = blockIdx.y, d = (int64_t)blockIdx.x * kCpb + cc;
-    const bool valid = d < p.Dm;                // invalid lanes still take part in the shuffles
+template <typename IO, int G>
+__global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdParams p) {
+    using Cfg = BwdCfg<G>;
+    constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb;
+    // sums over a channel's states: transposed butterfly every G steps (G <= S), else a
+    // butterfly per step
+    constexpr bool kTransposed = G <= kS;
+    constexpr int kGrp = kTransposed ? G : 1;
+    extern __shared__ float4 smem_bwd4[];
+    float *sm = reinterpret_cast<float *>(smem_bwd4);
+    const int tid = threadIdx.x, lane = tid & 31, g = tid % G, cc = tid / G;
+    const int64_t b = blockIdx.y, d0 = (int64_t)blockIdx.x * kCpb, d = d0 + cc;
+    const bool valid = d < p.Dm;                // invalid lanes still take part in the exchanges
     const int64_t dd = valid ? d : 0;
     const int64_t bd = b * p.Dm + dd;
     const float Dv = (valid && p.D) ? p.D[dd] : 0.0f;
-    float An[Q], Ap[Q], c[Q], dA[Q];
-    bool nv[Q];
+    float An[kQ], c[kQ];
+    bool nv[kQ];
 #pragma unroll
-    for (int q = 0; q < Q; ++q) {
+    for (int q = 0; q < kQ; ++q) {
         const int n = g + G * q;
         nv[q] = valid && n < p.N;
         An[q] = nv[q] ? p.A[dd * p.N + n] : 0.0f;
-        Ap[q] = An[q] * kLog2e;
         c[q] = (nv[q] && p.dlast) ? p.dlast[bd * p.N + n] : 0.0f;
-        dA[q] = 0.0f;
+    }
+    // as state pairs (q = 2k, 2k+1) for the packed arithmetic
+    float2 An2[2], Ap2[2], c2[2], dA2[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        An2[k] = make_float2(An[2 * k], An[2 * k + 1]);
+        Ap2[k] = make_float2(An[2 * k] * kLog2e, An[2 * k + 1] * kLog2e);
+        c2[k] = make_float2(c[2 * k], c[2 * k + 1]);
+        dA2[k] = make_float2(0.f, 0.f);
     }
     float dD = 0.0f, dbias = 0.0f;
-    const float *ck = p.ckpt + bd * (int64_t)p.nseg * (G * Q);
+    const float *ck = p.ckpt + bd * (int64_t)p.nseg * kNP;
+    const float *sB = sm + Cfg::kOffB + g * kQ, *sC = sm + Cfg::kOffC + g * kQ;
+    const float *sDt = sm + Cfg::kOffDt + cc * kS, *sU = sm + Cfg::kOffU + cc * kS;
+    const float *sDyh = sm + Cfg::kOffDyh + cc * kS, *sGz = sm + Cfg::kOffGz + cc * kS;
+    const float *sSg = sm + Cfg::kOffSg + cc * kS;
+    float *myPart = sm + Cfg::kOffPart + cc * Cfg::kPartCh;     // dB kind; dC at + kCpb * kPartCh
+
+    // the three per-step sums of a channel for the step this lane finishes: outputs
+    auto finish = [&](int i, int64_t t0, float yhs, float dus, float dds) {
+        const int64_t t = t0 + i;
+        if (!valid || t >= p.L) return;
+        const float dt = sDt[i], uu = sU[i], dyh = sDyh[i];
+        const float ddl = fmaf(uu, dus, dds) * sSg[i];
+        p.du[bd * p.L + t] = fmaf(dyh, Dv, dt * dus);
+        p.ddelta[bd * p.L + t] = ddl;
+        if (p.dz) p.dz[bd * p.L + t] = sGz[i] * fmaf(Dv, uu, yhs);
+        dD = fmaf(dyh, uu, dD);
+        dbias += ddl;
+    };
+
+    BwdFetch<IO, G, true> f;
+    f.fetch(p, b, (int64_t)(p.nseg - 1) * kS, d0);
+    // the segment's checkpoint, fetched with its inputs one segment ahead
+    auto fetch_ck = [&](int seg, float2 (&out)[2]) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            out[k] = valid ? make_float2(ck[(int64_t)seg * kNP + g + G * 2 * k], ck[(int64_t)seg * kNP + g + G * (2 * k + 1)])
+                           : make_float2(0.f, 0.f);
+    };
+    float2 ckn[2];
+    fetch_ck(p.nseg - 1, ckn);
     for (int seg = p.nseg - 1; seg >= 0; --seg) {
-        const int64_t t0 = (int64_t)seg * kBwdS;
-        __syncthreads();                        // the previous segment is done with the tile
-        tile.load(p, b, t0, true);
+        const int64_t t0 = (int64_t)seg * kS;
+        __syncthreads();                        // the previous segment is done with shared memory
+        f.stage(p, sm, t0, d0);
         __syncthreads();
-        float hs[Q][kBwdS + 1];                 // hs[q][0]: h before the segment; hs[q][i+1]: after step t0+i
-#pragma unroll
-        for (int q = 0; q < Q; ++q) hs[q][0] = valid ? ck[(int64_t)seg * (G * Q) + g + G * q] : 0.0f;
-#pragma unroll
-        for (int i = 0; i < kBwdS; ++i) {
-            const float dt = tile.dt[cc * kBwdS + i];
-            const float x = dt * tile.u[cc * kBwdS + i];
-#pragma unroll
-            for (int q = 0; q < Q; ++q)
-                hs[q][i + 1] = fmaf(ex2(dt * Ap[q]), hs[q][i], x * tile.B[(g + G * q) * kBwdS + i]);
+        // states as pairs (q = 2k, 2k+1): hs[k][0] before the segment, hs[k][i+1] after step t0+i
+        float2 hs[2][kS + 1];
+        hs[0][0] = ckn[0];
+        hs[1][0] = ckn[1];
+        if (seg > 0) {   // the next segment's inputs and checkpoint, in flight meanwhile
+            f.fetch(p, b, t0 - kS, d0);
+            fetch_ck(seg - 1, ckn);
         }
 #pragma unroll
-        for (int i = kBwdS - 1; i >= 0; --i) {
-            const int64_t t = t0 + i;
-            if (t >= p.L) {                     // uniform across the block (same t everywhere)
-                if ((threadIdx.x & 31) < G) {
+        for (int i = 0; i < kS; ++i) {
+            const float dt = sDt[i];
+            const float x = dt * sU[i];
+            const float4 bq = *reinterpret_cast<const float4 *>(sB + i * G * kQ);
+            const float2 bv[2] = {make_float2(bq.x, bq.y), make_float2(bq.z, bq.w)};
 #pragma unroll
-                    for (int q = 0; q < Q; ++q) sPart(0, warp, i, g + G * q) = sPart(1, warp, i, g + G * q) = 0.0f;
-                }
-                continue;
-            }
-            const float dt = tile.dt[cc * kBwdS + i];
-            const float uu = tile.u[cc * kBwdS + i];
-            float bq[Q], cq[Q], yh = 0.0f;
-#pragma unroll
-            for (int q = 0; q < Q; ++q) {
-                bq[q] = tile.B[(g + G * q) * kBwdS + i];
-                cq[q] = tile.C[(g + G * q) * kBwdS + i];
-                yh = fmaf(cq[q], hs[q][i + 1], yh);
-            }
-            yh = sum_lanes<G>(yh) + Dv * uu;    // yhat_t, before the gate
-            const float dyv = tile.dy[cc * kBwdS + i];
-            float dyh = dyv, dzv = 0.0f;
-            if (p.z) {
-                const float zz = tile.z[cc * kBwdS + i];
-                const float sg = 1.0f / (1.0f + ex2(-zz * kLog2e));
-                dyh = dyv * zz * sg;            // dy * SiLU(z)
-                dzv = dyv * yh * sg * (1.0f + zz * (1.0f - sg));
-            }
-            float du = 0.0f, ddt = 0.0f;
-#pragma unroll
-            for (int q = 0; q < Q; ++q) {
-                const float a = ex2(dt * Ap[q]);
-                const float lam = fmaf(dyh, cq[q], c[q]);
-                const float hp = hs[q][i];
-                du = fmaf(lam * dt, bq[q], du);
-                ddt = fmaf(lam, fmaf(uu, bq[q], An[q] * a * hp), ddt);
-                dA[q] = fmaf(lam * dt * a, hp, dA[q]);
-                c[q] = a * lam;
-                // sums over the warp's channels, staged for the CTA-wide sum after the segment
-                const float gb = sum_channels<G>(nv[q] ? lam * dt * uu : 0.0f);
-                const float gc = sum_channels<G>(nv[q] ? dyh * hs[q][i + 1] : 0.0f);
-                if ((threadIdx.x & 31) < G) {
-                    sPart(0, warp, i, g + G * q) = gb;
-                    sPart(1, warp, i, g + G * q) = gc;
-                }
-            }
-            du = sum_lanes<G>(du);
-            ddt = sum_lanes<G>(ddt);
-            if (valid && g == 0) {
-                const float ddl = ddt * tile.sg[cc * kBwdS + i];
-                p.du[bd * p.L + t] = fmaf(dyh, Dv, du);
-                p.ddelta[bd * p.L + t] = ddl;
-                if (p.dz) p.dz[bd * p.L + t] = dzv;
-                dD = fmaf(dyh, uu, dD);
-                dbias += ddl;
+            for (int k = 0; k < 2; ++k) {
+                const float2 e = __fmul2_rn(make_float2(dt, dt), Ap2[k]);
+                hs[k][i + 1] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), hs[k][i], __fmul2_rn(make_float2(x, x), bv[k]));
             }
         }
-        // dB, dC of the segment: sum the warps' partials, one atomic per (state, step)
-        __syncthreads();
-        for (int e = tid; e < 2 * kBwdS * G * Q; e += kBwdThreads) {
-            const int which = e / (kBwdS * G * Q), r = e % (kBwdS * G * Q);
-            const int i = r / (G * Q), n = r % (G * Q);
-            const int64_t t = t0 + i;
-            if (n >= p.N || t >= p.L) continue;
-            float acc = 0.0f;
+        float pb[kQ][4], pc[kQ][4];              // dB / dC terms of the current four steps
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) acc += sPart(which, w, i, n);
-            atomicAdd((which ? p.dC : p.dB) + (b * p.N + n) * p.L + t, acc);
+        for (int grp = kS / kGrp - 1; grp >= 0; --grp) {
+            float red[3][kGrp];
+#pragma unroll
+            for (int s = kGrp - 1; s >= 0; --s) {
+                const int i = grp * kGrp + s;
+                const float dt = sDt[i], dyh = sDyh[i];
+                const float x = dt * sU[i];
+                const float4 cq4 = *reinterpret_cast<const float4 *>(sC + i * G * kQ);
+                const float4 bq4 = *reinterpret_cast<const float4 *>(sB + i * G * kQ);
+                const float2 cv[2] = {make_float2(cq4.x, cq4.y), make_float2(cq4.z, cq4.w)};
+                const float2 bv[2] = {make_float2(bq4.x, bq4.y), make_float2(bq4.z, bq4.w)};
+                const float2 dt2 = make_float2(dt, dt), dyh2 = make_float2(dyh, dyh), x2 = make_float2(x, x);
+                float2 yh2 = make_float2(0.f, 0.f), du2 = make_float2(0.f, 0.f), dd22 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float2 e = __fmul2_rn(dt2, Ap2[k]);
+                    const float2 a = make_float2(ex2(e.x), ex2(e.y));
+                    const float2 lam = __ffma2_rn(dyh2, cv[k], c2[k]);
+                    yh2 = __ffma2_rn(cv[k], hs[k][i + 1], yh2);
+                    du2 = __ffma2_rn(lam, bv[k], du2);
+                    const float2 P = __fmul2_rn(lam, __fmul2_rn(a, hs[k][i]));
+                    dd22 = __ffma2_rn(An2[k], P, dd22);
+                    dA2[k] = __ffma2_rn(dt2, P, dA2[k]);
+                    c2[k] = __fmul2_rn(a, lam);
+                    const float2 vb = __fmul2_rn(lam, x2), vc = __fmul2_rn(dyh2, hs[k][i + 1]);
+                    pb[2 * k][i & 3] = vb.x;
+                    pb[2 * k + 1][i & 3] = vb.y;
+                    pc[2 * k][i & 3] = vc.x;
+                    pc[2 * k + 1][i & 3] = vc.y;
+                }
+                const float yh = yh2.x + yh2.y, du = du2.x + du2.y, dd2 = dd22.x + dd22.y;
+                if ((i & 3) == 0) {             // a full 4-step vector per state: to shared memory
+#pragma unroll
+                    for (int q = 0; q < kQ; ++q) {
+                        const int n = g + G * q;
+                        *reinterpret_cast<float4 *>(myPart + n * Cfg::kRow + i) =
+                            make_float4(pb[q][0], pb[q][1], pb[q][2], pb[q][3]);
+                        *reinterpret_cast<float4 *>(myPart + kCpb * Cfg::kPartCh + n * Cfg::kRow + i) =
+                            make_float4(pc[q][0], pc[q][1], pc[q][2], pc[q][3]);
+                    }
+                }
+                if constexpr (kTransposed) {
+                    red[0][s] = yh;
+                    red[1][s] = du;
+                    red[2][s] = dd2;
+                } else {
+                    // butterfly over the G lanes of the channel; lane g == 0 writes the step
+                    float ys = yh, us = du, ds = dd2;
+#pragma unroll
+                    for (int o = G / 2; o >= 1; o /= 2) {
+                        ys += __shfl_xor_sync(0xffffffffu, ys, o);
+                        us += __shfl_xor_sync(0xffffffffu, us, o);
+                        ds += __shfl_xor_sync(0xffffffffu, ds, o);
+                    }
+                    if (g == 0) finish(i, t0, ys, us, ds);
+                }
+            }
+            if constexpr (kTransposed) {
+                // lane g ends with the sums of step grp*G + g
+                const float yhs = group_reduce_transpose<kGrp>(red[0], lane);
+                const float dus = group_reduce_transpose<kGrp>(red[1], lane);
+                const float dds = group_reduce_transpose<kGrp>(red[2], lane);
+                finish(grp * kGrp + g, t0, yhs, dus, dds);
+            }
+        }
+        // dB, dC of the segment: sum the CTA's channels, one vector atomic per (state, 4 steps)
+        __syncthreads();
+        constexpr int kItems = 2 * kNP * (kS / 4);
+        for (int e = tid; e < kItems; e += kBwdThreads) {
+            const int kind = e / (kNP * (kS / 4)), r = e % (kNP * (kS / 4)), n = r / (kS / 4), tq = r % (kS / 4);
+            if (n >= p.N) continue;
+            const float *src = sm + Cfg::kOffPart + kind * kCpb * Cfg::kPartCh + n * Cfg::kRow + 4 * tq;
+            float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+#pragma unroll 8
+            for (int ch = 0; ch < kCpb; ++ch) {
+                const float4 v = *reinterpret_cast<const float4 *>(src + ch * Cfg::kPartCh);
+                lo = __fadd2_rn(lo, make_float2(v.x, v.y));
+                hi = __fadd2_rn(hi, make_float2(v.z, v.w));
+            }
+            const float4 acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+            const int64_t t = t0 + 4 * tq;
+            float *dst = (kind ? p.dC : p.dB) + (b * p.N + n) * p.L + t;
+            if (t + 3 < p.L && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc.x), "f"(acc.y),
+                             "f"(acc.z), "f"(acc.w)
+                             : "memory");
+            } else {
+                const float av[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (t + k < p.L) atomicAdd(dst + k, av[k]);
+            }
         }
     }
-    if (!valid) return;
+    // dA per state; dD and the dt bias summed over the channel's lanes first
 #pragma unroll
-    for (int q = 0; q < Q; ++q)
+    for (int o = G / 2; o >= 1; o /= 2) {
+        dD += __shfl_xor_sync(0xffffffffu, dD, o);
+        dbias += __shfl_xor_sync(0xffffffffu, dbias, o);
+    }
+    if (!valid) return;
+    const float dA[4] = {dA2[0].x, dA2[0].y, dA2[1].x, dA2[1].y};
+#pragma unroll
+    for (int q = 0; q < kQ; ++q)
         if (nv[q]) atomicAdd(p.dA + dd * p.N + g + G * q, dA[q]);
     if (g == 0) {
         if (p.dD) atomicAdd(p.dD + dd, dD);

@@ -734,15 +734,12 @@ size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
 }  // extern "C"
 
 namespace {
-// backward lane split: Q states per thread, G lanes per channel (a power of two, <= 32,
-// G * Q >= N). Two states per thread up to 64 states: the 16-step state history then fits in
-// registers with 4 CTAs per SM (measured on 8 x 1536 x 2048 x 16: 3.86 ms at four states per
-// thread, 3.23 ms at two).
-void bwd_split(int64_t N, int *G, int *Q) {
-    *Q = N <= 1 ? 1 : (N <= 64 ? 2 : 4);
+// backward lane split: four states per thread, G lanes per channel (the smallest power of
+// two with 4G >= N, at most 32)
+int bwd_lanes(int64_t N) {
     int g = 1;
-    while (g < 32 && (int64_t)g * *Q < N) g *= 2;
-    *G = g;
+    while (g < 32 && (int64_t)g * kBwdQ < N) g *= 2;
+    return g;
 }
 }  // namespace
 
@@ -751,10 +748,9 @@ extern "C" {
 size_t ssm_selective_scan_bwd_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
-    int G, Q;
-    bwd_split(dims->dstate, &G, &Q);
+    const int G = bwd_lanes(dims->dstate);
     const int64_t nseg = (dims->seqlen + kBwdS - 1) / kBwdS;
-    return (size_t)(dims->batch * dims->dim) * (size_t)nseg * (size_t)(G * Q) * sizeof(float);
+    return (size_t)(dims->batch * dims->dim) * (size_t)nseg * (size_t)(G * kBwdQ) * sizeof(float);
 }
 
 ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const void *delta, const float *A,
@@ -800,9 +796,7 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     BwdParams p{u, delta, z, B, C, dy, A, D, delta_bias, dlast_state, du, ddelta, dA, dB, dC, dD,
                 z ? dz : nullptr, ddelta_bias, static_cast<float *>(ws), d.batch, d.dim, d.seqlen,
                 d.dstate, delta_softplus ? 1 : 0, (int)((d.seqlen + kBwdS - 1) / kBwdS)};
-    int G, Q;
-    bwd_split(d.dstate, &G, &Q);
-    const cudaError_t e = launch_bwd(d.io_dtype, G, Q, p, s);
+    const cudaError_t e = launch_bwd(d.io_dtype, bwd_lanes(d.dstate), p, s);
     if (allocated) cudaFreeAsync(ws, s);
     if (e == cudaErrorInvalidConfiguration) return SSM_ERR_UNSUPPORTED;
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
