@@ -12,6 +12,11 @@ during the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long128k|m130|block512]
     python bench.py --impl reference ...   # the fp64 CPU oracle on a bounded sample
+    python bench.py --measure-ex2          # only the ex2 throughput probe (the roofline's peak)
+
+The line also carries one forward-scan line per other workload (`configs`), the maximum
+relative error of sampled output channels against the fp64 oracle (computed after the timed
+region), and the FP32-pipe bound beside the exponential (MUFU) bound.
 """
 from __future__ import annotations
 
@@ -34,13 +39,51 @@ import torch  # noqa: E402
 from selective_state_space_153_b300 import gen  # noqa: E402
 
 SM_COUNT = 148
-EX2_PER_CLK_SM = 32          # measured on B300: MUFU ex2.approx.f32 issue rate per SM per clock
+# MUFU ex2 lanes per SM and clock (4 sub-partitions x 8 lanes). `--measure-ex2` runs the probe
+# (selective_state_space_153_b300/probe/ex2_rate.cu): independent ex2 chains, timed per SM
+# with the SM's own cycle counter, measured 31.85 per SM clock on B300.
+EX2_PER_CLK_SM = 32
+FP32_LANES_PER_CLK_SM = 128  # FFMA lanes per SM and clock (packed f32x2 issue at the same lane rate)
 FALLBACK_HBM_GBS = 6400.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per scan call of the long-sequence workload
-# (aggregate pass + combine + full pass), from a one-pass ncu capture of the full-size call:
-# profiles/scan_pair_long128k_traffic.md. Valid for the default workload only; None elsewhere.
-TRAFFIC_BYTES_PER_LAUNCH = {"long128k": (811089408 + 19332864) + 21572608 + (865208320 + 374617344)}
+# dram__bytes_read.sum + dram__bytes_write.sum of one long-sequence scan call (aggregate pass +
+# combine + full pass), from a one-pass ncu capture of the full-size call, together with the
+# hash of the channel-pair kernel's sources it was taken on: a different hash (the kernels
+# changed since) reports the traffic as unknown (null) rather than a stale count.
+TRAFFIC_BYTES_PER_LAUNCH = {"long128k": (None, None)}   # (source hash, bytes)
+TRAFFIC_SOURCES = ("scan_pair.cuh", "k_pair_impl.cuh", "k_seq.cu", "common.cuh", "launch.h")
+
+
+def pair_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "selective_state_space_153_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    src_hash, nbytes = TRAFFIC_BYTES_PER_LAUNCH.get(workload, (None, None))
+    return nbytes if (src_hash is not None and src_hash == pair_source_hash()) else None
+
+
+def probe_ex2():
+    """ex2 per SM and clock measured on this device by the probe library (None if unavailable)."""
+    try:
+        from selective_state_space_153_b300 import build
+        lib = ctypes.CDLL(build.PROBE_LIB)
+        lib.ssm_probe_ex2_rate.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_double)]
+        lib.ssm_probe_ex2_rate.restype = ctypes.c_int
+        r, ms = ctypes.c_double(0), ctypes.c_double(0)
+        if lib.ssm_probe_ex2_rate(4096, ctypes.byref(r), ctypes.byref(ms)) != 0:
+            return None
+        return {"per_clk_sm": r.value, "probe_ms": ms.value,
+                "how": "16 CTAs x 128 threads per SM, 32 independent ex2 chains per thread; per SM, "
+                       "its CTAs' ex2 count over its first-start-to-last-end clock64 span; median over SMs"}
+    except OSError:
+        return None
 
 
 def count_kernel_launches(fn):
@@ -98,6 +141,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' forward-scan lines")
+    ap.add_argument("--no-check", action="store_true", help="skip the sampled oracle check of the output")
+    ap.add_argument("--measure-ex2", action="store_true", help="run only the ex2 throughput probe")
     return ap.parse_args()
 
 
@@ -322,7 +368,7 @@ def bench_ours(args, rank, ws, local):
         "tokens_per_s": ws * cfg.Bt * cfg.L / t_step,
         "roofline": {"bound": "alu", "achieved": achieved, "peak": ex2_peak, "unit": "Gexp/s",
                      "frac": achieved / ex2_peak,
-                     "traffic": TRAFFIC_BYTES_PER_LAUNCH.get(args.workload) if not args.seqlen else None,
+                     "traffic": measured_traffic(args.workload) if not args.seqlen else None,
                      "peak_source": f"MUFU ex2 {EX2_PER_CLK_SM}/clk/SM x {SM_COUNT} SMs x {sm_max:.0f} MHz",
                      "kernel": "whole scan call (%d launch%s: %s)" % (
                          launches_per_step, "es" if launches_per_step > 1 else "",
@@ -330,11 +376,30 @@ def bench_ours(args, rank, ws, local):
                      "hbm": {"achieved_gbs": io_bytes / t_step / 1e9, "peak_gbs": hbm, "peak_kind": peak_kind,
                              "frac": io_bytes / t_step / 1e9 / hbm},
                      "frac_at_sampled_clock": (achieved / (SM_COUNT * EX2_PER_CLK_SM * clocks["sm_mhz"] * 1e6 / 1e9)
-                                               if clocks["sm_mhz"] else None)},
+                                               if clocks["sm_mhz"] else None),
+                     # the second compute bound: dt*A, dt*u*B, the recurrence FMA and the readout
+                     # FMA per element on the FP32 pipe (128 lanes per SM and clock)
+                     "fp32_pipe": {"ops_per_element": 4,
+                                   "peak_gops": SM_COUNT * FP32_LANES_PER_CLK_SM * sm_max * 1e6 / 1e9,
+                                   "frac": 4 * elems / t_step / 1e9 / (SM_COUNT * FP32_LANES_PER_CLK_SM * sm_max * 1e6 / 1e9)},
+                     "ex2_probe": probe_ex2()},
         "clocks": clocks,
         "gpu_launches": args.steps * launches_per_step,
         "kernels_per_step": kernel_names,
     }
+    # maximum relative error of sampled channels (whole sequence) against the fp64 oracle, on
+    # the output of the last timed call (outside the timed region)
+    if not args.no_check and rank == 0:
+        out["check"] = oracle_check(inp, y, last, cfg)
+    # forward-scan lines for the other workloads (each its own inputs, timed the same way)
+    if not args.no_configs:
+        out["configs"] = {}
+        for name, c in gen.SCAN_CONFIGS.items():
+            if name == cfg.name:
+                continue
+            line = bench_config(c, dev, stream, timed, ex2_peak, hbm)
+            out["configs"][name] = line
+            out["gpu_launches"] += args.steps * line["launches_per_step"]
     # the exact zero-order-hold variant on the same workload, timed the same way
     if not args.no_zoh:
         def zstep():
@@ -415,6 +480,56 @@ def bench_ours(args, rank, ws, local):
                                "sample": f"{nch} of {cfg.Bt * cfg.D} channels, full L={cfg.L}, N={cfg.N}, "
                                          f"fp64 sequential C, {cores} threads, {secs:.1f} s"}
     return out
+
+
+def oracle_check(inp, y, last, cfg):
+    """Max relative error (against max(|oracle|, magnitude companion)) of a few sampled
+    channels of y and of the final state, over the whole sequence."""
+    import oracle
+    rng = np.random.default_rng(7)
+    k = 4 if cfg.L * cfg.N > 1e6 else 16
+    chs = sorted({(int(rng.integers(cfg.Bt)), int(rng.integers(cfg.D))) for _ in range(k)} | {(0, 0)})
+    bs = np.array([c[0] for c in chs]); ds = np.array([c[1] for c in chs])
+    f = gen.as_f64
+    rows = lambda t: None if t is None else t[torch.as_tensor(bs), torch.as_tensor(ds), :].to(torch.float64).numpy()  # noqa: E731
+    yo, ho, ym, hm = oracle.scan_rows(rows(inp["u"]), rows(inp["delta"]), f(inp["A"])[ds], f(inp["B"]), f(inp["C"]), bs,
+                                      D=None if inp["D"] is None else f(inp["D"])[ds], z=rows(inp["z"]),
+                                      delta_bias=None if inp["delta_bias"] is None else f(inp["delta_bias"])[ds],
+                                      delta_softplus=inp["delta_softplus"], with_mag=True, nthreads=len(chs))
+    yg = y[torch.as_tensor(bs), torch.as_tensor(ds), :].float().cpu().double().numpy()
+    out = {"channels": [list(c) for c in chs], "y_max_rel_err": float(oracle.rel_err(yg, yo, ym)),
+           "tol": 2e-2 if cfg.io == "bf16" else 1e-5,
+           "metric": "max |gpu - oracle| / max(|oracle|, magnitude companion), fp64 oracle, whole sequence"}
+    if last is not None:
+        hg = last[torch.as_tensor(bs), torch.as_tensor(ds), :].cpu().double().numpy()
+        out["state_max_rel_err"] = float(oracle.rel_err(hg, ho, hm))
+    return out
+
+
+def bench_config(cfg, dev, stream, timed, ex2_peak, hbm):
+    """The forward scan of one workload: ms per call (its own caller workspace), elements/s,
+    fraction of the exponential roofline and of HBM bandwidth."""
+    from selective_state_space_153_b300 import ssm
+    inp = gen.scan_inputs(cfg)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(g["u"])
+    last = torch.empty((cfg.Bt, cfg.D, cfg.N), dtype=torch.float32, device=dev) if cfg.last_state else None
+    io = ssm.SSM_BF16 if cfg.io == "bf16" else ssm.SSM_F32
+    ws_bytes = ssm.workspace_bytes(cfg.Bt, cfg.D, cfg.L, cfg.N, io)
+    wsb = torch.empty(max(1, ws_bytes), dtype=torch.uint8, device=dev)
+
+    def step():
+        ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                               delta_bias=g["delta_bias"], delta_softplus=cfg.softplus, y=y, last_state=last,
+                               stream=stream, workspace=wsb)
+    ms = timed(step)
+    t = ms / 1e3
+    return {"workload": config_json(cfg)["workload"], "ms_per_step": ms, "value": cfg.elements / t, "unit": "elem/s",
+            "tokens_per_s": cfg.Bt * cfg.L / t, "roofline_frac": cfg.elements / t / 1e9 / ex2_peak,
+            "hbm_frac": scan_io_bytes(cfg) / t / 1e9 / hbm,
+            "l2": "inputs %.1f MB: %s" % (scan_io_bytes(cfg) / 1e6,
+                                          "larger than L2" if scan_io_bytes(cfg) > 126e6 else "L2-resident between calls"),
+            "launches_per_step": 3 if ws_bytes > 0 else 1}
 
 
 def bench_backward(dev, ws):
@@ -551,8 +666,30 @@ def bench_reference(args, rank, ws):
             "gpu_launches": 0}
 
 
+def _spawned_rank(rank, n, port, argv):
+    os.environ.update({"RANK": str(rank), "LOCAL_RANK": str(rank), "WORLD_SIZE": str(n),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    sys.argv = argv
+    main()
+
+
 def main():
     args = parse()
+    if args.measure_ex2:
+        if torch.cuda.is_available():
+            torch.cuda.set_device(0)
+        print(json.dumps({"probe": "ex2.approx.ftz.f32 throughput", "result": probe_ex2(),
+                          "unit_rate_per_clk_sm": EX2_PER_CLK_SM}), flush=True)
+        return
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # no launcher: start the N ranks here, one process per GPU
+        import socket
+        import torch.multiprocessing as mp
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        mp.spawn(_spawned_rank, args=(args.gpus, port, list(sys.argv)), nprocs=args.gpus, join=True)
+        return
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         ws = int(os.environ.get("WORLD_SIZE", "1"))

@@ -83,5 +83,24 @@ def build(force: bool = False, verbose: bool = False, extra=(), lib: str = LIB, 
     return lib
 
 
+PROBE_SRC = os.path.join(PKG, "probe", "ex2_rate.cu")
+PROBE_LIB = os.path.join(PKG, "libssm_probe.so")
+
+
+def build_probe(force: bool = False, verbose: bool = False) -> str:
+    """The ex2-throughput probe the benchmark's roofline uses (not part of the scan library)."""
+    if not force and not _stale(PROBE_LIB, [PROBE_SRC, os.path.abspath(__file__)]):
+        return PROBE_LIB
+    cmd = [_nvcc(), *NVCC_FLAGS, "-shared", "-o", PROBE_LIB + ".tmp", PROBE_SRC]
+    if verbose:
+        print(" ".join(cmd), flush=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on the probe ({r.returncode}):\n{r.stderr[-8000:]}")
+    os.replace(PROBE_LIB + ".tmp", PROBE_LIB)
+    return PROBE_LIB
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))
+    print(build_probe(force="--force" in sys.argv, verbose=True))

@@ -42,3 +42,21 @@ def test_two_ranks_max_timing_and_weak_value():
     for rank, t, v in res:
         assert t == 2.0                      # max over ranks
         assert v == 2 * 100.0 / 2.0          # all ranks' units over the slowest rank
+
+
+def test_gpus_flag_spawns_ranks_without_a_launcher():
+    """`bench.py --gpus 2` run directly (no torchrun, WORLD_SIZE unset) starts two ranks
+    itself; only rank 0 prints its line (the reference arm runs on the host cores, so this
+    runs without a GPU)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "tiny", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, env=env, cwd=root, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1 and lines[0]["impl"] == "reference"
+    assert lines[0]["n_gpus"] == 2
