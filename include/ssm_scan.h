@@ -55,6 +55,10 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+/* The library is built with hidden symbol visibility; what this header declares is exported. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
 
 typedef enum {
     SSM_OK = 0,
@@ -65,7 +69,10 @@ typedef enum {
     SSM_ERR_UNSUPPORTED = 5, /* dstate > SSM_MAX_DSTATE, or no device / wrong architecture */
     SSM_ERR_CUDA = 6,        /* a CUDA runtime call failed */
     SSM_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up (see ssm_stream_status) */
-    SSM_ERR_WORKSPACE = 8    /* workspace missing or too small */
+    SSM_ERR_WORKSPACE = 8,   /* workspace missing or too small */
+    SSM_ERR_CHECK = 9        /* checked build only (-DSSM_CHECK): a bounds check on a global or
+                                shared-memory access failed and the access was skipped (see
+                                ssm_stream_status) */
 } ssm_status_t;
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
@@ -318,8 +325,9 @@ ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u,
                                          void *y, float *last_state, void *stream);
 
 /* Synchronises `stream` and returns (then clears) the library's device status word:
- * SSM_OK, SSM_ERR_TIMEOUT if a bounded device-side wait gave up since the last check, or
- * SSM_ERR_CUDA if the synchronisation itself failed. */
+ * SSM_OK, SSM_ERR_TIMEOUT if a bounded device-side wait gave up since the last check,
+ * SSM_ERR_CHECK (checked build) if a bounds check failed, or SSM_ERR_CUDA if the
+ * synchronisation itself failed. */
 ssm_status_t ssm_stream_status(void *stream);
 
 /*
@@ -361,6 +369,10 @@ int ssm_set_structured_a(int enable);
  *                           sets, with a short limit, so that it gives up and records
  *                           SSM_ERR_TIMEOUT (read by ssm_stream_status); tests the failure
  *                           path without faulting anything.
+ *   check_probe             checked build (-DSSM_CHECK) only: one thread of each channel-pair
+ *                           launch issues a checked load one element past the end of A, which
+ *                           the check skips and records as SSM_ERR_CHECK (a test that the
+ *                           checks fire). Ignored by the normal build.
  * ssm_set_plan_override(NULL) restores the planner. Returns SSM_ERR_UNSUPPORTED for an
  * unknown kernel, lane split or states-per-lane value and SSM_ERR_SHAPE for a negative count;
  * the previous override then stays in force.
@@ -381,6 +393,7 @@ typedef struct {
     int seq_lanes_per_channel;
     int decode_elementwise;
     int force_timeout;
+    int check_probe;
 } ssm_plan_override_t;
 
 ssm_status_t ssm_set_plan_override(const ssm_plan_override_t *ov);
@@ -390,9 +403,19 @@ ssm_status_t ssm_get_plan_override(ssm_plan_override_t *out);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char *ssm_status_string(ssm_status_t status);
 
+/* The CUDA runtime error (a cudaError_t value) behind the most recent SSM_ERR_CUDA that an
+ * entry point returned on the calling thread; 0 if none has. Thread-local; not reset by
+ * later successful calls. Its text: ssm_cuda_error_string. Callable without a GPU. */
+int ssm_last_cuda_error(void);
+/* The CUDA runtime's text for error `code` (static storage; never NULL). */
+const char *ssm_cuda_error_string(int code);
+
 /* Library ABI version: (major << 16) | minor. */
 int ssm_version(void);
 
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
 #ifdef __cplusplus
 }
 #endif

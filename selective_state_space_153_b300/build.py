@@ -20,7 +20,11 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libssm_scan.so")
 OBJ = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
+# Host symbols are hidden (only what include/ssm_scan.h declares is exported) and template
+# statics are not "unique" symbols, so that two builds of the library loaded into one process
+# (the normal and the checked build) share no state.
+NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden,-fno-gnu-unique",
+              "--expt-relaxed-constexpr"]
 
 
 def sources():
@@ -83,6 +87,16 @@ def build(force: bool = False, verbose: bool = False, extra=(), lib: str = LIB, 
     return lib
 
 
+CHECK_LIB = os.path.join(PKG, "libssm_scan_check.so")
+
+
+def build_checked(force: bool = False, verbose: bool = False) -> str:
+    """The checked build (-DSSM_CHECK): bounds checks on every global and shared-memory access
+    of the scan and state-update kernels, NaN-poisoned shared memory. For tests."""
+    return build(force=force, verbose=verbose, extra=("-DSSM_CHECK",), lib=CHECK_LIB,
+                 objdir=os.path.join(OBJ, "check"))
+
+
 PROBE_SRC = os.path.join(PKG, "probe", "ex2_rate.cu")
 PROBE_LIB = os.path.join(PKG, "libssm_probe.so")
 
@@ -104,3 +118,4 @@ def build_probe(force: bool = False, verbose: bool = False) -> str:
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))
     print(build_probe(force="--force" in sys.argv, verbose=True))
+    print(build_checked(force="--force" in sys.argv, verbose=True))

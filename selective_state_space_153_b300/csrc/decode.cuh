@@ -7,6 +7,7 @@
 // reduced across the N/4 lanes of a channel with shuffles (N/4 must divide 32, i.e.
 // N in {4, 8, 16, 32, 64, 128}); otherwise one thread per (b, d) walking all states.
 #pragma once
+#include "check.cuh"
 #include "common.cuh"
 
 namespace ssm {
@@ -30,6 +31,31 @@ struct DecodeParams {
     int zoh;   // nonzero: launch the zero-order-hold variant (B_bar = (exp(dt*A) - 1)/A * B)
 };
 
+// Checked build: the addresses a thread of channel row cl (= b*Dm + d) touches -- `cnt`
+// states from `n0` and the B, C elements of the same states, x, dt, z, y at cl, A and D of
+// channel d -- lie inside their arrays. Always true in the normal build.
+template <typename IO>
+__device__ __forceinline__ bool decode_addrs_ok(const DecodeParams &p, int64_t cl, int64_t b, int64_t d, int64_t n0,
+                                                int64_t cnt) {
+#ifdef SSM_CHECK
+    const uint64_t es = sizeof(IO), BD = (uint64_t)p.Bt * p.Dm, BN = (uint64_t)p.Bt * p.N;
+    bool ok = SSM_CHK_G(p.state, BD * p.N * 4, p.state + cl * p.N + n0, cnt * 4) &&
+              SSM_CHK_G(p.A, (uint64_t)p.Dm * p.N * 4, p.A + d * p.N + n0, cnt * 4) &&
+              SSM_CHK_G(p.x, BD * es, reinterpret_cast<const IO *>(p.x) + cl, es) &&
+              SSM_CHK_G(p.dt, BD * es, reinterpret_cast<const IO *>(p.dt) + cl, es) &&
+              SSM_CHK_G(p.y, BD * es, reinterpret_cast<const IO *>(p.y) + cl, es) &&
+              SSM_CHK_G(p.B, BN * es, reinterpret_cast<const IO *>(p.B) + b * p.N + n0, cnt * es) &&
+              SSM_CHK_G(p.C, BN * es, reinterpret_cast<const IO *>(p.C) + b * p.N + n0, cnt * es);
+    if (p.z != nullptr) ok = ok && SSM_CHK_G(p.z, BD * es, reinterpret_cast<const IO *>(p.z) + cl, es);
+    if (p.D != nullptr) ok = ok && SSM_CHK_G(p.D, (uint64_t)p.Dm * 4, p.D + d, 4);
+    return ok;
+#else
+    (void)p; (void)cl; (void)b; (void)d; (void)n0; (void)cnt;
+    return true;
+#endif
+}
+
+
 // Vector path: lane l of a warp owns the 16-byte piece q = l % LPC of channel
 // d = warp*(32/LPC) + l/LPC of batch row b = blockIdx.y (LPC = N/4 lanes per channel), so
 // every warp-wide load or store covers 512 contiguous bytes of the state and the index
@@ -42,7 +68,7 @@ __global__ void __launch_bounds__(256) decode_wide_kernel(const DecodeParams p) 
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     const int q = t % LPC;
     const int d = t / LPC;
-    const bool valid = d < p.Dm;
+    const bool valid = d < p.Dm && decode_addrs_ok<IO>(p, (int64_t)b * p.Dm + d, b, d, 4 * q, 4);
     float acc = 0.0f, xv = 0.0f, zv = 0.0f;
     if (valid) {
         const int64_t cl = (int64_t)b * p.Dm + d;
@@ -89,9 +115,9 @@ __global__ void __launch_bounds__(256) decode_vec_kernel(const DecodeParams p) {
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t chan = gid / LPC;   // b*Dm + d
     const int q = (int)(gid % LPC);
-    const bool valid = chan < p.Bt * p.Dm;
-    const int64_t cl = valid ? chan : 0;
+    const int64_t cl = chan < p.Bt * p.Dm ? chan : 0;
     const int64_t b = cl / p.Dm, d = cl % p.Dm;
+    const bool valid = chan < p.Bt * p.Dm && decode_addrs_ok<IO>(p, cl, b, d, 4 * q, 4);
     float acc = 0.0f;
     float xv = 0.0f, zv = 0.0f;
     if (valid) {
@@ -139,6 +165,7 @@ __global__ void __launch_bounds__(256) decode_scalar_kernel(const DecodeParams p
     const int64_t cl = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (cl >= p.Bt * p.Dm) return;
     const int64_t b = cl / p.Dm, d = cl % p.Dm;
+    if (!decode_addrs_ok<IO>(p, cl, b, d, 0, p.N)) return;   // no shuffles in this kernel
     const IO *Bm = reinterpret_cast<const IO *>(p.B);
     const IO *Cm = reinterpret_cast<const IO *>(p.C);
     const float xv = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.x)[cl]);

@@ -10,16 +10,14 @@ template <typename IO, int G>
 cudaError_t launch_bwd_t(const BwdParams &p, cudaStream_t s) {
     constexpr size_t ck = bwd_ckpt_smem_bytes<G>(), sm = bwd_smem_bytes<G>();
     const dim3 grid((unsigned)((p.Dm + BwdCfg<G>::kCpb - 1) / BwdCfg<G>::kCpb), (unsigned)p.Bt);
-    static unsigned long long attr_set = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<IO, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(scan_bwd_ckpt_kernel<IO, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ck);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= 1ull << dev;
-    }
+    static std::atomic<unsigned long long> attr_set{0};
+    const cudaError_t e = once_per_device(attr_set, [&] {
+        cudaError_t r = cudaFuncSetAttribute(scan_bwd_kernel<IO, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(scan_bwd_ckpt_kernel<IO, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ck);
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     scan_bwd_ckpt_kernel<IO, G><<<grid, kBwdThreads, ck, s>>>(p);
     scan_bwd_kernel<IO, G><<<grid, kBwdThreads, sm, s>>>(p);
     return cudaGetLastError();

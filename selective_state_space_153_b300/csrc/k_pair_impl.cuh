@@ -15,14 +15,11 @@ cudaError_t launch_pair_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
     constexpr int W = pair_warps(KS, GP, AGG);
     using Cfg = PairCfg<IO, KS, GP, W, kPairT, CONV>;
     auto k = scan_pair_kernel<IO, KS, GP, W, kPairT, AGG, ZOH, CONV>;
-    static unsigned long long attr_set = 0;  // per instantiation: bit i = set on device i
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= 1ull << dev;
-    }
+    static std::atomic<unsigned long long> attr_set{0};
+    const cudaError_t e = once_per_device(attr_set, [&] {
+        return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
+    });
+    if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(prm.Bt * prm.chan_blocks), (unsigned)grid_y);
     k<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(prm);
     return cudaGetLastError();

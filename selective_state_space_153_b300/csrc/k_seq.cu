@@ -34,14 +34,11 @@ template <typename IO, int NPER, int G, bool AGG, bool AL>
 cudaError_t launch_seq_t(const SeqParams &prm, int grid_y, cudaStream_t s) {
     using Cfg = SeqCfg<IO, NPER, G, kSeqWarps, kSeqTile>;
     auto k = scan_seq_kernel<IO, NPER, G, kSeqWarps, kSeqTile, AGG, AL>;
-    static unsigned long long attr_set = 0;  // per instantiation: bit i = set on device i
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= 1ull << dev;
-    }
+    static std::atomic<unsigned long long> attr_set{0};
+    const cudaError_t e = once_per_device(attr_set, [&] {
+        return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
+    });
+    if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(prm.Bt * prm.chan_blocks), (unsigned)grid_y);
     k<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(prm);
     return cudaGetLastError();

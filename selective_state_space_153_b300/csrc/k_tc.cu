@@ -17,16 +17,13 @@ template <typename IO, int G>
 cudaError_t launch_tc_t(const TcParams &prm, cudaStream_t s) {
     using Cfg = TcCfg<IO, G>;
     auto k = scan_tc_kernel<IO, G>;
-    static unsigned long long attr_set = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= 1ull << dev;
-    }
+    static std::atomic<unsigned long long> attr_set{0};
+    const cudaError_t e = once_per_device(attr_set, [&] {
+        cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+        if (r == cudaSuccess) r = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     k<<<(unsigned)sm_count_dev(), Cfg::W * 32, Cfg::SMEM, s>>>(prm);
     return cudaGetLastError();
 }
@@ -35,16 +32,13 @@ template <typename IO, int G>
 cudaError_t launch_tp_t(const TcParams &prm, cudaStream_t s) {
     using Cfg = TpCfg<IO, G>;
     auto k = scan_tp_kernel<IO, G>;
-    static unsigned long long attr_set = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= 1ull << dev;
-    }
+    static std::atomic<unsigned long long> attr_set{0};
+    const cudaError_t e = once_per_device(attr_set, [&] {
+        cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+        if (r == cudaSuccess) r = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     k<<<(unsigned)sm_count_dev(), Cfg::W * 32, Cfg::SMEM, s>>>(prm);
     return cudaGetLastError();
 }

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "ssm_scan.h"
 #include "scan_seq.cuh"
 #include "decode.cuh"
@@ -12,6 +14,19 @@
 #include "scan_tc.cuh"
 
 namespace ssm {
+
+// Runs `set` (a kernel's attribute calls) once per device: bit i of `done` records that it
+// succeeded on device i (devices from 64 on: every time). Safe to call from several threads;
+// a race only repeats the calls.
+template <typename F>
+cudaError_t once_per_device(std::atomic<unsigned long long> &done, F &&set) {
+    int dev = 0;
+    if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+    if (dev < 64 && (done.load(std::memory_order_acquire) >> dev & 1ull)) return cudaSuccess;
+    const cudaError_t e = set();
+    if (e == cudaSuccess && dev < 64) done.fetch_or(1ull << dev, std::memory_order_acq_rel);
+    return e;
+}
 
 // channel-pair scan (scan_pair.cuh). variant: 0 = Euler, 1 = zero-order hold, 2 = conv front
 #ifndef SSM_PAIR_T

@@ -43,6 +43,7 @@
 // section 2.2 of the lmnt.cn page, section 3.4 of "Mamba architecture principles and
 // industrial long-text practice", jsqmd.com -- so chunk end states compose exactly).
 #pragma once
+#include "check.cuh"
 #include "common.cuh"
 #include "scan_seq.cuh"
 
@@ -195,6 +196,17 @@ scan_pair_kernel(const SeqParams p) {
     const int ntiles = (int)((l_end - l_begin + T - 1) / T);
     const int N = (int)p.N;
     const int64_t BD = p.Bt * p.Dm;
+    SSM_POISON_SMEM(smem);
+    // array extents in bytes (used by the checked build's bounds checks; dead code otherwise)
+    const uint64_t kIoB = (uint64_t)p.Bt * p.Dm * p.L * sizeof(IO), kBcB = (uint64_t)p.Bt * p.N * p.L * sizeof(IO);
+    const uint64_t kAB = (uint64_t)p.Dm * p.N * 4, kDB = (uint64_t)p.Dm * 4;
+    const uint64_t kCarryB = (uint64_t)p.nchunks * BD * p.npad * 4, kSumB = (uint64_t)p.nchunks * BD * 4;
+    (void)kIoB; (void)kBcB; (void)kAB; (void)kDB; (void)kCarryB; (void)kSumB;
+    auto ldA = [&](int64_t i) -> float { return ld_chk_g(p.A, kAB, p.A + i); };
+#ifdef SSM_CHECK
+    // test of the checks themselves: one load one element past A, which the check must skip
+    if (p.check_probe && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) (void)ldA((int64_t)p.Dm * p.N);
+#endif
 
     const int pr = warp * Cfg::kPairsW + lane / GP;   // pair within the block
     const int g = lane % GP;
@@ -211,8 +223,8 @@ scan_pair_kernel(const SeqParams p) {
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp) {
                 const int n = 4 * (GP * q + g) + 2 * pp;
-                const float a0 = (cv[ch] && n < N) ? p.A[dch[ch] * p.N + n] * kLog2e : 0.0f;
-                const float a1 = (cv[ch] && n + 1 < N) ? p.A[dch[ch] * p.N + n + 1] * kLog2e : 0.0f;
+                const float a0 = (cv[ch] && n < N) ? ldA(dch[ch] * p.N + n) * kLog2e : 0.0f;
+                const float a1 = (cv[ch] && n + 1 < N) ? ldA(dch[ch] * p.N + n + 1) * kLog2e : 0.0f;
                 Ap[ch][q][pp] = make_float2(a0, a1);
             }
     // structured-A test for the lane's states; padded states (n >= N) never qualify
@@ -220,7 +232,7 @@ scan_pair_kernel(const SeqParams p) {
     bool lane_st = p.structured != 0;
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
-        const float A0 = cv[ch] ? p.A[dch[ch] * p.N] : 0.0f;
+        const float A0 = cv[ch] ? ldA(dch[ch] * p.N) : 0.0f;
         Ap0[ch] = A0 * kLog2e;
 #pragma unroll
         for (int q = 0; q < kQN; ++q)
@@ -228,7 +240,7 @@ scan_pair_kernel(const SeqParams p) {
             for (int jj = 0; jj < 4; ++jj) {
                 const int n = 4 * (GP * q + g) + jj;
                 if (n >= N) lane_st = false;
-                else if (cv[ch] && p.A[dch[ch] * p.N + n] != (float)(n + 1) * A0) lane_st = false;
+                else if (cv[ch] && ldA(dch[ch] * p.N + n) != (float)(n + 1) * A0) lane_st = false;
             }
     }
     const bool st = __all_sync(0xffffffffu, lane_st);
@@ -257,7 +269,7 @@ scan_pair_kernel(const SeqParams p) {
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const int n = 4 * (GP * q + g) + jj;
-                    if (cv[ch] && n < N) m = fminf(m, fabsf(p.A[dch[ch] * p.N + n] * kLog2e));
+                    if (cv[ch] && n < N) m = fminf(m, fabsf(ldA(dch[ch] * p.N + n) * kLog2e));
                 }
             zmin[ch] = m;
         }
@@ -270,14 +282,14 @@ scan_pair_kernel(const SeqParams p) {
             h[ch][q][0] = make_float2(0.f, 0.f);
             h[ch][q][1] = make_float2(0.f, 0.f);
             if (!AGG && p.hin != nullptr && cv[ch]) {
-                const float4 v = *reinterpret_cast<const float4 *>(
-                    p.hin + ((int64_t)k * BD + b * p.Dm + dch[ch]) * p.npad + 4 * (GP * q + g));
+                const float4 v = ld_chk_g(p.hin, kCarryB, reinterpret_cast<const float4 *>(
+                    p.hin + ((int64_t)k * BD + b * p.Dm + dch[ch]) * p.npad + 4 * (GP * q + g)));
                 h[ch][q][0] = make_float2(v.x, v.y);
                 h[ch][q][1] = make_float2(v.z, v.w);
             }
         }
-    const float Dd[2] = {(!AGG && p.D != nullptr && cv[0]) ? p.D[dch[0]] : 0.0f,
-                         (!AGG && p.D != nullptr && cv[1]) ? p.D[dch[1]] : 0.0f};
+    const float Dd[2] = {(!AGG && p.D != nullptr && cv[0]) ? ld_chk_g(p.D, kDB, p.D + dch[0]) : 0.0f,
+                         (!AGG && p.D != nullptr && cv[1]) ? ld_chk_g(p.D, kDB, p.D + dch[1]) : 0.0f};
 
     const IO *gU = reinterpret_cast<const IO *>(p.u);
     const IO *gDelta = reinterpret_cast<const IO *>(p.delta);
@@ -316,6 +328,24 @@ scan_pair_kernel(const SeqParams p) {
 #pragma unroll
         for (int k = 0; k < kItems; ++k) isrc[k] = item_src((tid + k * Cfg::kThreads) / kPieces);
     }
+    // checked build: a copy source must lie inside u, delta, z, B or C
+    auto src_ok = [&](const IO *src, int bytes) -> bool {
+#ifdef SSM_CHECK
+        auto in = [&](const IO *base, uint64_t total) {
+            const uint64_t a = reinterpret_cast<uint64_t>(src), b0 = reinterpret_cast<uint64_t>(base);
+            return base != nullptr && a >= b0 && a + (uint64_t)bytes <= b0 + total;
+        };
+        const bool ok = in(gU, kIoB) || in(gDelta, kIoB) || in(gZ, kIoB) || in(gB, kBcB) || in(gC, kBcB);
+        if (!ok) set_status(kStatusCheck);
+        return ok;
+#else
+        (void)src; (void)bytes;
+        return true;
+#endif
+    };
+    auto cp_chk = [&](uint32_t dst, const IO *src, int bytes) {
+        if (src_ok(src, bytes) && SSM_CHK_SU(smem_u32(smem), dst, 16u)) cp_async16(dst, src, bytes);
+    };
     auto issue_tile = [&](int j) {
         const uint32_t raw_s = smem_u32(raw_of(j));
         const int64_t toff = (int64_t)j * T;
@@ -325,16 +355,14 @@ scan_pair_kernel(const SeqParams p) {
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
                 if (isrc[k] != nullptr)
-                    cp_async16(raw_s + idst0 + k * kItemStride,
-                               avail > 0 ? (const void *)(isrc[k] + toff) : (const void *)gU,
-                               avail * (int)sizeof(IO));
+                    cp_chk(raw_s + idst0 + k * kItemStride, avail > 0 ? isrc[k] + toff : gU, avail * (int)sizeof(IO));
             }
         } else {
             for (int i = tid; i < kRows * kPieces; i += Cfg::kThreads) {
                 const IO *src = item_src(i / kPieces);
                 if (src != nullptr)
-                    cp_async16(raw_s + (uint32_t)(((i / kPieces) * kRS + e0_me) * sizeof(IO)),
-                               avail > 0 ? (const void *)(src + toff) : (const void *)gU, avail * (int)sizeof(IO));
+                    cp_chk(raw_s + (uint32_t)(((i / kPieces) * kRS + e0_me) * sizeof(IO)), avail > 0 ? src + toff : gU,
+                           avail * (int)sizeof(IO));
             }
         }
         cp_async_commit();
@@ -361,9 +389,11 @@ scan_pair_kernel(const SeqParams p) {
             const int i = tid + it * Cfg::kThreads;
             if (kDXItems % Cfg::kThreads != 0 && i >= kDXItems) break;
             const int cc = i % kCh, tq = (i / kCh) * kSI;
-            float uu[kSI], dl[kSI];
-            load_steps<kSI>(raw + (size_t)cc * kRS + tq, uu);
-            load_steps<kSI>(raw + (size_t)(kCh + cc) * kRS + tq, dl);
+            float uu[kSI] = {}, dl[kSI] = {};
+            if (SSM_CHK_S(smem, raw + (size_t)cc * kRS + tq, kSI * sizeof(IO)))
+                load_steps<kSI>(raw + (size_t)cc * kRS + tq, uu);
+            if (SSM_CHK_S(smem, raw + (size_t)(kCh + cc) * kRS + tq, kSI * sizeof(IO)))
+                load_steps<kSI>(raw + (size_t)(kCh + cc) * kRS + tq, dl);
             if constexpr (CONV) {
                 // u = SiLU(bias + sum_k w[k] x[t-3+k]) over the window x[tq-3 .. tq+kSI-1]; the
                 // three steps before the tile come from this tile's row, the previous tile's
@@ -373,22 +403,22 @@ scan_pair_kernel(const SeqParams p) {
                 for (int e = 0; e < kSI; ++e) xw[3 + e] = uu[e];
 #pragma unroll
                 for (int i = 0; i < 3; ++i) {
-                    if (tq > 0) xw[i] = io_traits<IO>::to_f(raw[(size_t)cc * kRS + tq - 3 + i]);
-                    else if (j > 0) xw[i] = io_traits<IO>::to_f(raw_of(j - 1)[(size_t)cc * kRS + T - 3 + i]);
-                    else xw[i] = sHalo[cc * 4 + i];
+                    if (tq > 0) xw[i] = io_traits<IO>::to_f(ld_chk_s(smem, raw + (size_t)cc * kRS + tq - 3 + i));
+                    else if (j > 0) xw[i] = io_traits<IO>::to_f(ld_chk_s(smem, raw_of(j - 1) + (size_t)cc * kRS + T - 3 + i));
+                    else xw[i] = ld_chk_s(smem, sHalo + cc * 4 + i);
                 }
                 float *su = sSu0 + (size_t)(j & 1) * kCh * T + (size_t)cc * T + tq;
 #pragma unroll
                 for (int e = 0; e < kSI; ++e) {
-                    float acc = sCb[cc];
+                    float acc = ld_chk_s(smem, sCb + cc);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) acc = fmaf(sCw[cc * 4 + k], xw[e + k], acc);
+                    for (int k = 0; k < 4; ++k) acc = fmaf(ld_chk_s(smem, sCw + cc * 4 + k), xw[e + k], acc);
                     uu[e] = silu_f(acc);
-                    su[e] = uu[e];
+                    st_chk_s(smem, su + e, uu[e]);
                 }
             }
             const bool ok = d0 + cc < p.Dm;
-            const float bb = sBias[cc];
+            const float bb = ld_chk_s(smem, sBias + cc);
             float dt[kSI];
 #pragma unroll
             for (int e = 0; e < kSI; ++e) dt[e] = dl[e] + bb;
@@ -407,10 +437,10 @@ scan_pair_kernel(const SeqParams p) {
                 if constexpr (ZOH) tm = in ? fminf(tm, d) : tm;
                 // (dt, dt*u) for the Euler step; (dt, u) for the zero-order hold, which forms
                 // u*B*dt*phi or (a - 1)*u*B/A
-                dst[(size_t)e * kPairs * 2] = make_float2(d, in ? (ZOH ? uu[e] : d * uu[e]) : 0.0f);
+                st_chk_s(smem, dst + (size_t)e * kPairs * 2, make_float2(d, in ? (ZOH ? uu[e] : d * uu[e]) : 0.0f));
             }
-            if constexpr (AGG) sTS0[(j & 1) * kDXItems + cc * (T / kSI) + tq / kSI] = ts;
-            if constexpr (ZOH) sTM0[(j & 1) * kDXItems + cc * (T / kSI) + tq / kSI] = tm;
+            if constexpr (AGG) st_chk_s(smem, sTS0 + (j & 1) * kDXItems + cc * (T / kSI) + tq / kSI, ts);
+            if constexpr (ZOH) st_chk_s(smem, sTM0 + (j & 1) * kDXItems + cc * (T / kSI) + tq / kSI, tm);
         }
 #pragma unroll
         for (int it = 0; it < kBCIter; ++it) {
@@ -419,14 +449,15 @@ scan_pair_kernel(const SeqParams p) {
             const int n = i % kNP, r = i / kNP, kind = r % kBCKinds, tq = (r / kBCKinds) * kEpr;
             float v[kEpr];
             if (n < N) {
-                unpack16(*reinterpret_cast<const uint4 *>(raw + (size_t)(kRowB + kind * kNP + n) * kRS + tq), v, IO(0.0f));
+                unpack16(ld_chk_s(smem, reinterpret_cast<const uint4 *>(raw + (size_t)(kRowB + kind * kNP + n) * kRS + tq)),
+                         v, IO(0.0f));
             } else {
 #pragma unroll
                 for (int e = 0; e < kEpr; ++e) v[e] = 0.0f;
             }
             float *dst = sBC + (size_t)tq * 2 * kNP + kind * kNP + n;
 #pragma unroll
-            for (int e = 0; e < kEpr; ++e) dst[(size_t)e * 2 * kNP] = v[e];
+            for (int e = 0; e < kEpr; ++e) st_chk_s(smem, dst + (size_t)e * 2 * kNP, v[e]);
         }
     };
     auto convert_tile = [&](int j) {
@@ -457,9 +488,9 @@ scan_pair_kernel(const SeqParams p) {
         if (e0_me >= len) return;
         auto put = [&](IO *dst, const IO *src) {
             if (e0_me + kEpr <= len) {
-                *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+                st_chk_g(gY, kIoB, reinterpret_cast<uint4 *>(dst), ld_chk_s(smem, reinterpret_cast<const uint4 *>(src)));
             } else {
-                for (int e = 0; e < len - e0_me; ++e) dst[e] = src[e];
+                for (int e = 0; e < len - e0_me; ++e) st_chk_g(gY, kIoB, dst + e, ld_chk_s(smem, src + e));
             }
         };
         if constexpr (kYItems <= 2) {
@@ -478,18 +509,21 @@ scan_pair_kernel(const SeqParams p) {
     };
 
     for (int i = tid; i < kCh; i += Cfg::kThreads)
-        sBias[i] = (p.bias != nullptr && d0 + i < p.Dm) ? p.bias[d0 + i] : 0.0f;
+        st_chk_s(smem, sBias + i, (p.bias != nullptr && d0 + i < p.Dm) ? ld_chk_g(p.bias, kDB, p.bias + d0 + i) : 0.0f);
     if constexpr (CONV) {
         for (int i = tid; i < kCh; i += Cfg::kThreads) {
             const bool okc = d0 + i < p.Dm;
             for (int k = 0; k < 4; ++k) {   // taps right-aligned: the last tap meets x[t]
                 const int kk = k - (4 - p.conv_k);
-                sCw[i * 4 + k] = (okc && kk >= 0) ? p.conv_w[(d0 + i) * p.conv_k + kk] : 0.0f;
+                st_chk_s(smem, sCw + i * 4 + k, (okc && kk >= 0)
+                                                    ? ld_chk_g(p.conv_w, (uint64_t)p.Dm * p.conv_k * 4, p.conv_w + (d0 + i) * p.conv_k + kk)
+                                                    : 0.0f);
             }
-            sCb[i] = (okc && p.conv_b != nullptr) ? p.conv_b[d0 + i] : 0.0f;
+            st_chk_s(smem, sCb + i, (okc && p.conv_b != nullptr) ? ld_chk_g(p.conv_b, kDB, p.conv_b + d0 + i) : 0.0f);
             for (int k = 0; k < 3; ++k) {
                 const int64_t s = l_begin - 3 + k;
-                sHalo[i * 4 + k] = (okc && s >= 0) ? io_traits<IO>::to_f(gU[(b * p.Dm + d0 + i) * p.L + s]) : 0.0f;
+                st_chk_s(smem, sHalo + i * 4 + k,
+                         (okc && s >= 0) ? io_traits<IO>::to_f(ld_chk_g(gU, kIoB, gU + (b * p.Dm + d0 + i) * p.L + s)) : 0.0f);
             }
         }
     }
@@ -523,11 +557,11 @@ scan_pair_kernel(const SeqParams p) {
             for (int ch = 0; ch < 2; ++ch) {
                 const float ysum = group_reduce_transpose<GP>(yp[ch], lane);
                 const int cc = c0 + ch;
-                const float uv = CONV ? sSu0[(size_t)(j & 1) * kCh * T + (size_t)cc * T + t]
-                                      : io_traits<IO>::to_f(raw[(size_t)cc * kRS + t]);
+                const float uv = CONV ? ld_chk_s(smem, sSu0 + (size_t)(j & 1) * kCh * T + (size_t)cc * T + t)
+                                      : io_traits<IO>::to_f(ld_chk_s(smem, raw + (size_t)cc * kRS + t));
                 float yv = fmaf(Dd[ch], uv, ysum);
-                if (has_z) yv *= silu_f(io_traits<IO>::to_f(raw[(size_t)(2 * kCh + cc) * kRS + t]));
-                store_io(ys + (size_t)cc * kRS + t, yv);
+                if (has_z) yv *= silu_f(io_traits<IO>::to_f(ld_chk_s(smem, raw + (size_t)(2 * kCh + cc) * kRS + t)));
+                if (SSM_CHK_S(smem, ys + (size_t)cc * kRS + t, sizeof(IO))) store_io(ys + (size_t)cc * kRS + t, yv);
             }
         };
         auto scan_tile = [&](auto st_c, auto zf_c) {
@@ -540,7 +574,7 @@ scan_pair_kernel(const SeqParams p) {
 #pragma unroll
                 for (int s = 0; s < GP; ++s) {
                     const int t = tb + s;
-                    const float4 dx = dxl[t * kPairs];
+                    const float4 dx = ld_chk_s(smem, dxl + t * kPairs);
                     const float2 dd[2] = {make_float2(dx.x, dx.x), make_float2(dx.z, dx.z)};
                     const float2 xx[2] = {make_float2(dx.y, dx.y), make_float2(dx.w, dx.w)};
                     // structured A: r = exp(dt*A[d, 0]) and (r^2, r^2) per channel
@@ -556,9 +590,9 @@ scan_pair_kernel(const SeqParams p) {
                     float2 ya[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                     for (int q = 0; q < kQN; ++q) {
-                        const float4 bq = *reinterpret_cast<const float4 *>(bcl + t * 2 * kNP + 4 * GP * q);
+                        const float4 bq = ld_chk_s(smem, reinterpret_cast<const float4 *>(bcl + t * 2 * kNP + 4 * GP * q));
                         float4 cq = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (!AGG) cq = *reinterpret_cast<const float4 *>(bcl + t * 2 * kNP + kNP + 4 * GP * q);
+                        if (!AGG) cq = ld_chk_s(smem, reinterpret_cast<const float4 *>(bcl + t * 2 * kNP + kNP + 4 * GP * q));
 #pragma unroll
                         for (int ch = 0; ch < 2; ++ch) {
                             float2 e0, e1, a0, a1;
@@ -670,9 +704,9 @@ scan_pair_kernel(const SeqParams p) {
             float *dst = p.agg_h + ((int64_t)k * BD + bd) * p.npad;
 #pragma unroll
             for (int q = 0; q < kQN; ++q)
-                *reinterpret_cast<float4 *>(dst + 4 * (GP * q + g)) =
-                    make_float4(h[ch][q][0].x, h[ch][q][0].y, h[ch][q][1].x, h[ch][q][1].y);
-            if (g == 0) p.agg_s[(int64_t)k * BD + bd] = dsum[ch];
+                st_chk_g(p.agg_h, kCarryB, reinterpret_cast<float4 *>(dst + 4 * (GP * q + g)),
+                         make_float4(h[ch][q][0].x, h[ch][q][0].y, h[ch][q][1].x, h[ch][q][1].y));
+            if (g == 0) st_chk_g(p.agg_s, kSumB, p.agg_s + (int64_t)k * BD + bd, dsum[ch]);
         } else if (p.last_state != nullptr && k == p.nchunks - 1) {
             float *dst = p.last_state + bd * p.N;
 #pragma unroll
@@ -681,7 +715,7 @@ scan_pair_kernel(const SeqParams p) {
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const int n = 4 * (GP * q + g) + jj;
-                    if (n < N) dst[n] = v[jj];
+                    if (n < N) st_chk_g(p.last_state, (uint64_t)BD * p.N * 4, dst + n, v[jj]);
                 }
             }
         }

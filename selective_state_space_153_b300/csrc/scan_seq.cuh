@@ -28,6 +28,7 @@
 // of the lmnt.cn page, section 3.4 of "Mamba architecture principles and industrial
 // long-text practice", jsqmd.com -- so chunk end states compose exactly).
 #pragma once
+#include "check.cuh"
 #include "common.cuh"
 
 namespace ssm {
@@ -51,6 +52,7 @@ struct SeqParams {
     const float *conv_b;   // [Dm] fp32 or null
     int conv_k;            // 1..4
     int structured;        // channel-pair kernel: 1 = detect structured A per warp, 0 = never
+    int check_probe;       // checked build: one deliberately out-of-range checked load (test)
 };
 
 template <typename IO, int NPER, int G, int WARPS, int T>
@@ -98,6 +100,12 @@ scan_seq_kernel(const SeqParams p) {
     const int64_t l_end = min(p.L, l_begin + p.chunk_len);
     const int ntiles = (int)((l_end - l_begin + T - 1) / T);
     const int N = (int)p.N;
+    SSM_POISON_SMEM(smem);
+    // array extents in bytes (the checked build's bounds checks; dead code otherwise)
+    const uint64_t kIoB = (uint64_t)p.Bt * p.Dm * p.L * sizeof(IO), kBcB = (uint64_t)p.Bt * p.N * p.L * sizeof(IO);
+    const uint64_t kAB = (uint64_t)p.Dm * p.N * 4, kDB = (uint64_t)p.Dm * 4;
+    const uint64_t kCarryB = (uint64_t)p.nchunks * p.Bt * p.Dm * p.npad * 4, kSumB = (uint64_t)p.nchunks * p.Bt * p.Dm * 4;
+    (void)kIoB; (void)kBcB; (void)kAB; (void)kDB; (void)kCarryB; (void)kSumB;
 
     const int c = warp * Cfg::kCPW + lane / G;   // this lane's channel within the block
     const int g = lane % G;
@@ -112,7 +120,7 @@ scan_seq_kernel(const SeqParams p) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int n = 4 * (G * q + g) + j;
-            Ap[4 * q + j] = (cvalid && n < N) ? p.A[d * p.N + n] * kLog2e : 0.0f;
+            Ap[4 * q + j] = (cvalid && n < N) ? ld_chk_g(p.A, kAB, p.A + d * p.N + n) * kLog2e : 0.0f;
         }
     float h[NPER];
 #pragma unroll
@@ -121,18 +129,18 @@ scan_seq_kernel(const SeqParams p) {
         const float *src = p.hin + ((int64_t)k * p.Bt * p.Dm + bd) * p.npad;
 #pragma unroll
         for (int q = 0; q < NPER / 4; ++q) {
-            const float4 v = *reinterpret_cast<const float4 *>(src + 4 * (G * q + g));
+            const float4 v = ld_chk_g(p.hin, kCarryB, reinterpret_cast<const float4 *>(src + 4 * (G * q + g)));
             h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
         }
     }
-    const float Dd = (!AGG && p.D != nullptr && cvalid) ? p.D[d] : 0.0f;
-    const float bias_d = (p.bias != nullptr && cvalid) ? p.bias[d] : 0.0f;
+    const float Dd = (!AGG && p.D != nullptr && cvalid) ? ld_chk_g(p.D, kDB, p.D + d) : 0.0f;
+    const float bias_d = (p.bias != nullptr && cvalid) ? ld_chk_g(p.bias, kDB, p.bias + d) : 0.0f;
 
     // zero the padded B/C columns once (never overwritten)
     for (int i = tid; i < T * (kNpad - N); i += Cfg::kThreads) {
         const int t = i / (kNpad - N), n = N + i % (kNpad - N);
-        sB[t * kBS + n] = 0.0f;
-        sC[t * kBS + n] = 0.0f;
+        st_chk_s(smem, sB + t * kBS + n, 0.0f);
+        st_chk_s(smem, sC + t * kBS + n, 0.0f);
     }
 
     const IO *gU = reinterpret_cast<const IO *>(p.u);
@@ -170,11 +178,17 @@ scan_seq_kernel(const SeqParams p) {
                 dst = raw + (3 * kCh + kind * kNpad + n) * T + e0;
             }
             const int avail = ok ? max(0, min(Cfg::kEpr, len - e0)) : 0;
+            const uint64_t total = row < nrows_ch ? kIoB : kBcB;
+            const void *sbase = row < nrows_ch ? (const void *)(row / kCh == 0 ? gU : (row / kCh == 1 ? gDelta : gZ))
+                                               : (const void *)((row - nrows_ch) / N == 0 ? gB : gC);
+            (void)total; (void)sbase;
             if (ALIGNED) {
-                cp_async16(dst, avail > 0 ? (const void *)src : (const void *)gU, avail * (int)sizeof(IO));
+                if (SSM_CHK_S(smem, dst, 16) && (avail == 0 || SSM_CHK_G(sbase, total, src, avail * sizeof(IO))))
+                    cp_async16(dst, avail > 0 ? (const void *)src : (const void *)gU, avail * (int)sizeof(IO));
             } else {
 #pragma unroll
-                for (int e = 0; e < Cfg::kEpr; ++e) dst[e] = e < avail ? src[e] : IO(0.0f);
+                for (int e = 0; e < Cfg::kEpr; ++e)
+                    st_chk_s(smem, dst + e, e < avail ? ld_chk_g(sbase, total, src + e) : IO(0.0f));
             }
         }
     };
@@ -197,18 +211,19 @@ scan_seq_kernel(const SeqParams p) {
             const int t = i % T, cc = i / T;
             float dt = 0.0f, x = 0.0f;
             if (t < len && d0 + cc < p.Dm) {
-                const float uu = io_traits<IO>::to_f(raw[cc * T + t]);
-                const float bb = (p.bias != nullptr) ? p.bias[d0 + cc] : 0.0f;
-                dt = io_traits<IO>::to_f(raw[(kCh + cc) * T + t]) + bb;
+                const float uu = io_traits<IO>::to_f(ld_chk_s(smem, raw + cc * T + t));
+                const float bb = (p.bias != nullptr) ? ld_chk_g(p.bias, kDB, p.bias + d0 + cc) : 0.0f;
+                dt = io_traits<IO>::to_f(ld_chk_s(smem, raw + (kCh + cc) * T + t)) + bb;
                 if (p.softplus) dt = softplus_f(dt);
                 x = dt * uu;
             }
-            sDX[t * kCh + cc] = make_float2(dt, x);
+            st_chk_s(smem, sDX + t * kCh + cc, make_float2(dt, x));
         }
         for (int i = tid; i < N * T; i += Cfg::kThreads) {
             const int t = i % T, n = i / T;
-            sB[t * kBS + n] = io_traits<IO>::to_f(raw[(3 * kCh + n) * T + t]);
-            if (!AGG) sC[t * kBS + n] = io_traits<IO>::to_f(raw[(3 * kCh + kNpad + n) * T + t]);
+            st_chk_s(smem, sB + t * kBS + n, io_traits<IO>::to_f(ld_chk_s(smem, raw + (3 * kCh + n) * T + t)));
+            if (!AGG)
+                st_chk_s(smem, sC + t * kBS + n, io_traits<IO>::to_f(ld_chk_s(smem, raw + (3 * kCh + kNpad + n) * T + t)));
         }
         __syncthreads();
         // ---- recurrence over the tile
@@ -219,16 +234,16 @@ scan_seq_kernel(const SeqParams p) {
 #pragma unroll
             for (int s = 0; s < G; ++s) {
                 const int t = tb + s;
-                const float2 dx = sDX[t * kCh + c];
+                const float2 dx = ld_chk_s(smem, sDX + t * kCh + c);
                 tsum += dx.x;
                 float y0 = 0.0f, y1 = 0.0f;
 #pragma unroll
                 for (int q = 0; q < NPER / 4; ++q) {
-                    const float4 bv = *reinterpret_cast<const float4 *>(sB + t * kBS + 4 * (G * q + g));
+                    const float4 bv = ld_chk_s(smem, reinterpret_cast<const float4 *>(sB + t * kBS + 4 * (G * q + g)));
                     const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
                     float cc4[4] = {0.f, 0.f, 0.f, 0.f};
                     if (!AGG) {
-                        const float4 cv = *reinterpret_cast<const float4 *>(sC + t * kBS + 4 * (G * q + g));
+                        const float4 cv = ld_chk_s(smem, reinterpret_cast<const float4 *>(sC + t * kBS + 4 * (G * q + g)));
                         cc4[0] = cv.x; cc4[1] = cv.y; cc4[2] = cv.z; cc4[3] = cv.w;
                     }
 #pragma unroll
@@ -248,10 +263,10 @@ scan_seq_kernel(const SeqParams p) {
                 const float ys = group_reduce_transpose<G>(ypart, lane);
                 const int t = tb + g;  // the timestep this lane finished
                 if (t < len && cvalid) {
-                    const float uu = io_traits<IO>::to_f(raw[c * T + t]);
+                    const float uu = io_traits<IO>::to_f(ld_chk_s(smem, raw + c * T + t));
                     float yv = fmaf(Dd, uu, ys);
-                    if (has_z) yv *= silu_f(io_traits<IO>::to_f(raw[(2 * kCh + c) * T + t]));
-                    sY[c * kYS + t] = yv;
+                    if (has_z) yv *= silu_f(io_traits<IO>::to_f(ld_chk_s(smem, raw + (2 * kCh + c) * T + t)));
+                    st_chk_s(smem, sY + c * kYS + t, yv);
                 }
             }
         }
@@ -274,17 +289,19 @@ scan_seq_kernel(const SeqParams p) {
                     if (e0 + Cfg::kEpr <= len) {
                         float tmp[Cfg::kEpr];
 #pragma unroll
-                        for (int e = 0; e < Cfg::kEpr; ++e) tmp[e] = srcf[e];
-                        *reinterpret_cast<uint4 *>(dst) = pack16(tmp, IO(0.0f));
+                        for (int e = 0; e < Cfg::kEpr; ++e) tmp[e] = ld_chk_s(smem, srcf + e);
+                        st_chk_g(gY, kIoB, reinterpret_cast<uint4 *>(dst), pack16(tmp, IO(0.0f)));
                     } else {
-                        for (int e = 0; e < len - e0; ++e) store_io(dst + e, srcf[e]);
+                        for (int e = 0; e < len - e0; ++e)
+                            if (SSM_CHK_G(gY, kIoB, dst + e, sizeof(IO))) store_io(dst + e, ld_chk_s(smem, srcf + e));
                     }
                 }
             } else {
                 for (int i = tid; i < kCh * T; i += Cfg::kThreads) {
                     const int cc = i / T, t = i % T;
                     if (d0 + cc >= p.Dm || t >= len) continue;
-                    store_io(gY + (b * p.Dm + d0 + cc) * p.L + t0 + t, sY[cc * kYS + t]);
+                    if (SSM_CHK_G(gY, kIoB, gY + (b * p.Dm + d0 + cc) * p.L + t0 + t, sizeof(IO)))
+                        store_io(gY + (b * p.Dm + d0 + cc) * p.L + t0 + t, ld_chk_s(smem, sY + cc * kYS + t));
                 }
             }
         }
@@ -296,9 +313,9 @@ scan_seq_kernel(const SeqParams p) {
         float *dst = p.agg_h + ((int64_t)k * p.Bt * p.Dm + bd) * p.npad;
 #pragma unroll
         for (int q = 0; q < NPER / 4; ++q)
-            *reinterpret_cast<float4 *>(dst + 4 * (G * q + g)) =
-                make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-        if (g == 0) p.agg_s[(int64_t)k * p.Bt * p.Dm + bd] = dsum;
+            st_chk_g(p.agg_h, kCarryB, reinterpret_cast<float4 *>(dst + 4 * (G * q + g)),
+                     make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]));
+        if (g == 0) st_chk_g(p.agg_s, kSumB, p.agg_s + (int64_t)k * p.Bt * p.Dm + bd, dsum);
     } else if (p.last_state != nullptr && k == p.nchunks - 1) {
         float *dst = p.last_state + bd * p.N;
 #pragma unroll
@@ -306,7 +323,7 @@ scan_seq_kernel(const SeqParams p) {
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int n = 4 * (G * q + g) + jj;
-                if (n < N) dst[n] = h[4 * q + jj];
+                if (n < N) st_chk_g(p.last_state, (uint64_t)p.Bt * p.Dm * p.N * 4, dst + n, h[4 * q + jj]);
             }
     }
 }

@@ -39,6 +39,18 @@ ssm_plan_override_t plan_override() {
     return g_override;
 }
 
+// ---- the CUDA error behind the last SSM_ERR_CUDA of this thread (ssm_last_cuda_error) -----
+thread_local int t_last_cuda_error = 0;
+
+// SSM_OK for cudaSuccess; otherwise records `e` for ssm_last_cuda_error, clears the runtime's
+// last-error slot (so that the next launch check does not find it) and returns SSM_ERR_CUDA.
+ssm_status_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return SSM_OK;
+    t_last_cuda_error = (int)e;
+    cudaGetLastError();
+    return SSM_ERR_CUDA;
+}
+
 // ---- registered default workspace (ssm_set_workspace), one per device --------------------
 constexpr int kMaxDevices = 64;
 std::mutex g_ws_mu;
@@ -243,7 +255,7 @@ ssm_status_t run_scan_tc(const ssm_dims_t &d, const TcPlan &t, const ssm_plan_ov
     if (!make_map(&prm.map_u, u, d, cpw, t.T) || !make_map(&prm.map_delta, delta, d, cpw, t.T) ||
         !make_map(&prm.map_z, z ? z : u, d, cpw, t.T) || !make_map(&prm.map_y, y, d, cpw, t.T) ||
         !make_map(&prm.map_y8, y, d, cpw, 8))
-        return SSM_ERR_CUDA;
+        return cuda_status(cudaErrorInvalidValue);
     prm.bc = reinterpret_cast<const float *>(ws + t.off_bc);
     prm.A = A; prm.D = D; prm.bias = delta_bias; prm.last_state = last_state;
     prm.ctrl = reinterpret_cast<int *>(ws);
@@ -256,11 +268,12 @@ ssm_status_t run_scan_tc(const ssm_dims_t &d, const TcPlan &t, const ssm_plan_ov
     prm.spin_limit = 1u << 24;
     prm.force_timeout = 0;
     if (ov.force_timeout) { prm.force_timeout = 1; prm.spin_limit = 256; }
-    if (cudaMemsetAsync(ws, 0, t.ctrl_bytes, s) != cudaSuccess) return SSM_ERR_CUDA;
-    if (launch_bc_prep(d.io_dtype, B, C, reinterpret_cast<float *>(ws + t.off_bc), d.dstate, d.seqlen, t.Lp, t.np,
-                       d.batch, s) != cudaSuccess)
-        return SSM_ERR_CUDA;
-    return launch_tc(d.io_dtype, t.pipelined, t.G, prm, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(ws, 0, t.ctrl_bytes, s);
+    if (e == cudaSuccess)
+        e = launch_bc_prep(d.io_dtype, B, C, reinterpret_cast<float *>(ws + t.off_bc), d.dstate, d.seqlen, t.Lp, t.np,
+                           d.batch, s);
+    if (e == cudaSuccess) e = launch_tc(d.io_dtype, t.pipelined, t.G, prm, s);
+    return cuda_status(e);
 }
 
 ssm_status_t scan_checks(const ssm_dims_t *dims, const void *u, const void *delta, const float *A,
@@ -375,10 +388,7 @@ ssm_status_t acquire_workspace(void **ws, size_t ws_bytes, size_t need, bool may
     if (need == 0) return SSM_OK;
     if (*ws == nullptr || ws_bytes < need) {
         if (!may_alloc) return SSM_ERR_WORKSPACE;
-        if (cudaMallocAsync(ws, need, s) != cudaSuccess) {
-            cudaGetLastError();
-            return SSM_ERR_CUDA;
-        }
+        if (const cudaError_t e = cudaMallocAsync(ws, need, s); e != cudaSuccess) return cuda_status(e);
         *allocated = true;
     } else if (!aligned16(*ws)) {
         return SSM_ERR_ALIGN;
@@ -404,6 +414,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
     prm.zoh = zoh ? 1 : 0;
     prm.conv_w = conv_w; prm.conv_b = conv_b; prm.conv_k = conv_k;
     prm.structured = g_structured_a.load();
+    prm.check_probe = plan_override().check_probe;
     const int variant = conv_w != nullptr ? kPairConv : (zoh ? kPairZoh : kPairEuler);
     cudaError_t e = cudaSuccess;
     if (pl.nchunks > 1) {
@@ -422,7 +433,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
     prm.chan_blocks = pl.cb_full;
     if (e == cudaSuccess) e = launch_pair(d.io_dtype, variant, pl.ks, pl.gp, false, prm, pl.nchunks, s);
     if (allocated) cudaFreeAsync(workspace, s);
-    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    return cuda_status(e);
 }
 
 // Workspace bytes the scan of `d` needs under the current plan (0 if none).
@@ -443,8 +454,7 @@ ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, 
     const ssm_dims_t d = *dims;
     if (d.batch == 0 || d.dim == 0) return SSM_OK;
     if (d.seqlen == 0) {
-        if (last_state && launch_zero_f32(last_state, d.batch * d.dim * d.dstate, s) != cudaSuccess)
-            return SSM_ERR_CUDA;
+        if (last_state) return cuda_status(launch_zero_f32(last_state, d.batch * d.dim * d.dstate, s));
         return SSM_OK;
     }
     const ssm_plan_override_t ov = plan_override();
@@ -494,7 +504,7 @@ ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, 
     }
     if (e == cudaSuccess) e = launch_seq(d.io_dtype, pl.nper, pl.g, false, aligned, prm, pl.nchunks, s);
     if (allocated) cudaFreeAsync(workspace, s);
-    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    return cuda_status(e);
 }
 
 // ---- fixed scratch for ssm_selective_scan_fwd_noalloc -------------------------------------
@@ -541,16 +551,10 @@ unsigned long long g_scratch_ctx[kMaxDevices] = {};
 // capture) and cached for the later calls in the same context.
 ssm_status_t scratch_address(void **out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return SSM_ERR_CUDA;
-    }
+    if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_status(e);
     const bool cached = dev >= 0 && dev < kMaxDevices;
     // establishes the primary context if the call is the first CUDA work of this thread
-    if (cudaFree(nullptr) != cudaSuccess) {
-        cudaGetLastError();
-        return SSM_ERR_CUDA;
-    }
+    if (const cudaError_t e = cudaFree(nullptr); e != cudaSuccess) return cuda_status(e);
     const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (cached && ctx != 0 && g_scratch_addr[dev] != nullptr && g_scratch_ctx[dev] == ctx) {
@@ -558,10 +562,8 @@ ssm_status_t scratch_address(void **out) {
         return SSM_OK;
     }
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-        cudaGetLastError();   // do not leave the error for the next launch check to find
-        return SSM_ERR_CUDA;
-    }
+    if (const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch); e != cudaSuccess || p == nullptr)
+        return cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
     if (cached) {
         g_scratch_addr[dev] = p;
         g_scratch_ctx[dev] = ctx;
@@ -607,10 +609,7 @@ ssm_status_t ssm_set_workspace(void *dev_ptr, size_t bytes) {
     if (dev_ptr != nullptr && bytes == 0) return SSM_ERR_WORKSPACE;
     if (dev_ptr != nullptr && !aligned16(dev_ptr)) return SSM_ERR_ALIGN;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return SSM_ERR_CUDA;
-    }
+    if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_status(e);
     if (dev < 0 || dev >= kMaxDevices) return SSM_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_ws_mu);
     g_ws_ptr[dev] = dev_ptr;
@@ -666,8 +665,11 @@ ssm_status_t state_update_impl(const ssm_dims_t *dims, float *state, const void 
                       dims->dim * lpc < (int64_t)1 << 30 && !plan_override().decode_elementwise;
     const int kind = vec ? (wide ? 0 : 1) : 2;
     const cudaError_t e = launch_decode(dims->io_dtype, kind, lpc, zoh != 0, p, static_cast<cudaStream_t>(stream));
-    if (e == cudaErrorInvalidConfiguration) return SSM_ERR_UNSUPPORTED;
-    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    if (e == cudaErrorInvalidConfiguration) {
+        cudaGetLastError();
+        return SSM_ERR_UNSUPPORTED;
+    }
+    return cuda_status(e);
 }
 }  // namespace
 
@@ -782,13 +784,14 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     if (!empty && need > 0 && !w.may_alloc && (w.ptr == nullptr || w.bytes < need)) return SSM_ERR_WORKSPACE;
     // gradients summed over the sequence, the batch or the channels start at zero
     const size_t BD = (size_t)(d.batch * d.dim), NL = (size_t)(d.dstate * d.seqlen);
-    if (cudaMemsetAsync(dA, 0, (size_t)(d.dim * d.dstate) * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
-    if (dD && cudaMemsetAsync(dD, 0, (size_t)d.dim * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
-    if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)d.dim * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
-    if (empty) return SSM_OK;
-    if (cudaMemsetAsync(dB, 0, (size_t)d.batch * NL * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
-    if (cudaMemsetAsync(dC, 0, (size_t)d.batch * NL * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
-    if (dz && !z && cudaMemsetAsync(dz, 0, BD * (size_t)d.seqlen * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
+    cudaError_t ez = cudaMemsetAsync(dA, 0, (size_t)(d.dim * d.dstate) * 4, s);
+    if (ez == cudaSuccess && dD) ez = cudaMemsetAsync(dD, 0, (size_t)d.dim * 4, s);
+    if (ez == cudaSuccess && ddelta_bias) ez = cudaMemsetAsync(ddelta_bias, 0, (size_t)d.dim * 4, s);
+    if (ez != cudaSuccess || empty) return cuda_status(ez);
+    ez = cudaMemsetAsync(dB, 0, (size_t)d.batch * NL * 4, s);
+    if (ez == cudaSuccess) ez = cudaMemsetAsync(dC, 0, (size_t)d.batch * NL * 4, s);
+    if (ez == cudaSuccess && dz && !z) ez = cudaMemsetAsync(dz, 0, BD * (size_t)d.seqlen * 4, s);
+    if (ez != cudaSuccess) return cuda_status(ez);
     void *ws = w.ptr;
     bool allocated = false;
     st = acquire_workspace(&ws, w.bytes, need, w.may_alloc, s, &allocated);
@@ -798,8 +801,11 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
                 d.dstate, delta_softplus ? 1 : 0, (int)((d.seqlen + kBwdS - 1) / kBwdS)};
     const cudaError_t e = launch_bwd(d.io_dtype, bwd_lanes(d.dstate), p, s);
     if (allocated) cudaFreeAsync(ws, s);
-    if (e == cudaErrorInvalidConfiguration) return SSM_ERR_UNSUPPORTED;
-    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    if (e == cudaErrorInvalidConfiguration) {
+        cudaGetLastError();
+        return SSM_ERR_UNSUPPORTED;
+    }
+    return cuda_status(e);
 }
 
 ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, const void *delta,
@@ -832,7 +838,7 @@ ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, 
     void *bu[2] = {nullptr, nullptr}, *bdl[2] = {nullptr, nullptr}, *bz[2] = {nullptr, nullptr};
     void *by[2] = {nullptr, nullptr}, *bst[2] = {nullptr, nullptr};
     const size_t row_bytes = blk * L * esz;
-    auto CK = [&](cudaError_t e) { if (e != cudaSuccess && rc == SSM_OK) rc = SSM_ERR_CUDA; return e == cudaSuccess; };
+    auto CK = [&](cudaError_t e) { if (e != cudaSuccess && rc == SSM_OK) rc = cuda_status(e); return e == cudaSuccess; };
     CK(cudaStreamCreateWithFlags(&ss[0], cudaStreamNonBlocking));
     CK(cudaStreamCreateWithFlags(&ss[1], cudaStreamNonBlocking));
     CK(cudaEventCreateWithFlags(&ev_in, cudaEventDisableTiming));
@@ -903,12 +909,15 @@ ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, 
 }
 
 ssm_status_t ssm_stream_status(void *stream) {
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSM_ERR_CUDA;
+    if (const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream)); e != cudaSuccess)
+        return cuda_status(e);
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, ssm::g_ssm_status, sizeof(int)) != cudaSuccess) return SSM_ERR_CUDA;
+    if (const cudaError_t e = cudaMemcpyFromSymbol(&v, ssm::g_ssm_status, sizeof(int)); e != cudaSuccess)
+        return cuda_status(e);
     if (v != 0) {
         const int zero = 0;
-        if (cudaMemcpyToSymbol(ssm::g_ssm_status, &zero, sizeof(int)) != cudaSuccess) return SSM_ERR_CUDA;
+        if (const cudaError_t e = cudaMemcpyToSymbol(ssm::g_ssm_status, &zero, sizeof(int)); e != cudaSuccess)
+            return cuda_status(e);
         return static_cast<ssm_status_t>(v);
     }
     return SSM_OK;
@@ -925,8 +934,16 @@ const char *ssm_status_string(ssm_status_t status) {
         case SSM_ERR_CUDA: return "SSM_ERR_CUDA: CUDA runtime error";
         case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT: a bounded device-side wait gave up";
         case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE: workspace missing or too small";
+        case SSM_ERR_CHECK: return "SSM_ERR_CHECK: a bounds check of the checked build failed";
         default: return "SSM_ERR_UNKNOWN";
     }
+}
+
+int ssm_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char *ssm_cuda_error_string(int code) {
+    const char *t = cudaGetErrorString(static_cast<cudaError_t>(code));
+    return t ? t : "unknown CUDA error";
 }
 
 int ssm_set_structured_a(int enable) { return g_structured_a.exchange(enable ? 1 : 0); }
@@ -955,6 +972,6 @@ ssm_status_t ssm_get_plan_override(ssm_plan_override_t *out) {
     return SSM_OK;
 }
 
-int ssm_version(void) { return (1 << 16) | 1; }
+int ssm_version(void) { return (1 << 16) | 2; }
 
 }  // extern "C"

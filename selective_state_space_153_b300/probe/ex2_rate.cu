@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(128) ex2_chains(int iters, float seed, float *
 }  // namespace
 
 extern "C" {
+#pragma GCC visibility push(default)
 
 // Measures ex2 per SM per clock on the current device. Returns 0 on success with *per_clk_sm
 // set; otherwise the cudaError_t of the failing call. Allocates and frees its own buffers.
@@ -105,4 +106,5 @@ int ssm_probe_ex2_rate(int iters, double *per_clk_sm, double *elapsed_ms) {
     return (int)e;
 }
 
+#pragma GCC visibility pop
 }  // extern "C"

@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libssm_scan.so")
 
 SSM_OK, SSM_ERR_NULL, SSM_ERR_SHAPE, SSM_ERR_DTYPE, SSM_ERR_ALIGN = 0, 1, 2, 3, 4
-SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = 5, 6, 7, 8
+SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE, SSM_ERR_CHECK = 5, 6, 7, 8, 9
 SSM_F32, SSM_BF16 = 0, 1
 SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
 _DISC = {"euler": SSM_DISC_EULER, "zoh": SSM_DISC_ZOH}
@@ -33,7 +33,7 @@ EXPORTS = ("ssm_selective_scan_fwd", "ssm_selective_scan_workspace_bytes",
            "ssm_conv_selective_scan_fwd", "ssm_conv_selective_scan_workspace_bytes",
            "ssm_selective_scan_bwd", "ssm_selective_scan_bwd_workspace_bytes",
            "ssm_set_structured_a", "ssm_set_workspace", "ssm_set_plan_override",
-           "ssm_get_plan_override")
+           "ssm_get_plan_override", "ssm_last_cuda_error", "ssm_cuda_error_string")
 
 # ssm_kernel_t
 SSM_KERNEL_AUTO, SSM_KERNEL_PAIR, SSM_KERNEL_SEQ, SSM_KERNEL_TC, SSM_KERNEL_TP = range(5)
@@ -50,13 +50,18 @@ class PlanOverride(ctypes.Structure):
     """ssm_plan_override_t: every field 0 = the planner's choice."""
     _fields_ = [("kernel", ctypes.c_int), ("pair_states_per_lane", ctypes.c_int), ("chunks", ctypes.c_int),
                 ("seq_states_per_lane", ctypes.c_int), ("seq_lanes_per_channel", ctypes.c_int),
-                ("decode_elementwise", ctypes.c_int), ("force_timeout", ctypes.c_int)]
+                ("decode_elementwise", ctypes.c_int), ("force_timeout", ctypes.c_int),
+                ("check_probe", ctypes.c_int)]
 
 
 class SsmError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {status_string(code)}")
+        msg = f"{where}: {status_string(code)}"
+        if code == SSM_ERR_CUDA and _lib is not None:
+            e = _lib.ssm_last_cuda_error()
+            msg += f" ({e}: {_lib.ssm_cuda_error_string(e).decode()})"
+        super().__init__(msg)
 
 
 _lib = None
@@ -69,6 +74,25 @@ def load(path: str = LIB_PATH):
     global _lib
     if _lib is not None:
         return _lib
+    _lib = load_library(path)
+    return _lib
+
+
+@contextlib.contextmanager
+def using(lib):
+    """Route this module's calls to another loaded build of the library (for instance the
+    checked build, -DSSM_CHECK) inside the block."""
+    global _lib
+    prev = load()
+    _lib = lib
+    try:
+        yield lib
+    finally:
+        _lib = prev
+
+
+def load_library(path: str):
+    """Load a build of the library at ``path`` with its argument types set (not cached)."""
     if not os.path.exists(path):
         raise ImportError(f"CUDA library not built: {path}")
     lib = ctypes.CDLL(path)
@@ -103,6 +127,10 @@ def load(path: str = LIB_PATH):
     lib.ssm_status_string.argtypes = [ctypes.c_int]
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_version.argtypes = []
+    lib.ssm_last_cuda_error.argtypes = []
+    lib.ssm_last_cuda_error.restype = ctypes.c_int
+    lib.ssm_cuda_error_string.argtypes = [ctypes.c_int]
+    lib.ssm_cuda_error_string.restype = ctypes.c_char_p
     lib.ssm_version.restype = ctypes.c_int
     lib.ssm_set_structured_a.argtypes = [ctypes.c_int]
     lib.ssm_set_structured_a.restype = ctypes.c_int
@@ -112,7 +140,6 @@ def load(path: str = LIB_PATH):
     lib.ssm_set_plan_override.restype = ctypes.c_int
     lib.ssm_get_plan_override.argtypes = [ctypes.POINTER(PlanOverride)]
     lib.ssm_get_plan_override.restype = ctypes.c_int
-    _lib = lib
     return lib
 
 
@@ -346,13 +373,13 @@ def set_plan_override(ov: Optional[PlanOverride]) -> None:
 @contextlib.contextmanager
 def plan_override(kernel: str = "auto", pair_states_per_lane: int = 0, chunks: int = 0,
                   seq_split: Optional[Tuple[int, int]] = None, decode_elementwise: bool = False,
-                  force_timeout: bool = False):
+                  force_timeout: bool = False, check_probe: bool = False):
     """Force a launch plan for the calls inside the block (ssm_set_plan_override; a test and
     tuning hook), then restore the override that was in force before."""
     prev = get_plan_override()
     ov = PlanOverride(_KERNELS[kernel], int(pair_states_per_lane), int(chunks),
                       int(seq_split[0]) if seq_split else 0, int(seq_split[1]) if seq_split else 0,
-                      int(bool(decode_elementwise)), int(bool(force_timeout)))
+                      int(bool(decode_elementwise)), int(bool(force_timeout)), int(bool(check_probe)))
     set_plan_override(ov)
     try:
         yield ov

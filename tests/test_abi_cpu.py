@@ -34,12 +34,37 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_exports_nothing_else_and_no_shared_statics():
+    """Only the header's functions (and the device-link registration hooks) are exported, and
+    no symbol is a GNU "unique" object: two builds of the library in one process (the normal
+    and the checked build) must not share, say, a kernel's attributes-already-set flag."""
+    import shutil
+    import subprocess
+    if shutil.which("nm") is None:
+        pytest.skip("nm not installed")
+    out = subprocess.run(["nm", "-D", "--defined-only", ssm.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout.split("\n")
+    syms = [ln.split() for ln in out if ln.strip()]
+    assert not [x for x in syms if x[1] == "u"], "GNU unique symbols exported"
+    names = {x[2] for x in syms}
+    extra = {n for n in names if not n.startswith("__cudaRegisterLinkedBinary_")} - set(declared_functions())
+    assert not extra, sorted(extra)[:10]
+
+
 def test_status_strings_and_version(lib):
-    for code in range(9):
+    for code in range(10):
         s = ssm.status_string(code)
         assert s.startswith("SSM_")
     assert ssm.status_string(99) == "SSM_ERR_UNKNOWN"
-    assert ssm.version() == (1, 1)   # 1.1: ssm_set_workspace and the plan override
+    assert ssm.version() == (1, 2)   # 1.1: workspace, plan override; 1.2: last CUDA error
+
+
+def test_last_cuda_error_query(lib):
+    # nothing has failed on this thread: 0; the text comes from the runtime, with no GPU
+    assert lib.ssm_last_cuda_error() == 0
+    assert lib.ssm_cuda_error_string(0).decode() == "no error"
+    assert len(lib.ssm_cuda_error_string(2).decode()) > 0      # cudaErrorMemoryAllocation
+    assert len(lib.ssm_cuda_error_string(123456).decode()) > 0
 
 
 A = ctypes.c_void_p(0x1000)      # fake, 16-byte aligned "device" pointers: never dereferenced
@@ -149,13 +174,13 @@ def test_plan_override_roundtrip_and_errors(lib):
         got = ssm.get_plan_override()
         assert got.chunks == 7 and got.kernel == 0
         assert _chunks_from_workspace(1, 1536, 131072, 64) == 7
-        bad = ssm.PlanOverride(9, 0, 0, 0, 0, 0, 0)
+        bad = ssm.PlanOverride(9, 0, 0, 0, 0, 0, 0, 0)
         assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
-        bad = ssm.PlanOverride(0, 5, 0, 0, 0, 0, 0)
+        bad = ssm.PlanOverride(0, 5, 0, 0, 0, 0, 0, 0)
         assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
-        bad = ssm.PlanOverride(0, 0, -1, 0, 0, 0, 0)
+        bad = ssm.PlanOverride(0, 0, -1, 0, 0, 0, 0, 0)
         assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_SHAPE
-        bad = ssm.PlanOverride(0, 0, 0, 16, 3, 0, 0)   # a lane split that is not built
+        bad = ssm.PlanOverride(0, 0, 0, 16, 3, 0, 0, 0)   # a lane split that is not built
         assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
         assert ssm.get_plan_override().chunks == 7
         assert ov.chunks == 7
