@@ -373,6 +373,8 @@ int ssm_set_structured_a(int enable);
  *                           launch issues a checked load one element past the end of A, which
  *                           the check skips and records as SSM_ERR_CHECK (a test that the
  *                           checks fire). Ignored by the normal build.
+ *   bwd_states_per_lane     ssm_selective_scan_bwd: 4 (the default) or 2 states per lane (taken
+ *                           for dstate <= 32; more lanes per channel, fewer registers).
  * ssm_set_plan_override(NULL) restores the planner. Returns SSM_ERR_UNSUPPORTED for an
  * unknown kernel, lane split or states-per-lane value and SSM_ERR_SHAPE for a negative count;
  * the previous override then stays in force.
@@ -394,6 +396,7 @@ typedef struct {
     int decode_elementwise;
     int force_timeout;
     int check_probe;
+    int bwd_states_per_lane;
 } ssm_plan_override_t;
 
 ssm_status_t ssm_set_plan_override(const ssm_plan_override_t *ov);

@@ -63,6 +63,7 @@ cudaError_t launch_tc(ssm_dtype_t io, bool pipelined, int G, const TcParams &prm
 cudaError_t launch_decode(ssm_dtype_t io, int kind, int lpc, bool zoh, const DecodeParams &p, cudaStream_t s);
 
 // backward (scan_bwd.cuh): checkpoint pass then adjoint pass; G lanes per channel
-cudaError_t launch_bwd(ssm_dtype_t io, int G, const BwdParams &p, cudaStream_t s);
+// backward: G lanes per channel, Q (2 or 4) states per lane
+cudaError_t launch_bwd(ssm_dtype_t io, int G, int Q, const BwdParams &p, cudaStream_t s);
 
 }  // namespace ssm

@@ -12,11 +12,11 @@
 //     dA   += lambda_t dt_t a_t h_{t-1}   dD += dyhat_t u_t   dz_t = dy_t yhat_t SiLU'(z_t)
 // (v = delta + bias; sigmoid is the softplus derivative; without softplus ddelta = ddt).
 //
-// Work decomposition: a thread owns four states n = g + G*q (q < 4) of one channel, G lanes
-// per channel (a power of two, 4G >= N), 32/G channels per warp, 128/G per CTA; the batch
-// row is grid.y. Pass 1 (scan_bwd_ckpt_kernel) runs the recurrence forward and stores h at
+// Work decomposition: a thread owns Q states n = g + G*q (q < Q; Q = 4, or 2 where four
+// states per lane leave the GPU short of warps) of one channel, G lanes per channel (a power
+// of two, QG >= N), 32/G channels per warp, 128/G per CTA; the batch row is grid.y. Pass 1 (scan_bwd_ckpt_kernel) runs the recurrence forward and stores h at
 // the start of every S-step segment. Pass 2 (scan_bwd_kernel) walks the segments backwards:
-//   * the CTA stages the segment's B, C rows (as [t][g][q], so a lane's four states are one
+//   * the CTA stages the segment's B, C rows (as [t][g][q], so a lane's states are one
 //     16-byte read) and, once per (channel, step), dt, the softplus derivative, u,
 //     dyhat = dy*SiLU(z) and the gate derivative factor dy*SiLU'(z); the raw inputs of the
 //     next segment are fetched into registers while the current one computes;
@@ -37,21 +37,23 @@ namespace ssm {
 
 constexpr int kBwdS = 8;         // steps per checkpoint segment
 constexpr int kBwdThreads = 128;
-constexpr int kBwdQ = 4;         // states per thread
+constexpr int kBwdQ = 4;         // states per thread (the default; 2 is also built)
 
 struct BwdParams {
     const void *u, *delta, *z, *B, *C, *dy;
     const float *A, *D, *bias, *dlast;
     float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *dbias;
-    float *ckpt;                  // [Bt*Dm][nseg][4G]: h before each segment's first step
+    float *ckpt;                  // [Bt*Dm][nseg][Q*G]: h before each segment's first step
     int64_t Bt, Dm, L, N;
     int softplus, nseg;
 };
 
-// Shared-memory layout (floats) of the backward kernels for G lanes per channel.
-template <int G>
+// Shared-memory layout (floats) of the backward kernels for G lanes per channel and Q states
+// per lane (2 or 4: one or two packed pairs).
+template <int G, int Q = kBwdQ>
 struct BwdCfg {
-    static constexpr int kQ = kBwdQ, kNP = G * kQ, kS = kBwdS;
+    static constexpr int kQ = Q, kNP = G * kQ, kS = kBwdS, kP = Q / 2;
+    static_assert(Q == 2 || Q == 4, "2 or 4 states per lane");
     static constexpr int kCpb = kBwdThreads / G;          // channels per CTA
     static constexpr int kTileBC = kS * kNP;              // B or C: [S][G][Q]
     static constexpr int kChan = kCpb * kS;               // per-channel arrays [kCpb][S]
@@ -65,16 +67,16 @@ struct BwdCfg {
     static constexpr int kFloats = kOffPart + 2 * kCpb * kPartCh;
     static_assert(kS % 4 == 0 && (kOffPart % 4) == 0 && (kPartCh % 4) == 0 && (kRow % 4) == 0, "16-byte rows");
 };
-template <int G>
-constexpr size_t bwd_smem_bytes() { return (size_t)BwdCfg<G>::kFloats * sizeof(float); }
+template <int G, int Q>
+constexpr size_t bwd_smem_bytes() { return (size_t)BwdCfg<G, Q>::kFloats * sizeof(float); }
 
 // Raw inputs of one segment [t0, t0+S) of batch row b for the CTA's channels d0 .. d0+kCpb-1,
 // fetched into registers one segment ahead (the loads are in flight while the previous
 // segment computes) and then staged into shared memory (stage). FULL = false: only B, dt
 // and u (the checkpoint pass).
-template <typename IO, int G, bool FULL>
+template <typename IO, int G, int Q, bool FULL>
 struct BwdFetch {
-    using Cfg = BwdCfg<G>;
+    using Cfg = BwdCfg<G, Q>;
     static constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kCpb = Cfg::kCpb;
     static constexpr int kBC = (FULL ? 2 : 1) * kNP * kS, kBCI = (kBC + kBwdThreads - 1) / kBwdThreads;
     static constexpr int kCH = kCpb * kS, kCHI = (kCH + kBwdThreads - 1) / kBwdThreads;
@@ -155,34 +157,46 @@ struct BwdFetch {
 
 // Checkpoint pass: the forward recurrence, h stored before every S-step segment; the next
 // segment's raw inputs are fetched into registers while the current one computes.
-template <int G>
-constexpr size_t bwd_ckpt_smem_bytes() { return (size_t)(BwdCfg<G>::kOffU + BwdCfg<G>::kChan) * sizeof(float); }
+template <int G, int Q>
+constexpr size_t bwd_ckpt_smem_bytes() { return (size_t)(BwdCfg<G, Q>::kOffU + BwdCfg<G, Q>::kChan) * sizeof(float); }
 
-template <typename IO, int G>
+// A lane's Q consecutive floats at p (16-byte or 8-byte aligned) as Q/2 packed pairs.
+template <int P>
+__device__ __forceinline__ void load_pairs(const float *p, float2 (&out)[P]) {
+    if constexpr (P == 2) {
+        const float4 v = *reinterpret_cast<const float4 *>(p);
+        out[0] = make_float2(v.x, v.y);
+        out[1] = make_float2(v.z, v.w);
+    } else {
+        out[0] = *reinterpret_cast<const float2 *>(p);
+    }
+}
+
+template <typename IO, int G, int Q>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdParams p) {
-    using Cfg = BwdCfg<G>;
-    constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb;
+    using Cfg = BwdCfg<G, Q>;
+    constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
     extern __shared__ float4 smem_bwd4[];
     float *sm = reinterpret_cast<float *>(smem_bwd4);
     const int tid = threadIdx.x, g = tid % G, cc = tid / G;
     const int64_t b = blockIdx.y, d0 = (int64_t)blockIdx.x * kCpb, d = d0 + cc;
     const bool valid = d < p.Dm;                 // every thread takes part in the staging
     const int64_t bd = b * p.Dm + (valid ? d : 0);
-    float2 Ap2[2], h2[2];
+    float2 Ap2[kP], h2[kP];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kP; ++k) {
         const int n0 = g + G * 2 * k, n1 = n0 + G;
         Ap2[k] = make_float2((valid && n0 < p.N) ? p.A[(valid ? d : 0) * p.N + n0] * kLog2e : 0.0f,
                              (valid && n1 < p.N) ? p.A[(valid ? d : 0) * p.N + n1] * kLog2e : 0.0f);
         h2[k] = make_float2(0.f, 0.f);
     }
     float *ck = p.ckpt + bd * (int64_t)p.nseg * kNP;
-    BwdFetch<IO, G, false> f;
+    BwdFetch<IO, G, Q, false> f;
     f.fetch(p, b, 0, d0);
     for (int seg = 0; seg < p.nseg; ++seg) {
         if (valid) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < kP; ++k) {
                 ck[(int64_t)seg * kNP + g + G * 2 * k] = h2[k].x;
                 ck[(int64_t)seg * kNP + g + G * (2 * k + 1)] = h2[k].y;
             }
@@ -195,10 +209,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
         for (int i = 0; i < kS; ++i) {
             const float dt = sm[Cfg::kOffDt + cc * kS + i];
             const float x = dt * sm[Cfg::kOffU + cc * kS + i];
-            const float4 bq = *reinterpret_cast<const float4 *>(sm + Cfg::kOffB + (i * G + g) * kQ);
-            const float2 bv[2] = {make_float2(bq.x, bq.y), make_float2(bq.z, bq.w)};
+            float2 bv[kP];
+            load_pairs<kP>(sm + Cfg::kOffB + (i * G + g) * kQ, bv);
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < kP; ++k) {
                 const float2 e = __fmul2_rn(make_float2(dt, dt), Ap2[k]);
                 h2[k] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), h2[k], __fmul2_rn(make_float2(x, x), bv[k]));
             }
@@ -206,10 +220,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
     }
 }
 
-template <typename IO, int G>
-__global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdParams p) {
-    using Cfg = BwdCfg<G>;
-    constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb;
+template <typename IO, int G, int Q>
+__global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(const BwdParams p) {
+    using Cfg = BwdCfg<G, Q>;
+    constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
     // sums over a channel's states: transposed butterfly every G steps (G <= S), else a
     // butterfly per step
     constexpr bool kTransposed = G <= kS;
@@ -232,9 +246,9 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdParam
         c[q] = (nv[q] && p.dlast) ? p.dlast[bd * p.N + n] : 0.0f;
     }
     // as state pairs (q = 2k, 2k+1) for the packed arithmetic
-    float2 An2[2], Ap2[2], c2[2], dA2[2];
+    float2 An2[kP], Ap2[kP], c2[kP], dA2[kP];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kP; ++k) {
         An2[k] = make_float2(An[2 * k], An[2 * k + 1]);
         Ap2[k] = make_float2(An[2 * k] * kLog2e, An[2 * k + 1] * kLog2e);
         c2[k] = make_float2(c[2 * k], c[2 * k + 1]);
@@ -261,16 +275,16 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdParam
         dbias += ddl;
     };
 
-    BwdFetch<IO, G, true> f;
+    BwdFetch<IO, G, Q, true> f;
     f.fetch(p, b, (int64_t)(p.nseg - 1) * kS, d0);
     // the segment's checkpoint, fetched with its inputs one segment ahead
-    auto fetch_ck = [&](int seg, float2 (&out)[2]) {
+    auto fetch_ck = [&](int seg, float2 (&out)[kP]) {
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
+        for (int k = 0; k < kP; ++k)
             out[k] = valid ? make_float2(ck[(int64_t)seg * kNP + g + G * 2 * k], ck[(int64_t)seg * kNP + g + G * (2 * k + 1)])
                            : make_float2(0.f, 0.f);
     };
-    float2 ckn[2];
+    float2 ckn[kP];
     fetch_ck(p.nseg - 1, ckn);
     for (int seg = p.nseg - 1; seg >= 0; --seg) {
         const int64_t t0 = (int64_t)seg * kS;
@@ -278,9 +292,9 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdParam
         f.stage(p, sm, t0, d0);
         __syncthreads();
         // states as pairs (q = 2k, 2k+1): hs[k][0] before the segment, hs[k][i+1] after step t0+i
-        float2 hs[2][kS + 1];
-        hs[0][0] = ckn[0];
-        hs[1][0] = ckn[1];
+        float2 hs[kP][kS + 1];
+#pragma unroll
+        for (int k = 0; k < kP; ++k) hs[k][0] = ckn[k];
         if (seg > 0) {   // the next segment's inputs and checkpoint, in flight meanwhile
             f.fetch(p, b, t0 - kS, d0);
             fetch_ck(seg - 1, ckn);
@@ -289,10 +303,10 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdParam
         for (int i = 0; i < kS; ++i) {
             const float dt = sDt[i];
             const float x = dt * sU[i];
-            const float4 bq = *reinterpret_cast<const float4 *>(sB + i * G * kQ);
-            const float2 bv[2] = {make_float2(bq.x, bq.y), make_float2(bq.z, bq.w)};
+            float2 bv[kP];
+            load_pairs<kP>(sB + i * G * kQ, bv);
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < kP; ++k) {
                 const float2 e = __fmul2_rn(make_float2(dt, dt), Ap2[k]);
                 hs[k][i + 1] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), hs[k][i], __fmul2_rn(make_float2(x, x), bv[k]));
             }
@@ -306,14 +320,13 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdParam
                 const int i = grp * kGrp + s;
                 const float dt = sDt[i], dyh = sDyh[i];
                 const float x = dt * sU[i];
-                const float4 cq4 = *reinterpret_cast<const float4 *>(sC + i * G * kQ);
-                const float4 bq4 = *reinterpret_cast<const float4 *>(sB + i * G * kQ);
-                const float2 cv[2] = {make_float2(cq4.x, cq4.y), make_float2(cq4.z, cq4.w)};
-                const float2 bv[2] = {make_float2(bq4.x, bq4.y), make_float2(bq4.z, bq4.w)};
+                float2 cv[kP], bv[kP];
+                load_pairs<kP>(sC + i * G * kQ, cv);
+                load_pairs<kP>(sB + i * G * kQ, bv);
                 const float2 dt2 = make_float2(dt, dt), dyh2 = make_float2(dyh, dyh), x2 = make_float2(x, x);
                 float2 yh2 = make_float2(0.f, 0.f), du2 = make_float2(0.f, 0.f), dd22 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
+                for (int k = 0; k < kP; ++k) {
                     const float2 e = __fmul2_rn(dt2, Ap2[k]);
                     const float2 a = make_float2(ex2(e.x), ex2(e.y));
                     const float2 lam = __ffma2_rn(dyh2, cv[k], c2[k]);
@@ -400,7 +413,12 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdParam
         dbias += __shfl_xor_sync(0xffffffffu, dbias, o);
     }
     if (!valid) return;
-    const float dA[4] = {dA2[0].x, dA2[0].y, dA2[1].x, dA2[1].y};
+    float dA[kQ];
+#pragma unroll
+    for (int k = 0; k < kP; ++k) {
+        dA[2 * k] = dA2[k].x;
+        dA[2 * k + 1] = dA2[k].y;
+    }
 #pragma unroll
     for (int q = 0; q < kQ; ++q)
         if (nv[q]) atomicAdd(p.dA + dd * p.N + g + G * q, dA[q]);

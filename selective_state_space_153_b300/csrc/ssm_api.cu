@@ -108,6 +108,7 @@ ssm_status_t check_dims(const ssm_dims_t *dims, bool need_L) {
 int sm_count() {
     int dev = 0, n = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    else cudaGetLastError();   // no device (planning on a host without one): the B300's count
     return n;
 }
 
@@ -736,12 +737,26 @@ size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
 }  // extern "C"
 
 namespace {
-// backward lane split: four states per thread, G lanes per channel (the smallest power of
-// two with 4G >= N, at most 32)
-int bwd_lanes(int64_t N) {
-    int g = 1;
-    while (g < 32 && (int64_t)g * kBwdQ < N) g *= 2;
-    return g;
+// backward lane split: Q states per thread, G lanes per channel (the smallest power of two
+// with Q*G >= N: 1-32 at four states, 2-16 at two). Two states per thread for N <= 32 when
+// four give fewer than half a warp per SM sub-partition: the passes are latency-bound, so
+// twice the lanes nearly halve the time there. Measured on B300 (bf16, gate), four vs two:
+// 1 x 768 x 8192 x 16 3.45 vs 2.03 ms, 2 x 512 x 4096 x 8 2.84 vs 1.32 ms; with more channels
+// four win or tie: 1 x 1536 x 4096 x 32 1.36 vs 1.52 ms, 8 x 1536 x 2048 x 16 1.24 vs 1.24 ms.
+struct BwdSplit {
+    int G, Q;
+};
+BwdSplit bwd_split(int64_t batch_dim, int64_t N) {
+    auto lanes = [&](int q) {
+        int g = q == 2 ? 2 : 1;
+        while (g < 32 && (int64_t)g * q < N) g *= 2;
+        return g;
+    };
+    const int forced = plan_override().bwd_states_per_lane;
+    bool two = N <= 32 && batch_dim * lanes(4) < 64 * sm_count();
+    if (forced == 4 || N > 32) two = false;
+    if (forced == 2 && N <= 32) two = true;
+    return two ? BwdSplit{lanes(2), 2} : BwdSplit{lanes(4), 4};
 }
 }  // namespace
 
@@ -750,9 +765,9 @@ extern "C" {
 size_t ssm_selective_scan_bwd_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
-    const int G = bwd_lanes(dims->dstate);
+    const BwdSplit sp = bwd_split(dims->batch * dims->dim, dims->dstate);
     const int64_t nseg = (dims->seqlen + kBwdS - 1) / kBwdS;
-    return (size_t)(dims->batch * dims->dim) * (size_t)nseg * (size_t)(G * kBwdQ) * sizeof(float);
+    return (size_t)(dims->batch * dims->dim) * (size_t)nseg * (size_t)(sp.G * sp.Q) * sizeof(float);
 }
 
 ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const void *delta, const float *A,
@@ -799,7 +814,8 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     BwdParams p{u, delta, z, B, C, dy, A, D, delta_bias, dlast_state, du, ddelta, dA, dB, dC, dD,
                 z ? dz : nullptr, ddelta_bias, static_cast<float *>(ws), d.batch, d.dim, d.seqlen,
                 d.dstate, delta_softplus ? 1 : 0, (int)((d.seqlen + kBwdS - 1) / kBwdS)};
-    const cudaError_t e = launch_bwd(d.io_dtype, bwd_lanes(d.dstate), p, s);
+    const BwdSplit sp = bwd_split(d.batch * d.dim, d.dstate);
+    const cudaError_t e = launch_bwd(d.io_dtype, sp.G, sp.Q, p, s);
     if (allocated) cudaFreeAsync(ws, s);
     if (e == cudaErrorInvalidConfiguration) {
         cudaGetLastError();
@@ -957,6 +973,8 @@ ssm_status_t ssm_set_plan_override(const ssm_plan_override_t *ov) {
             v.pair_states_per_lane != 16)
             return SSM_ERR_UNSUPPORTED;
         if (v.chunks < 0 || v.seq_states_per_lane < 0 || v.seq_lanes_per_channel < 0) return SSM_ERR_SHAPE;
+        if (v.bwd_states_per_lane != 0 && v.bwd_states_per_lane != 2 && v.bwd_states_per_lane != 4)
+            return SSM_ERR_UNSUPPORTED;
         if ((v.seq_states_per_lane != 0 || v.seq_lanes_per_channel != 0) &&
             !seq_plan_supported(v.seq_states_per_lane, v.seq_lanes_per_channel))
             return SSM_ERR_UNSUPPORTED;

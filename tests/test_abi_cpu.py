@@ -174,19 +174,30 @@ def test_plan_override_roundtrip_and_errors(lib):
         got = ssm.get_plan_override()
         assert got.chunks == 7 and got.kernel == 0
         assert _chunks_from_workspace(1, 1536, 131072, 64) == 7
-        bad = ssm.PlanOverride(9, 0, 0, 0, 0, 0, 0, 0)
+        bad = ssm.PlanOverride(9, 0, 0, 0, 0, 0, 0, 0, 0)
         assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
-        bad = ssm.PlanOverride(0, 5, 0, 0, 0, 0, 0, 0)
+        bad = ssm.PlanOverride(0, 5, 0, 0, 0, 0, 0, 0, 0)
         assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
-        bad = ssm.PlanOverride(0, 0, -1, 0, 0, 0, 0, 0)
+        bad = ssm.PlanOverride(0, 0, -1, 0, 0, 0, 0, 0, 0)
         assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_SHAPE
-        bad = ssm.PlanOverride(0, 0, 0, 16, 3, 0, 0, 0)   # a lane split that is not built
+        bad = ssm.PlanOverride(0, 0, 0, 16, 3, 0, 0, 0, 0)   # a lane split that is not built
+        assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
+        bad = ssm.PlanOverride(0, 0, 0, 0, 0, 0, 0, 0, 3)    # backward: 2 or 4 states per lane
         assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_UNSUPPORTED
         assert ssm.get_plan_override().chunks == 7
         assert ov.chunks == 7
     assert ssm.get_plan_override().chunks == 0
     assert ssm.workspace_bytes(1, 1536, 131072, 64) == base
     assert lib.ssm_get_plan_override(None) == ssm.SSM_ERR_NULL
+    # two states per lane in the backward: twice the lanes, the same checkpoint bytes per state
+    d = ssm.dims(8, 1536, 2048, 16, ssm.SSM_BF16)
+    b4 = lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(d))
+    with ssm.plan_override(bwd_states_per_lane=2):
+        assert lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(d)) == b4
+        d64 = ssm.dims(1, 8, 64, 64, ssm.SSM_F32)    # N > 32 keeps four states per lane
+        with ssm.plan_override(bwd_states_per_lane=4):
+            b64 = lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(d64))
+        assert lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(d64)) == b64
     with ssm.plan_override(kernel="tc"):
         # the time-split plan keeps fp32 B/C of the whole sequence in its workspace
         assert ssm.workspace_bytes(1, 1536, 131072, 64) > 2 * 64 * 131072 * 4

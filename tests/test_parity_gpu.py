@@ -159,6 +159,19 @@ def _grad_err(got, ref):
 
 @pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,bias,dlast,a_kind", BWD_CASES)
 def test_backward_gradients(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind):
+    _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind)
+
+
+@pytest.mark.parametrize("q", [2, 4])
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,bias,dlast,a_kind", [c for c in BWD_CASES if c[3] <= 32])
+def test_backward_gradients_forced_split(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind, q):
+    """Both lane splits of the backward on every case that has both (the planner takes two
+    states per lane for small channel counts, four otherwise)."""
+    with ssm.plan_override(bwd_states_per_lane=q):
+        _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind)
+
+
+def _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind):
     from oracle import backward as obwd
     cfg = gen.ScanConfig("bwd", Bt, D, L, N, io=io, gate=gate, dskip=dskip, bias=bias, seed=3 * L + N,
                          a_kind=a_kind)
