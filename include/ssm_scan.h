@@ -314,8 +314,11 @@ size_t ssm_selective_scan_bwd_workspace_bytes(const ssm_dims_t *dims);
  * HOST memory (pinned memory gives the fastest copies). The call copies the inputs to the
  * device, scans, copies y (and last_state) back, and returns when the results are in the
  * host buffers. Device buffers are allocated stream-ordered on `stream` and freed before
- * returning. The channels are processed in blocks so that copies in both directions
- * overlap the scans of neighbouring blocks. Same argument meanings and errors as
+ * returning; the work starts after what the caller queued on `stream`. The channels are
+ * processed in blocks (up to 32 per call, at least 8 MB of input each) that flow through
+ * three streams -- copies in,
+ * scans, copies out -- with three buffer sets, so that each block's copies overlap the
+ * scans of its neighbours. Same argument meanings and errors as
  * ssm_selective_scan_fwd (alignment is not required of host pointers).
  */
 ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u,

@@ -824,6 +824,18 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     return cuda_status(e);
 }
 
+// Channel blocks of the host-buffer entry: up to kHostBlocks per call, each with at least
+// kHostBlockBytes of input. More blocks shorten the exposed head (the first block's input
+// copy) and tail (the last block's scan and output copy). Measured on B300 for
+// 1 x 1536 x 131072 x 64 bf16 (839 MB in, 403 MB out per call; both directions copied
+// concurrently alone take 18.6 ms): 4 / 8 / 16 / 24 / 32 blocks 23.7 / 21.5 / 20.3 / 19.9 /
+// 19.7 ms per call.
+#ifndef SSM_HOST_BLOCKS
+#define SSM_HOST_BLOCKS 32
+#endif
+constexpr int kHostBlocks = SSM_HOST_BLOCKS;
+constexpr size_t kHostBlockBytes = (size_t)8 << 20;
+
 ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, const void *delta,
                                          const float *A, const void *B, const void *C,
                                          const float *D, const void *z, const float *delta_bias,
@@ -841,86 +853,119 @@ ssm_status_t ssm_selective_scan_fwd_host(const ssm_dims_t *dims, const void *u, 
     cudaStream_t s0 = static_cast<cudaStream_t>(stream);
     const size_t esz = io_size(d.io_dtype);
     const size_t L = (size_t)d.seqlen, N = (size_t)d.dstate, Dm = (size_t)d.dim;
-    // blocks of channels within a batch row; two pipelines alternate
-    const size_t nblk_per_row = std::max<size_t>(1, std::min<size_t>(Dm, 4));
-    // blocks start on multiples of 4 channels so that A + d0*N, D + d0 and bias + d0 stay
-    // 16-byte aligned; each batch row of B and C gets its own 256-byte aligned slot
-    const size_t blk = ((Dm + nblk_per_row - 1) / nblk_per_row + 3) / 4 * 4;
+    // Channel blocks (at least one per batch row) flow through three streams: copies in,
+    // scans, copies out. Three buffer sets rotate, so block k's input
+    // copy overlaps block k-1's scan and block k-2's output copy; the first block's input
+    // copy and the last block's scan and output copy are the exposed head and tail.
+    // Blocks start on multiples of 4 channels so that A + d0*N, D + d0 and bias + d0 stay
+    // 16-byte aligned; each batch row of B and C gets its own 256-byte aligned slot.
+    constexpr int kBufs = 3;
+    const size_t row_in_bytes = Dm * L * esz * (z ? 3 : 2);
+    const size_t per_row = std::max<size_t>(
+        1, std::min<size_t>({(Dm + 3) / 4, (row_in_bytes + kHostBlockBytes - 1) / kHostBlockBytes,
+                             (size_t)std::max<int64_t>(1, kHostBlocks / d.batch)}));
+    const size_t blk = ((Dm + per_row - 1) / per_row + 3) / 4 * 4;
     const size_t bc_row = up256(N * L * esz);
-    cudaStream_t ss[2] = {nullptr, nullptr};
-    cudaEvent_t ev_in = nullptr;
+    const size_t row_bytes = blk * L * esz;
+    enum { kIn = 0, kScan = 1, kOut = 2 };
+    cudaStream_t ss[3] = {nullptr, nullptr, nullptr};
+    cudaEvent_t ev_start = nullptr, ev_const = nullptr;
+    cudaEvent_t ev_in[kBufs] = {}, ev_scan[kBufs] = {}, ev_out[kBufs] = {};
     ssm_status_t rc = SSM_OK;
     void *dA = nullptr, *dD = nullptr, *dbias = nullptr, *dB = nullptr, *dC = nullptr;
-    void *bu[2] = {nullptr, nullptr}, *bdl[2] = {nullptr, nullptr}, *bz[2] = {nullptr, nullptr};
-    void *by[2] = {nullptr, nullptr}, *bst[2] = {nullptr, nullptr};
-    const size_t row_bytes = blk * L * esz;
+    void *bu[kBufs] = {}, *bdl[kBufs] = {}, *bz[kBufs] = {}, *by[kBufs] = {}, *bst[kBufs] = {};
     auto CK = [&](cudaError_t e) { if (e != cudaSuccess && rc == SSM_OK) rc = cuda_status(e); return e == cudaSuccess; };
-    CK(cudaStreamCreateWithFlags(&ss[0], cudaStreamNonBlocking));
-    CK(cudaStreamCreateWithFlags(&ss[1], cudaStreamNonBlocking));
-    CK(cudaEventCreateWithFlags(&ev_in, cudaEventDisableTiming));
+    for (auto &q : ss) CK(cudaStreamCreateWithFlags(&q, cudaStreamNonBlocking));
+    CK(cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming));
+    CK(cudaEventCreateWithFlags(&ev_const, cudaEventDisableTiming));
+    for (int i = 0; i < kBufs; ++i) {
+        CK(cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming));
+        CK(cudaEventCreateWithFlags(&ev_scan[i], cudaEventDisableTiming));
+        CK(cudaEventCreateWithFlags(&ev_out[i], cudaEventDisableTiming));
+    }
     if (rc == SSM_OK) {
         CK(cudaMallocAsync(&dA, Dm * N * 4, s0));
         if (D) CK(cudaMallocAsync(&dD, Dm * 4, s0));
         if (delta_bias) CK(cudaMallocAsync(&dbias, Dm * 4, s0));
         CK(cudaMallocAsync(&dB, (size_t)d.batch * bc_row, s0));
         CK(cudaMallocAsync(&dC, (size_t)d.batch * bc_row, s0));
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kBufs; ++i) {
             CK(cudaMallocAsync(&bu[i], row_bytes, s0));
             CK(cudaMallocAsync(&bdl[i], row_bytes, s0));
             if (z) CK(cudaMallocAsync(&bz[i], row_bytes, s0));
             CK(cudaMallocAsync(&by[i], row_bytes, s0));
             if (last_state) CK(cudaMallocAsync(&bst[i], blk * N * 4, s0));
         }
+        // the pipeline starts after the allocations and whatever the caller queued on `stream`
+        CK(cudaEventRecord(ev_start, s0));
+        for (auto &q : ss) CK(cudaStreamWaitEvent(q, ev_start, 0));
     }
     if (rc == SSM_OK) {
-        CK(cudaMemcpyAsync(dA, A, Dm * N * 4, cudaMemcpyHostToDevice, s0));
-        if (D) CK(cudaMemcpyAsync(dD, D, Dm * 4, cudaMemcpyHostToDevice, s0));
-        if (delta_bias) CK(cudaMemcpyAsync(dbias, delta_bias, Dm * 4, cudaMemcpyHostToDevice, s0));
+        cudaStream_t si = ss[kIn];
+        CK(cudaMemcpyAsync(dA, A, Dm * N * 4, cudaMemcpyHostToDevice, si));
+        if (D) CK(cudaMemcpyAsync(dD, D, Dm * 4, cudaMemcpyHostToDevice, si));
+        if (delta_bias) CK(cudaMemcpyAsync(dbias, delta_bias, Dm * 4, cudaMemcpyHostToDevice, si));
         for (int64_t b = 0; b < d.batch; ++b) {
             CK(cudaMemcpyAsync(static_cast<char *>(dB) + b * bc_row, static_cast<const char *>(B) + b * N * L * esz,
-                               N * L * esz, cudaMemcpyHostToDevice, s0));
+                               N * L * esz, cudaMemcpyHostToDevice, si));
             CK(cudaMemcpyAsync(static_cast<char *>(dC) + b * bc_row, static_cast<const char *>(C) + b * N * L * esz,
-                               N * L * esz, cudaMemcpyHostToDevice, s0));
+                               N * L * esz, cudaMemcpyHostToDevice, si));
         }
-        CK(cudaEventRecord(ev_in, s0));
-        CK(cudaStreamWaitEvent(ss[0], ev_in, 0));
-        CK(cudaStreamWaitEvent(ss[1], ev_in, 0));
+        CK(cudaEventRecord(ev_const, si));
+        CK(cudaStreamWaitEvent(ss[kScan], ev_const, 0));
     }
-    size_t it = 0;
+    size_t k = 0;
     for (int64_t b = 0; b < d.batch && rc == SSM_OK; ++b) {
-        for (size_t d0 = 0; d0 < Dm && rc == SSM_OK; d0 += blk, ++it) {
-            const int k = (int)(it & 1);
-            cudaStream_t s = ss[k];
+        for (size_t d0 = 0; d0 < Dm && rc == SSM_OK; d0 += blk, ++k) {
+            const int j = (int)(k % kBufs);
             const size_t nd = std::min(blk, Dm - d0);
             const size_t off = ((size_t)b * Dm + d0) * L * esz;
-            CK(cudaMemcpyAsync(bu[k], static_cast<const char *>(u) + off, nd * L * esz, cudaMemcpyHostToDevice, s));
-            CK(cudaMemcpyAsync(bdl[k], static_cast<const char *>(delta) + off, nd * L * esz, cudaMemcpyHostToDevice, s));
-            if (z) CK(cudaMemcpyAsync(bz[k], static_cast<const char *>(z) + off, nd * L * esz, cudaMemcpyHostToDevice, s));
+            // copies in: buffer j is free once block k-3's scan has read it
+            if (k >= kBufs) CK(cudaStreamWaitEvent(ss[kIn], ev_scan[j], 0));
+            CK(cudaMemcpyAsync(bu[j], static_cast<const char *>(u) + off, nd * L * esz, cudaMemcpyHostToDevice, ss[kIn]));
+            CK(cudaMemcpyAsync(bdl[j], static_cast<const char *>(delta) + off, nd * L * esz, cudaMemcpyHostToDevice,
+                               ss[kIn]));
+            if (z) CK(cudaMemcpyAsync(bz[j], static_cast<const char *>(z) + off, nd * L * esz, cudaMemcpyHostToDevice,
+                                      ss[kIn]));
+            CK(cudaEventRecord(ev_in[j], ss[kIn]));
+            // scan: after its inputs, and after block k-3's output copy has read y and the state
+            CK(cudaStreamWaitEvent(ss[kScan], ev_in[j], 0));
+            if (k >= kBufs) CK(cudaStreamWaitEvent(ss[kScan], ev_out[j], 0));
+            if (rc != SSM_OK) break;
             ssm_dims_t sub{1, (int64_t)nd, d.seqlen, d.dstate, d.io_dtype};
             const size_t boff = (size_t)b * bc_row;
-            // the two pipelines overlap on the GPU: each block's chunk carries get a stream-ordered
-            // allocation of its own, never the registered workspace (which they would share)
-            ssm_status_t r = run_scan(
-                &sub, bu[k], bdl[k], static_cast<float *>(dA) + d0 * N, static_cast<char *>(dB) + boff,
-                static_cast<char *>(dC) + boff, D ? static_cast<float *>(dD) + d0 : nullptr, z ? bz[k] : nullptr,
-                delta_bias ? static_cast<float *>(dbias) + d0 : nullptr, delta_softplus, by[k],
-                last_state ? static_cast<float *>(bst[k]) : nullptr, nullptr, 0, true, s);
+            // the scans are queued on one stream; their chunk carries are stream-ordered
+            // allocations (never the registered workspace)
+            const ssm_status_t r = run_scan(
+                &sub, bu[j], bdl[j], static_cast<float *>(dA) + d0 * N, static_cast<char *>(dB) + boff,
+                static_cast<char *>(dC) + boff, D ? static_cast<float *>(dD) + d0 : nullptr, z ? bz[j] : nullptr,
+                delta_bias ? static_cast<float *>(dbias) + d0 : nullptr, delta_softplus, by[j],
+                last_state ? static_cast<float *>(bst[j]) : nullptr, nullptr, 0, true, ss[kScan]);
             if (r != SSM_OK) { rc = r; break; }
-            CK(cudaMemcpyAsync(static_cast<char *>(y) + off, by[k], nd * L * esz, cudaMemcpyDeviceToHost, s));
+            CK(cudaEventRecord(ev_scan[j], ss[kScan]));
+            // copies out
+            CK(cudaStreamWaitEvent(ss[kOut], ev_scan[j], 0));
+            CK(cudaMemcpyAsync(static_cast<char *>(y) + off, by[j], nd * L * esz, cudaMemcpyDeviceToHost, ss[kOut]));
             if (last_state)
-                CK(cudaMemcpyAsync(last_state + ((size_t)b * Dm + d0) * N, bst[k], nd * N * 4, cudaMemcpyDeviceToHost, s));
+                CK(cudaMemcpyAsync(last_state + ((size_t)b * Dm + d0) * N, bst[j], nd * N * 4, cudaMemcpyDeviceToHost,
+                                   ss[kOut]));
+            CK(cudaEventRecord(ev_out[j], ss[kOut]));
         }
     }
-    for (int i = 0; i < 2; ++i)
-        if (ss[i]) CK(cudaStreamSynchronize(ss[i]));
-    // release everything on s0 after both pipelines finished
-    void *all[] = {dA, dD, dbias, dB, dC, bu[0], bu[1], bdl[0], bdl[1], bz[0], bz[1], by[0], by[1], bst[0], bst[1]};
+    for (auto &q : ss)
+        if (q) CK(cudaStreamSynchronize(q));
+    // release everything on s0 after the pipeline finished
+    void *all[] = {dA, dD, dbias, dB, dC, bu[0], bu[1], bu[2], bdl[0], bdl[1], bdl[2], bz[0], bz[1], bz[2],
+                   by[0], by[1], by[2], bst[0], bst[1], bst[2]};
     for (void *q : all)
         if (q) cudaFreeAsync(q, s0);
     CK(cudaStreamSynchronize(s0));
-    for (int i = 0; i < 2; ++i)
-        if (ss[i]) cudaStreamDestroy(ss[i]);
-    if (ev_in) cudaEventDestroy(ev_in);
+    for (auto &q : ss)
+        if (q) cudaStreamDestroy(q);
+    cudaEvent_t evs[] = {ev_start, ev_const, ev_in[0], ev_in[1], ev_in[2], ev_scan[0], ev_scan[1], ev_scan[2],
+                         ev_out[0], ev_out[1], ev_out[2]};
+    for (cudaEvent_t e : evs)
+        if (e) cudaEventDestroy(e);
     return rc;
 }
 

@@ -429,6 +429,23 @@ def test_host_buffer_entry(cfg):
     compare_scan(inp, yh, hh)
 
 
+def test_host_buffer_entry_many_blocks():
+    """Enough input bytes for several channel blocks per batch row (8 blocks through three
+    rotating buffer sets): every block boundary and every buffer reuse is checked, on channels
+    sampled at the block edges, against the oracle, and all of y against the device entry."""
+    cfg = gen.ScanConfig("hb", 2, 256, 16384, 16, io="bf16", gate=True, dskip="normal", seed=21, a_kind="random")
+    inp = gen.scan_inputs(cfg)
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    yh, hh = ssm.selective_scan_fwd_host(pin["u"], pin["delta"], pin["A"], pin["B"], pin["C"], D=pin["D"],
+                                         z=pin["z"], delta_bias=pin["delta_bias"], return_last_state=True)
+    edges = [(b, d) for b in (0, 1) for d in (0, 63, 64, 127, 128, 191, 192, 255)]
+    compare_scan(inp, yh, hh, channels=edges)
+    yd, hd = gpu_scan(inp)
+    ref = yd.float().cpu()
+    assert float((yh.float() - ref).abs().max()) <= 2e-2 * max(float(ref.abs().max()), 1.0)
+    assert torch.allclose(hh, hd.cpu(), rtol=1e-4, atol=1e-5)
+
+
 # ---- decode ---------------------------------------------------------------------------------
 def _decode_gpu(inp, steps):
     g = to_dev(inp)
