@@ -182,9 +182,10 @@ ssm_status_t ssm_set_workspace(void *dev_ptr, size_t bytes);
  * work ticket and per-segment carry flags) must be zero when that kernel starts; every
  * call clears them on `stream` (cudaMemsetAsync) before its launch. Everything else in
  * the scratch is written before it is read within the call.
- * First use: the first call on each device resolves the scratch's device address with
- * cudaGetSymbolAddress, which may load the library's module. Make that first call before
- * any stream capture begins. A failure there returns SSM_ERR_CUDA.
+ * First use: the first call in each device context (and again after the context is reset)
+ * resolves the scratch's device address with cudaGetSymbolAddress, which may load the
+ * library's module. Make that first call before any stream capture begins. A failure there
+ * returns SSM_ERR_CUDA.
  * Concurrency: there is ONE scratch per device. Calls whose GPU work overlaps on the same
  * device race on it, whichever streams or host threads issue them, and give wrong results.
  * Queue such calls on one stream, or order them with events.

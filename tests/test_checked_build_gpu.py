@@ -117,22 +117,24 @@ def test_conv_front_checked(checked):
     compare_scan(ref, y, h)
 
 
-@pytest.mark.parametrize("N,io,unaligned", [(16, "bf16", False), (5, "f32", False), (64, "bf16", True)])
-def test_decode_checked(checked, N, io, unaligned):
+@pytest.mark.parametrize("N,io,unaligned,Dm", [(16, "bf16", False, 50), (5, "f32", False, 50), (64, "bf16", True, 50),
+                                               (16, "bf16", False, 264), (64, "f32", False, 76)])
+def test_decode_checked(checked, N, io, unaligned, Dm):
     """Wide (16-byte B/C), element-wise (B/C rows at an odd offset) and scalar (N % 4 != 0)
-    state-update kernels, with guard words around the state and y."""
-    inp = gen.decode_inputs(gen.DECODE, Bt=3, D=50, N=N, gate=True, dskip="ones", steps=3, a_kind="random")
+    state-update kernels, with guard words around the state and y, on channel counts that
+    leave a partial last block."""
+    inp = gen.decode_inputs(gen.DECODE, Bt=3, D=Dm, N=N, gate=True, dskip="ones", steps=3, a_kind="random")
     if io == "f32":
         for k in ("x", "dt", "B", "C", "z"):
             inp[k] = inp[k].float()
     g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    sbig, st = _guarded((3, 50, N), torch.float32)
+    sbig, st = _guarded((3, Dm, N), torch.float32)
     st.copy_(g["state0"])
     f = gen.as_f64
     so = f(inp["state0"])
     sm = np.abs(so)
     for s in range(3):
-        ybig, y = _guarded((3, 50), g["x"].dtype)
+        ybig, y = _guarded((3, Dm), g["x"].dtype)
         Bv, Cv = g["B"][s], g["C"][s]
         if unaligned:
             bufs = []

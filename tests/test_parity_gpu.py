@@ -446,6 +446,47 @@ def test_host_buffer_entry_many_blocks():
     assert torch.allclose(hh, hd.cpu(), rtol=1e-4, atol=1e-5)
 
 
+def test_cuda_graph_capture_and_replay():
+    """The device entry points queue only kernels (and, given a workspace, nothing else) on
+    the caller's stream, so a CUDA graph can capture them: a chunked scan with a caller
+    workspace followed by three recurrent steps from its final state, captured once (after
+    one eager call has set the kernels' attributes) and replayed, gives the eager results
+    bit for bit."""
+    cfg = gen.ScanConfig("graph", 1, 96, 8192, 16, io="bf16", gate=True, dskip="normal", seed=31, a_kind="random")
+    inp = gen.scan_inputs(cfg)
+    dec = gen.decode_inputs(gen.DECODE, Bt=1, D=96, N=16, gate=True, dskip="ones", steps=3, a_kind="random")
+    g = to_dev(inp)
+    dg = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in dec.items()}
+    ws = torch.empty(max(ssm.workspace_bytes(1, 96, 8192, 16), 16), dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(g["u"])
+    h = torch.empty((1, 96, 16), dtype=torch.float32, device="cuda")
+    ys = torch.empty((3, 1, 96), dtype=torch.bfloat16, device="cuda")
+
+    def work(stream):
+        ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                               delta_bias=g["delta_bias"], y=y, last_state=h, workspace=ws, stream=stream)
+        for s in range(3):
+            ssm.state_update(h, dg["x"][s], dg["dt"][s], g["A"], dg["B"][s], dg["C"][s], D=g["D"], z=dg["z"][s],
+                             y=ys[s], stream=stream)
+
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        work(side)
+    torch.cuda.synchronize()
+    eager = (y.clone(), h.clone(), ys.clone())
+    assert ssm.workspace_bytes(1, 96, 8192, 16) > 0        # the captured scan is chunked
+    graph = torch.cuda.CUDAGraph()
+    y.zero_(); h.zero_(); ys.zero_()
+    with torch.cuda.graph(graph, stream=side):
+        work(side)
+    for _ in range(2):
+        y.zero_(); h.zero_(); ys.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, eager[0]) and torch.equal(h, eager[1]) and torch.equal(ys, eager[2])
+    assert ssm.stream_status() == ssm.SSM_OK
+
+
 # ---- decode ---------------------------------------------------------------------------------
 def _decode_gpu(inp, steps):
     g = to_dev(inp)
