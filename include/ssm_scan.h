@@ -109,6 +109,11 @@ typedef struct {
  * small; nothing is allocated then), else one the library allocates stream-ordered
  * (cudaMallocAsync / cudaFreeAsync on `stream`). ssm_selective_scan_fwd_ws takes a
  * workspace per call instead.
+ * Rows whose byte length (seqlen * io size) is not a multiple of 16: the default kernel moves
+ * rows in 16-byte pieces, so u, delta, z, B and C are first copied to a padded row stride in
+ * the workspace and y comes back through a padded buffer (the workspace then also holds
+ * those copies). With a workspace too small for them (a registered or caller workspace, or
+ * the no-allocation entry's scratch), such rows take the slower element-wise kernel.
  */
 ssm_status_t ssm_selective_scan_fwd(const ssm_dims_t *dims, const void *u, const void *delta,
                                     const float *A, const void *B, const void *C,
@@ -116,7 +121,8 @@ ssm_status_t ssm_selective_scan_fwd(const ssm_dims_t *dims, const void *u, const
                                     int delta_softplus, void *y, float *last_state,
                                     void *stream);
 
-/* Bytes of device workspace ssm_selective_scan_fwd_ws needs for `dims` (0 if none). */
+/* Bytes of device workspace ssm_selective_scan_fwd_ws needs for `dims` (0 if none): the
+ * default plan's, including the padded row copies of rows that are not 16-byte multiples. */
 size_t ssm_selective_scan_workspace_bytes(const ssm_dims_t *dims);
 
 /* As ssm_selective_scan_fwd, with a caller-owned device workspace (16-byte aligned, at
@@ -227,9 +233,9 @@ typedef enum {
  * ssm_selective_scan_fwd with the discretisation chosen (ssm_disc_t). `workspace` may be
  * NULL (the library then allocates stream-ordered, as ssm_selective_scan_fwd), or a
  * caller-owned buffer as for ssm_selective_scan_fwd_ws. The zero-order hold runs on the
- * default channel-pair kernel, i.e. for rows whose byte length (seqlen * io size) is a
- * multiple of 16; other shapes return SSM_ERR_UNSUPPORTED (as does an unknown
- * `discretization`). B_bar*u is formed as dt*u*B * phi(dt*A), phi(x) = (e^x - 1)/x, with a
+ * default channel-pair kernel; rows that are not 16-byte multiples go through the padded
+ * copies described at ssm_selective_scan_fwd, and a workspace too small for them returns
+ * SSM_ERR_UNSUPPORTED (as does an unknown `discretization`). B_bar*u is formed as dt*u*B * phi(dt*A), phi(x) = (e^x - 1)/x, with a
  * cubic polynomial for |x| < 1/8 and (exp(x) - 1)/x otherwise: relative error of phi about
  * 2e-6 at most, no extra exponential per element. Other arguments and errors: as
  * ssm_selective_scan_fwd / ssm_selective_scan_fwd_ws.
@@ -262,8 +268,10 @@ ssm_status_t ssm_state_update_disc(const ssm_dims_t *dims, float *state, const v
  *   conv_width  K, 1..4 (SSM_ERR_UNSUPPORTED otherwise).
  *   workspace   NULL (stream-ordered allocation by the library) or a caller buffer of at
  *               least ssm_conv_selective_scan_workspace_bytes(dims) bytes.
- * Runs on the channel-pair kernel: rows whose byte length is not a multiple of 16 return
- * SSM_ERR_UNSUPPORTED. Other arguments, layouts and errors: as ssm_selective_scan_fwd.
+ * Runs on the channel-pair kernel; rows whose byte length is not a multiple of 16 go through
+ * padded copies in the workspace (ssm_conv_selective_scan_workspace_bytes counts them), and
+ * a caller or registered workspace too small for them returns SSM_ERR_WORKSPACE. Other
+ * arguments, layouts and errors: as ssm_selective_scan_fwd.
  */
 ssm_status_t ssm_conv_selective_scan_fwd(const ssm_dims_t *dims, const void *x,
                                          const float *conv_w, const float *conv_b,

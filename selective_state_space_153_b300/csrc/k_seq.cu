@@ -27,6 +27,44 @@ __global__ void chunk_combine_kernel(const float *__restrict__ A, const float *_
     }
 }
 
+// Rows of `len` io elements at stride src_ld copied to stride dst_ld, elements len..dst_ld-1
+// of each destination row zeroed: puts rows whose byte length is not a multiple of 16 on
+// 16-byte boundaries for the channel-pair kernel (and takes its y rows back). A thread moves
+// one 16-byte piece of a destination row: 16-byte loads and stores on whichever side is
+// aligned, element by element on the other. Rows on blockIdx.y (+ k*gridDim.y).
+template <typename IO>
+__global__ void restride_kernel(const IO *__restrict__ src, int64_t src_ld, IO *__restrict__ dst, int64_t dst_ld,
+                                int64_t rows, int64_t len) {
+    constexpr int E = 16 / (int)sizeof(IO);
+    const int64_t pieces = (dst_ld + E - 1) / E;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const IO *s = src + r * src_ld;
+        IO *d = dst + r * dst_ld;
+        const bool dvec = (reinterpret_cast<uintptr_t>(d) & 15u) == 0;
+        for (int64_t pc = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; pc < pieces;
+             pc += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t t0 = pc * E;
+            union {
+                uint4 q;
+                IO e[E];
+            } v;
+            if ((reinterpret_cast<uintptr_t>(s + t0) & 15u) == 0 && t0 + E <= len) {
+                v.q = __ldg(reinterpret_cast<const uint4 *>(s + t0));
+            } else {
+#pragma unroll
+                for (int k = 0; k < E; ++k) v.e[k] = t0 + k < len ? s[t0 + k] : IO(0.0f);
+            }
+            if (dvec && t0 + E <= dst_ld) {
+                *reinterpret_cast<uint4 *>(d + t0) = v.q;
+            } else {
+#pragma unroll
+                for (int k = 0; k < E; ++k)
+                    if (t0 + k < dst_ld) d[t0 + k] = v.e[k];
+            }
+        }
+    }
+}
+
 namespace {
 using bf16 = __nv_bfloat16;
 
@@ -90,6 +128,20 @@ cudaError_t launch_chunk_combine(const float *A, const float *agg_h, const float
     const int64_t total = BD * npad;
     chunk_combine_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(A, agg_h, agg_s, hin, BD, Dm, N, npad,
                                                                           nchunks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_restride(ssm_dtype_t io, const void *src, int64_t src_ld, void *dst, int64_t dst_ld, int64_t rows,
+                            int64_t len, cudaStream_t s) {
+    if (rows <= 0 || dst_ld <= 0) return cudaSuccess;
+    const int64_t pieces = (dst_ld * (int64_t)(io == SSM_BF16 ? 2 : 4) + 15) / 16;
+    const dim3 grid((unsigned)std::min<int64_t>((pieces + 255) / 256, 64), (unsigned)std::min<int64_t>(rows, 65535));
+    if (io == SSM_BF16)
+        restride_kernel<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16 *>(src), src_ld, static_cast<bf16 *>(dst),
+                                                   dst_ld, rows, len);
+    else
+        restride_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(src), src_ld, static_cast<float *>(dst),
+                                                    dst_ld, rows, len);
     return cudaGetLastError();
 }
 

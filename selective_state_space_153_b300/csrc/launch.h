@@ -51,6 +51,9 @@ cudaError_t launch_seq(ssm_dtype_t io, int nper, int g, bool agg, bool aligned, 
 bool seq_plan_supported(int nper, int g);
 cudaError_t launch_chunk_combine(const float *A, const float *agg_h, const float *agg_s, float *hin,
                                  int64_t BD, int64_t Dm, int64_t N, int npad, int nchunks, cudaStream_t s);
+// rows of `len` io elements from stride src_ld to stride dst_ld (destination tails zeroed)
+cudaError_t launch_restride(ssm_dtype_t io, const void *src, int64_t src_ld, void *dst, int64_t dst_ld, int64_t rows,
+                            int64_t len, cudaStream_t s);
 cudaError_t launch_zero_f32(float *p, int64_t n, cudaStream_t s);
 
 // persistent time-split scans (scan_tc.cuh / scan_tp.cuh): B/C preparation, then the kernel

@@ -198,7 +198,7 @@ scan_pair_kernel(const SeqParams p) {
     const int64_t BD = p.Bt * p.Dm;
     SSM_POISON_SMEM(smem);
     // array extents in bytes (used by the checked build's bounds checks; dead code otherwise)
-    const uint64_t kIoB = (uint64_t)p.Bt * p.Dm * p.L * sizeof(IO), kBcB = (uint64_t)p.Bt * p.N * p.L * sizeof(IO);
+    const uint64_t kIoB = (uint64_t)p.Bt * p.Dm * p.ld * sizeof(IO), kBcB = (uint64_t)p.Bt * p.N * p.ld * sizeof(IO);
     const uint64_t kAB = (uint64_t)p.Dm * p.N * 4, kDB = (uint64_t)p.Dm * 4;
     const uint64_t kCarryB = (uint64_t)p.nchunks * BD * p.npad * 4, kSumB = (uint64_t)p.nchunks * BD * 4;
     (void)kIoB; (void)kBcB; (void)kAB; (void)kDB; (void)kCarryB; (void)kSumB;
@@ -316,12 +316,12 @@ scan_pair_kernel(const SeqParams p) {
             const int kind = row / kCh, cc = row % kCh;
             if (d0 + cc >= p.Dm || (kind == 2 && !has_z)) return nullptr;
             const IO *base = kind == 0 ? gU : (kind == 1 ? gDelta : gZ);
-            return base + ((b * p.Dm + d0 + cc) * p.L + l_begin + e0_me);
+            return base + ((b * p.Dm + d0 + cc) * p.ld + l_begin + e0_me);
         }
         if (row >= kRows) return nullptr;
         const int r = row - kRowB, kind = r / kNP, n = r % kNP;
         if (n >= N) return nullptr;
-        return (kind == 0 ? gB : gC) + ((b * p.N + n) * p.L + l_begin + e0_me);
+        return (kind == 0 ? gB : gC) + ((b * p.N + n) * p.ld + l_begin + e0_me);
     };
     const IO *isrc[kPre ? kItems : 1];
     if constexpr (kPre) {
@@ -478,7 +478,7 @@ scan_pair_kernel(const SeqParams p) {
         for (int k = 0; k < kYItems; ++k) {
             const int i = tid + k * Cfg::kThreads, cc = i / kPieces;
             ydst[k] = (!AGG && i < kCh * kPieces && d0 + cc < p.Dm)
-                          ? gY + ((b * p.Dm + d0 + cc) * p.L + l_begin + e0_me) : nullptr;
+                          ? gY + ((b * p.Dm + d0 + cc) * p.ld + l_begin + e0_me) : nullptr;
         }
     }
     auto store_y = [&](int j) {
@@ -503,7 +503,7 @@ scan_pair_kernel(const SeqParams p) {
             for (int i = tid; i < kCh * kPieces; i += Cfg::kThreads) {
                 const int cc = i / kPieces;
                 if (d0 + cc >= p.Dm) continue;
-                put(gY + ((b * p.Dm + d0 + cc) * p.L + l_begin + e0_me) + toff, ys + (size_t)cc * kRS + e0_me);
+                put(gY + ((b * p.Dm + d0 + cc) * p.ld + l_begin + e0_me) + toff, ys + (size_t)cc * kRS + e0_me);
             }
         }
     };
@@ -523,7 +523,7 @@ scan_pair_kernel(const SeqParams p) {
             for (int k = 0; k < 3; ++k) {
                 const int64_t s = l_begin - 3 + k;
                 st_chk_s(smem, sHalo + i * 4 + k,
-                         (okc && s >= 0) ? io_traits<IO>::to_f(ld_chk_g(gU, kIoB, gU + (b * p.Dm + d0 + i) * p.L + s)) : 0.0f);
+                         (okc && s >= 0) ? io_traits<IO>::to_f(ld_chk_g(gU, kIoB, gU + (b * p.Dm + d0 + i) * p.ld + s)) : 0.0f);
             }
         }
     }

@@ -39,6 +39,7 @@ struct SeqParams {
     void *y;
     float *last_state;
     int64_t Bt, Dm, L, N;
+    int64_t ld;         // channel-pair kernel: row stride (elements) of u, delta, z, y, B, C (>= L)
     int softplus;
     int64_t chunk_len;  // multiple of the tile length except possibly the last chunk
     int nchunks;

@@ -311,11 +311,17 @@ int pair_gp(int64_t N, int ks) {
     return gp;
 }
 
-PairPlan plan_pair(const ssm_dims_t &d, const ssm_plan_override_t &ov, bool conv = false) {
+// restrided = the rows will be copied to a padded stride first (rows that are not 16-byte
+// multiples), so their own length need not be one
+PairPlan plan_pair(const ssm_dims_t &d, const ssm_plan_override_t &ov, bool conv = false, bool restrided = false) {
     PairPlan p;
     if (ov.kernel == SSM_KERNEL_SEQ || ov.kernel == SSM_KERNEL_TC || ov.kernel == SSM_KERNEL_TP) return p;
     const size_t esz = io_size(d.io_dtype);
-    if (((size_t)d.seqlen * esz) % 16 != 0 || d.dstate > 128) return p;   // rows move in 16-byte pieces
+    if (d.dstate > 128) return p;
+    if (((size_t)d.seqlen * esz) % 16 != 0) {   // rows move in 16-byte pieces
+        // a forced sequential-lane split keeps ragged rows on that kernel
+        if (!restrided || ov.seq_states_per_lane != 0 || ov.seq_lanes_per_channel != 0) return p;
+    }
     const int64_t N = d.dstate, BD = d.batch * d.dim, sms = sm_count();
     // eight states per lane and channel, unless four give the GPU at least one warp per SM
     // sub-partition where eight do not (few channels with few states)
@@ -401,7 +407,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
                            const void *B, const void *C, const float *D, const void *z, const float *delta_bias,
                            int delta_softplus, void *y, float *last_state, void *workspace, size_t ws_bytes,
                            bool may_alloc, cudaStream_t s, int zoh, const float *conv_w = nullptr,
-                           const float *conv_b = nullptr, int conv_k = 0) {
+                           const float *conv_b = nullptr, int conv_k = 0, int64_t ld = 0) {
     bool allocated = false;
     ssm_status_t st = acquire_workspace(&workspace, ws_bytes, pair_workspace_bytes(d, pl), may_alloc, s, &allocated);
     if (st != SSM_OK) return st;
@@ -409,6 +415,7 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
     prm.u = u; prm.delta = delta; prm.z = z; prm.B = B; prm.C = C;
     prm.A = A; prm.D = D; prm.bias = delta_bias; prm.y = y; prm.last_state = last_state;
     prm.Bt = d.batch; prm.Dm = d.dim; prm.L = d.seqlen; prm.N = d.dstate;
+    prm.ld = ld > 0 ? ld : d.seqlen;
     prm.softplus = delta_softplus ? 1 : 0;
     prm.chunk_len = pl.chunk_len; prm.nchunks = pl.nchunks;
     prm.npad = pl.np;
@@ -437,12 +444,78 @@ ssm_status_t run_scan_pair(const ssm_dims_t &d, const PairPlan &pl, const void *
     return cuda_status(e);
 }
 
+// Rows whose byte length is not a multiple of 16: the channel-pair kernel runs on copies of
+// u, delta, z, B, C at the padded stride ld (L rounded up to 16 bytes) in the workspace, and
+// its y comes back through a padded buffer. The workspace holds [u | delta | z | B | C | y |
+// chunk carries]; the z slot is kept even without z, so the size depends on the shape only.
+struct RaggedPlan {
+    int64_t ld = 0;
+    size_t off_dl = 0, off_z = 0, off_b = 0, off_c = 0, off_y = 0, off_carry = 0, bytes = 0;
+};
+RaggedPlan plan_ragged(const ssm_dims_t &d, const PairPlan &pp) {
+    RaggedPlan r;
+    const size_t esz = io_size(d.io_dtype), epp = 16 / esz;
+    r.ld = (int64_t)(((size_t)d.seqlen + epp - 1) / epp * epp);
+    const size_t io = up256((size_t)(d.batch * d.dim) * (size_t)r.ld * esz);
+    const size_t bc = up256((size_t)(d.batch * d.dstate) * (size_t)r.ld * esz);
+    r.off_dl = io;
+    r.off_z = 2 * io;
+    r.off_b = 3 * io;
+    r.off_c = r.off_b + bc;
+    r.off_y = r.off_c + bc;
+    r.off_carry = r.off_y + io;
+    r.bytes = r.off_carry + pair_workspace_bytes(d, pp);
+    return r;
+}
+
+ssm_status_t run_scan_ragged(const ssm_dims_t &d, const PairPlan &pp, const RaggedPlan &rg, const void *u,
+                             const void *delta, const float *A, const void *B, const void *C, const float *D,
+                             const void *z, const float *delta_bias, int delta_softplus, void *y, float *last_state,
+                             void *workspace, size_t ws_bytes, bool may_alloc, cudaStream_t s, int zoh,
+                             const float *conv_w = nullptr, const float *conv_b = nullptr, int conv_k = 0) {
+    bool allocated = false;
+    ssm_status_t st = acquire_workspace(&workspace, ws_bytes, rg.bytes, may_alloc, s, &allocated);
+    if (st != SSM_OK) return st;
+    char *w = static_cast<char *>(workspace);
+    const int64_t BD = d.batch * d.dim, BN = d.batch * d.dstate, L = d.seqlen;
+    cudaError_t e = launch_restride(d.io_dtype, u, L, w, rg.ld, BD, L, s);
+    if (e == cudaSuccess) e = launch_restride(d.io_dtype, delta, L, w + rg.off_dl, rg.ld, BD, L, s);
+    if (e == cudaSuccess && z) e = launch_restride(d.io_dtype, z, L, w + rg.off_z, rg.ld, BD, L, s);
+    if (e == cudaSuccess) e = launch_restride(d.io_dtype, B, L, w + rg.off_b, rg.ld, BN, L, s);
+    if (e == cudaSuccess) e = launch_restride(d.io_dtype, C, L, w + rg.off_c, rg.ld, BN, L, s);
+    if (e == cudaSuccess) {
+        st = run_scan_pair(d, pp, w, w + rg.off_dl, A, w + rg.off_b, w + rg.off_c, D, z ? w + rg.off_z : nullptr,
+                           delta_bias, delta_softplus, w + rg.off_y, last_state, w + rg.off_carry,
+                           rg.bytes - rg.off_carry, false, s, zoh, conv_w, conv_b, conv_k, rg.ld);
+        if (st == SSM_OK) e = launch_restride(d.io_dtype, w + rg.off_y, rg.ld, y, L, BD, L, s);
+    }
+    if (allocated) cudaFreeAsync(workspace, s);
+    if (st != SSM_OK) return st;
+    return cuda_status(e);
+}
+
+// The restrided channel-pair plan for `d` when its rows are not 16-byte multiples and the
+// workspace allows it (the library may allocate, or the given workspace is large enough).
+bool use_ragged(const ssm_dims_t &d, const ssm_plan_override_t &ov, bool conv, void *workspace, size_t ws_bytes,
+                bool may_alloc, PairPlan *pp, RaggedPlan *rg) {
+    if (((size_t)d.seqlen * io_size(d.io_dtype)) % 16 == 0) return false;
+    *pp = plan_pair(d, ov, conv, true);
+    if (!pp->use) return false;
+    *rg = plan_ragged(d, *pp);
+    return may_alloc || (workspace != nullptr && ws_bytes >= rg->bytes);
+}
+
 // Workspace bytes the scan of `d` needs under the current plan (0 if none).
-size_t scan_workspace_bytes(const ssm_dims_t &d) {
+// small = the plan without the restrided rows (what a workspace too small for them gets).
+size_t scan_workspace_bytes(const ssm_dims_t &d, bool small = false) {
     if (d.batch == 0 || d.dim == 0 || d.seqlen == 0) return 0;
     const ssm_plan_override_t ov = plan_override();
     const PairPlan pp = plan_pair(d, ov);
     if (pp.use) return pair_workspace_bytes(d, pp);
+    if (!small) {
+        const PairPlan pr = plan_pair(d, ov, false, true);
+        if (pr.use) return plan_ragged(d, pr).bytes;
+    }
     const TcPlan tp = plan_tc(d, ov);
     if (tp.use) return tp.bytes;
     return seq_workspace_bytes(d, plan_scan(d, ov));
@@ -463,6 +536,11 @@ ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, 
     if (pp.use)
         return run_scan_pair(d, pp, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, workspace,
                              ws_bytes, may_alloc, s, zoh);
+    PairPlan pr;
+    RaggedPlan rg;
+    if (use_ragged(d, ov, false, workspace, ws_bytes, may_alloc, &pr, &rg))
+        return run_scan_ragged(d, pr, rg, u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
+                               workspace, ws_bytes, may_alloc, s, zoh);
     if (zoh) return SSM_ERR_UNSUPPORTED;   // the zero-order hold runs on the channel-pair kernel only
     const TcPlan tp = plan_tc(d, ov);
     if (tp.use) {
@@ -482,7 +560,7 @@ ssm_status_t run_scan(const ssm_dims_t *dims, const void *u, const void *delta, 
     SeqParams prm{};
     prm.u = u; prm.delta = delta; prm.z = z; prm.B = B; prm.C = C;
     prm.A = A; prm.D = D; prm.bias = delta_bias; prm.y = y; prm.last_state = last_state;
-    prm.Bt = d.batch; prm.Dm = d.dim; prm.L = d.seqlen; prm.N = d.dstate;
+    prm.Bt = d.batch; prm.Dm = d.dim; prm.L = d.seqlen; prm.N = d.dstate; prm.ld = d.seqlen;
     prm.softplus = delta_softplus ? 1 : 0;
     prm.chunk_len = pl.chunk_len; prm.nchunks = pl.nchunks;
     const int cpc = kSeqWarps * 32 / pl.g;
@@ -625,7 +703,8 @@ ssm_status_t ssm_selective_scan_fwd_noalloc(const ssm_dims_t *dims, const void *
                                             void *stream) {
     ssm_status_t st = scan_checks(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
     if (st != SSM_OK) return st;
-    const size_t need = scan_workspace_bytes(*dims);
+    size_t need = scan_workspace_bytes(*dims);
+    if (need > SSM_SCRATCH_MAX_BYTES) need = scan_workspace_bytes(*dims, true);   // without restrided rows
     if (need > SSM_SCRATCH_MAX_BYTES) return SSM_ERR_WORKSPACE;
     void *scratch = nullptr;
     if (need > 0) {
@@ -722,16 +801,30 @@ ssm_status_t ssm_conv_selective_scan_fwd(const ssm_dims_t *dims, const void *x, 
                         w.may_alloc, static_cast<cudaStream_t>(stream));
     if (conv_w == nullptr) return SSM_ERR_NULL;
     if (!aligned_to(conv_w, 4)) return SSM_ERR_ALIGN;
-    const PairPlan pp = plan_pair(d, plan_override(), true);
-    if (!pp.use) return SSM_ERR_UNSUPPORTED;   // the conv front runs on the channel-pair kernel only
-    return run_scan_pair(d, pp, x, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, w.ptr, w.bytes,
-                         w.may_alloc, static_cast<cudaStream_t>(stream), 0, conv_w, conv_b, conv_width);
+    const ssm_plan_override_t ov = plan_override();
+    const PairPlan pp = plan_pair(d, ov, true);
+    if (pp.use)
+        return run_scan_pair(d, pp, x, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, w.ptr,
+                             w.bytes, w.may_alloc, static_cast<cudaStream_t>(stream), 0, conv_w, conv_b, conv_width);
+    PairPlan pr;
+    RaggedPlan rg;
+    if (use_ragged(d, ov, true, w.ptr, w.bytes, w.may_alloc, &pr, &rg))   // x goes into the u slot
+        return run_scan_ragged(d, pr, rg, x, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state, w.ptr,
+                               w.bytes, w.may_alloc, static_cast<cudaStream_t>(stream), 0, conv_w, conv_b,
+                               conv_width);
+    // the conv front runs on the channel-pair kernel only
+    return ((size_t)d.seqlen * io_size(d.io_dtype)) % 16 != 0 && plan_pair(d, ov, true, true).use ? SSM_ERR_WORKSPACE
+                                                                                                   : SSM_ERR_UNSUPPORTED;
 }
 
 size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
-    return pair_workspace_bytes(*dims, plan_pair(*dims, plan_override(), true));
+    const ssm_plan_override_t ov = plan_override();
+    const PairPlan pp = plan_pair(*dims, ov, true);
+    if (pp.use) return pair_workspace_bytes(*dims, pp);
+    const PairPlan pr = plan_pair(*dims, ov, true, true);
+    return pr.use ? plan_ragged(*dims, pr).bytes : 0;
 }
 
 }  // extern "C"

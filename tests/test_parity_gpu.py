@@ -238,12 +238,26 @@ def test_conv_front_shapes(Bt, D, L, N, io, gate, dskip, K, chunks, a_kind):
     compare_scan(ref, y, h)
 
 
-def test_conv_front_ragged_rows_unsupported():
-    inp, w, cb = _conv_case(1, 8, 1001, 16, "bf16", False, "ones", 4, 3)
+@pytest.mark.parametrize("L,io", [(1001, "bf16"), (77, "f32")])
+def test_conv_front_ragged_rows(L, io):
+    """Rows that are not 16-byte multiples: padded copies in the workspace, then the fused
+    conv front and scan; equal to the oracle. With a caller workspace too small for the
+    copies the call returns SSM_ERR_WORKSPACE."""
+    inp, w, cb = _conv_case(2, 9, L, 16, io, True, "ones", 4, 7 * L, "random")
     g = to_dev(inp)
+    y, h = ssm.conv_selective_scan_fwd(g["u"], w.cuda(), cb.cuda(), g["delta"], g["A"], g["B"], g["C"], D=g["D"],
+                                       z=g["z"], delta_bias=g["delta_bias"], delta_softplus=True,
+                                       return_last_state=True)
+    torch.cuda.synchronize()
+    u = oracle.conv_silu(gen.as_f64(inp["u"]), np.broadcast_to(w.double().numpy(), (2, 9, 4)),
+                         np.broadcast_to(cb.double().numpy(), (2, 9)))
+    ref = dict(inp)
+    ref["u"] = torch.from_numpy(u)
+    compare_scan(ref, y, h)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
     with pytest.raises(ssm.SsmError) as ei:
-        ssm.conv_selective_scan_fwd(g["u"], w.cuda(), cb.cuda(), g["delta"], g["A"], g["B"], g["C"])
-    assert ei.value.code == ssm.SSM_ERR_UNSUPPORTED
+        ssm.conv_selective_scan_fwd(g["u"], w.cuda(), cb.cuda(), g["delta"], g["A"], g["B"], g["C"], workspace=small)
+    assert ei.value.code == ssm.SSM_ERR_WORKSPACE
 
 
 # ---- exact zero-order hold (jsqmd.com section 2.3), on the channel-pair kernel ----------
@@ -296,11 +310,18 @@ def test_zoh_long128k_sampled():
     compare_scan(inp, y, h, channels=sample_channels(1, 1536, 8, seed=5), zoh=True)
 
 
-def test_zoh_ragged_rows_unsupported():
-    cfg = gen.ScanConfig("zr", 1, 8, 1001, 16, io="bf16", seed=3)
-    g = to_dev(gen.scan_inputs(cfg))
+def test_zoh_ragged_rows():
+    """Rows that are not 16-byte multiples take the channel-pair kernel on padded copies, so
+    the zero-order hold covers them; with a workspace too small for the copies it returns
+    SSM_ERR_UNSUPPORTED (the element-wise kernel has no zero-order hold)."""
+    cfg = gen.ScanConfig("zr", 2, 8, 1001, 16, io="bf16", gate=True, seed=3, a_kind="scaled")
+    inp = _zoh_inputs(cfg)
+    y, h = gpu_scan(inp, discretization="zoh")
+    compare_scan(inp, y, h, zoh=True)
+    g = to_dev(inp)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
     with pytest.raises(ssm.SsmError) as ei:
-        ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], discretization="zoh")
+        ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], discretization="zoh", workspace=small)
     assert ei.value.code == ssm.SSM_ERR_UNSUPPORTED
 
 

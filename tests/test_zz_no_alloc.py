@@ -175,3 +175,20 @@ def test_noalloc_oversize_raises_clear_error(lib, time_split_plan):
         ssm.selective_scan_fwd_noalloc(u, u, A, Bm, Bm)
     assert ei.value.code == ssm.SSM_ERR_WORKSPACE
     assert str(ssm.SCRATCH_MAX_BYTES) in str(ei.value)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("Bt,D,L,N", [(2, 48, 1001, 16), (1, 1536, 16383, 64)], ids=["copies_fit", "copies_too_big"])
+def test_noalloc_ragged_rows(lib, Bt, D, L, N):
+    """Rows that are not 16-byte multiples: the padded copies of the default kernel go into the
+    scratch when they fit there; when they do not, the call takes the element-wise kernel
+    (it needs only its chunk carries) instead of failing. Both match the fp64 oracle."""
+    from parity import compare_scan, sample_channels
+    cfg = gen.ScanConfig("nr", Bt, D, L, N, io="bf16", gate=True, dskip="ones", seed=L, a_kind="random")
+    inp = gen.scan_inputs(cfg)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y, h = ssm.selective_scan_fwd_noalloc(g["u"], g["delta"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                                          delta_bias=g["delta_bias"], return_last_state=True)
+    torch.cuda.synchronize()
+    assert ssm.stream_status() == ssm.SSM_OK
+    compare_scan(inp, y, h, channels=sample_channels(Bt, D, 6, seed=3))
