@@ -27,6 +27,55 @@ __global__ void chunk_combine_kernel(const float *__restrict__ A, const float *_
     }
 }
 
+// The same incoming states for many chunks, in three phases of one CTA per 32 (channel,
+// state) pairs: thread (pair, group g) composes the aggregates of chunk group g (kCombGroups
+// groups of consecutive chunks; the group's decay is exp(A * its summed dt)), one thread per
+// pair then chains the group aggregates, and every thread replays its group from the group's
+// incoming state. The sequential depth is about 2*nchunks/kCombGroups + kCombGroups steps
+// instead of nchunks (the composition of affine maps is associative).
+constexpr int kCombPairs = 32, kCombGroups = 16;
+__global__ void __launch_bounds__(kCombPairs * kCombGroups)
+    chunk_combine_grouped_kernel(const float *__restrict__ A, const float *__restrict__ agg_h,
+                                 const float *__restrict__ agg_s, float *__restrict__ hin, int64_t BD, int64_t Dm,
+                                 int64_t N, int npad, int nchunks) {
+    __shared__ float sS[kCombGroups][kCombPairs], sH[kCombGroups][kCombPairs];
+    const int pl = threadIdx.x % kCombPairs, g = threadIdx.x / kCombPairs;
+    const int64_t i = (int64_t)blockIdx.x * kCombPairs + pl;
+    const bool valid = i < BD * npad;
+    const int64_t bd = valid ? i / npad : 0;
+    const int n = valid ? (int)(i % npad) : 0;
+    const float Ap = (valid && n < N) ? A[(bd % Dm) * N + n] * kLog2e : 0.0f;
+    const int cpg = (nchunks + kCombGroups - 1) / kCombGroups;
+    const int k0 = min(g * cpg, nchunks), k1 = min(k0 + cpg, nchunks);
+    // group aggregate of the chunks k0..k1-1 that have one (all but the last chunk)
+    float h = 0.0f, S = 0.0f;
+    if (valid) {
+        for (int k = k0; k < min(k1, nchunks - 1); ++k) {
+            const float sdt = agg_s[(int64_t)k * BD + bd];
+            h = fmaf(ex2(Ap * sdt), h, agg_h[((int64_t)k * BD + bd) * npad + n]);
+            S += sdt;
+        }
+    }
+    sS[g][pl] = S;
+    sH[g][pl] = h;
+    __syncthreads();
+    if (g == 0) {   // incoming state of every group
+        float x = 0.0f;
+        for (int gg = 0; gg < kCombGroups; ++gg) {
+            const float hg = sH[gg][pl];
+            sH[gg][pl] = x;
+            x = fmaf(ex2(Ap * sS[gg][pl]), x, hg);
+        }
+    }
+    __syncthreads();
+    if (!valid) return;
+    float x = sH[g][pl];
+    for (int k = k0; k < k1; ++k) {
+        hin[((int64_t)k * BD + bd) * npad + n] = x;
+        if (k + 1 < nchunks) x = fmaf(ex2(Ap * agg_s[(int64_t)k * BD + bd]), x, agg_h[((int64_t)k * BD + bd) * npad + n]);
+    }
+}
+
 // Rows of `len` io elements at stride src_ld copied to stride dst_ld, elements len..dst_ld-1
 // of each destination row zeroed: puts rows whose byte length is not a multiple of 16 on
 // 16-byte boundaries for the channel-pair kernel (and takes its y rows back). A thread moves
@@ -126,8 +175,16 @@ bool seq_plan_supported(int nper, int g) {
 cudaError_t launch_chunk_combine(const float *A, const float *agg_h, const float *agg_s, float *hin,
                                  int64_t BD, int64_t Dm, int64_t N, int npad, int nchunks, cudaStream_t s) {
     const int64_t total = BD * npad;
-    chunk_combine_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(A, agg_h, agg_s, hin, BD, Dm, N, npad,
-                                                                          nchunks);
+    // deep chains over few (channel, state) pairs: grouped (sequential depth ~2*nchunks/16 + 16).
+    // Measured on B300, 1 x 48 x 131072 x 64 (444 chunks, 3072 pairs): 75 -> 8 us; with many
+    // pairs the plain kernel is faster (1 x 1536 x 131072 x 64, 54 chunks: 18 vs 64 us;
+    // 1 x 384 x 131072 x 64: 16 vs 21 us).
+    if (nchunks > 2 * kCombGroups && total < 8192)
+        chunk_combine_grouped_kernel<<<(unsigned)((total + kCombPairs - 1) / kCombPairs), kCombPairs * kCombGroups, 0,
+                                       s>>>(A, agg_h, agg_s, hin, BD, Dm, N, npad, nchunks);
+    else
+        chunk_combine_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(A, agg_h, agg_s, hin, BD, Dm, N, npad,
+                                                                              nchunks);
     return cudaGetLastError();
 }
 

@@ -120,6 +120,8 @@ PAIR_CASES = [
     (1, 20, 520, 100, "bf16", True, "ones", "8", 4),     # KS 8, sixteen lanes per pair
     (2, 33, 40, 128, "f32", False, "normal", "8", 1),    # KS 8, sixteen lanes, a short ragged tile
     (1, 40, 2000, 64, "f32", False, "ones", "16", 5),    # KS 16, four lanes per pair
+    (1, 24, 8192, 16, "bf16", True, "normal", "4", 100),  # 86 chunks, 384 pairs: the grouped combine
+    (1, 24, 8192, 64, "f32", False, "ones", "16", 200),   # 128 chunks (the cap at L/64), grouped
     (2, 70, 520, 48, "bf16", True, "normal", "16", 3),   # KS 16, padded states, partial channel block
     (3, 9, 136, 40, "f32", True, "ones", "16", 0),       # KS 16, padded states, planner's chunks
 ]
