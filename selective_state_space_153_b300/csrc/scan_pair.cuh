@@ -18,6 +18,9 @@
 //   y: per channel each lane keeps its partial sum over its KS states; every GP timesteps
 //   the GP lanes exchange partials with a transposed butterfly (lane g ends with the sum for
 //   timestep tb+g), add D*u, apply the gate and store y.
+// Rows of u, delta, z, y, B, C are addressed with the row stride p.ld: L, or the padded
+// stride of rows the host copied onto 16-byte boundaries (rows that are not 16-byte
+// multiples); the scan itself covers the L steps.
 // Pipeline per tile: raw io rows (u, delta, z, B, C) arrive by cp.async three tiles deep;
 // one barrier per tile; then tile j+1 is converted (softplus, dt*u per (channel, t); B, C to
 // fp32, transposed to [t][n]) while tile j is scanned from the previous conversion.
