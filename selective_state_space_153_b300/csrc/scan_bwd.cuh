@@ -19,7 +19,8 @@
 //   * the CTA stages the segment's B, C rows (as [t][g][q], so a lane's states are one
 //     16-byte read) and, once per (channel, step), dt, the softplus derivative, u,
 //     dyhat = dy*SiLU(z) and the gate derivative factor dy*SiLU'(z); the raw inputs of the
-//     next segment are fetched into registers while the current one computes;
+//     next segment are fetched into registers while the current one computes, two steps of a
+//     row per load where the length is even and the rows start on 2-element boundaries;
 //   * each lane recomputes its states' S steps from the checkpoint, then runs the adjoint in
 //     reverse;
 //   * sums over the states of a channel (yhat, sum lambda*B, sum lambda*A*a*h) are kept per
@@ -46,6 +47,7 @@ struct BwdParams {
     float *ckpt;                  // [Bt*Dm][nseg][Q*G]: h before each segment's first step
     int64_t Bt, Dm, L, N;
     int softplus, nseg;
+    int pair2;                    // 1: rows read two steps at a time (L even, bases 2-element aligned)
 };
 
 // Shared-memory layout (floats) of the backward kernels for G lanes per channel and Q states
@@ -78,15 +80,61 @@ template <typename IO, int G, int Q, bool FULL>
 struct BwdFetch {
     using Cfg = BwdCfg<G, Q>;
     static constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kCpb = Cfg::kCpb;
-    static constexpr int kBC = (FULL ? 2 : 1) * kNP * kS, kBCI = (kBC + kBwdThreads - 1) / kBwdThreads;
-    static constexpr int kCH = kCpb * kS, kCHI = (kCH + kBwdThreads - 1) / kBwdThreads;
+    // register slots per thread: an even count, so that reading two steps per item also covers
+    // every element
+    static constexpr int kBC = (FULL ? 2 : 1) * kNP * kS, kBCI = 2 * ((kBC + 2 * kBwdThreads - 1) / (2 * kBwdThreads));
+    static constexpr int kCH = kCpb * kS, kCHI = 2 * ((kCH + 2 * kBwdThreads - 1) / (2 * kBwdThreads));
+    static_assert(kS % 2 == 0, "two steps per item stay in one row");
     float bc[kBCI];
     float dl[kCHI], uu[kCHI], dy[kCHI], zz[kCHI];
+
+    // two io elements (8 bytes for fp32, 4 for bf16) as floats
+    __device__ __forceinline__ static float2 ld2(const IO *q) {
+        if constexpr (sizeof(IO) == 4) {
+            return __ldg(reinterpret_cast<const float2 *>(q));
+        } else {
+            const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(q));
+            return make_float2(bf16lo(w), bf16hi(w));
+        }
+    }
 
     __device__ __forceinline__ void fetch(const BwdParams &p, int64_t b, int64_t t0, int64_t d0) {
         const int tid = threadIdx.x;
         const IO *Bm = reinterpret_cast<const IO *>(p.B) + b * p.N * p.L;
         const IO *Cm = reinterpret_cast<const IO *>(p.C) + b * p.N * p.L;
+        if (p.pair2) {   // item k2 of a thread: two consecutive steps of one row (slots 2*k2, 2*k2+1)
+#pragma unroll
+            for (int k2 = 0; k2 < kBCI / 2; ++k2) {
+                const int e = 2 * (tid + k2 * kBwdThreads);
+                const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
+                const int64_t t = t0 + i;
+                float2 v = make_float2(0.f, 0.f);
+                if (e < kBC && n < p.N && t < p.L) v = ld2((kind ? Cm : Bm) + n * p.L + t);
+                bc[2 * k2] = v.x;
+                bc[2 * k2 + 1] = v.y;
+            }
+#pragma unroll
+            for (int k2 = 0; k2 < kCHI / 2; ++k2) {
+                const int e = 2 * (tid + k2 * kBwdThreads);
+                const int cc = e / kS, i = e % kS;
+                const int64_t d = d0 + cc, t = t0 + i;
+                float2 a = make_float2(0.f, 0.f), c = a, f = a, g = a;
+                if (e < kCH && d < p.Dm && t < p.L) {
+                    const int64_t idx = (b * p.Dm + d) * p.L + t;
+                    a = ld2(reinterpret_cast<const IO *>(p.delta) + idx);
+                    c = ld2(reinterpret_cast<const IO *>(p.u) + idx);
+                    if (FULL) {
+                        f = ld2(reinterpret_cast<const IO *>(p.dy) + idx);
+                        if (p.z) g = ld2(reinterpret_cast<const IO *>(p.z) + idx);
+                    }
+                }
+                dl[2 * k2] = a.x; dl[2 * k2 + 1] = a.y;
+                uu[2 * k2] = c.x; uu[2 * k2 + 1] = c.y;
+                dy[2 * k2] = f.x; dy[2 * k2 + 1] = f.y;
+                zz[2 * k2] = g.x; zz[2 * k2 + 1] = g.y;
+            }
+            return;
+        }
 #pragma unroll
         for (int k = 0; k < kBCI; ++k) {   // consecutive e: consecutive steps of one row
             const int e = tid + k * kBwdThreads;
@@ -114,19 +162,25 @@ struct BwdFetch {
 
     // dt, the softplus derivative, u and (FULL) dyhat = dy*SiLU(z), dy*SiLU'(z) once per
     // (channel, step); B, C as [t][g][q] (state n = g + G*q), zeros beyond N, L or Dm
+    // element of register slot k: tid + k*128 (one step per item), or 2*(tid + (k/2)*128) + k%2
+    // (two steps per item)
+    __device__ __forceinline__ static int slot_elem(const BwdParams &p, int tid, int k) {
+        return p.pair2 ? 2 * (tid + (k / 2) * kBwdThreads) + (k & 1) : tid + k * kBwdThreads;
+    }
+
     __device__ __forceinline__ void stage(const BwdParams &p, float *sm, int64_t t0, int64_t d0) const {
         const int tid = threadIdx.x;
 #pragma unroll
         for (int k = 0; k < kBCI; ++k) {
-            const int e = tid + k * kBwdThreads;
+            const int e = slot_elem(p, tid, k);
             if (e >= kBC) break;
             const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
             sm[(kind ? Cfg::kOffC : Cfg::kOffB) + (i * G + n % G) * Cfg::kQ + n / G] = bc[k];
         }
 #pragma unroll
         for (int k = 0; k < kCHI; ++k) {
-            const int e = tid + k * kBwdThreads;
-            if (e >= kCH) break;
+            const int e = slot_elem(p, tid, k);
+            if (e >= kCH) continue;
             const int cc = e / kS, i = e % kS;
             const int64_t d = d0 + cc, t = t0 + i;
             float dtv = 0.0f, sgv = 0.0f, dyh = 0.0f, gz = 0.0f;

@@ -173,7 +173,24 @@ def test_backward_gradients_forced_split(Bt, D, L, N, io, gate, dskip, bias, dla
         _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind)
 
 
-def _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind):
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_backward_rows_off_pair_alignment(io):
+    """Even length with every input one element off a 2-element boundary: the rows are read
+    one step per load instead of two."""
+    _check_backward(2, 9, 70, 16, io, True, "normal", True, True, "scaled", odd_offset=True)
+
+
+def _odd_offset(t):
+    """t's values at a storage offset of one element (no 2-element alignment)."""
+    if t is None:
+        return None
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = buf[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind, odd_offset=False):
     from oracle import backward as obwd
     cfg = gen.ScanConfig("bwd", Bt, D, L, N, io=io, gate=gate, dskip=dskip, bias=bias, seed=3 * L + N,
                          a_kind=a_kind)
@@ -182,7 +199,12 @@ def _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind):
     dy = torch.from_numpy(rng.standard_normal((Bt, D, L)).astype(np.float32)).to(inp["u"].dtype)
     dl = torch.from_numpy(rng.standard_normal((Bt, D, N)).astype(np.float32)) if dlast else None
     g = to_dev(inp)
-    got = ssm.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.cuda(), D=g["D"], z=g["z"],
+    dyd = dy.cuda()
+    if odd_offset:
+        for k in ("u", "delta", "B", "C", "z"):
+            g[k] = _odd_offset(g[k])
+        dyd = _odd_offset(dyd)
+    got = ssm.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dyd, D=g["D"], z=g["z"],
                                  delta_bias=g["delta_bias"], delta_softplus=True,
                                  dlast_state=None if dl is None else dl.cuda())
     torch.cuda.synchronize()
