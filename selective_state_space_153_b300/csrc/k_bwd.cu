@@ -8,7 +8,7 @@ using bf16 = __nv_bfloat16;
 
 template <typename IO, int G, int Q>
 cudaError_t launch_bwd_t(const BwdParams &p, cudaStream_t s) {
-    constexpr size_t ck = bwd_ckpt_smem_bytes<G, Q>(), sm = bwd_smem_bytes<G, Q>();
+    constexpr size_t ck = bwd_ckpt_smem_bytes<IO, G, Q>(), sm = bwd_smem_bytes<IO, G, Q>();
     constexpr int kCpb = BwdCfg<G, Q>::kCpb;
     const dim3 grid((unsigned)((p.Dm + kCpb - 1) / kCpb), (unsigned)p.Bt);
     static std::atomic<unsigned long long> attr_set{0};

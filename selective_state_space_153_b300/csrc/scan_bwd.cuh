@@ -18,9 +18,11 @@
 // the start of every S-step segment. Pass 2 (scan_bwd_kernel) walks the segments backwards:
 //   * the CTA stages the segment's B, C rows (as [t][g][q], so a lane's states are one
 //     16-byte read) and, once per (channel, step), dt, the softplus derivative, u,
-//     dyhat = dy*SiLU(z) and the gate derivative factor dy*SiLU'(z); the raw inputs of the
-//     next segment are fetched into registers while the current one computes, two steps of a
-//     row per load where the length is even and the rows start on 2-element boundaries;
+//     dyhat = dy*SiLU(z) and the gate derivative factor dy*SiLU'(z). The raw inputs of the
+//     next segments are in flight while the current one computes: copied by cp.async into a
+//     shared-memory ring where every row is a multiple of 16 bytes long and 16-byte aligned,
+//     else fetched into registers (two steps of a row per load where the length is even and
+//     the rows start on 2-element boundaries);
 //   * each lane recomputes its states' S steps from the checkpoint, then runs the adjoint in
 //     reverse;
 //   * sums over the states of a channel (yhat, sum lambda*B, sum lambda*A*a*h) are kept per
@@ -48,6 +50,8 @@ struct BwdParams {
     int64_t Bt, Dm, L, N;
     int softplus, nseg;
     int pair2;                    // 1: rows read two steps at a time (L even, bases 2-element aligned)
+    int ring;                     // 1: rows staged by asynchronous 16-byte copies (L*esz % 16 == 0,
+                                  //    16-byte aligned bases)
 };
 
 // Shared-memory layout (floats) of the backward kernels for G lanes per channel and Q states
@@ -69,8 +73,10 @@ struct BwdCfg {
     static constexpr int kFloats = kOffPart + 2 * kCpb * kPartCh;
     static_assert(kS % 4 == 0 && (kOffPart % 4) == 0 && (kPartCh % 4) == 0 && (kRow % 4) == 0, "16-byte rows");
 };
-template <int G, int Q>
-constexpr size_t bwd_smem_bytes() { return (size_t)BwdCfg<G, Q>::kFloats * sizeof(float); }
+template <typename IO, int G, int Q, bool FULL>
+struct BwdRing;
+template <typename IO, int G, int Q>
+constexpr size_t bwd_smem_bytes();
 
 // Raw inputs of one segment [t0, t0+S) of batch row b for the CTA's channels d0 .. d0+kCpb-1,
 // fetched into registers one segment ahead (the loads are in flight while the previous
@@ -209,10 +215,131 @@ struct BwdFetch {
     }
 };
 
+// Raw inputs of one segment copied into a shared-memory ring by cp.async, kStages - 1 segments
+// ahead, where every row is a multiple of 16 bytes long and starts on a 16-byte boundary. A
+// slot holds the segment's rows as [row][S] io elements -- B (FULL: then C) rows n < kNP, then
+// delta, u (FULL: dy, z) rows of the CTA's channels -- and (FULL) the checkpoints of the CTA's
+// channels as [channel][kNP] floats. Pieces of rows beyond N, Dm or L are not copied; stage()
+// reads zeros in their place.
+template <typename IO, int G, int Q, bool FULL>
+struct BwdRing {
+    using Cfg = BwdCfg<G, Q>;
+    static constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kCpb = Cfg::kCpb, kQ = Cfg::kQ;
+    static constexpr int kStepsPerPiece = 16 / (int)sizeof(IO);
+    static constexpr int kGran = kS / kStepsPerPiece;                 // pieces per row segment
+    static constexpr int kRowsBC = (FULL ? 2 : 1) * kNP, kRowsCH = (FULL ? 4 : 2) * kCpb;
+    static constexpr int kRows = kRowsBC + kRowsCH;
+    static constexpr int kCkFloats = FULL ? kCpb * kNP : 0;
+    // measured on B300: deeper rings change neither pass (adjoint 3 stages, checkpoint 6); a
+    // 2-stage checkpoint ring is 8-35% slower
+    static constexpr int kStages = FULL ? 2 : 4;
+    static constexpr int kSlotBytes = kRows * kS * (int)sizeof(IO) + kCkFloats * 4;
+    static constexpr int kRowPieces = kRows * kGran, kPieces = kRowPieces + kCkFloats / 4;
+    static constexpr int kPerThread = (kPieces + kBwdThreads - 1) / kBwdThreads;
+    static_assert(kS % kStepsPerPiece == 0 && kNP % 4 == 0 && kSlotBytes % 16 == 0, "16-byte pieces");
+    static constexpr size_t bytes() { return (size_t)kStages * kSlotBytes; }
+
+    // copies of segment seg into its slot (seg % kStages); the caller commits the group
+    __device__ __forceinline__ static void issue(const BwdParams &p, unsigned char *ring, int64_t b, int seg,
+                                                 int64_t d0) {
+        unsigned char *slot = ring + (seg % kStages) * kSlotBytes;
+        const int64_t t0 = (int64_t)seg * kS;
+#pragma unroll
+        for (int m = 0; m < kPerThread; ++m) {
+            const int j = threadIdx.x + m * kBwdThreads;
+            if (j >= kPieces) break;
+            const void *src = nullptr;
+            if (j < kRowPieces) {
+                const int row = j / kGran, part = j % kGran;
+                const int64_t t = t0 + part * kStepsPerPiece;
+                if (t < p.L) {
+                    if (row < kRowsBC) {
+                        const int kind = row / kNP, n = row % kNP;
+                        if (n < p.N)
+                            src = reinterpret_cast<const IO *>(kind ? p.C : p.B) + (b * p.N + n) * p.L + t;
+                    } else {
+                        const int r = row - kRowsBC, arr = r / kCpb, cc = r % kCpb;
+                        const int64_t d = d0 + cc;
+                        const void *base = arr == 0 ? p.delta : arr == 1 ? p.u : arr == 2 ? p.dy : p.z;
+                        if (d < p.Dm && base != nullptr)
+                            src = reinterpret_cast<const IO *>(base) + (b * p.Dm + d) * p.L + t;
+                    }
+                }
+            } else {
+                const int r = j - kRowPieces, cc = r / (kNP / 4), part = r % (kNP / 4);
+                const int64_t d = d0 + cc;
+                if (d < p.Dm) src = p.ckpt + ((b * p.Dm + d) * p.nseg + seg) * kNP + 4 * part;
+            }
+            if (src != nullptr) cp_async16(slot + 16 * j, src, 16);
+        }
+    }
+
+    // converted segment into the compute layout (as BwdFetch::stage); ckn: this lane's
+    // checkpoint pairs (FULL)
+    __device__ __forceinline__ static void stage(const BwdParams &p, const unsigned char *ring, float *sm, int seg,
+                                                 int64_t d0, float2 (&ckn)[Cfg::kP]) {
+        const int tid = threadIdx.x;
+        const IO *raw = reinterpret_cast<const IO *>(ring + (seg % kStages) * kSlotBytes);
+        const int64_t t0 = (int64_t)seg * kS;
+        constexpr int kBC = kRowsBC * kS, kCH = kCpb * kS;
+        for (int e = tid; e < kBC; e += kBwdThreads) {
+            const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
+            const float v = (n < p.N && t0 + i < p.L) ? io_traits<IO>::to_f(raw[e]) : 0.0f;
+            sm[(kind ? Cfg::kOffC : Cfg::kOffB) + (i * G + n % G) * kQ + n / G] = v;
+        }
+        for (int e = tid; e < kCH; e += kBwdThreads) {
+            const int cc = e / kS, i = e % kS;
+            const int64_t d = d0 + cc, t = t0 + i;
+            float dtv = 0.0f, sgv = 0.0f, dyh = 0.0f, gz = 0.0f, uu = 0.0f;
+            if (d < p.Dm && t < p.L) {
+                const float dl = io_traits<IO>::to_f(raw[kBC + e]);
+                uu = io_traits<IO>::to_f(raw[kBC + kCH + e]);
+                const float v = dl + (p.bias ? p.bias[d] : 0.0f);
+                dtv = p.softplus ? softplus_f(v) : v;
+                sgv = p.softplus ? rcp_approx(1.0f + ex2(-v * kLog2e)) : 1.0f;
+                if (FULL) {
+                    const float dy = io_traits<IO>::to_f(raw[kBC + 2 * kCH + e]);
+                    if (p.z) {
+                        const float zz = io_traits<IO>::to_f(raw[kBC + 3 * kCH + e]);
+                        const float sz = rcp_approx(1.0f + ex2(-zz * kLog2e));
+                        dyh = dy * zz * sz;                            // dy * SiLU(z)
+                        gz = dy * sz * (1.0f + zz * (1.0f - sz));      // dy * SiLU'(z)
+                    } else {
+                        dyh = dy;
+                    }
+                }
+            }
+            sm[Cfg::kOffDt + e] = dtv;
+            sm[Cfg::kOffU + e] = uu;
+            if (FULL) {
+                sm[Cfg::kOffSg + e] = sgv;
+                sm[Cfg::kOffDyh + e] = dyh;
+                sm[Cfg::kOffGz + e] = gz;
+            }
+        }
+        if (FULL) {
+            const int g = tid % G, cc = tid / G;
+            const float *ck = reinterpret_cast<const float *>(reinterpret_cast<const unsigned char *>(raw) +
+                                                              kRows * kS * sizeof(IO)) + cc * kNP;
+            const bool valid = d0 + cc < p.Dm;
+#pragma unroll
+            for (int k = 0; k < Cfg::kP; ++k)
+                ckn[k] = valid ? make_float2(ck[g + G * 2 * k], ck[g + G * (2 * k + 1)]) : make_float2(0.f, 0.f);
+        }
+    }
+};
+
 // Checkpoint pass: the forward recurrence, h stored before every S-step segment; the next
-// segment's raw inputs are fetched into registers while the current one computes.
-template <int G, int Q>
-constexpr size_t bwd_ckpt_smem_bytes() { return (size_t)(BwdCfg<G, Q>::kOffU + BwdCfg<G, Q>::kChan) * sizeof(float); }
+// segments' raw inputs are in flight (in registers, or in the copy ring) while the current one
+// computes.
+template <typename IO, int G, int Q>
+constexpr size_t bwd_ckpt_smem_bytes() {
+    return (size_t)(BwdCfg<G, Q>::kOffU + BwdCfg<G, Q>::kChan) * sizeof(float) + BwdRing<IO, G, Q, false>::bytes();
+}
+template <typename IO, int G, int Q>
+constexpr size_t bwd_smem_bytes() {
+    return (size_t)BwdCfg<G, Q>::kFloats * sizeof(float) + BwdRing<IO, G, Q, true>::bytes();
+}
 
 // A lane's Q consecutive floats at p (16-byte or 8-byte aligned) as Q/2 packed pairs.
 template <int P>
@@ -245,8 +372,19 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
         h2[k] = make_float2(0.f, 0.f);
     }
     float *ck = p.ckpt + bd * (int64_t)p.nseg * kNP;
+    using Ring = BwdRing<IO, G, Q, false>;
+    unsigned char *ring = reinterpret_cast<unsigned char *>(sm + Cfg::kOffU + Cfg::kChan);
     BwdFetch<IO, G, Q, false> f;
-    f.fetch(p, b, 0, d0);
+    float2 ck_unused[kP];
+    if (p.ring) {
+#pragma unroll
+        for (int s = 0; s < Ring::kStages - 1; ++s) {
+            if (s < p.nseg) Ring::issue(p, ring, b, s, d0);
+            cp_async_commit();
+        }
+    } else {
+        f.fetch(p, b, 0, d0);
+    }
     for (int seg = 0; seg < p.nseg; ++seg) {
         if (valid) {
 #pragma unroll
@@ -255,10 +393,17 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
                 ck[(int64_t)seg * kNP + g + G * (2 * k + 1)] = h2[k].y;
             }
         }
+        if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();
-        f.stage(p, sm, (int64_t)seg * kS, d0);
+        if (p.ring) Ring::stage(p, ring, sm, seg, d0, ck_unused);
+        else f.stage(p, sm, (int64_t)seg * kS, d0);
         __syncthreads();
-        if (seg + 1 < p.nseg) f.fetch(p, b, (int64_t)(seg + 1) * kS, d0);   // in flight during this segment
+        if (p.ring) {            // the slot of segment seg - 1, staged before the barriers above
+            if (seg + Ring::kStages - 1 < p.nseg) Ring::issue(p, ring, b, seg + Ring::kStages - 1, d0);
+            cp_async_commit();
+        } else if (seg + 1 < p.nseg) {
+            f.fetch(p, b, (int64_t)(seg + 1) * kS, d0);   // in flight during this segment
+        }
 #pragma unroll
         for (int i = 0; i < kS; ++i) {
             const float dt = sm[Cfg::kOffDt + cc * kS + i];
@@ -329,8 +474,9 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
         dbias += ddl;
     };
 
+    using Ring = BwdRing<IO, G, Q, true>;
+    unsigned char *ring = reinterpret_cast<unsigned char *>(sm + Cfg::kFloats);
     BwdFetch<IO, G, Q, true> f;
-    f.fetch(p, b, (int64_t)(p.nseg - 1) * kS, d0);
     // the segment's checkpoint, fetched with its inputs one segment ahead
     auto fetch_ck = [&](int seg, float2 (&out)[kP]) {
 #pragma unroll
@@ -339,17 +485,31 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
                            : make_float2(0.f, 0.f);
     };
     float2 ckn[kP];
-    fetch_ck(p.nseg - 1, ckn);
+    if (p.ring) {
+#pragma unroll
+        for (int s = 0; s < Ring::kStages - 1; ++s) {
+            if (p.nseg - 1 - s >= 0) Ring::issue(p, ring, b, p.nseg - 1 - s, d0);
+            cp_async_commit();
+        }
+    } else {
+        f.fetch(p, b, (int64_t)(p.nseg - 1) * kS, d0);
+        fetch_ck(p.nseg - 1, ckn);
+    }
     for (int seg = p.nseg - 1; seg >= 0; --seg) {
         const int64_t t0 = (int64_t)seg * kS;
+        if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();                        // the previous segment is done with shared memory
-        f.stage(p, sm, t0, d0);
+        if (p.ring) Ring::stage(p, ring, sm, seg, d0, ckn);
+        else f.stage(p, sm, t0, d0);
         __syncthreads();
         // states as pairs (q = 2k, 2k+1): hs[k][0] before the segment, hs[k][i+1] after step t0+i
         float2 hs[kP][kS + 1];
 #pragma unroll
         for (int k = 0; k < kP; ++k) hs[k][0] = ckn[k];
-        if (seg > 0) {   // the next segment's inputs and checkpoint, in flight meanwhile
+        if (p.ring) {   // into the slot of segment seg + 1, staged before the barriers above
+            if (seg - (Ring::kStages - 1) >= 0) Ring::issue(p, ring, b, seg - (Ring::kStages - 1), d0);
+            cp_async_commit();
+        } else if (seg > 0) {   // the next segment's inputs and checkpoint, in flight meanwhile
             f.fetch(p, b, t0 - kS, d0);
             fetch_ck(seg - 1, ckn);
         }

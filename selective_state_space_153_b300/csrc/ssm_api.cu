@@ -906,12 +906,17 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     if (st != SSM_OK) return st;
     BwdParams p{u, delta, z, B, C, dy, A, D, delta_bias, dlast_state, du, ddelta, dA, dB, dC, dD,
                 z ? dz : nullptr, ddelta_bias, static_cast<float *>(ws), d.batch, d.dim, d.seqlen,
-                d.dstate, delta_softplus ? 1 : 0, (int)((d.seqlen + kBwdS - 1) / kBwdS), 0};
+                d.dstate, delta_softplus ? 1 : 0, (int)((d.seqlen + kBwdS - 1) / kBwdS), 0, 0};
     // rows read two steps per load: an even length and every row base on a 2-element boundary
     bool pair2 = d.seqlen % 2 == 0;
     for (const void *q : io_ptrs)
         if (q != nullptr && !aligned_to(q, 2 * esz)) pair2 = false;
     p.pair2 = pair2 ? 1 : 0;
+    // rows staged by 16-byte asynchronous copies: rows of whole 16-byte pieces, aligned bases
+    bool ring = (d.seqlen * (int64_t)esz) % 16 == 0;
+    for (const void *q : io_ptrs)
+        if (q != nullptr && !aligned16(q)) ring = false;
+    p.ring = ring ? 1 : 0;
     const BwdSplit sp = bwd_split(d.batch * d.dim, d.dstate);
     const cudaError_t e = launch_bwd(d.io_dtype, sp.G, sp.Q, p, s);
     if (allocated) cudaFreeAsync(ws, s);

@@ -147,6 +147,7 @@ BWD_CASES = [
     (2, 9, 70, 16, "bf16", True, "normal", True, False, "scaled"),
     (1, 40, 48, 8, "f32", False, "ones", True, False, "random"),
     (3, 33, 130, 32, "f32", True, "normal", True, True, "scaled"),
+    (2, 37, 96, 16, "bf16", True, "ones", True, True, "random"),   # bf16 rows of whole 16-byte pieces
 ]
 
 
