@@ -50,7 +50,7 @@ FALLBACK_HBM_GBS = 6400.0
 # combine + full pass), from a one-pass ncu capture of the full-size call, together with the
 # hash of the channel-pair kernel's sources it was taken on: a different hash (the kernels
 # changed since) reports the traffic as unknown (null) rather than a stale count.
-TRAFFIC_BYTES_PER_LAUNCH = {"long128k": ("0d2e58686e40a463", 2094405376)}   # (source hash, bytes)
+TRAFFIC_BYTES_PER_LAUNCH = {"long128k": ("5f5490c890997e64", 2094679808)}   # (source hash, bytes)
 TRAFFIC_SOURCES = ("scan_pair.cuh", "scan_seq.cuh", "check.cuh", "k_pair_impl.cuh", "k_seq.cu", "common.cuh",
                    "launch.h", "ptx.cuh")
 
