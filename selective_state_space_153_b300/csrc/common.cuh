@@ -30,8 +30,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // evaluated from the identity log1p(e) = 2*atanh(s), s = e / (2 + e) in (0, 1/3], as the
 // odd series 2*s*(1 + s^2/3 + s^4/5 + ... + s^12/13); the first omitted term is below
 // 1.6e-8 relative at s = 1/3, under half an fp32 ulp.
-__device__ __forceinline__ float softplus_f(float v) {
-    const float e = ex2(-fabsf(v) * kLog2e);
+__device__ __forceinline__ float softplus_of(float v, float e) {   // e = exp(-|v|)
     const float s = e * rcp_approx(2.0f + e);
     const float s2 = s * s;
     float p = 1.0f / 13.0f;
@@ -43,6 +42,16 @@ __device__ __forceinline__ float softplus_f(float v) {
     p = fmaf(p, s2, 1.0f);
     const float r = fmaxf(v, 0.0f) + 2.0f * s * p;
     return v > 20.0f ? v : r;
+}
+__device__ __forceinline__ float softplus_f(float v) { return softplus_of(v, ex2(-fabsf(v) * kLog2e)); }
+
+// softplus(v) and its derivative sigmoid(v) from one exponential e = exp(-|v|):
+// sigmoid(v) = 1/(1+e) for v >= 0, e/(1+e) for v < 0.
+__device__ __forceinline__ float softplus_sigmoid(float v, float &sg) {
+    const float e = ex2(-fabsf(v) * kLog2e);
+    const float r = rcp_approx(1.0f + e);
+    sg = v >= 0.0f ? r : e * r;
+    return softplus_of(v, e);
 }
 
 // SiLU(z) = z * sigmoid(z) = z / (1 + e^-z).

@@ -174,7 +174,8 @@ struct BwdFetch {
         return p.pair2 ? 2 * (tid + (k / 2) * kBwdThreads) + (k & 1) : tid + k * kBwdThreads;
     }
 
-    __device__ __forceinline__ void stage(const BwdParams &p, float *sm, int64_t t0, int64_t d0) const {
+    __device__ __forceinline__ void stage(const BwdParams &p, float *sm, const float *sbias, int64_t t0,
+                                          int64_t d0) const {
         const int tid = threadIdx.x;
 #pragma unroll
         for (int k = 0; k < kBCI; ++k) {
@@ -191,9 +192,10 @@ struct BwdFetch {
             const int64_t d = d0 + cc, t = t0 + i;
             float dtv = 0.0f, sgv = 0.0f, dyh = 0.0f, gz = 0.0f;
             if (d < p.Dm && t < p.L) {
-                const float v = dl[k] + (p.bias ? p.bias[d] : 0.0f);
-                dtv = p.softplus ? softplus_f(v) : v;
-                sgv = p.softplus ? rcp_approx(1.0f + ex2(-v * kLog2e)) : 1.0f;
+                const float v = dl[k] + sbias[cc];
+                if (!FULL) dtv = p.softplus ? softplus_f(v) : v;
+                else if (p.softplus) dtv = softplus_sigmoid(v, sgv);
+                else dtv = v, sgv = 1.0f;
                 if (FULL) {
                     if (p.z) {
                         const float sz = rcp_approx(1.0f + ex2(-zz[k] * kLog2e));
@@ -236,7 +238,7 @@ struct BwdRing {
     static constexpr int kSlotBytes = kRows * kS * (int)sizeof(IO) + kCkFloats * 4;
     static constexpr int kRowPieces = kRows * kGran, kPieces = kRowPieces + kCkFloats / 4;
     static constexpr int kPerThread = (kPieces + kBwdThreads - 1) / kBwdThreads;
-    static_assert(kS % kStepsPerPiece == 0 && kNP % 4 == 0 && kSlotBytes % 16 == 0, "16-byte pieces");
+    static_assert(kS % kStepsPerPiece == 0 && kNP % 4 == 0 && kSlotBytes % 16 == 0 && kCpb % 4 == 0, "16-byte pieces");
     static constexpr size_t bytes() { return (size_t)kStages * kSlotBytes; }
 
     // copies of segment seg into its slot (seg % kStages); the caller commits the group
@@ -276,8 +278,8 @@ struct BwdRing {
 
     // converted segment into the compute layout (as BwdFetch::stage); ckn: this lane's
     // checkpoint pairs (FULL)
-    __device__ __forceinline__ static void stage(const BwdParams &p, const unsigned char *ring, float *sm, int seg,
-                                                 int64_t d0, float2 (&ckn)[Cfg::kP]) {
+    __device__ __forceinline__ static void stage(const BwdParams &p, const unsigned char *ring, float *sm,
+                                                 const float *sbias, int seg, int64_t d0, float2 (&ckn)[Cfg::kP]) {
         const int tid = threadIdx.x;
         const IO *raw = reinterpret_cast<const IO *>(ring + (seg % kStages) * kSlotBytes);
         const int64_t t0 = (int64_t)seg * kS;
@@ -294,9 +296,10 @@ struct BwdRing {
             if (d < p.Dm && t < p.L) {
                 const float dl = io_traits<IO>::to_f(raw[kBC + e]);
                 uu = io_traits<IO>::to_f(raw[kBC + kCH + e]);
-                const float v = dl + (p.bias ? p.bias[d] : 0.0f);
-                dtv = p.softplus ? softplus_f(v) : v;
-                sgv = p.softplus ? rcp_approx(1.0f + ex2(-v * kLog2e)) : 1.0f;
+                const float v = dl + sbias[cc];
+                if (!FULL) dtv = p.softplus ? softplus_f(v) : v;
+                else if (p.softplus) dtv = softplus_sigmoid(v, sgv);
+                else dtv = v, sgv = 1.0f;
                 if (FULL) {
                     const float dy = io_traits<IO>::to_f(raw[kBC + 2 * kCH + e]);
                     if (p.z) {
@@ -334,11 +337,12 @@ struct BwdRing {
 // computes.
 template <typename IO, int G, int Q>
 constexpr size_t bwd_ckpt_smem_bytes() {
-    return (size_t)(BwdCfg<G, Q>::kOffU + BwdCfg<G, Q>::kChan) * sizeof(float) + BwdRing<IO, G, Q, false>::bytes();
+    return (size_t)(BwdCfg<G, Q>::kOffU + BwdCfg<G, Q>::kChan + BwdCfg<G, Q>::kCpb) * sizeof(float) +
+           BwdRing<IO, G, Q, false>::bytes();
 }
 template <typename IO, int G, int Q>
 constexpr size_t bwd_smem_bytes() {
-    return (size_t)BwdCfg<G, Q>::kFloats * sizeof(float) + BwdRing<IO, G, Q, true>::bytes();
+    return (size_t)(BwdCfg<G, Q>::kFloats + BwdCfg<G, Q>::kCpb) * sizeof(float) + BwdRing<IO, G, Q, true>::bytes();
 }
 
 // A lane's Q consecutive floats at p (16-byte or 8-byte aligned) as Q/2 packed pairs.
@@ -373,7 +377,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
     }
     float *ck = p.ckpt + bd * (int64_t)p.nseg * kNP;
     using Ring = BwdRing<IO, G, Q, false>;
-    unsigned char *ring = reinterpret_cast<unsigned char *>(sm + Cfg::kOffU + Cfg::kChan);
+    float *sbias = sm + Cfg::kOffU + Cfg::kChan;    // the CTA's channels' dt bias (0 without one)
+    unsigned char *ring = reinterpret_cast<unsigned char *>(sbias + kCpb);
+    for (int c = tid; c < kCpb; c += kBwdThreads)
+        sbias[c] = (p.bias && d0 + c < p.Dm) ? p.bias[d0 + c] : 0.0f;   // read after the loop's first barrier
     BwdFetch<IO, G, Q, false> f;
     float2 ck_unused[kP];
     if (p.ring) {
@@ -395,8 +402,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
         }
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();
-        if (p.ring) Ring::stage(p, ring, sm, seg, d0, ck_unused);
-        else f.stage(p, sm, (int64_t)seg * kS, d0);
+        if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ck_unused);
+        else f.stage(p, sm, sbias, (int64_t)seg * kS, d0);
         __syncthreads();
         if (p.ring) {            // the slot of segment seg - 1, staged before the barriers above
             if (seg + Ring::kStages - 1 < p.nseg) Ring::issue(p, ring, b, seg + Ring::kStages - 1, d0);
@@ -475,7 +482,10 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
     };
 
     using Ring = BwdRing<IO, G, Q, true>;
-    unsigned char *ring = reinterpret_cast<unsigned char *>(sm + Cfg::kFloats);
+    float *sbias = sm + Cfg::kFloats;               // the CTA's channels' dt bias (0 without one)
+    unsigned char *ring = reinterpret_cast<unsigned char *>(sbias + kCpb);
+    for (int c = tid; c < kCpb; c += kBwdThreads)
+        sbias[c] = (p.bias && d0 + c < p.Dm) ? p.bias[d0 + c] : 0.0f;   // read after the loop's first barrier
     BwdFetch<IO, G, Q, true> f;
     // the segment's checkpoint, fetched with its inputs one segment ahead
     auto fetch_ck = [&](int seg, float2 (&out)[kP]) {
@@ -499,8 +509,8 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
         const int64_t t0 = (int64_t)seg * kS;
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();                        // the previous segment is done with shared memory
-        if (p.ring) Ring::stage(p, ring, sm, seg, d0, ckn);
-        else f.stage(p, sm, t0, d0);
+        if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ckn);
+        else f.stage(p, sm, sbias, t0, d0);
         __syncthreads();
         // states as pairs (q = 2k, 2k+1): hs[k][0] before the segment, hs[k][i+1] after step t0+i
         float2 hs[kP][kS + 1];
