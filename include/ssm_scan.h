@@ -387,6 +387,8 @@ int ssm_set_structured_a(int enable);
  *                           checks fire). Ignored by the normal build.
  *   bwd_states_per_lane     ssm_selective_scan_bwd: 4 (the default) or 2 states per lane (taken
  *                           for dstate <= 32; more lanes per channel, fewer registers).
+ *   bwd_chunks              ssm_selective_scan_bwd: the number of sequence chunks of the time
+ *                           split (1 = none; clamped to the number of 8-step segments).
  * ssm_set_plan_override(NULL) restores the planner. Returns SSM_ERR_UNSUPPORTED for an
  * unknown kernel, lane split or states-per-lane value and SSM_ERR_SHAPE for a negative count;
  * the previous override then stays in force.
@@ -409,6 +411,7 @@ typedef struct {
     int force_timeout;
     int check_probe;
     int bwd_states_per_lane;
+    int bwd_chunks;
 } ssm_plan_override_t;
 
 ssm_status_t ssm_set_plan_override(const ssm_plan_override_t *ov);

@@ -52,6 +52,15 @@ struct BwdParams {
     int pair2;                    // 1: rows read two steps at a time (L even, bases 2-element aligned)
     int ring;                     // 1: rows staged by asynchronous 16-byte copies (L*esz % 16 == 0,
                                   //    16-byte aligned bases)
+    // time split: chunk k covers segments [k*seg_per_chunk, min(nseg, (k+1)*seg_per_chunk));
+    // with nchunk > 1 (the arrays below are then in the workspace after ckpt):
+    int nchunk, seg_per_chunk;
+    float *cumdt;                 // [Bt*Dm][nseg]: sum of dt from the chunk's first step to the segment's
+    float *hloc;                  // [Bt*Dm][nchunk][Q*G]: chunk-end state of the recurrence from 0;
+                                  //    after the combine, the state entering the chunk
+    float *sdt;                   // [Bt*Dm][nchunk]: sum of dt over the chunk
+    float *cloc;                  // [Bt*Dm][nchunk][Q*G]: adjoint carry out of the chunk's start, from 0
+    float *cin;                   // [Bt*Dm][nchunk][Q*G]: adjoint carry into the chunk's last step
 };
 
 // Shared-memory layout (floats) of the backward kernels for G lanes per channel and Q states
@@ -73,7 +82,7 @@ struct BwdCfg {
     static constexpr int kFloats = kOffPart + 2 * kCpb * kPartCh;
     static_assert(kS % 4 == 0 && (kOffPart % 4) == 0 && (kPartCh % 4) == 0 && (kRow % 4) == 0, "16-byte rows");
 };
-template <typename IO, int G, int Q, bool FULL>
+template <typename IO, int G, int Q, bool FULL, bool CK>
 struct BwdRing;
 template <typename IO, int G, int Q>
 constexpr size_t bwd_smem_bytes();
@@ -220,10 +229,10 @@ struct BwdFetch {
 // Raw inputs of one segment copied into a shared-memory ring by cp.async, kStages - 1 segments
 // ahead, where every row is a multiple of 16 bytes long and starts on a 16-byte boundary. A
 // slot holds the segment's rows as [row][S] io elements -- B (FULL: then C) rows n < kNP, then
-// delta, u (FULL: dy, z) rows of the CTA's channels -- and (FULL) the checkpoints of the CTA's
+// delta, u (FULL: dy, z) rows of the CTA's channels -- and (CK) the checkpoints of the CTA's
 // channels as [channel][kNP] floats. Pieces of rows beyond N, Dm or L are not copied; stage()
 // reads zeros in their place.
-template <typename IO, int G, int Q, bool FULL>
+template <typename IO, int G, int Q, bool FULL, bool CK = FULL>
 struct BwdRing {
     using Cfg = BwdCfg<G, Q>;
     static constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kCpb = Cfg::kCpb, kQ = Cfg::kQ;
@@ -231,7 +240,7 @@ struct BwdRing {
     static constexpr int kGran = kS / kStepsPerPiece;                 // pieces per row segment
     static constexpr int kRowsBC = (FULL ? 2 : 1) * kNP, kRowsCH = (FULL ? 4 : 2) * kCpb;
     static constexpr int kRows = kRowsBC + kRowsCH;
-    static constexpr int kCkFloats = FULL ? kCpb * kNP : 0;
+    static constexpr int kCkFloats = CK ? kCpb * kNP : 0;
     // measured on B300: deeper rings change neither pass (adjoint 3 stages, checkpoint 6); a
     // 2-stage checkpoint ring is 8-35% slower
     static constexpr int kStages = FULL ? 2 : 4;
@@ -320,7 +329,7 @@ struct BwdRing {
                 sm[Cfg::kOffGz + e] = gz;
             }
         }
-        if (FULL) {
+        if (CK) {
             const int g = tid % G, cc = tid / G;
             const float *ck = reinterpret_cast<const float *>(reinterpret_cast<const unsigned char *>(raw) +
                                                               kRows * kS * sizeof(IO)) + cc * kNP;
@@ -339,6 +348,11 @@ template <typename IO, int G, int Q>
 constexpr size_t bwd_ckpt_smem_bytes() {
     return (size_t)(BwdCfg<G, Q>::kOffU + BwdCfg<G, Q>::kChan + BwdCfg<G, Q>::kCpb) * sizeof(float) +
            BwdRing<IO, G, Q, false>::bytes();
+}
+// the adjoint aggregate pass: the adjoint's staging without the partial sums or checkpoints
+template <typename IO, int G, int Q>
+constexpr size_t bwd_agg_smem_bytes() {
+    return (size_t)(BwdCfg<G, Q>::kOffPart + BwdCfg<G, Q>::kCpb) * sizeof(float) + BwdRing<IO, G, Q, true, false>::bytes();
 }
 template <typename IO, int G, int Q>
 constexpr size_t bwd_smem_bytes() {
@@ -376,6 +390,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
         h2[k] = make_float2(0.f, 0.f);
     }
     float *ck = p.ckpt + bd * (int64_t)p.nseg * kNP;
+    // this CTA's chunk of segments; the state starts from 0 at the chunk (time split: the
+    // true state is added to these checkpoints once the chunks' end states are combined)
+    const int kc = blockIdx.z, s0 = kc * p.seg_per_chunk, s1 = min(p.nseg, s0 + p.seg_per_chunk);
+    float cum = 0.0f;                               // sum of dt from the chunk's first step
     using Ring = BwdRing<IO, G, Q, false>;
     float *sbias = sm + Cfg::kOffU + Cfg::kChan;    // the CTA's channels' dt bias (0 without one)
     unsigned char *ring = reinterpret_cast<unsigned char *>(sbias + kCpb);
@@ -386,19 +404,20 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
     if (p.ring) {
 #pragma unroll
         for (int s = 0; s < Ring::kStages - 1; ++s) {
-            if (s < p.nseg) Ring::issue(p, ring, b, s, d0);
+            if (s0 + s < s1) Ring::issue(p, ring, b, s0 + s, d0);
             cp_async_commit();
         }
     } else {
-        f.fetch(p, b, 0, d0);
+        f.fetch(p, b, (int64_t)s0 * kS, d0);
     }
-    for (int seg = 0; seg < p.nseg; ++seg) {
+    for (int seg = s0; seg < s1; ++seg) {
         if (valid) {
 #pragma unroll
             for (int k = 0; k < kP; ++k) {
                 ck[(int64_t)seg * kNP + g + G * 2 * k] = h2[k].x;
                 ck[(int64_t)seg * kNP + g + G * (2 * k + 1)] = h2[k].y;
             }
+            if (p.nchunk > 1 && g == 0) p.cumdt[bd * p.nseg + seg] = cum;
         }
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();
@@ -406,15 +425,16 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
         else f.stage(p, sm, sbias, (int64_t)seg * kS, d0);
         __syncthreads();
         if (p.ring) {            // the slot of segment seg - 1, staged before the barriers above
-            if (seg + Ring::kStages - 1 < p.nseg) Ring::issue(p, ring, b, seg + Ring::kStages - 1, d0);
+            if (seg + Ring::kStages - 1 < s1) Ring::issue(p, ring, b, seg + Ring::kStages - 1, d0);
             cp_async_commit();
-        } else if (seg + 1 < p.nseg) {
+        } else if (seg + 1 < s1) {
             f.fetch(p, b, (int64_t)(seg + 1) * kS, d0);   // in flight during this segment
         }
 #pragma unroll
         for (int i = 0; i < kS; ++i) {
             const float dt = sm[Cfg::kOffDt + cc * kS + i];
             const float x = dt * sm[Cfg::kOffU + cc * kS + i];
+            cum += dt;
             float2 bv[kP];
             load_pairs<kP>(sm + Cfg::kOffB + (i * G + g) * kQ, bv);
 #pragma unroll
@@ -422,6 +442,89 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
                 const float2 e = __fmul2_rn(make_float2(dt, dt), Ap2[k]);
                 h2[k] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), h2[k], __fmul2_rn(make_float2(x, x), bv[k]));
             }
+        }
+    }
+    if (p.nchunk > 1 && valid) {            // the chunk's end state from 0 and its dt sum
+        float *hl = p.hloc + (bd * p.nchunk + kc) * kNP;
+#pragma unroll
+        for (int k = 0; k < kP; ++k) {
+            hl[g + G * 2 * k] = h2[k].x;
+            hl[g + G * (2 * k + 1)] = h2[k].y;
+        }
+        if (g == 0) p.sdt[bd * p.nchunk + kc] = cum;
+    }
+}
+
+// Time split, adjoint aggregate pass (chunks 1 .. nchunk-1): the reverse recurrence
+// c_{t-1} = a_t (dyhat_t C_t + c_t) over the chunk from c = 0 at its last step; stores the
+// carry leaving its first step (cloc). The carry that actually enters each chunk is then
+// cin_{k-1} = (prod of a_t over chunk k) cin_k + cloc_k, with cin_{last} = dlast.
+template <typename IO, int G, int Q>
+__global__ void __launch_bounds__(kBwdThreads) scan_bwd_agg_kernel(const BwdParams p) {
+    using Cfg = BwdCfg<G, Q>;
+    constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
+    extern __shared__ float4 smem_bwd4[];
+    float *sm = reinterpret_cast<float *>(smem_bwd4);
+    const int tid = threadIdx.x, g = tid % G, cc = tid / G;
+    const int64_t b = blockIdx.y, d0 = (int64_t)blockIdx.x * kCpb, d = d0 + cc;
+    const bool valid = d < p.Dm;
+    const int64_t bd = b * p.Dm + (valid ? d : 0);
+    const int kc = blockIdx.z + 1, s0 = kc * p.seg_per_chunk, s1 = min(p.nseg, s0 + p.seg_per_chunk);
+    float2 Ap2[kP], c2[kP];
+#pragma unroll
+    for (int k = 0; k < kP; ++k) {
+        const int n0 = g + G * 2 * k, n1 = n0 + G;
+        Ap2[k] = make_float2((valid && n0 < p.N) ? p.A[(valid ? d : 0) * p.N + n0] * kLog2e : 0.0f,
+                             (valid && n1 < p.N) ? p.A[(valid ? d : 0) * p.N + n1] * kLog2e : 0.0f);
+        c2[k] = make_float2(0.f, 0.f);
+    }
+    using Ring = BwdRing<IO, G, Q, true, false>;
+    float *sbias = sm + Cfg::kOffPart;
+    unsigned char *ring = reinterpret_cast<unsigned char *>(sbias + kCpb);
+    for (int c = tid; c < kCpb; c += kBwdThreads)
+        sbias[c] = (p.bias && d0 + c < p.Dm) ? p.bias[d0 + c] : 0.0f;   // read after the loop's first barrier
+    BwdFetch<IO, G, Q, true> f;
+    float2 ck_unused[kP];
+    if (p.ring) {
+#pragma unroll
+        for (int s = 0; s < Ring::kStages - 1; ++s) {
+            if (s1 - 1 - s >= s0) Ring::issue(p, ring, b, s1 - 1 - s, d0);
+            cp_async_commit();
+        }
+    } else {
+        f.fetch(p, b, (int64_t)(s1 - 1) * kS, d0);
+    }
+    for (int seg = s1 - 1; seg >= s0; --seg) {
+        if (p.ring) cp_async_wait<Ring::kStages - 2>();
+        __syncthreads();
+        if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ck_unused);
+        else f.stage(p, sm, sbias, (int64_t)seg * kS, d0);
+        __syncthreads();
+        if (p.ring) {
+            if (seg - (Ring::kStages - 1) >= s0) Ring::issue(p, ring, b, seg - (Ring::kStages - 1), d0);
+            cp_async_commit();
+        } else if (seg > s0) {
+            f.fetch(p, b, (int64_t)(seg - 1) * kS, d0);
+        }
+#pragma unroll
+        for (int i = kS - 1; i >= 0; --i) {
+            const float dt = sm[Cfg::kOffDt + cc * kS + i], dyh = sm[Cfg::kOffDyh + cc * kS + i];
+            float2 cv[kP];
+            load_pairs<kP>(sm + Cfg::kOffC + (i * G + g) * kQ, cv);
+#pragma unroll
+            for (int k = 0; k < kP; ++k) {
+                const float2 e = __fmul2_rn(make_float2(dt, dt), Ap2[k]);
+                const float2 lam = __ffma2_rn(make_float2(dyh, dyh), cv[k], c2[k]);
+                c2[k] = __fmul2_rn(make_float2(ex2(e.x), ex2(e.y)), lam);
+            }
+        }
+    }
+    if (valid) {
+        float *cl = p.cloc + (bd * p.nchunk + kc) * kNP;
+#pragma unroll
+        for (int k = 0; k < kP; ++k) {
+            cl[g + G * 2 * k] = c2[k].x;
+            cl[g + G * (2 * k + 1)] = c2[k].y;
         }
     }
 }
@@ -449,7 +552,9 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
         const int n = g + G * q;
         nv[q] = valid && n < p.N;
         An[q] = nv[q] ? p.A[dd * p.N + n] : 0.0f;
-        c[q] = (nv[q] && p.dlast) ? p.dlast[bd * p.N + n] : 0.0f;
+        c[q] = !nv[q] ? 0.0f
+               : p.nchunk > 1 ? p.cin[(bd * p.nchunk + blockIdx.z) * kNP + n]
+               : p.dlast ? p.dlast[bd * p.N + n] : 0.0f;
     }
     // as state pairs (q = 2k, 2k+1) for the packed arithmetic
     float2 An2[kP], Ap2[kP], c2[kP], dA2[kP];
@@ -495,17 +600,19 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
                            : make_float2(0.f, 0.f);
     };
     float2 ckn[kP];
+    // this CTA's chunk of segments, walked backwards from its last
+    const int s0 = blockIdx.z * p.seg_per_chunk, s1 = min(p.nseg, s0 + p.seg_per_chunk);
     if (p.ring) {
 #pragma unroll
         for (int s = 0; s < Ring::kStages - 1; ++s) {
-            if (p.nseg - 1 - s >= 0) Ring::issue(p, ring, b, p.nseg - 1 - s, d0);
+            if (s1 - 1 - s >= s0) Ring::issue(p, ring, b, s1 - 1 - s, d0);
             cp_async_commit();
         }
     } else {
-        f.fetch(p, b, (int64_t)(p.nseg - 1) * kS, d0);
-        fetch_ck(p.nseg - 1, ckn);
+        f.fetch(p, b, (int64_t)(s1 - 1) * kS, d0);
+        fetch_ck(s1 - 1, ckn);
     }
-    for (int seg = p.nseg - 1; seg >= 0; --seg) {
+    for (int seg = s1 - 1; seg >= s0; --seg) {
         const int64_t t0 = (int64_t)seg * kS;
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();                        // the previous segment is done with shared memory
@@ -517,9 +624,9 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
 #pragma unroll
         for (int k = 0; k < kP; ++k) hs[k][0] = ckn[k];
         if (p.ring) {   // into the slot of segment seg + 1, staged before the barriers above
-            if (seg - (Ring::kStages - 1) >= 0) Ring::issue(p, ring, b, seg - (Ring::kStages - 1), d0);
+            if (seg - (Ring::kStages - 1) >= s0) Ring::issue(p, ring, b, seg - (Ring::kStages - 1), d0);
             cp_async_commit();
-        } else if (seg > 0) {   // the next segment's inputs and checkpoint, in flight meanwhile
+        } else if (seg > s0) {   // the next segment's inputs and checkpoint, in flight meanwhile
             f.fetch(p, b, t0 - kS, d0);
             fetch_ck(seg - 1, ckn);
         }

@@ -830,26 +830,60 @@ size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims) {
 }  // extern "C"
 
 namespace {
-// backward lane split: Q states per thread, G lanes per channel (the smallest power of two
-// with Q*G >= N: 1-32 at four states, 2-16 at two). Two states per thread for N <= 32 when
-// four give fewer than half a warp per SM sub-partition: the passes are latency-bound, so
-// twice the lanes nearly halve the time there. Measured on B300 (bf16, gate), four vs two:
-// 1 x 768 x 8192 x 16 3.45 vs 2.03 ms, 2 x 512 x 4096 x 8 2.84 vs 1.32 ms; with more channels
-// four win or tie: 1 x 1536 x 4096 x 32 1.36 vs 1.52 ms, 8 x 1536 x 2048 x 16 1.24 vs 1.24 ms.
-struct BwdSplit {
-    int G, Q;
+// Backward plan. Lane split: Q states per thread, G lanes per channel (the smallest power of
+// two with Q*G >= N: 1-32 at four states, 2-16 at two), 128/G channels per CTA. Time split:
+// with fewer than two CTAs per SM, the sequence is cut into K chunks of whole 8-step segments
+// (at least 16 segments each, K <= 32) aiming at about 8 CTAs per SM; each chunk is a CTA of
+// the checkpoint, aggregate and adjoint passes. Q = 2 for N <= 8, else 4; without a possible
+// time split, also Q = 2 when four states per lane give fewer than half a warp per SM
+// sub-partition. Measured on B300 (bf16, gate, ms; planner's choice first):
+//   1 x 768 x 8192 x 16:   Q4 K50 0.39; Q4 K16 0.41; Q2 K37 0.42; Q2 unsplit 1.89
+//   1 x 1536 x 4096 x 32:  Q4 K13 0.66; Q4 K4 0.69; Q2 K10 0.97; Q4 unsplit 1.27
+//   2 x 512 x 4096 x 8:    Q2 K32 ~0.20; Q4 K74 0.28; Q2 unsplit 1.30
+//   1 x 5120 x 4096 x 16:  Q4 K8 1.12; Q4 K3 1.38; Q2 unsplit 1.32
+//   2 x 1536 x 16384 x 16: Q4 K13 2.66; Q4 K4 2.95; Q2 K10 2.96; Q2 unsplit 4.38
+//   4 x 1536 x 2048 x 16:  Q4 K7 0.73; Q2 unsplit 0.67
+//   8 x 1536 x 2048 x 16:  Q4 unsplit 1.10; Q4 K4 1.30; Q2 unsplit 1.29
+struct BwdPlan {
+    int G, Q, nchunk, seg_per_chunk;
+    int64_t nseg;
 };
-BwdSplit bwd_split(int64_t batch_dim, int64_t N) {
+BwdPlan bwd_plan(const ssm_dims_t &d) {
+    const int64_t N = d.dstate, nseg = (d.seqlen + kBwdS - 1) / kBwdS, sms = sm_count();
     auto lanes = [&](int q) {
         int g = q == 2 ? 2 : 1;
         while (g < 32 && (int64_t)g * q < N) g *= 2;
         return g;
     };
-    const int forced = plan_override().bwd_states_per_lane;
-    bool two = N <= 32 && batch_dim * lanes(4) < 64 * sm_count();
-    if (forced == 4 || N > 32) two = false;
-    if (forced == 2 && N <= 32) two = true;
-    return two ? BwdSplit{lanes(2), 2} : BwdSplit{lanes(4), 4};
+    auto ctas = [&](int q) {
+        const int64_t cpb = 128 / lanes(q);
+        return (d.dim + cpb - 1) / cpb * d.batch;
+    };
+    const ssm_plan_override_t ov = plan_override();
+    auto chunks = [&](int q) -> int64_t {
+        int64_t k = 1;
+        if (ov.bwd_chunks > 0) k = ov.bwd_chunks;
+        else if (ctas(q) < 2 * sms) k = std::min<int64_t>({(8 * sms + ctas(q) - 1) / ctas(q), nseg / 16, 32});
+        return std::max<int64_t>(1, std::min<int64_t>({k, nseg, 65535}));
+    };
+    int q = 4;
+    if (ov.bwd_states_per_lane == 2 && N <= 32) q = 2;
+    else if (ov.bwd_states_per_lane == 0 && N <= 8) q = 2;
+    else if (ov.bwd_states_per_lane == 0 && N <= 32 && chunks(4) == 1 && d.batch * d.dim * lanes(4) < 64 * sms)
+        q = 2;
+    if (nseg == 0) return BwdPlan{lanes(q), q, 1, 0, 0};
+    const int64_t k = chunks(q), spc = (nseg + k - 1) / k;
+    return BwdPlan{lanes(q), q, (int)((nseg + spc - 1) / spc), (int)spc, nseg};
+}
+// workspace floats of a backward plan: the checkpoints, and with a time split the per-segment
+// dt sums and the per-chunk states and carries (hloc, sdt, cloc, cin); the two per-row arrays
+// are padded to 4 floats so that every array starts on a 16-byte boundary
+int64_t round4(int64_t x) { return (x + 3) / 4 * 4; }
+int64_t bwd_workspace_floats(const ssm_dims_t &d, const BwdPlan &pl) {
+    const int64_t BD = d.batch * d.dim, np = pl.G * pl.Q;
+    int64_t f = BD * pl.nseg * np;
+    if (pl.nchunk > 1) f += round4(BD * pl.nseg) + round4(BD * pl.nchunk) + 3 * BD * pl.nchunk * np;
+    return f;
 }
 }  // namespace
 
@@ -858,9 +892,7 @@ extern "C" {
 size_t ssm_selective_scan_bwd_workspace_bytes(const ssm_dims_t *dims) {
     if (check_dims(dims, true) != SSM_OK) return 0;
     if (dims->batch == 0 || dims->dim == 0 || dims->seqlen == 0) return 0;
-    const BwdSplit sp = bwd_split(dims->batch * dims->dim, dims->dstate);
-    const int64_t nseg = (dims->seqlen + kBwdS - 1) / kBwdS;
-    return (size_t)(dims->batch * dims->dim) * (size_t)nseg * (size_t)(sp.G * sp.Q) * sizeof(float);
+    return (size_t)bwd_workspace_floats(*dims, bwd_plan(*dims)) * sizeof(float);
 }
 
 ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const void *delta, const float *A,
@@ -904,9 +936,24 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     bool allocated = false;
     st = acquire_workspace(&ws, w.bytes, need, w.may_alloc, s, &allocated);
     if (st != SSM_OK) return st;
+    const BwdPlan pl = bwd_plan(d);
     BwdParams p{u, delta, z, B, C, dy, A, D, delta_bias, dlast_state, du, ddelta, dA, dB, dC, dD,
                 z ? dz : nullptr, ddelta_bias, static_cast<float *>(ws), d.batch, d.dim, d.seqlen,
-                d.dstate, delta_softplus ? 1 : 0, (int)((d.seqlen + kBwdS - 1) / kBwdS), 0, 0};
+                d.dstate, delta_softplus ? 1 : 0, (int)pl.nseg, 0, 0, pl.nchunk, pl.seg_per_chunk,
+                nullptr, nullptr, nullptr, nullptr, nullptr};
+    if (pl.nchunk > 1) {   // after the checkpoints: cumdt, hloc, sdt, cloc, cin
+        const int64_t BD = d.batch * d.dim, np = pl.G * pl.Q, K = pl.nchunk;
+        float *q = static_cast<float *>(ws) + BD * pl.nseg * np;
+        p.cumdt = q;
+        q += round4(BD * pl.nseg);
+        p.hloc = q;
+        q += BD * K * np;
+        p.sdt = q;
+        q += round4(BD * K);
+        p.cloc = q;
+        q += BD * K * np;
+        p.cin = q;
+    }
     // rows read two steps per load: an even length and every row base on a 2-element boundary
     bool pair2 = d.seqlen % 2 == 0;
     for (const void *q : io_ptrs)
@@ -917,8 +964,7 @@ ssm_status_t ssm_selective_scan_bwd(const ssm_dims_t *dims, const void *u, const
     for (const void *q : io_ptrs)
         if (q != nullptr && !aligned16(q)) ring = false;
     p.ring = ring ? 1 : 0;
-    const BwdSplit sp = bwd_split(d.batch * d.dim, d.dstate);
-    const cudaError_t e = launch_bwd(d.io_dtype, sp.G, sp.Q, p, s);
+    const cudaError_t e = launch_bwd(d.io_dtype, pl.G, pl.Q, p, s);
     if (allocated) cudaFreeAsync(ws, s);
     if (e == cudaErrorInvalidConfiguration) {
         cudaGetLastError();
@@ -1123,6 +1169,7 @@ ssm_status_t ssm_set_plan_override(const ssm_plan_override_t *ov) {
         if (v.chunks < 0 || v.seq_states_per_lane < 0 || v.seq_lanes_per_channel < 0) return SSM_ERR_SHAPE;
         if (v.bwd_states_per_lane != 0 && v.bwd_states_per_lane != 2 && v.bwd_states_per_lane != 4)
             return SSM_ERR_UNSUPPORTED;
+        if (v.bwd_chunks < 0) return SSM_ERR_SHAPE;
         if ((v.seq_states_per_lane != 0 || v.seq_lanes_per_channel != 0) &&
             !seq_plan_supported(v.seq_states_per_lane, v.seq_lanes_per_channel))
             return SSM_ERR_UNSUPPORTED;
@@ -1138,6 +1185,6 @@ ssm_status_t ssm_get_plan_override(ssm_plan_override_t *out) {
     return SSM_OK;
 }
 
-int ssm_version(void) { return (1 << 16) | 2; }
+int ssm_version(void) { return (1 << 16) | 3; }
 
 }  // extern "C"

@@ -51,7 +51,8 @@ class PlanOverride(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("pair_states_per_lane", ctypes.c_int), ("chunks", ctypes.c_int),
                 ("seq_states_per_lane", ctypes.c_int), ("seq_lanes_per_channel", ctypes.c_int),
                 ("decode_elementwise", ctypes.c_int), ("force_timeout", ctypes.c_int),
-                ("check_probe", ctypes.c_int), ("bwd_states_per_lane", ctypes.c_int)]
+                ("check_probe", ctypes.c_int), ("bwd_states_per_lane", ctypes.c_int),
+                ("bwd_chunks", ctypes.c_int)]
 
 
 class SsmError(RuntimeError):
@@ -373,14 +374,15 @@ def set_plan_override(ov: Optional[PlanOverride]) -> None:
 @contextlib.contextmanager
 def plan_override(kernel: str = "auto", pair_states_per_lane: int = 0, chunks: int = 0,
                   seq_split: Optional[Tuple[int, int]] = None, decode_elementwise: bool = False,
-                  force_timeout: bool = False, check_probe: bool = False, bwd_states_per_lane: int = 0):
+                  force_timeout: bool = False, check_probe: bool = False, bwd_states_per_lane: int = 0,
+                  bwd_chunks: int = 0):
     """Force a launch plan for the calls inside the block (ssm_set_plan_override; a test and
     tuning hook), then restore the override that was in force before."""
     prev = get_plan_override()
     ov = PlanOverride(_KERNELS[kernel], int(pair_states_per_lane), int(chunks),
                       int(seq_split[0]) if seq_split else 0, int(seq_split[1]) if seq_split else 0,
                       int(bool(decode_elementwise)), int(bool(force_timeout)), int(bool(check_probe)),
-                      int(bwd_states_per_lane))
+                      int(bwd_states_per_lane), int(bwd_chunks))
     set_plan_override(ov)
     try:
         yield ov

@@ -56,7 +56,8 @@ def test_status_strings_and_version(lib):
         s = ssm.status_string(code)
         assert s.startswith("SSM_")
     assert ssm.status_string(99) == "SSM_ERR_UNKNOWN"
-    assert ssm.version() == (1, 2)   # 1.1: workspace, plan override; 1.2: last CUDA error
+    assert ssm.version() == (1, 3)   # 1.1: workspace, plan override; 1.2: last CUDA error;
+    # 1.3: the backward time split (plan override field bwd_chunks)
 
 
 def test_last_cuda_error_query(lib):
@@ -203,6 +204,17 @@ def test_plan_override_roundtrip_and_errors(lib):
         with ssm.plan_override(bwd_states_per_lane=4):
             b64 = lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(d64))
         assert lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(d64)) == b64
+    # backward time split: checkpoints [BD][nseg][np], then per-segment dt sums [BD][nseg] and
+    # per-chunk hloc, cloc, cin [BD][K][np] and sdt [BD][K], the two per-row arrays padded to
+    # 4 floats (2 x 7 x 100 x 16: np = 16, 13 segments, 3 chunks of 5 segments)
+    d7 = ssm.dims(2, 7, 100, 16, ssm.SSM_F32)
+    with ssm.plan_override(bwd_states_per_lane=2):
+        assert lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(d7)) == 4 * 14 * 13 * 16
+        with ssm.plan_override(bwd_states_per_lane=2, bwd_chunks=3):
+            assert lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(d7)) == \
+                4 * (14 * 13 * 16 + 184 + 44 + 3 * 14 * 3 * 16)    # 14*13, 14*3 padded to 4
+    bad = ssm.PlanOverride(0, 0, 0, 0, 0, 0, 0, 0, 0, -1)     # negative chunk count
+    assert lib.ssm_set_plan_override(ctypes.byref(bad)) == ssm.SSM_ERR_SHAPE
     with ssm.plan_override(kernel="tc"):
         # the time-split plan keeps fp32 B/C of the whole sequence in its workspace
         assert ssm.workspace_bytes(1, 1536, 131072, 64) > 2 * 64 * 131072 * 4

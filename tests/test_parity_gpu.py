@@ -174,11 +174,36 @@ def test_backward_gradients_forced_split(Bt, D, L, N, io, gate, dskip, bias, dla
         _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind)
 
 
+@pytest.mark.parametrize("chunks", [1, 3])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_backward_rows_off_pair_alignment(io):
+def test_backward_rows_off_pair_alignment(io, chunks):
     """Even length with every input one element off a 2-element boundary: the rows are read
-    one step per load instead of two."""
-    _check_backward(2, 9, 70, 16, io, True, "normal", True, True, "scaled", odd_offset=True)
+    one step per load instead of two (also under a time split)."""
+    with ssm.plan_override(bwd_chunks=chunks):
+        _check_backward(2, 9, 70, 16, io, True, "normal", True, True, "scaled", odd_offset=True)
+
+
+@pytest.mark.parametrize("chunks", [2, 3, 7])
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,bias,dlast,a_kind", BWD_CASES)
+def test_backward_gradients_time_split(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind, chunks):
+    """The sequence cut into chunks of whole 8-step segments (the last one ragged where the
+    segments do not divide evenly; 7 is clamped to the segment count on the shortest cases):
+    chunk-local checkpoints corrected by the combined chunk states, adjoint carries from the
+    aggregate pass."""
+    with ssm.plan_override(bwd_chunks=chunks):
+        _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind)
+
+
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,bias,dlast,a_kind", [c for c in BWD_CASES if c[3] <= 32])
+def test_backward_time_split_two_states_per_lane(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind):
+    with ssm.plan_override(bwd_chunks=3, bwd_states_per_lane=2):
+        _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind)
+
+
+def test_backward_planner_time_split():
+    """One channel block over 2048 steps: the planner cuts the sequence into 16 chunks by
+    itself (fewer than two CTAs per SM otherwise)."""
+    _check_backward(1, 32, 2048, 16, "bf16", True, "ones", True, True, "random")
 
 
 def _odd_offset(t):
