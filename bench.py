@@ -469,8 +469,10 @@ def bench_ours(args, rank, ws, local):
                       "entry": "ssm_selective_scan_fwd_host (pinned host buffers)"}
         del pin, yh
     if not args.no_bwd:
-        out["backward"] = bench_backward(dev, ws)
+        out["backward"] = bench_backward(dev, ws, gen.M130)
         out["gpu_launches"] += out["backward"]["launches"]
+        out["backward_long"] = bench_backward(dev, ws, gen.BWD_LONG)
+        out["gpu_launches"] += out["backward_long"]["launches"]
     if not args.no_decode:
         out["decode"] = bench_decode(dev)
         out["gpu_launches"] += out["decode"]["launches"]
@@ -533,11 +535,12 @@ def bench_config(cfg, dev, stream, timed, ex2_peak, hbm):
             "launches_per_step": 3 if ws_bytes > 0 else 1}
 
 
-def bench_backward(dev, ws):
-    """Gradients of the scan (ssm_selective_scan_bwd) on the batch-8 workload (8 x 1536 x 2048
-    x 16, bf16, gate and bias): checkpointed forward + reverse adjoint, fp32 gradients."""
+def bench_backward(dev, ws, cfg):
+    """Gradients of the scan (ssm_selective_scan_bwd), bf16 io with gate and bias, fp32
+    gradients: checkpointed forward + reverse adjoint, with the planner's time split where the
+    channel blocks alone do not fill the GPU (the batch-8 workload 8 x 1536 x 2048 x 16 runs
+    unsplit; 1 x 1536 x 16384 x 16 split)."""
     from selective_state_space_153_b300 import ssm
-    cfg = gen.M130
     inp = gen.scan_inputs(cfg)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     dy = torch.randn(g["u"].shape, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).to(dev)
@@ -551,6 +554,13 @@ def bench_backward(dev, ws):
     for _ in range(2):
         step()
     torch.cuda.synchronize()
+    # kernels of one call, counted once outside the timed region
+    from torch.profiler import profile, ProfilerActivity
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        step()
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if e.device_type.name == "CUDA" and "bwd" in e.name]
+    per_call = len(names)
     k = 5
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
@@ -565,7 +575,8 @@ def bench_backward(dev, ws):
             "ms_per_step": ms, "value": ws * elems / (ms / 1e3), "unit": "elem/s",
             "exps_per_element": 3,
             "roofline_frac_of_ex2_peak": 3 * elems / (ms / 1e3) / (SM_COUNT * EX2_PER_CLK_SM * 2032.0e6),
-            "launches": 2 * k + 2 * 2}
+            "kernels_per_call": sorted(set(n.split("(")[0] for n in names)),
+            "launches": per_call * (k + 2 + 1)}
 
 
 def ctypes_dims(Bt, Dm, L, N):

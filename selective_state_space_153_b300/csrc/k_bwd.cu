@@ -1,12 +1,8 @@
 // Selective scan backward launches (scan_bwd.cuh): checkpoint pass; with a time split the
-// adjoint aggregate pass, the chunk combine and the checkpoint correction; then the adjoint
-// pass.
+// adjoint aggregate pass and the chunk combine; then the adjoint pass.
 #include "launch.h"
 
 namespace ssm {
-
-namespace {
-using bf16 = __nv_bfloat16;
 
 // Time split, combine: one thread per (batch row and channel, state slot n < np). Walks the
 // chunks forwards with the state entering each (H_0 = 0, H_{k+1} = exp(A*sdt_k) H_k + hloc_k),
@@ -32,36 +28,21 @@ __global__ void __launch_bounds__(256) bwd_chunk_combine_kernel(const BwdParams 
     }
 }
 
-// Time split, checkpoints of chunks 1..: the checkpoint pass took the state from 0 at the
-// chunk; add exp(A*cumdt) H_k, H_k the state entering the chunk. One thread per four state
-// slots of one (batch row and channel, segment).
-__global__ void __launch_bounds__(256) bwd_ckpt_fix_kernel(const BwdParams p, int np) {
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int nq = np / 4;
-    if (idx >= p.Bt * p.Dm * p.nseg * nq) return;
-    const int64_t row = idx / nq, bd = row / p.nseg, d = bd % p.Dm;
-    const int seg = (int)(row % p.nseg), n = 4 * (int)(idx % nq), kc = seg / p.seg_per_chunk;
-    if (kc == 0) return;
-    const float e = p.cumdt[bd * p.nseg + seg] * kLog2e;
-    const float4 H = *reinterpret_cast<const float4 *>(p.hloc + (bd * p.nchunk + kc) * np + n);
-    float4 *q = reinterpret_cast<float4 *>(p.ckpt + row * np + n);
-    float4 v = *q;
-    v.x = fmaf(n + 0 < p.N ? ex2(p.A[d * p.N + n + 0] * e) : 1.0f, H.x, v.x);
-    v.y = fmaf(n + 1 < p.N ? ex2(p.A[d * p.N + n + 1] * e) : 1.0f, H.y, v.y);
-    v.z = fmaf(n + 2 < p.N ? ex2(p.A[d * p.N + n + 2] * e) : 1.0f, H.z, v.z);
-    v.w = fmaf(n + 3 < p.N ? ex2(p.A[d * p.N + n + 3] * e) : 1.0f, H.w, v.w);
-    *q = v;
-}
+namespace {
+using bf16 = __nv_bfloat16;
 
 template <typename IO, int G, int Q>
 cudaError_t launch_bwd_t(const BwdParams &p, cudaStream_t s) {
-    constexpr size_t ck = bwd_ckpt_smem_bytes<IO, G, Q>(), sm = bwd_smem_bytes<IO, G, Q>();
+    constexpr size_t ck = bwd_ckpt_smem_bytes<IO, G, Q>(), sm = bwd_smem_bytes<IO, G, Q, false>();
+    constexpr size_t sms = bwd_smem_bytes<IO, G, Q, true>();
     constexpr size_t ag = bwd_agg_smem_bytes<IO, G, Q>();
     constexpr int kCpb = BwdCfg<G, Q>::kCpb;
     const dim3 grid((unsigned)((p.Dm + kCpb - 1) / kCpb), (unsigned)p.Bt, (unsigned)p.nchunk);
     static std::atomic<unsigned long long> attr_set{0};
     const cudaError_t e = once_per_device(attr_set, [&] {
-        cudaError_t r = cudaFuncSetAttribute(scan_bwd_kernel<IO, G, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        cudaError_t r = cudaFuncSetAttribute(scan_bwd_kernel<IO, G, Q, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(scan_bwd_kernel<IO, G, Q, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(scan_bwd_ckpt_kernel<IO, G, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ck);
         if (r == cudaSuccess)
@@ -74,10 +55,9 @@ cudaError_t launch_bwd_t(const BwdParams &p, cudaStream_t s) {
         scan_bwd_agg_kernel<IO, G, Q><<<dim3(grid.x, grid.y, grid.z - 1), kBwdThreads, ag, s>>>(p);
         const int64_t threads = p.Bt * p.Dm * (int64_t)(G * Q);
         bwd_chunk_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p, G * Q);
-        const int64_t fix = p.Bt * p.Dm * (int64_t)p.nseg * (G * Q / 4);
-        bwd_ckpt_fix_kernel<<<(unsigned)((fix + 255) / 256), 256, 0, s>>>(p, G * Q);
     }
-    scan_bwd_kernel<IO, G, Q><<<grid, kBwdThreads, sm, s>>>(p);
+    if (p.nchunk > 1) scan_bwd_kernel<IO, G, Q, true><<<grid, kBwdThreads, sms, s>>>(p);
+    else scan_bwd_kernel<IO, G, Q, false><<<grid, kBwdThreads, sm, s>>>(p);
     return cudaGetLastError();
 }
 

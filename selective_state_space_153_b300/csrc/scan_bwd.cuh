@@ -42,6 +42,11 @@ constexpr int kBwdS = 8;         // steps per checkpoint segment
 constexpr int kBwdThreads = 128;
 constexpr int kBwdQ = 4;         // states per thread (the default; 2 is also built)
 
+// 4-byte asynchronous global->shared copy (through L1)
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+
 struct BwdParams {
     const void *u, *delta, *z, *B, *C, *dy;
     const float *A, *D, *bias, *dlast;
@@ -82,10 +87,8 @@ struct BwdCfg {
     static constexpr int kFloats = kOffPart + 2 * kCpb * kPartCh;
     static_assert(kS % 4 == 0 && (kOffPart % 4) == 0 && (kPartCh % 4) == 0 && (kRow % 4) == 0, "16-byte rows");
 };
-template <typename IO, int G, int Q, bool FULL, bool CK>
+template <typename IO, int G, int Q, bool FULL, bool CK, bool CUM>
 struct BwdRing;
-template <typename IO, int G, int Q>
-constexpr size_t bwd_smem_bytes();
 
 // Raw inputs of one segment [t0, t0+S) of batch row b for the CTA's channels d0 .. d0+kCpb-1,
 // fetched into registers one segment ahead (the loads are in flight while the previous
@@ -230,9 +233,10 @@ struct BwdFetch {
 // ahead, where every row is a multiple of 16 bytes long and starts on a 16-byte boundary. A
 // slot holds the segment's rows as [row][S] io elements -- B (FULL: then C) rows n < kNP, then
 // delta, u (FULL: dy, z) rows of the CTA's channels -- and (CK) the checkpoints of the CTA's
-// channels as [channel][kNP] floats. Pieces of rows beyond N, Dm or L are not copied; stage()
+// channels as [channel][kNP] floats, then (CUM, time split) their dt sums from the chunk's
+// first step as [channel] floats. Pieces of rows beyond N, Dm or L are not copied; stage()
 // reads zeros in their place.
-template <typename IO, int G, int Q, bool FULL, bool CK = FULL>
+template <typename IO, int G, int Q, bool FULL, bool CK = FULL, bool CUM = false>
 struct BwdRing {
     using Cfg = BwdCfg<G, Q>;
     static constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kCpb = Cfg::kCpb, kQ = Cfg::kQ;
@@ -240,12 +244,13 @@ struct BwdRing {
     static constexpr int kGran = kS / kStepsPerPiece;                 // pieces per row segment
     static constexpr int kRowsBC = (FULL ? 2 : 1) * kNP, kRowsCH = (FULL ? 4 : 2) * kCpb;
     static constexpr int kRows = kRowsBC + kRowsCH;
-    static constexpr int kCkFloats = CK ? kCpb * kNP : 0;
+    static constexpr int kCkFloats = CK ? kCpb * kNP : 0, kCumFloats = CUM ? kCpb : 0;
     // measured on B300: deeper rings change neither pass (adjoint 3 stages, checkpoint 6); a
     // 2-stage checkpoint ring is 8-35% slower
     static constexpr int kStages = FULL ? 2 : 4;
-    static constexpr int kSlotBytes = kRows * kS * (int)sizeof(IO) + kCkFloats * 4;
-    static constexpr int kRowPieces = kRows * kGran, kPieces = kRowPieces + kCkFloats / 4;
+    static constexpr int kSlotBytes = kRows * kS * (int)sizeof(IO) + (kCkFloats + kCumFloats) * 4;
+    static constexpr int kRowPieces = kRows * kGran, kCkEnd = kRowPieces + kCkFloats / 4;
+    static constexpr int kPieces = kCkEnd + kCumFloats;    // the dt sums: one 4-byte copy each
     static constexpr int kPerThread = (kPieces + kBwdThreads - 1) / kBwdThreads;
     static_assert(kS % kStepsPerPiece == 0 && kNP % 4 == 0 && kSlotBytes % 16 == 0 && kCpb % 4 == 0, "16-byte pieces");
     static constexpr size_t bytes() { return (size_t)kStages * kSlotBytes; }
@@ -276,19 +281,26 @@ struct BwdRing {
                             src = reinterpret_cast<const IO *>(base) + (b * p.Dm + d) * p.L + t;
                     }
                 }
-            } else {
+            } else if (j < kCkEnd) {
                 const int r = j - kRowPieces, cc = r / (kNP / 4), part = r % (kNP / 4);
                 const int64_t d = d0 + cc;
                 if (d < p.Dm) src = p.ckpt + ((b * p.Dm + d) * p.nseg + seg) * kNP + 4 * part;
+            } else {
+                const int cc = j - kCkEnd;
+                const int64_t d = d0 + cc;
+                if (p.nchunk > 1 && d < p.Dm)
+                    cp_async4(slot + 16 * kCkEnd + 4 * cc, p.cumdt + (b * p.Dm + d) * p.nseg + seg);
+                continue;
             }
             if (src != nullptr) cp_async16(slot + 16 * j, src, 16);
         }
     }
 
-    // converted segment into the compute layout (as BwdFetch::stage); ckn: this lane's
-    // checkpoint pairs (FULL)
+    // converted segment into the compute layout (as BwdFetch::stage); (CK) ckn: this lane's
+    // checkpoint pairs, cum: its channel's dt sum from the chunk's first step (time split)
     __device__ __forceinline__ static void stage(const BwdParams &p, const unsigned char *ring, float *sm,
-                                                 const float *sbias, int seg, int64_t d0, float2 (&ckn)[Cfg::kP]) {
+                                                 const float *sbias, int seg, int64_t d0, float2 (&ckn)[Cfg::kP],
+                                                 float &cum) {
         const int tid = threadIdx.x;
         const IO *raw = reinterpret_cast<const IO *>(ring + (seg % kStages) * kSlotBytes);
         const int64_t t0 = (int64_t)seg * kS;
@@ -331,12 +343,14 @@ struct BwdRing {
         }
         if (CK) {
             const int g = tid % G, cc = tid / G;
-            const float *ck = reinterpret_cast<const float *>(reinterpret_cast<const unsigned char *>(raw) +
-                                                              kRows * kS * sizeof(IO)) + cc * kNP;
+            const float *cks = reinterpret_cast<const float *>(reinterpret_cast<const unsigned char *>(raw) +
+                                                               kRows * kS * sizeof(IO));
+            const float *ck = cks + cc * kNP;
             const bool valid = d0 + cc < p.Dm;
 #pragma unroll
             for (int k = 0; k < Cfg::kP; ++k)
                 ckn[k] = valid ? make_float2(ck[g + G * 2 * k], ck[g + G * (2 * k + 1)]) : make_float2(0.f, 0.f);
+            if (CUM) cum = (valid && p.nchunk > 1) ? cks[kCpb * kNP + cc] : 0.0f;
         }
     }
 };
@@ -354,9 +368,11 @@ template <typename IO, int G, int Q>
 constexpr size_t bwd_agg_smem_bytes() {
     return (size_t)(BwdCfg<G, Q>::kOffPart + BwdCfg<G, Q>::kCpb) * sizeof(float) + BwdRing<IO, G, Q, true, false>::bytes();
 }
-template <typename IO, int G, int Q>
+// the adjoint pass; SPLIT: a time-split chunk (the incoming-state table, the dt sums in the ring)
+template <typename IO, int G, int Q, bool SPLIT>
 constexpr size_t bwd_smem_bytes() {
-    return (size_t)(BwdCfg<G, Q>::kFloats + BwdCfg<G, Q>::kCpb) * sizeof(float) + BwdRing<IO, G, Q, true>::bytes();
+    return (size_t)(BwdCfg<G, Q>::kFloats + BwdCfg<G, Q>::kCpb * (1 + (SPLIT ? BwdCfg<G, Q>::kNP : 0))) * sizeof(float) +
+           BwdRing<IO, G, Q, true, true, SPLIT>::bytes();
 }
 
 // A lane's Q consecutive floats at p (16-byte or 8-byte aligned) as Q/2 packed pairs.
@@ -401,6 +417,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
         sbias[c] = (p.bias && d0 + c < p.Dm) ? p.bias[d0 + c] : 0.0f;   // read after the loop's first barrier
     BwdFetch<IO, G, Q, false> f;
     float2 ck_unused[kP];
+    float cum_unused;
     if (p.ring) {
 #pragma unroll
         for (int s = 0; s < Ring::kStages - 1; ++s) {
@@ -421,7 +438,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
         }
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();
-        if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ck_unused);
+        if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ck_unused, cum_unused);
         else f.stage(p, sm, sbias, (int64_t)seg * kS, d0);
         __syncthreads();
         if (p.ring) {            // the slot of segment seg - 1, staged before the barriers above
@@ -485,6 +502,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_agg_kernel(const BwdPara
         sbias[c] = (p.bias && d0 + c < p.Dm) ? p.bias[d0 + c] : 0.0f;   // read after the loop's first barrier
     BwdFetch<IO, G, Q, true> f;
     float2 ck_unused[kP];
+    float cum_unused;
     if (p.ring) {
 #pragma unroll
         for (int s = 0; s < Ring::kStages - 1; ++s) {
@@ -497,7 +515,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_agg_kernel(const BwdPara
     for (int seg = s1 - 1; seg >= s0; --seg) {
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();
-        if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ck_unused);
+        if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ck_unused, cum_unused);
         else f.stage(p, sm, sbias, (int64_t)seg * kS, d0);
         __syncthreads();
         if (p.ring) {
@@ -529,7 +547,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_agg_kernel(const BwdPara
     }
 }
 
-template <typename IO, int G, int Q>
+template <typename IO, int G, int Q, bool SPLIT>
 __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(const BwdParams p) {
     using Cfg = BwdCfg<G, Q>;
     constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
@@ -586,20 +604,33 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
         dbias += ddl;
     };
 
-    using Ring = BwdRing<IO, G, Q, true>;
+    using Ring = BwdRing<IO, G, Q, true, true, SPLIT>;
     float *sbias = sm + Cfg::kFloats;               // the CTA's channels' dt bias (0 without one)
-    unsigned char *ring = reinterpret_cast<unsigned char *>(sbias + kCpb);
+    // time split: the state entering this chunk, [channel][kNP]; the checkpoint pass took the
+    // chunk's checkpoints from 0, so each is corrected by exp(A*cum) times this state
+    float *shin = sbias + kCpb;
+    unsigned char *ring = reinterpret_cast<unsigned char *>(shin + (SPLIT ? kCpb * kNP : 0));
+    const bool fold = SPLIT && blockIdx.z > 0;
     for (int c = tid; c < kCpb; c += kBwdThreads)
         sbias[c] = (p.bias && d0 + c < p.Dm) ? p.bias[d0 + c] : 0.0f;   // read after the loop's first barrier
+    if (fold) {
+        for (int e = tid; e < kCpb * kNP; e += kBwdThreads) {
+            const int64_t dc = d0 + e / kNP;
+            shin[e] = dc < p.Dm ? p.hloc[((b * p.Dm + dc) * p.nchunk + blockIdx.z) * kNP + e % kNP] : 0.0f;
+        }
+    }
     BwdFetch<IO, G, Q, true> f;
-    // the segment's checkpoint, fetched with its inputs one segment ahead
-    auto fetch_ck = [&](int seg, float2 (&out)[kP]) {
+    // the segment's checkpoint (and time split: its dt sum from the chunk's first step),
+    // fetched with its inputs one segment ahead
+    auto fetch_ck = [&](int seg, float2 (&out)[kP], float &cm) {
 #pragma unroll
         for (int k = 0; k < kP; ++k)
             out[k] = valid ? make_float2(ck[(int64_t)seg * kNP + g + G * 2 * k], ck[(int64_t)seg * kNP + g + G * (2 * k + 1)])
                            : make_float2(0.f, 0.f);
+        cm = (valid && fold) ? p.cumdt[bd * p.nseg + seg] : 0.0f;
     };
     float2 ckn[kP];
+    float cumn = 0.0f;
     // this CTA's chunk of segments, walked backwards from its last
     const int s0 = blockIdx.z * p.seg_per_chunk, s1 = min(p.nseg, s0 + p.seg_per_chunk);
     if (p.ring) {
@@ -610,25 +641,32 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
         }
     } else {
         f.fetch(p, b, (int64_t)(s1 - 1) * kS, d0);
-        fetch_ck(s1 - 1, ckn);
+        fetch_ck(s1 - 1, ckn, cumn);
     }
     for (int seg = s1 - 1; seg >= s0; --seg) {
         const int64_t t0 = (int64_t)seg * kS;
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();                        // the previous segment is done with shared memory
-        if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ckn);
+        if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ckn, cumn);
         else f.stage(p, sm, sbias, t0, d0);
         __syncthreads();
         // states as pairs (q = 2k, 2k+1): hs[k][0] before the segment, hs[k][i+1] after step t0+i
         float2 hs[kP][kS + 1];
 #pragma unroll
-        for (int k = 0; k < kP; ++k) hs[k][0] = ckn[k];
+        for (int k = 0; k < kP; ++k) {
+            hs[k][0] = ckn[k];
+            if (fold) {
+                const float2 e = __fmul2_rn(make_float2(cumn, cumn), Ap2[k]);
+                const float2 H = make_float2(shin[cc * kNP + g + G * 2 * k], shin[cc * kNP + g + G * (2 * k + 1)]);
+                hs[k][0] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), H, ckn[k]);
+            }
+        }
         if (p.ring) {   // into the slot of segment seg + 1, staged before the barriers above
             if (seg - (Ring::kStages - 1) >= s0) Ring::issue(p, ring, b, seg - (Ring::kStages - 1), d0);
             cp_async_commit();
         } else if (seg > s0) {   // the next segment's inputs and checkpoint, in flight meanwhile
             f.fetch(p, b, t0 - kS, d0);
-            fetch_ck(seg - 1, ckn);
+            fetch_ck(seg - 1, ckn, cumn);
         }
 #pragma unroll
         for (int i = 0; i < kS; ++i) {

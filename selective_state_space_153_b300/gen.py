@@ -19,6 +19,9 @@ Workloads (Bt = batch, D = channels "d_inner", L = sequence length, N = state si
                 variance); no gate; D-skip = 1; the final state is returned.
                 (N=64 for >100K tokens follows the d_state advice on the
                 "Python Mamba" page.)
+* ``bwd_long``  1 x 1536 x 16384, N=16, bf16; z ~ N(0,1) gate; D-skip = 1: the
+                backward at batch 1 over a long sequence (m130's channels), whose
+                channel blocks alone give the GPU well under one CTA per SM.
 * ``decode``    256 x 5120, N=16, 64 successive single-token steps from an N(0,1)
                 fp32 state (d_inner of the 2.8B row, 2 x 2560).
 
@@ -83,6 +86,7 @@ class DecodeConfig:
 TINY = ScanConfig("tiny", 1, 4, 64, 4, io="f32", gate=False, dskip="ones", seed=0)
 BLOCK512 = ScanConfig("block512", 1, 512, 1024, 16, gate=True, dskip="normal", seed=1)
 M130 = ScanConfig("m130", 8, 1536, 2048, 16, gate=True, dskip="ones", seed=2)
+BWD_LONG = ScanConfig("bwd_long", 1, 1536, 16384, 16, gate=True, dskip="ones", seed=3)
 LONG128K = ScanConfig("long128k", 1, 1536, 131072, 64, gate=False, dskip="ones",
                       u_kind="ar1", last_state=True, seed=3)
 DECODE = DecodeConfig("decode", 256, 5120, 16, 64, seed=4)
