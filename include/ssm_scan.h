@@ -290,8 +290,12 @@ size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims);
  * to Mamba" section 2.2; the loop is section 3.2): gradients of
  *     sum_{b,d,t} y[b,d,t] * dy[b,d,t]  +  sum_{b,d,n} last_state[b,d,n] * dlast_state[b,d,n]
  * with respect to every input of ssm_selective_scan_fwd (Euler discretisation). The forward
- * states are recomputed from checkpoints taken every 16 steps (workspace) and the adjoint
- * recurrence lambda_t = dyhat_t C_t + exp(dt_{t+1} A) lambda_{t+1} is run backwards.
+ * states are recomputed from checkpoints taken every 8 steps (workspace) and the adjoint
+ * recurrence lambda_t = dyhat_t C_t + exp(dt_{t+1} A) lambda_{t+1} is run backwards. Where
+ * the batch rows and channels alone would give fewer than two thread blocks per SM, the
+ * sequence is also cut into chunks of whole 8-step segments that run in parallel (chunk-local
+ * states and adjoint carries, combined between the passes); the workspace then also holds
+ * per-segment dt sums and per-chunk states and carries.
  *   u, delta, A, B, C, D, z, delta_bias, delta_softplus: as ssm_selective_scan_fwd.
  *   dy           device, [batch][dim][seqlen] io dtype (gradient of y).
  *   dlast_state  device, [batch][dim][dstate] fp32 gradient of the final state, or NULL.
