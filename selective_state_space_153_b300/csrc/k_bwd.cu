@@ -13,18 +13,21 @@ __global__ void __launch_bounds__(256) bwd_chunk_combine_kernel(const BwdParams 
     if (idx >= p.Bt * p.Dm * np) return;
     const int64_t bd = idx / np, d = bd % p.Dm;
     const int n = (int)(idx % np);
-    const float Ap = n < p.N ? p.A[d * p.N + n] * kLog2e : 0.0f;
+    const float Ap = n < p.N ? ld_chk_g(p.A, bwd_dn_bytes(p), p.A + d * p.N + n) * kLog2e : 0.0f;
+    const uint64_t cb = bwd_chunk_bytes(p, np), sb = bwd_chunk_bytes(p, 1);
     float H = 0.0f;
     for (int kc = 0; kc < p.nchunk; ++kc) {
         float *hl = p.hloc + (bd * p.nchunk + kc) * np + n;
-        const float loc = *hl;
-        *hl = H;
-        H = fmaf(ex2(Ap * p.sdt[bd * p.nchunk + kc]), H, loc);
+        const float loc = ld_chk_g(p.hloc, cb, hl);
+        st_chk_g(p.hloc, cb, hl, H);
+        H = fmaf(ex2(Ap * ld_chk_g(p.sdt, sb, p.sdt + bd * p.nchunk + kc)), H, loc);
     }
-    float c = (n < p.N && p.dlast) ? p.dlast[bd * p.N + n] : 0.0f;
+    float c = (n < p.N && p.dlast) ? ld_chk_g(p.dlast, (uint64_t)(p.Bt * p.Dm * p.N) * 4, p.dlast + bd * p.N + n) : 0.0f;
     for (int kc = p.nchunk - 1; kc >= 0; --kc) {
-        p.cin[(bd * p.nchunk + kc) * np + n] = c;
-        if (kc > 0) c = fmaf(ex2(Ap * p.sdt[bd * p.nchunk + kc]), c, p.cloc[(bd * p.nchunk + kc) * np + n]);
+        st_chk_g(p.cin, cb, p.cin + (bd * p.nchunk + kc) * np + n, c);
+        if (kc > 0)
+            c = fmaf(ex2(Ap * ld_chk_g(p.sdt, sb, p.sdt + bd * p.nchunk + kc)), c,
+                     ld_chk_g(p.cloc, cb, p.cloc + (bd * p.nchunk + kc) * np + n));
     }
 }
 

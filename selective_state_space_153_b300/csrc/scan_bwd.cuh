@@ -34,6 +34,7 @@
 //     atomic per (state, 4 steps);
 //   * dA, dD and the dt bias are summed in registers and added once at the end.
 #pragma once
+#include "check.cuh"
 #include "common.cuh"
 
 namespace ssm {
@@ -67,6 +68,29 @@ struct BwdParams {
     float *cloc;                  // [Bt*Dm][nchunk][Q*G]: adjoint carry out of the chunk's start, from 0
     float *cin;                   // [Bt*Dm][nchunk][Q*G]: adjoint carry into the chunk's last step
 };
+
+// The backward kernels' dynamic shared memory (one declaration for all of them).
+extern __shared__ float4 smem_bwd4[];
+
+// Extents in bytes of the backward's arrays, for the checked build's bounds checks
+// (-DSSM_CHECK; in the normal build the checks are the constant `true` and these go unused).
+__device__ __forceinline__ uint64_t bwd_rows_bytes(const BwdParams &p, int esz) {   // [Bt][Dm][L]
+    return (uint64_t)(p.Bt * p.Dm * p.L) * (uint64_t)esz;
+}
+__device__ __forceinline__ uint64_t bwd_bc_bytes(const BwdParams &p, int esz) {     // [Bt][N][L]
+    return (uint64_t)(p.Bt * p.N * p.L) * (uint64_t)esz;
+}
+__device__ __forceinline__ uint64_t bwd_ck_bytes(const BwdParams &p, int np) {      // checkpoints
+    return (uint64_t)(p.Bt * p.Dm * p.nseg) * (uint64_t)np * 4;
+}
+__device__ __forceinline__ uint64_t bwd_cum_bytes(const BwdParams &p) {             // cumdt
+    return (uint64_t)(p.Bt * p.Dm * p.nseg) * 4;
+}
+__device__ __forceinline__ uint64_t bwd_chunk_bytes(const BwdParams &p, int np) {   // hloc, cloc, cin
+    return (uint64_t)(p.Bt * p.Dm * p.nchunk) * (uint64_t)np * 4;
+}
+__device__ __forceinline__ uint64_t bwd_dn_bytes(const BwdParams &p) { return (uint64_t)(p.Dm * p.N) * 4; }
+__device__ __forceinline__ uint64_t bwd_d_bytes(const BwdParams &p) { return (uint64_t)p.Dm * 4; }
 
 // Shared-memory layout (floats) of the backward kernels for G lanes per channel and Q states
 // per lane (2 or 4: one or two packed pairs).
@@ -127,7 +151,10 @@ struct BwdFetch {
                 const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
                 const int64_t t = t0 + i;
                 float2 v = make_float2(0.f, 0.f);
-                if (e < kBC && n < p.N && t < p.L) v = ld2((kind ? Cm : Bm) + n * p.L + t);
+                const IO *q = (kind ? Cm : Bm) + n * p.L + t;
+                if (e < kBC && n < p.N && t < p.L &&
+                    SSM_CHK_G(kind ? p.C : p.B, bwd_bc_bytes(p, sizeof(IO)), q, 2 * sizeof(IO)))
+                    v = ld2(q);
                 bc[2 * k2] = v.x;
                 bc[2 * k2 + 1] = v.y;
             }
@@ -139,11 +166,16 @@ struct BwdFetch {
                 float2 a = make_float2(0.f, 0.f), c = a, f = a, g = a;
                 if (e < kCH && d < p.Dm && t < p.L) {
                     const int64_t idx = (b * p.Dm + d) * p.L + t;
-                    a = ld2(reinterpret_cast<const IO *>(p.delta) + idx);
-                    c = ld2(reinterpret_cast<const IO *>(p.u) + idx);
+                    const uint64_t rb = bwd_rows_bytes(p, sizeof(IO));
+                    auto row2 = [&](const void *base) {
+                        const IO *q = reinterpret_cast<const IO *>(base) + idx;
+                        return SSM_CHK_G(base, rb, q, 2 * sizeof(IO)) ? ld2(q) : make_float2(0.f, 0.f);
+                    };
+                    a = row2(p.delta);
+                    c = row2(p.u);
                     if (FULL) {
-                        f = ld2(reinterpret_cast<const IO *>(p.dy) + idx);
-                        if (p.z) g = ld2(reinterpret_cast<const IO *>(p.z) + idx);
+                        f = row2(p.dy);
+                        if (p.z) g = row2(p.z);
                     }
                 }
                 dl[2 * k2] = a.x; dl[2 * k2 + 1] = a.y;
@@ -158,7 +190,10 @@ struct BwdFetch {
             const int e = tid + k * kBwdThreads;
             const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
             const int64_t t = t0 + i;
-            bc[k] = (e < kBC && n < p.N && t < p.L) ? io_traits<IO>::to_f((kind ? Cm : Bm)[n * p.L + t]) : 0.0f;
+            const IO *q = (kind ? Cm : Bm) + n * p.L + t;
+            bc[k] = (e < kBC && n < p.N && t < p.L &&
+                     SSM_CHK_G(kind ? p.C : p.B, bwd_bc_bytes(p, sizeof(IO)), q, sizeof(IO)))
+                        ? io_traits<IO>::to_f(*q) : 0.0f;
         }
 #pragma unroll
         for (int k = 0; k < kCHI; ++k) {
@@ -168,11 +203,16 @@ struct BwdFetch {
             dl[k] = uu[k] = dy[k] = zz[k] = 0.0f;
             if (e < kCH && d < p.Dm && t < p.L) {
                 const int64_t idx = (b * p.Dm + d) * p.L + t;
-                dl[k] = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.delta)[idx]);
-                uu[k] = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.u)[idx]);
+                const uint64_t rb = bwd_rows_bytes(p, sizeof(IO));
+                auto row1 = [&](const void *base) {
+                    const IO *q = reinterpret_cast<const IO *>(base) + idx;
+                    return SSM_CHK_G(base, rb, q, sizeof(IO)) ? io_traits<IO>::to_f(*q) : 0.0f;
+                };
+                dl[k] = row1(p.delta);
+                uu[k] = row1(p.u);
                 if (FULL) {
-                    dy[k] = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.dy)[idx]);
-                    if (p.z) zz[k] = io_traits<IO>::to_f(reinterpret_cast<const IO *>(p.z)[idx]);
+                    dy[k] = row1(p.dy);
+                    if (p.z) zz[k] = row1(p.z);
                 }
             }
         }
@@ -194,7 +234,7 @@ struct BwdFetch {
             const int e = slot_elem(p, tid, k);
             if (e >= kBC) break;
             const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
-            sm[(kind ? Cfg::kOffC : Cfg::kOffB) + (i * G + n % G) * Cfg::kQ + n / G] = bc[k];
+            st_chk_s(smem_bwd4, sm + (kind ? Cfg::kOffC : Cfg::kOffB) + (i * G + n % G) * Cfg::kQ + n / G, bc[k]);
         }
 #pragma unroll
         for (int k = 0; k < kCHI; ++k) {
@@ -218,12 +258,12 @@ struct BwdFetch {
                     }
                 }
             }
-            sm[Cfg::kOffDt + e] = dtv;
-            sm[Cfg::kOffU + e] = uu[k];
+            st_chk_s(smem_bwd4, sm + Cfg::kOffDt + e, dtv);
+            st_chk_s(smem_bwd4, sm + Cfg::kOffU + e, uu[k]);
             if (FULL) {
-                sm[Cfg::kOffSg + e] = sgv;
-                sm[Cfg::kOffDyh + e] = dyh;
-                sm[Cfg::kOffGz + e] = gz;
+                st_chk_s(smem_bwd4, sm + Cfg::kOffSg + e, sgv);
+                st_chk_s(smem_bwd4, sm + Cfg::kOffDyh + e, dyh);
+                st_chk_s(smem_bwd4, sm + Cfg::kOffGz + e, gz);
             }
         }
     }
@@ -264,35 +304,43 @@ struct BwdRing {
         for (int m = 0; m < kPerThread; ++m) {
             const int j = threadIdx.x + m * kBwdThreads;
             if (j >= kPieces) break;
-            const void *src = nullptr;
+            const void *src = nullptr, *sbase = nullptr;   // the piece and its array
+            uint64_t stotal = 0;
             if (j < kRowPieces) {
                 const int row = j / kGran, part = j % kGran;
                 const int64_t t = t0 + part * kStepsPerPiece;
                 if (t < p.L) {
                     if (row < kRowsBC) {
                         const int kind = row / kNP, n = row % kNP;
-                        if (n < p.N)
-                            src = reinterpret_cast<const IO *>(kind ? p.C : p.B) + (b * p.N + n) * p.L + t;
+                        sbase = kind ? p.C : p.B;
+                        stotal = bwd_bc_bytes(p, sizeof(IO));
+                        if (n < p.N) src = reinterpret_cast<const IO *>(sbase) + (b * p.N + n) * p.L + t;
                     } else {
                         const int r = row - kRowsBC, arr = r / kCpb, cc = r % kCpb;
                         const int64_t d = d0 + cc;
-                        const void *base = arr == 0 ? p.delta : arr == 1 ? p.u : arr == 2 ? p.dy : p.z;
-                        if (d < p.Dm && base != nullptr)
-                            src = reinterpret_cast<const IO *>(base) + (b * p.Dm + d) * p.L + t;
+                        sbase = arr == 0 ? p.delta : arr == 1 ? p.u : arr == 2 ? p.dy : p.z;
+                        stotal = bwd_rows_bytes(p, sizeof(IO));
+                        if (d < p.Dm && sbase != nullptr)
+                            src = reinterpret_cast<const IO *>(sbase) + (b * p.Dm + d) * p.L + t;
                     }
                 }
             } else if (j < kCkEnd) {
                 const int r = j - kRowPieces, cc = r / (kNP / 4), part = r % (kNP / 4);
                 const int64_t d = d0 + cc;
+                sbase = p.ckpt;
+                stotal = bwd_ck_bytes(p, kNP);
                 if (d < p.Dm) src = p.ckpt + ((b * p.Dm + d) * p.nseg + seg) * kNP + 4 * part;
             } else {
                 const int cc = j - kCkEnd;
                 const int64_t d = d0 + cc;
-                if (p.nchunk > 1 && d < p.Dm)
-                    cp_async4(slot + 16 * kCkEnd + 4 * cc, p.cumdt + (b * p.Dm + d) * p.nseg + seg);
+                const float *q = p.cumdt + (b * p.Dm + d) * p.nseg + seg;
+                if (p.nchunk > 1 && d < p.Dm && SSM_CHK_G(p.cumdt, bwd_cum_bytes(p), q, 4) &&
+                    SSM_CHK_S(smem_bwd4, slot + 16 * kCkEnd + 4 * cc, 4))
+                    cp_async4(slot + 16 * kCkEnd + 4 * cc, q);
                 continue;
             }
-            if (src != nullptr) cp_async16(slot + 16 * j, src, 16);
+            if (src != nullptr && SSM_CHK_G(sbase, stotal, src, 16) && SSM_CHK_S(smem_bwd4, slot + 16 * j, 16))
+                cp_async16(slot + 16 * j, src, 16);
         }
     }
 
@@ -307,24 +355,24 @@ struct BwdRing {
         constexpr int kBC = kRowsBC * kS, kCH = kCpb * kS;
         for (int e = tid; e < kBC; e += kBwdThreads) {
             const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
-            const float v = (n < p.N && t0 + i < p.L) ? io_traits<IO>::to_f(raw[e]) : 0.0f;
-            sm[(kind ? Cfg::kOffC : Cfg::kOffB) + (i * G + n % G) * kQ + n / G] = v;
+            const float v = (n < p.N && t0 + i < p.L) ? io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + e)) : 0.0f;
+            st_chk_s(smem_bwd4, sm + (kind ? Cfg::kOffC : Cfg::kOffB) + (i * G + n % G) * kQ + n / G, v);
         }
         for (int e = tid; e < kCH; e += kBwdThreads) {
             const int cc = e / kS, i = e % kS;
             const int64_t d = d0 + cc, t = t0 + i;
             float dtv = 0.0f, sgv = 0.0f, dyh = 0.0f, gz = 0.0f, uu = 0.0f;
             if (d < p.Dm && t < p.L) {
-                const float dl = io_traits<IO>::to_f(raw[kBC + e]);
-                uu = io_traits<IO>::to_f(raw[kBC + kCH + e]);
+                const float dl = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + e));
+                uu = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + kCH + e));
                 const float v = dl + sbias[cc];
                 if (!FULL) dtv = p.softplus ? softplus_f(v) : v;
                 else if (p.softplus) dtv = softplus_sigmoid(v, sgv);
                 else dtv = v, sgv = 1.0f;
                 if (FULL) {
-                    const float dy = io_traits<IO>::to_f(raw[kBC + 2 * kCH + e]);
+                    const float dy = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + 2 * kCH + e));
                     if (p.z) {
-                        const float zz = io_traits<IO>::to_f(raw[kBC + 3 * kCH + e]);
+                        const float zz = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + 3 * kCH + e));
                         const float sz = rcp_approx(1.0f + ex2(-zz * kLog2e));
                         dyh = dy * zz * sz;                            // dy * SiLU(z)
                         gz = dy * sz * (1.0f + zz * (1.0f - sz));      // dy * SiLU'(z)
@@ -333,12 +381,12 @@ struct BwdRing {
                     }
                 }
             }
-            sm[Cfg::kOffDt + e] = dtv;
-            sm[Cfg::kOffU + e] = uu;
+            st_chk_s(smem_bwd4, sm + Cfg::kOffDt + e, dtv);
+            st_chk_s(smem_bwd4, sm + Cfg::kOffU + e, uu);
             if (FULL) {
-                sm[Cfg::kOffSg + e] = sgv;
-                sm[Cfg::kOffDyh + e] = dyh;
-                sm[Cfg::kOffGz + e] = gz;
+                st_chk_s(smem_bwd4, sm + Cfg::kOffSg + e, sgv);
+                st_chk_s(smem_bwd4, sm + Cfg::kOffDyh + e, dyh);
+                st_chk_s(smem_bwd4, sm + Cfg::kOffGz + e, gz);
             }
         }
         if (CK) {
@@ -349,8 +397,9 @@ struct BwdRing {
             const bool valid = d0 + cc < p.Dm;
 #pragma unroll
             for (int k = 0; k < Cfg::kP; ++k)
-                ckn[k] = valid ? make_float2(ck[g + G * 2 * k], ck[g + G * (2 * k + 1)]) : make_float2(0.f, 0.f);
-            if (CUM) cum = (valid && p.nchunk > 1) ? cks[kCpb * kNP + cc] : 0.0f;
+                ckn[k] = valid ? make_float2(ld_chk_s(smem_bwd4, ck + g + G * 2 * k), ld_chk_s(smem_bwd4, ck + g + G * (2 * k + 1)))
+                               : make_float2(0.f, 0.f);
+            if (CUM) cum = (valid && p.nchunk > 1) ? ld_chk_s(smem_bwd4, cks + kCpb * kNP + cc) : 0.0f;
         }
     }
 };
@@ -391,8 +440,8 @@ template <typename IO, int G, int Q>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdParams p) {
     using Cfg = BwdCfg<G, Q>;
     constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
-    extern __shared__ float4 smem_bwd4[];
     float *sm = reinterpret_cast<float *>(smem_bwd4);
+    SSM_POISON_SMEM(smem_bwd4);
     const int tid = threadIdx.x, g = tid % G, cc = tid / G;
     const int64_t b = blockIdx.y, d0 = (int64_t)blockIdx.x * kCpb, d = d0 + cc;
     const bool valid = d < p.Dm;                 // every thread takes part in the staging
@@ -401,8 +450,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
 #pragma unroll
     for (int k = 0; k < kP; ++k) {
         const int n0 = g + G * 2 * k, n1 = n0 + G;
-        Ap2[k] = make_float2((valid && n0 < p.N) ? p.A[(valid ? d : 0) * p.N + n0] * kLog2e : 0.0f,
-                             (valid && n1 < p.N) ? p.A[(valid ? d : 0) * p.N + n1] * kLog2e : 0.0f);
+        Ap2[k] = make_float2((valid && n0 < p.N) ? ld_chk_g(p.A, bwd_dn_bytes(p), p.A + (valid ? d : 0) * p.N + n0) * kLog2e : 0.0f,
+                             (valid && n1 < p.N) ? ld_chk_g(p.A, bwd_dn_bytes(p), p.A + (valid ? d : 0) * p.N + n1) * kLog2e : 0.0f);
         h2[k] = make_float2(0.f, 0.f);
     }
     float *ck = p.ckpt + bd * (int64_t)p.nseg * kNP;
@@ -413,8 +462,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
     using Ring = BwdRing<IO, G, Q, false>;
     float *sbias = sm + Cfg::kOffU + Cfg::kChan;    // the CTA's channels' dt bias (0 without one)
     unsigned char *ring = reinterpret_cast<unsigned char *>(sbias + kCpb);
-    for (int c = tid; c < kCpb; c += kBwdThreads)
-        sbias[c] = (p.bias && d0 + c < p.Dm) ? p.bias[d0 + c] : 0.0f;   // read after the loop's first barrier
+    for (int c = tid; c < kCpb; c += kBwdThreads)   // read after the loop's first barrier
+        st_chk_s(smem_bwd4, sbias + c, (p.bias && d0 + c < p.Dm) ? ld_chk_g(p.bias, bwd_d_bytes(p), p.bias + d0 + c) : 0.0f);
     BwdFetch<IO, G, Q, false> f;
     float2 ck_unused[kP];
     float cum_unused;
@@ -431,10 +480,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
         if (valid) {
 #pragma unroll
             for (int k = 0; k < kP; ++k) {
-                ck[(int64_t)seg * kNP + g + G * 2 * k] = h2[k].x;
-                ck[(int64_t)seg * kNP + g + G * (2 * k + 1)] = h2[k].y;
+                st_chk_g(p.ckpt, bwd_ck_bytes(p, kNP), ck + (int64_t)seg * kNP + g + G * 2 * k, h2[k].x);
+                st_chk_g(p.ckpt, bwd_ck_bytes(p, kNP), ck + (int64_t)seg * kNP + g + G * (2 * k + 1), h2[k].y);
             }
-            if (p.nchunk > 1 && g == 0) p.cumdt[bd * p.nseg + seg] = cum;
+            if (p.nchunk > 1 && g == 0) st_chk_g(p.cumdt, bwd_cum_bytes(p), p.cumdt + bd * p.nseg + seg, cum);
         }
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();
@@ -465,10 +514,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
         float *hl = p.hloc + (bd * p.nchunk + kc) * kNP;
 #pragma unroll
         for (int k = 0; k < kP; ++k) {
-            hl[g + G * 2 * k] = h2[k].x;
-            hl[g + G * (2 * k + 1)] = h2[k].y;
+            st_chk_g(p.hloc, bwd_chunk_bytes(p, kNP), hl + g + G * 2 * k, h2[k].x);
+            st_chk_g(p.hloc, bwd_chunk_bytes(p, kNP), hl + g + G * (2 * k + 1), h2[k].y);
         }
-        if (g == 0) p.sdt[bd * p.nchunk + kc] = cum;
+        if (g == 0) st_chk_g(p.sdt, bwd_chunk_bytes(p, 1), p.sdt + bd * p.nchunk + kc, cum);
     }
 }
 
@@ -480,8 +529,8 @@ template <typename IO, int G, int Q>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_agg_kernel(const BwdParams p) {
     using Cfg = BwdCfg<G, Q>;
     constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
-    extern __shared__ float4 smem_bwd4[];
     float *sm = reinterpret_cast<float *>(smem_bwd4);
+    SSM_POISON_SMEM(smem_bwd4);
     const int tid = threadIdx.x, g = tid % G, cc = tid / G;
     const int64_t b = blockIdx.y, d0 = (int64_t)blockIdx.x * kCpb, d = d0 + cc;
     const bool valid = d < p.Dm;
@@ -491,15 +540,15 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_agg_kernel(const BwdPara
 #pragma unroll
     for (int k = 0; k < kP; ++k) {
         const int n0 = g + G * 2 * k, n1 = n0 + G;
-        Ap2[k] = make_float2((valid && n0 < p.N) ? p.A[(valid ? d : 0) * p.N + n0] * kLog2e : 0.0f,
-                             (valid && n1 < p.N) ? p.A[(valid ? d : 0) * p.N + n1] * kLog2e : 0.0f);
+        Ap2[k] = make_float2((valid && n0 < p.N) ? ld_chk_g(p.A, bwd_dn_bytes(p), p.A + (valid ? d : 0) * p.N + n0) * kLog2e : 0.0f,
+                             (valid && n1 < p.N) ? ld_chk_g(p.A, bwd_dn_bytes(p), p.A + (valid ? d : 0) * p.N + n1) * kLog2e : 0.0f);
         c2[k] = make_float2(0.f, 0.f);
     }
     using Ring = BwdRing<IO, G, Q, true, false>;
     float *sbias = sm + Cfg::kOffPart;
     unsigned char *ring = reinterpret_cast<unsigned char *>(sbias + kCpb);
-    for (int c = tid; c < kCpb; c += kBwdThreads)
-        sbias[c] = (p.bias && d0 + c < p.Dm) ? p.bias[d0 + c] : 0.0f;   // read after the loop's first barrier
+    for (int c = tid; c < kCpb; c += kBwdThreads)   // read after the loop's first barrier
+        st_chk_s(smem_bwd4, sbias + c, (p.bias && d0 + c < p.Dm) ? ld_chk_g(p.bias, bwd_d_bytes(p), p.bias + d0 + c) : 0.0f);
     BwdFetch<IO, G, Q, true> f;
     float2 ck_unused[kP];
     float cum_unused;
@@ -541,8 +590,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_agg_kernel(const BwdPara
         float *cl = p.cloc + (bd * p.nchunk + kc) * kNP;
 #pragma unroll
         for (int k = 0; k < kP; ++k) {
-            cl[g + G * 2 * k] = c2[k].x;
-            cl[g + G * (2 * k + 1)] = c2[k].y;
+            st_chk_g(p.cloc, bwd_chunk_bytes(p, kNP), cl + g + G * 2 * k, c2[k].x);
+            st_chk_g(p.cloc, bwd_chunk_bytes(p, kNP), cl + g + G * (2 * k + 1), c2[k].y);
         }
     }
 }
@@ -555,24 +604,24 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
     // butterfly per step
     constexpr bool kTransposed = G <= kS;
     constexpr int kGrp = kTransposed ? G : 1;
-    extern __shared__ float4 smem_bwd4[];
     float *sm = reinterpret_cast<float *>(smem_bwd4);
+    SSM_POISON_SMEM(smem_bwd4);
     const int tid = threadIdx.x, lane = tid & 31, g = tid % G, cc = tid / G;
     const int64_t b = blockIdx.y, d0 = (int64_t)blockIdx.x * kCpb, d = d0 + cc;
     const bool valid = d < p.Dm;                // invalid lanes still take part in the exchanges
     const int64_t dd = valid ? d : 0;
     const int64_t bd = b * p.Dm + dd;
-    const float Dv = (valid && p.D) ? p.D[dd] : 0.0f;
+    const float Dv = (valid && p.D) ? ld_chk_g(p.D, bwd_d_bytes(p), p.D + dd) : 0.0f;
     float An[kQ], c[kQ];
     bool nv[kQ];
 #pragma unroll
     for (int q = 0; q < kQ; ++q) {
         const int n = g + G * q;
         nv[q] = valid && n < p.N;
-        An[q] = nv[q] ? p.A[dd * p.N + n] : 0.0f;
+        An[q] = nv[q] ? ld_chk_g(p.A, bwd_dn_bytes(p), p.A + dd * p.N + n) : 0.0f;
         c[q] = !nv[q] ? 0.0f
-               : p.nchunk > 1 ? p.cin[(bd * p.nchunk + blockIdx.z) * kNP + n]
-               : p.dlast ? p.dlast[bd * p.N + n] : 0.0f;
+               : p.nchunk > 1 ? ld_chk_g(p.cin, bwd_chunk_bytes(p, kNP), p.cin + (bd * p.nchunk + blockIdx.z) * kNP + n)
+               : p.dlast ? ld_chk_g(p.dlast, (uint64_t)(p.Bt * p.Dm * p.N) * 4, p.dlast + bd * p.N + n) : 0.0f;
     }
     // as state pairs (q = 2k, 2k+1) for the packed arithmetic
     float2 An2[kP], Ap2[kP], c2[kP], dA2[kP];
@@ -597,9 +646,9 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
         if (!valid || t >= p.L) return;
         const float dt = sDt[i], uu = sU[i], dyh = sDyh[i];
         const float ddl = fmaf(uu, dus, dds) * sSg[i];
-        p.du[bd * p.L + t] = fmaf(dyh, Dv, dt * dus);
-        p.ddelta[bd * p.L + t] = ddl;
-        if (p.dz) p.dz[bd * p.L + t] = sGz[i] * fmaf(Dv, uu, yhs);
+        st_chk_g(p.du, bwd_rows_bytes(p, 4), p.du + bd * p.L + t, fmaf(dyh, Dv, dt * dus));
+        st_chk_g(p.ddelta, bwd_rows_bytes(p, 4), p.ddelta + bd * p.L + t, ddl);
+        if (p.dz) st_chk_g(p.dz, bwd_rows_bytes(p, 4), p.dz + bd * p.L + t, sGz[i] * fmaf(Dv, uu, yhs));
         dD = fmaf(dyh, uu, dD);
         dbias += ddl;
     };
@@ -611,12 +660,14 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
     float *shin = sbias + kCpb;
     unsigned char *ring = reinterpret_cast<unsigned char *>(shin + (SPLIT ? kCpb * kNP : 0));
     const bool fold = SPLIT && blockIdx.z > 0;
-    for (int c = tid; c < kCpb; c += kBwdThreads)
-        sbias[c] = (p.bias && d0 + c < p.Dm) ? p.bias[d0 + c] : 0.0f;   // read after the loop's first barrier
+    for (int c = tid; c < kCpb; c += kBwdThreads)   // read after the loop's first barrier
+        st_chk_s(smem_bwd4, sbias + c, (p.bias && d0 + c < p.Dm) ? ld_chk_g(p.bias, bwd_d_bytes(p), p.bias + d0 + c) : 0.0f);
     if (fold) {
         for (int e = tid; e < kCpb * kNP; e += kBwdThreads) {
             const int64_t dc = d0 + e / kNP;
-            shin[e] = dc < p.Dm ? p.hloc[((b * p.Dm + dc) * p.nchunk + blockIdx.z) * kNP + e % kNP] : 0.0f;
+            st_chk_s(smem_bwd4, shin + e,
+                     dc < p.Dm ? ld_chk_g(p.hloc, bwd_chunk_bytes(p, kNP), p.hloc + ((b * p.Dm + dc) * p.nchunk + blockIdx.z) * kNP + e % kNP)
+                               : 0.0f);
         }
     }
     BwdFetch<IO, G, Q, true> f;
@@ -625,9 +676,10 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
     auto fetch_ck = [&](int seg, float2 (&out)[kP], float &cm) {
 #pragma unroll
         for (int k = 0; k < kP; ++k)
-            out[k] = valid ? make_float2(ck[(int64_t)seg * kNP + g + G * 2 * k], ck[(int64_t)seg * kNP + g + G * (2 * k + 1)])
+            out[k] = valid ? make_float2(ld_chk_g(p.ckpt, bwd_ck_bytes(p, kNP), ck + (int64_t)seg * kNP + g + G * 2 * k),
+                                         ld_chk_g(p.ckpt, bwd_ck_bytes(p, kNP), ck + (int64_t)seg * kNP + g + G * (2 * k + 1)))
                            : make_float2(0.f, 0.f);
-        cm = (valid && fold) ? p.cumdt[bd * p.nseg + seg] : 0.0f;
+        cm = (valid && fold) ? ld_chk_g(p.cumdt, bwd_cum_bytes(p), p.cumdt + bd * p.nseg + seg) : 0.0f;
     };
     float2 ckn[kP];
     float cumn = 0.0f;
@@ -716,10 +768,10 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
 #pragma unroll
                     for (int q = 0; q < kQ; ++q) {
                         const int n = g + G * q;
-                        *reinterpret_cast<float4 *>(myPart + n * Cfg::kRow + i) =
-                            make_float4(pb[q][0], pb[q][1], pb[q][2], pb[q][3]);
-                        *reinterpret_cast<float4 *>(myPart + kCpb * Cfg::kPartCh + n * Cfg::kRow + i) =
-                            make_float4(pc[q][0], pc[q][1], pc[q][2], pc[q][3]);
+                        st_chk_s(smem_bwd4, reinterpret_cast<float4 *>(myPart + n * Cfg::kRow + i),
+                                 make_float4(pb[q][0], pb[q][1], pb[q][2], pb[q][3]));
+                        st_chk_s(smem_bwd4, reinterpret_cast<float4 *>(myPart + kCpb * Cfg::kPartCh + n * Cfg::kRow + i),
+                                 make_float4(pc[q][0], pc[q][1], pc[q][2], pc[q][3]));
                     }
                 }
                 if constexpr (kTransposed) {
@@ -756,22 +808,24 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
             float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
 #pragma unroll 8
             for (int ch = 0; ch < kCpb; ++ch) {
-                const float4 v = *reinterpret_cast<const float4 *>(src + ch * Cfg::kPartCh);
+                const float4 v = ld_chk_s(smem_bwd4, reinterpret_cast<const float4 *>(src + ch * Cfg::kPartCh));
                 lo = __fadd2_rn(lo, make_float2(v.x, v.y));
                 hi = __fadd2_rn(hi, make_float2(v.z, v.w));
             }
             const float4 acc = make_float4(lo.x, lo.y, hi.x, hi.y);
             const int64_t t = t0 + 4 * tq;
             float *dst = (kind ? p.dC : p.dB) + (b * p.N + n) * p.L + t;
+            float *dbase = kind ? p.dC : p.dB;
             if (t + 3 < p.L && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc.x), "f"(acc.y),
-                             "f"(acc.z), "f"(acc.w)
-                             : "memory");
+                if (SSM_CHK_G(dbase, bwd_bc_bytes(p, 4), dst, 16))
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc.x), "f"(acc.y),
+                                 "f"(acc.z), "f"(acc.w)
+                                 : "memory");
             } else {
                 const float av[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    if (t + k < p.L) atomicAdd(dst + k, av[k]);
+                    if (t + k < p.L && SSM_CHK_G(dbase, bwd_bc_bytes(p, 4), dst + k, 4)) atomicAdd(dst + k, av[k]);
             }
         }
     }
@@ -790,10 +844,11 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
     }
 #pragma unroll
     for (int q = 0; q < kQ; ++q)
-        if (nv[q]) atomicAdd(p.dA + dd * p.N + g + G * q, dA[q]);
+        if (nv[q] && SSM_CHK_G(p.dA, bwd_dn_bytes(p), p.dA + dd * p.N + g + G * q, 4))
+            atomicAdd(p.dA + dd * p.N + g + G * q, dA[q]);
     if (g == 0) {
-        if (p.dD) atomicAdd(p.dD + dd, dD);
-        if (p.dbias) atomicAdd(p.dbias + dd, dbias);
+        if (p.dD && SSM_CHK_G(p.dD, bwd_d_bytes(p), p.dD + dd, 4)) atomicAdd(p.dD + dd, dD);
+        if (p.dbias && SSM_CHK_G(p.dbias, bwd_d_bytes(p), p.dbias + dd, 4)) atomicAdd(p.dbias + dd, dbias);
     }
 }
 

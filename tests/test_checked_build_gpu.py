@@ -169,3 +169,78 @@ def test_check_records_a_caught_access(checked):
     assert ssm.stream_status() == ssm.SSM_ERR_CHECK
     compare_scan(inp, y, h)
     _scan_checked(inp)      # asserts status OK again
+
+
+def _bwd_checked(inp, dy, dl, odd=False):
+    """ssm_selective_scan_bwd through the checked library with every output and the workspace
+    between guard words; returns the gradients (fp32 device tensors)."""
+    import ctypes
+    lib = ssm.load()
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    dyd = dy.cuda()
+    if odd:      # every io input one element off a 2-element boundary
+        def off(t):
+            if t is None:
+                return None
+            big = torch.empty(t.numel() + 1, dtype=t.dtype, device="cuda")
+            v = big[1:].view(t.shape)
+            v.copy_(t)
+            return v
+        for k in ("u", "delta", "B", "C", "z"):
+            g[k] = off(g[k])
+        dyd = off(dyd)
+    Bt, Dm, L = g["u"].shape
+    N = g["A"].shape[1]
+    shapes = {"u": (Bt, Dm, L), "delta": (Bt, Dm, L), "A": (Dm, N), "B": (Bt, N, L), "C": (Bt, N, L),
+              "D": (Dm,), "z": (Bt, Dm, L), "delta_bias": (Dm,)}
+    outs = {k: _guarded(s, torch.float32) for k, s in shapes.items()}
+    dm = ssm.dims(Bt, Dm, L, N, ssm._io_code(g["u"]))
+    wsb = lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(dm))
+    wbig, ws = _guarded((max(wsb, 4) // 4,), torch.float32)
+    p = ssm._p
+    rc = lib.ssm_selective_scan_bwd(ctypes.byref(dm), p(g["u"]), p(g["delta"]), p(g["A"]), p(g["B"]), p(g["C"]),
+                                    p(g["D"]), p(g["z"]), p(g["delta_bias"]), 1, p(dyd),
+                                    None if dl is None else p(dl.cuda()),
+                                    *[p(outs[k][1]) for k in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")],
+                                    p(ws), wsb, None)
+    assert rc == ssm.SSM_OK, ssm.status_string(rc)
+    torch.cuda.synchronize()
+    assert ssm.stream_status() == ssm.SSM_OK, "a bounds check failed"
+    for k, (big, _) in outs.items():
+        assert _guards_intact(big), f"write outside d{k}"
+    assert _guards_intact(wbig), "write outside the workspace"
+    return {k: v for k, (_, v) in outs.items()}
+
+
+BWD_CHECK_CASES = [
+    # Bt, D, L, N, io, chunks, lanes split (states per lane), odd offset -- every input path
+    # (copy ring, two-step register loads, single steps) with and without the time split
+    (2, 37, 96, 16, "bf16", 3, 0, False),    # ring, split, partial channel block
+    (1, 9, 100, 16, "f32", 2, 2, False),     # ring with a half last segment, split, two states per lane
+    (2, 7, 33, 8, "f32", 2, 0, False),       # single steps (odd L), split
+    (1, 20, 70, 32, "bf16", 1, 0, False),    # two-step loads, unsplit
+    (2, 9, 70, 16, "bf16", 3, 0, True),      # inputs off alignment: single steps, split
+    (1, 5, 40, 100, "f32", 1, 0, False),     # N = 100: 32 lanes per channel
+]
+
+
+@pytest.mark.parametrize("Bt,D,L,N,io,chunks,q,odd", BWD_CHECK_CASES)
+def test_backward_checked(checked, Bt, D, L, N, io, chunks, q, odd):
+    """The backward through the checked build: status OK, guards intact, and gradients equal
+    to the normal build's within fp32 summation-order noise (shared memory starts as NaN, so
+    a read of an unwritten word would show)."""
+    cfg = gen.ScanConfig("chkb", Bt, D, L, N, io=io, gate=True, dskip="normal", bias=True, seed=L + N,
+                         a_kind="random")
+    inp = gen.scan_inputs(cfg)
+    rng = np.random.default_rng(L)
+    dy = torch.from_numpy(rng.standard_normal((Bt, D, L)).astype(np.float32)).to(inp["u"].dtype)
+    dl = torch.from_numpy(rng.standard_normal((Bt, D, N)).astype(np.float32))
+    with ssm.plan_override(bwd_chunks=chunks, bwd_states_per_lane=q):
+        got = _bwd_checked(inp, dy, dl, odd)
+        with ssm.using(ssm.load_library(ssm.LIB_PATH)):
+            ref = _bwd_checked(inp, dy, dl, odd)
+    for k in got:
+        r, v = ref[k].double(), got[k].double()
+        assert torch.isfinite(v).all(), f"d{k}: non-finite"
+        err = float((v - r).abs().max() / r.abs().max().clamp_min(1e-30))
+        assert err <= 1e-5, f"d{k}: {err:.2e} against the normal build"
