@@ -15,19 +15,27 @@ __global__ void __launch_bounds__(256) bwd_chunk_combine_kernel(const BwdParams 
     const int n = (int)(idx % np);
     const float Ap = n < p.N ? ld_chk_g(p.A, bwd_dn_bytes(p), p.A + d * p.N + n) * kLog2e : 0.0f;
     const uint64_t cb = bwd_chunk_bytes(p, np), sb = bwd_chunk_bytes(p, 1);
+    // every address is read (through the read-only path) before this thread writes it, and no
+    // other thread touches it, so the loads of later chunks may run ahead of the stores
+    auto ldro = [](const float *base, uint64_t total, const float *q) {
+        return SSM_CHK_G(base, total, q, 4) ? __ldg(q) : 0.0f;
+    };
     float H = 0.0f;
+#pragma unroll 8
     for (int kc = 0; kc < p.nchunk; ++kc) {
         float *hl = p.hloc + (bd * p.nchunk + kc) * np + n;
-        const float loc = ld_chk_g(p.hloc, cb, hl);
+        const float loc = ldro(p.hloc, cb, hl);
+        const float a = ex2(Ap * ldro(p.sdt, sb, p.sdt + bd * p.nchunk + kc));
         st_chk_g(p.hloc, cb, hl, H);
-        H = fmaf(ex2(Ap * ld_chk_g(p.sdt, sb, p.sdt + bd * p.nchunk + kc)), H, loc);
+        H = fmaf(a, H, loc);
     }
     float c = (n < p.N && p.dlast) ? ld_chk_g(p.dlast, (uint64_t)(p.Bt * p.Dm * p.N) * 4, p.dlast + bd * p.N + n) : 0.0f;
+#pragma unroll 8
     for (int kc = p.nchunk - 1; kc >= 0; --kc) {
         st_chk_g(p.cin, cb, p.cin + (bd * p.nchunk + kc) * np + n, c);
         if (kc > 0)
-            c = fmaf(ex2(Ap * ld_chk_g(p.sdt, sb, p.sdt + bd * p.nchunk + kc)), c,
-                     ld_chk_g(p.cloc, cb, p.cloc + (bd * p.nchunk + kc) * np + n));
+            c = fmaf(ex2(Ap * ldro(p.sdt, sb, p.sdt + bd * p.nchunk + kc)), c,
+                     ldro(p.cloc, cb, p.cloc + (bd * p.nchunk + kc) * np + n));
     }
 }
 

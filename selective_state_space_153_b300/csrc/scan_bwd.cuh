@@ -815,9 +815,8 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
             const float4 acc = make_float4(lo.x, lo.y, hi.x, hi.y);
             const int64_t t = t0 + 4 * tq;
             float *dst = (kind ? p.dC : p.dB) + (b * p.N + n) * p.L + t;
-            float *dbase = kind ? p.dC : p.dB;
             if (t + 3 < p.L && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-                if (SSM_CHK_G(dbase, bwd_bc_bytes(p, 4), dst, 16))
+                if (SSM_CHK_G(kind ? p.dC : p.dB, bwd_bc_bytes(p, 4), dst, 16))
                     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc.x), "f"(acc.y),
                                  "f"(acc.z), "f"(acc.w)
                                  : "memory");
@@ -825,7 +824,8 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
                 const float av[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    if (t + k < p.L && SSM_CHK_G(dbase, bwd_bc_bytes(p, 4), dst + k, 4)) atomicAdd(dst + k, av[k]);
+                    if (t + k < p.L && SSM_CHK_G(kind ? p.dC : p.dB, bwd_bc_bytes(p, 4), dst + k, 4))
+                        atomicAdd(dst + k, av[k]);
             }
         }
     }
