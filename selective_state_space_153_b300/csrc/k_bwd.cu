@@ -55,13 +55,16 @@ cudaError_t launch_bwd_t(const BwdParams &p, cudaStream_t s) {
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(scan_bwd_kernel<IO, G, Q, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(scan_bwd_ckpt_kernel<IO, G, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ck);
+            r = cudaFuncSetAttribute(scan_bwd_ckpt_kernel<IO, G, Q, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ck);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(scan_bwd_ckpt_kernel<IO, G, Q, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ck);
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(scan_bwd_agg_kernel<IO, G, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ag);
         return r;
     });
     if (e != cudaSuccess) return e;
-    scan_bwd_ckpt_kernel<IO, G, Q><<<grid, kBwdThreads, ck, s>>>(p);
+    if (p.nchunk > 1) scan_bwd_ckpt_kernel<IO, G, Q, true><<<grid, kBwdThreads, ck, s>>>(p);
+    else scan_bwd_ckpt_kernel<IO, G, Q, false><<<grid, kBwdThreads, ck, s>>>(p);
     if (p.nchunk > 1) {   // time split: the adjoint carries of chunks 1.., then both combines
         scan_bwd_agg_kernel<IO, G, Q><<<dim3(grid.x, grid.y, grid.z - 1), kBwdThreads, ag, s>>>(p);
         const int64_t threads = p.Bt * p.Dm * (int64_t)(G * Q);

@@ -111,7 +111,10 @@ struct BwdCfg {
     static constexpr int kFloats = kOffPart + 2 * kCpb * kPartCh;
     static_assert(kS % 4 == 0 && (kOffPart % 4) == 0 && (kPartCh % 4) == 0 && (kRow % 4) == 0, "16-byte rows");
 };
-template <typename IO, int G, int Q, bool FULL, bool CK, bool CUM>
+// what a copy-ring slot holds: the checkpoint pass's rows (B, delta, u), the adjoint's (B, C,
+// delta, u, dy, z), or the adjoint aggregate pass's (C, delta, dy, z)
+enum : int { kRingCkpt = 0, kRingFull = 1, kRingAgg = 2 };
+template <typename IO, int G, int Q, int MODE, bool CK, bool CUM>
 struct BwdRing;
 
 // Raw inputs of one segment [t0, t0+S) of batch row b for the CTA's channels d0 .. d0+kCpb-1,
@@ -271,18 +274,22 @@ struct BwdFetch {
 
 // Raw inputs of one segment copied into a shared-memory ring by cp.async, kStages - 1 segments
 // ahead, where every row is a multiple of 16 bytes long and starts on a 16-byte boundary. A
-// slot holds the segment's rows as [row][S] io elements -- B (FULL: then C) rows n < kNP, then
-// delta, u (FULL: dy, z) rows of the CTA's channels -- and (CK) the checkpoints of the CTA's
-// channels as [channel][kNP] floats, then (CUM, time split) their dt sums from the chunk's
-// first step as [channel] floats. Pieces of rows beyond N, Dm or L are not copied; stage()
-// reads zeros in their place.
-template <typename IO, int G, int Q, bool FULL, bool CK = FULL, bool CUM = false>
+// slot holds the segment's rows as [row][S] io elements -- the B and/or C rows n < kNP of the
+// mode, then its channel rows (delta, u, dy, z, or a subset) of the CTA's channels -- and (CK)
+// the checkpoints of the CTA's channels as [channel][kNP] floats, then (CUM, time split) their
+// dt sums from the chunk's first step as [channel] floats. Pieces of rows beyond N, Dm or L
+// are not copied; stage() reads zeros in their place.
+template <typename IO, int G, int Q, int MODE, bool CK = (MODE == kRingFull), bool CUM = false>
 struct BwdRing {
     using Cfg = BwdCfg<G, Q>;
     static constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kCpb = Cfg::kCpb, kQ = Cfg::kQ;
     static constexpr int kStepsPerPiece = 16 / (int)sizeof(IO);
     static constexpr int kGran = kS / kStepsPerPiece;                 // pieces per row segment
-    static constexpr int kRowsBC = (FULL ? 2 : 1) * kNP, kRowsCH = (FULL ? 4 : 2) * kCpb;
+    static constexpr bool FULL = MODE == kRingFull, AGG = MODE == kRingAgg;
+    static constexpr int kRowsBC = (FULL ? 2 : 1) * kNP, kRowsCH = (FULL ? 4 : AGG ? 3 : 2) * kCpb;
+    // B/C row block -> 0 B, 1 C; channel row block -> 0 delta, 1 u, 2 dy, 3 z
+    __device__ __forceinline__ static int bc_kind(int blk) { return AGG ? 1 : blk; }
+    __device__ __forceinline__ static int ch_array(int blk) { return AGG && blk > 0 ? blk + 1 : blk; }
     static constexpr int kRows = kRowsBC + kRowsCH;
     static constexpr int kCkFloats = CK ? kCpb * kNP : 0, kCumFloats = CUM ? kCpb : 0;
     // measured on B300: deeper rings change neither pass (adjoint 3 stages, checkpoint 6); a
@@ -311,12 +318,12 @@ struct BwdRing {
                 const int64_t t = t0 + part * kStepsPerPiece;
                 if (t < p.L) {
                     if (row < kRowsBC) {
-                        const int kind = row / kNP, n = row % kNP;
+                        const int kind = bc_kind(row / kNP), n = row % kNP;
                         sbase = kind ? p.C : p.B;
                         stotal = bwd_bc_bytes(p, sizeof(IO));
                         if (n < p.N) src = reinterpret_cast<const IO *>(sbase) + (b * p.N + n) * p.L + t;
                     } else {
-                        const int r = row - kRowsBC, arr = r / kCpb, cc = r % kCpb;
+                        const int r = row - kRowsBC, arr = ch_array(r / kCpb), cc = r % kCpb;
                         const int64_t d = d0 + cc;
                         sbase = arr == 0 ? p.delta : arr == 1 ? p.u : arr == 2 ? p.dy : p.z;
                         stotal = bwd_rows_bytes(p, sizeof(IO));
@@ -354,7 +361,7 @@ struct BwdRing {
         const int64_t t0 = (int64_t)seg * kS;
         constexpr int kBC = kRowsBC * kS, kCH = kCpb * kS;
         for (int e = tid; e < kBC; e += kBwdThreads) {
-            const int kind = e / (kNP * kS), r = e % (kNP * kS), n = r / kS, i = r % kS;
+            const int kind = bc_kind(e / (kNP * kS)), r = e % (kNP * kS), n = r / kS, i = r % kS;
             const float v = (n < p.N && t0 + i < p.L) ? io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + e)) : 0.0f;
             st_chk_s(smem_bwd4, sm + (kind ? Cfg::kOffC : Cfg::kOffB) + (i * G + n % G) * kQ + n / G, v);
         }
@@ -362,27 +369,30 @@ struct BwdRing {
             const int cc = e / kS, i = e % kS;
             const int64_t d = d0 + cc, t = t0 + i;
             float dtv = 0.0f, sgv = 0.0f, dyh = 0.0f, gz = 0.0f, uu = 0.0f;
+            // the channel row blocks of this mode: delta first, then u (not AGG), dy, z (not CKPT)
+            constexpr int kU = 1, kDy = AGG ? 1 : 2, kZ = AGG ? 2 : 3;
             if (d < p.Dm && t < p.L) {
                 const float dl = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + e));
-                uu = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + kCH + e));
+                if (!AGG) uu = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + kU * kCH + e));
                 const float v = dl + sbias[cc];
                 if (!FULL) dtv = p.softplus ? softplus_f(v) : v;
                 else if (p.softplus) dtv = softplus_sigmoid(v, sgv);
                 else dtv = v, sgv = 1.0f;
-                if (FULL) {
-                    const float dy = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + 2 * kCH + e));
+                if (FULL || AGG) {
+                    const float dy = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + kDy * kCH + e));
                     if (p.z) {
-                        const float zz = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + 3 * kCH + e));
+                        const float zz = io_traits<IO>::to_f(ld_chk_s(smem_bwd4, raw + kBC + kZ * kCH + e));
                         const float sz = rcp_approx(1.0f + ex2(-zz * kLog2e));
                         dyh = dy * zz * sz;                            // dy * SiLU(z)
-                        gz = dy * sz * (1.0f + zz * (1.0f - sz));      // dy * SiLU'(z)
+                        if (FULL) gz = dy * sz * (1.0f + zz * (1.0f - sz));   // dy * SiLU'(z)
                     } else {
                         dyh = dy;
                     }
                 }
             }
             st_chk_s(smem_bwd4, sm + Cfg::kOffDt + e, dtv);
-            st_chk_s(smem_bwd4, sm + Cfg::kOffU + e, uu);
+            if (!AGG) st_chk_s(smem_bwd4, sm + Cfg::kOffU + e, uu);
+            if (AGG) st_chk_s(smem_bwd4, sm + Cfg::kOffDyh + e, dyh);
             if (FULL) {
                 st_chk_s(smem_bwd4, sm + Cfg::kOffSg + e, sgv);
                 st_chk_s(smem_bwd4, sm + Cfg::kOffDyh + e, dyh);
@@ -406,22 +416,25 @@ struct BwdRing {
 
 // Checkpoint pass: the forward recurrence, h stored before every S-step segment; the next
 // segments' raw inputs are in flight (in registers, or in the copy ring) while the current one
-// computes.
+// computes. SPLIT (a time-split chunk): held to 64 registers, as the aggregate pass, for eight
+// CTAs per SM, the density the time split aims at (one lane per channel keeps 128 channels'
+// staging slots per thread and gets more); unsplit grids (at least two CTAs per SM, at most a
+// few) keep the registers for the prefetch: 8% faster on 8 x 1536 x 2048 x 16.
 template <typename IO, int G, int Q>
 constexpr size_t bwd_ckpt_smem_bytes() {
     return (size_t)(BwdCfg<G, Q>::kOffU + BwdCfg<G, Q>::kChan + BwdCfg<G, Q>::kCpb) * sizeof(float) +
-           BwdRing<IO, G, Q, false>::bytes();
+           BwdRing<IO, G, Q, kRingCkpt>::bytes();
 }
 // the adjoint aggregate pass: the adjoint's staging without the partial sums or checkpoints
 template <typename IO, int G, int Q>
 constexpr size_t bwd_agg_smem_bytes() {
-    return (size_t)(BwdCfg<G, Q>::kOffPart + BwdCfg<G, Q>::kCpb) * sizeof(float) + BwdRing<IO, G, Q, true, false>::bytes();
+    return (size_t)(BwdCfg<G, Q>::kOffPart + BwdCfg<G, Q>::kCpb) * sizeof(float) + BwdRing<IO, G, Q, kRingAgg>::bytes();
 }
 // the adjoint pass; SPLIT: a time-split chunk (the incoming-state table, the dt sums in the ring)
 template <typename IO, int G, int Q, bool SPLIT>
 constexpr size_t bwd_smem_bytes() {
     return (size_t)(BwdCfg<G, Q>::kFloats + BwdCfg<G, Q>::kCpb * (1 + (SPLIT ? BwdCfg<G, Q>::kNP : 0))) * sizeof(float) +
-           BwdRing<IO, G, Q, true, true, SPLIT>::bytes();
+           BwdRing<IO, G, Q, kRingFull, true, SPLIT>::bytes();
 }
 
 // A lane's Q consecutive floats at p (16-byte or 8-byte aligned) as Q/2 packed pairs.
@@ -436,8 +449,8 @@ __device__ __forceinline__ void load_pairs(const float *p, float2 (&out)[P]) {
     }
 }
 
-template <typename IO, int G, int Q>
-__global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdParams p) {
+template <typename IO, int G, int Q, bool SPLIT>
+__global__ void __launch_bounds__(kBwdThreads, SPLIT ? (G >= 2 ? 8 : 4) : 1) scan_bwd_ckpt_kernel(const BwdParams p) {
     using Cfg = BwdCfg<G, Q>;
     constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
     float *sm = reinterpret_cast<float *>(smem_bwd4);
@@ -459,7 +472,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
     // true state is added to these checkpoints once the chunks' end states are combined)
     const int kc = blockIdx.z, s0 = kc * p.seg_per_chunk, s1 = min(p.nseg, s0 + p.seg_per_chunk);
     float cum = 0.0f;                               // sum of dt from the chunk's first step
-    using Ring = BwdRing<IO, G, Q, false>;
+    using Ring = BwdRing<IO, G, Q, kRingCkpt>;
     float *sbias = sm + Cfg::kOffU + Cfg::kChan;    // the CTA's channels' dt bias (0 without one)
     unsigned char *ring = reinterpret_cast<unsigned char *>(sbias + kCpb);
     for (int c = tid; c < kCpb; c += kBwdThreads)   // read after the loop's first barrier
@@ -483,7 +496,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
                 st_chk_g(p.ckpt, bwd_ck_bytes(p, kNP), ck + (int64_t)seg * kNP + g + G * 2 * k, h2[k].x);
                 st_chk_g(p.ckpt, bwd_ck_bytes(p, kNP), ck + (int64_t)seg * kNP + g + G * (2 * k + 1), h2[k].y);
             }
-            if (p.nchunk > 1 && g == 0) st_chk_g(p.cumdt, bwd_cum_bytes(p), p.cumdt + bd * p.nseg + seg, cum);
+            if (SPLIT && g == 0) st_chk_g(p.cumdt, bwd_cum_bytes(p), p.cumdt + bd * p.nseg + seg, cum);
         }
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();
@@ -510,7 +523,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
             }
         }
     }
-    if (p.nchunk > 1 && valid) {            // the chunk's end state from 0 and its dt sum
+    if (SPLIT && valid) {                   // the chunk's end state from 0 and its dt sum
         float *hl = p.hloc + (bd * p.nchunk + kc) * kNP;
 #pragma unroll
         for (int k = 0; k < kP; ++k) {
@@ -526,7 +539,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_ckpt_kernel(const BwdPar
 // carry leaving its first step (cloc). The carry that actually enters each chunk is then
 // cin_{k-1} = (prod of a_t over chunk k) cin_k + cloc_k, with cin_{last} = dlast.
 template <typename IO, int G, int Q>
-__global__ void __launch_bounds__(kBwdThreads) scan_bwd_agg_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, G >= 2 ? 8 : 4) scan_bwd_agg_kernel(const BwdParams p) {
     using Cfg = BwdCfg<G, Q>;
     constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
     float *sm = reinterpret_cast<float *>(smem_bwd4);
@@ -544,7 +557,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_agg_kernel(const BwdPara
                              (valid && n1 < p.N) ? ld_chk_g(p.A, bwd_dn_bytes(p), p.A + (valid ? d : 0) * p.N + n1) * kLog2e : 0.0f);
         c2[k] = make_float2(0.f, 0.f);
     }
-    using Ring = BwdRing<IO, G, Q, true, false>;
+    using Ring = BwdRing<IO, G, Q, kRingAgg>;
     float *sbias = sm + Cfg::kOffPart;
     unsigned char *ring = reinterpret_cast<unsigned char *>(sbias + kCpb);
     for (int c = tid; c < kCpb; c += kBwdThreads)   // read after the loop's first barrier
@@ -653,7 +666,7 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
         dbias += ddl;
     };
 
-    using Ring = BwdRing<IO, G, Q, true, true, SPLIT>;
+    using Ring = BwdRing<IO, G, Q, kRingFull, true, SPLIT>;
     float *sbias = sm + Cfg::kFloats;               // the CTA's channels' dt bias (0 without one)
     // time split: the state entering this chunk, [channel][kNP]; the checkpoint pass took the
     // chunk's checkpoints from 0, so each is corrected by exp(A*cum) times this state
