@@ -1,5 +1,7 @@
 // Selective scan backward launches (scan_bwd.cuh): checkpoint pass; with a time split the
 // adjoint aggregate pass and the chunk combine; then the adjoint pass.
+#include <algorithm>
+
 #include "launch.h"
 
 namespace ssm {
@@ -75,8 +77,33 @@ cudaError_t launch_bwd_t(const BwdParams &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// CTAs of the split adjoint pass that fit one SM: its launch bound, or what its shared memory
+// allows (228 KB per SM, 1 KB of it reserved per CTA)
+template <typename IO, int G, int Q>
+int split_adjoint_ctas_t() {
+    constexpr int by_smem = (int)(233472 / (bwd_smem_bytes<IO, G, Q, true>() + 1024));
+    return std::min(Q == 4 ? 3 : 4, by_smem);
+}
+
 // lane splits built: four states per lane with 1-32 lanes per channel, two states per lane
 // with 2-16
+template <typename IO>
+int split_adjoint_ctas_io(int G, int Q) {
+    switch (Q * 100 + G) {
+        case 401: return split_adjoint_ctas_t<IO, 1, 4>();
+        case 402: return split_adjoint_ctas_t<IO, 2, 4>();
+        case 404: return split_adjoint_ctas_t<IO, 4, 4>();
+        case 408: return split_adjoint_ctas_t<IO, 8, 4>();
+        case 416: return split_adjoint_ctas_t<IO, 16, 4>();
+        case 432: return split_adjoint_ctas_t<IO, 32, 4>();
+        case 202: return split_adjoint_ctas_t<IO, 2, 2>();
+        case 204: return split_adjoint_ctas_t<IO, 4, 2>();
+        case 208: return split_adjoint_ctas_t<IO, 8, 2>();
+        case 216: return split_adjoint_ctas_t<IO, 16, 2>();
+        default: return 1;
+    }
+}
+
 template <typename IO>
 cudaError_t launch_bwd_io(int G, int Q, const BwdParams &p, cudaStream_t s) {
     switch (Q * 100 + G) {
@@ -97,6 +124,10 @@ cudaError_t launch_bwd_io(int G, int Q, const BwdParams &p, cudaStream_t s) {
 
 cudaError_t launch_bwd(ssm_dtype_t io, int G, int Q, const BwdParams &p, cudaStream_t s) {
     return io == SSM_BF16 ? launch_bwd_io<bf16>(G, Q, p, s) : launch_bwd_io<float>(G, Q, p, s);
+}
+
+int bwd_split_adjoint_ctas_per_sm(ssm_dtype_t io, int G, int Q) {
+    return io == SSM_BF16 ? split_adjoint_ctas_io<bf16>(G, Q) : split_adjoint_ctas_io<float>(G, Q);
 }
 
 }  // namespace ssm

@@ -833,17 +833,18 @@ namespace {
 // Backward plan. Lane split: Q states per thread, G lanes per channel (the smallest power of
 // two with Q*G >= N: 1-32 at four states, 2-16 at two), 128/G channels per CTA. Time split:
 // with fewer than two CTAs per SM, the sequence is cut into K chunks of whole 8-step segments
-// (at least 16 segments each, K <= 32) aiming at about 8 CTAs per SM; each chunk is a CTA of
-// the checkpoint, aggregate and adjoint passes. Q = 2 for N <= 8, else 4; without a possible
+// (at least 16 segments each, K <= 64), each a CTA of the checkpoint, aggregate and adjoint
+// passes; K gives the adjoint at least two waves and, among those counts, the fullest last
+// wave (1 x 1536 x 16384 x 16: 25 chunks 1.24 ms, 18 1.17, 37 1.15). Q = 2 for N <= 8, else 4; without a possible
 // time split, also Q = 2 when four states per lane give fewer than half a warp per SM
-// sub-partition. Measured on B300 (bf16, gate, ms; planner's choice first):
-//   1 x 768 x 8192 x 16:   Q4 K50 0.39; Q4 K16 0.41; Q2 K37 0.42; Q2 unsplit 1.89
-//   1 x 1536 x 4096 x 32:  Q4 K13 0.66; Q4 K4 0.69; Q2 K10 0.97; Q4 unsplit 1.27
-//   2 x 512 x 4096 x 8:    Q2 K32 ~0.20; Q4 K74 0.28; Q2 unsplit 1.30
-//   1 x 5120 x 4096 x 16:  Q4 K8 1.12; Q4 K3 1.38; Q2 unsplit 1.32
-//   2 x 1536 x 16384 x 16: Q4 K13 2.66; Q4 K4 2.95; Q2 K10 2.96; Q2 unsplit 4.38
-//   4 x 1536 x 2048 x 16:  Q4 K7 0.73; Q2 unsplit 0.67
-//   8 x 1536 x 2048 x 16:  Q4 unsplit 1.10; Q4 K4 1.30; Q2 unsplit 1.29
+// sub-partition. Measured on B300 (bf16, gate, ms; the planner's choice first; K = chunks):
+//   8 x 1536 x 2048 x 16:   Q4 unsplit 1.08; Q4 K4 1.30; Q2 unsplit 1.29
+//   4 x 1536 x 2048 x 16:   Q4 K16 0.59; Q2 unsplit 0.67; Q4 unsplit 0.89
+//   1 x 768 x 8192 x 16:    Q4 K37 0.31; Q4 K32 0.35; Q2 unsplit 1.89
+//   1 x 1536 x 4096 x 32:   Q4 K23 0.55; Q4 unsplit 1.27
+//   2 x 512 x 4096 x 8:     Q2 K32 0.16; Q4 K74 0.28; Q2 unsplit 1.30
+//   1 x 5120 x 4096 x 16:   Q4 K11 0.94; Q4 K8 0.97; Q2 unsplit 1.32
+//   2 x 1536 x 16384 x 16:  Q4 K37 2.21; Q4 K13 2.35; Q2 unsplit 4.38
 struct BwdPlan {
     int G, Q, nchunk, seg_per_chunk;
     int64_t nseg;
@@ -862,8 +863,20 @@ BwdPlan bwd_plan(const ssm_dims_t &d) {
     const ssm_plan_override_t ov = plan_override();
     auto chunks = [&](int q) -> int64_t {
         int64_t k = 1;
-        if (ov.bwd_chunks > 0) k = ov.bwd_chunks;
-        else if (ctas(q) < 2 * sms) k = std::min<int64_t>({(8 * sms + ctas(q) - 1) / ctas(q), nseg / 16, 32});
+        if (ov.bwd_chunks > 0) {
+            k = ov.bwd_chunks;
+        } else if (ctas(q) < 2 * sms) {
+            // the adjoint's CTAs are equal and latency-bound, so its time goes with whole waves:
+            // from at least two waves up, the chunk count whose last wave is fullest
+            const int64_t slots = (int64_t)bwd_split_adjoint_ctas_per_sm(d.io_dtype, lanes(q), q) * sms;
+            const int64_t hi = std::min<int64_t>(nseg / 16, 64), lo = std::min(hi, (2 * slots + ctas(q) - 1) / ctas(q));
+            double best = -1.0;
+            for (int64_t c = std::max<int64_t>(lo, 1); c <= hi; ++c) {
+                const int64_t cta = ctas(q) * c, waves = (cta + slots - 1) / slots;
+                const double fill = (double)cta / (double)(waves * slots);
+                if (fill > best + 1e-9) best = fill, k = c;
+            }
+        }
         return std::max<int64_t>(1, std::min<int64_t>({k, nseg, 65535}));
     };
     int q = 4;
