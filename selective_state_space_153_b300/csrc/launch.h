@@ -68,7 +68,5 @@ cudaError_t launch_decode(ssm_dtype_t io, int kind, int lpc, bool zoh, const Dec
 // backward (scan_bwd.cuh): checkpoint pass then adjoint pass; G lanes per channel
 // backward: G lanes per channel, Q (2 or 4) states per lane
 cudaError_t launch_bwd(ssm_dtype_t io, int G, int Q, const BwdParams &p, cudaStream_t s);
-// CTAs of the time-split adjoint pass that fit one SM (launch bound and shared memory)
-int bwd_split_adjoint_ctas_per_sm(ssm_dtype_t io, int G, int Q);
 
 }  // namespace ssm

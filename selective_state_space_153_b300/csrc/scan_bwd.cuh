@@ -865,4 +865,8 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
     }
 }
 
+// CTAs of the time-split adjoint pass that fit one SM (launch bound and shared memory); in
+// k_bwd.cu
+int bwd_split_adjoint_ctas_per_sm(ssm_dtype_t io, int G, int Q);
+
 }  // namespace ssm
