@@ -558,6 +558,44 @@ def test_cuda_graph_capture_and_replay():
     assert ssm.stream_status() == ssm.SSM_OK
 
 
+def test_backward_cuda_graph_capture_and_replay():
+    """The backward with a caller workspace queues only memsets and kernels on the caller's
+    stream: captured in a CUDA graph on a shape the planner splits in time (all four passes)
+    and replayed, it reproduces the eager gradients (up to the order of fp32 atomic sums)."""
+    import ctypes
+    cfg = gen.ScanConfig("graphb", 1, 64, 4096, 16, io="bf16", gate=True, dskip="ones", seed=33, a_kind="random")
+    inp = gen.scan_inputs(cfg)
+    g = to_dev(inp)
+    dy = torch.from_numpy(np.random.default_rng(34).standard_normal((1, 64, 4096)).astype(np.float32)).to(
+        torch.bfloat16).cuda()
+    dm = ssm.dims(1, 64, 4096, 16, ssm.SSM_BF16)
+    wsb = ssm.load().ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(dm))
+    assert wsb > 4 * 64 * 512 * 16            # checkpoints plus the time split's arrays
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+
+    def work():
+        return ssm.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, D=g["D"], z=g["z"],
+                                      delta_bias=g["delta_bias"], delta_softplus=True, workspace=ws, stream=side)
+
+    with torch.cuda.stream(side):
+        eager = {k: v.clone() for k, v in work().items() if v is not None}
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        out = work()
+    for _ in range(2):
+        for v in out.values():
+            if v is not None:
+                v.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        for k, r in eager.items():
+            err = float((out[k] - r).abs().max() / r.abs().max().clamp_min(1e-30))
+            assert err <= 1e-5, f"d{k}: {err:.2e}"
+    assert ssm.stream_status() == ssm.SSM_OK
+
+
 # ---- decode ---------------------------------------------------------------------------------
 def _decode_gpu(inp, steps):
     g = to_dev(inp)
