@@ -12,10 +12,17 @@
 //     dA   += lambda_t dt_t a_t h_{t-1}   dD += dyhat_t u_t   dz_t = dy_t yhat_t SiLU'(z_t)
 // (v = delta + bias; sigmoid is the softplus derivative; without softplus ddelta = ddt).
 //
-// Work decomposition: a thread owns Q states n = g + G*q (q < Q; Q = 4, or 2 where four
-// states per lane leave the GPU short of warps) of one channel, G lanes per channel (a power
-// of two, QG >= N), 32/G channels per warp, 128/G per CTA; the batch row is grid.y. Pass 1 (scan_bwd_ckpt_kernel) runs the recurrence forward and stores h at
-// the start of every S-step segment. Pass 2 (scan_bwd_kernel) walks the segments backwards:
+// Work decomposition: a thread owns Q states n = g + G*q (q < Q; Q = 4, or 2 for small N or
+// where four states per lane leave the GPU short of warps) of one channel, G lanes per
+// channel (a power of two, QG >= N), 32/G channels per warp, 128/G per CTA; the batch row is
+// grid.y and the time-split chunk grid.z. Pass 1 (scan_bwd_ckpt_kernel) runs the recurrence
+// forward and stores h at the start of every S-step segment. With a time split (chunks of
+// whole segments, each a CTA), pass 1 starts every chunk from 0, an aggregate pass
+// (scan_bwd_agg_kernel) runs the adjoint of each chunk but the first from a zero carry, and a
+// combine forms each chunk's incoming state and carry from those chunk-local results (the
+// recurrences are linear in their initial values). Pass 2 (scan_bwd_kernel) walks the
+// segments backwards (a split chunk from its incoming carry, correcting each chunk-local
+// checkpoint by exp(A*cum) times the chunk's incoming state):
 //   * the CTA stages the segment's B, C rows (as [t][g][q], so a lane's states are one
 //     16-byte read) and, once per (channel, step), dt, the softplus derivative, u,
 //     dyhat = dy*SiLU(z) and the gate derivative factor dy*SiLU'(z). The raw inputs of the
