@@ -174,6 +174,34 @@ def test_backward_gradients_forced_split(Bt, D, L, N, io, gate, dskip, bias, dla
         _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind)
 
 
+@pytest.mark.parametrize("cfg", [gen.M130, gen.BWD_LONG], ids=["m130", "bwd_long"])
+def test_backward_full_size_sampled_channels(cfg):
+    """The bench's backward workloads at full size, in the launch configuration the planner
+    gives them (8 x 1536 x 2048 x 16 unsplit; 1 x 1536 x 16384 x 16 split into 37 chunks):
+    the gradients that belong to one channel -- du, ddelta, dz over every batch row and step,
+    and dA, dD, dbias -- for sampled channels, against the float64 oracle run on those
+    channels alone (the channels of the scan are independent given B and C). dB and dC sum
+    over every channel, so they are compared at the small sizes above."""
+    from oracle import backward as obwd
+    inp = gen.scan_inputs(cfg)
+    rng = np.random.default_rng(cfg.L)
+    dy = torch.from_numpy(rng.standard_normal((cfg.Bt, cfg.D, cfg.L)).astype(np.float32)).to(inp["u"].dtype)
+    g = to_dev(inp)
+    got = ssm.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy.cuda(), D=g["D"], z=g["z"],
+                                 delta_bias=g["delta_bias"], delta_softplus=True)
+    torch.cuda.synchronize()
+    f = gen.as_f64
+    for d in (0, 777, cfg.D - 1):
+        sl = slice(d, d + 1)
+        ref = obwd.scan_backward(f(inp["u"][:, sl]), f(inp["delta"][:, sl]), f(inp["A"][sl]), f(inp["B"]), f(inp["C"]),
+                                 D=f(inp["D"][sl]), z=f(inp["z"][:, sl]), delta_bias=f(inp["delta_bias"][sl]),
+                                 delta_softplus=True, dy=f(dy[:, sl]))
+        for k, gk in (("u", got["u"][:, sl]), ("delta", got["delta"][:, sl]), ("z", got["z"][:, sl]),
+                      ("A", got["A"][sl]), ("D", got["D"][sl]), ("delta_bias", got["delta_bias"][sl])):
+            err = _grad_err(gk.double().cpu().numpy(), ref[k])
+            assert err <= 5e-2, f"channel {d}, d{k}: element-wise error {err:.3e}"
+
+
 @pytest.mark.parametrize("chunks", [1, 3])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_backward_rows_off_pair_alignment(io, chunks):
