@@ -1,5 +1,5 @@
-// Selective scan backward launches (scan_bwd.cuh): checkpoint pass; with a time split the
-// adjoint aggregate pass and the chunk combine; then the adjoint pass.
+// Selective scan backward launches (scan_bwd.cuh): checkpoint pass (with a time split, in one
+// launch with the adjoint aggregate pass, then the chunk combine); then the adjoint pass.
 #include <algorithm>
 
 #include "launch.h"
@@ -48,7 +48,7 @@ template <typename IO, int G, int Q>
 cudaError_t launch_bwd_t(const BwdParams &p, cudaStream_t s) {
     constexpr size_t ck = bwd_ckpt_smem_bytes<IO, G, Q>(), sm = bwd_smem_bytes<IO, G, Q, false>();
     constexpr size_t sms = bwd_smem_bytes<IO, G, Q, true>();
-    constexpr size_t ag = bwd_agg_smem_bytes<IO, G, Q>();
+    constexpr size_t ag = bwd_agg_smem_bytes<IO, G, Q>(), fr = ck > ag ? ck : ag;
     constexpr int kCpb = BwdCfg<G, Q>::kCpb;
     const dim3 grid((unsigned)((p.Dm + kCpb - 1) / kCpb), (unsigned)p.Bt, (unsigned)p.nchunk);
     static std::atomic<unsigned long long> attr_set{0};
@@ -57,23 +57,22 @@ cudaError_t launch_bwd_t(const BwdParams &p, cudaStream_t s) {
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(scan_bwd_kernel<IO, G, Q, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(scan_bwd_ckpt_kernel<IO, G, Q, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ck);
+            r = cudaFuncSetAttribute(scan_bwd_ckpt_kernel<IO, G, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ck);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(scan_bwd_ckpt_kernel<IO, G, Q, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ck);
-        if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(scan_bwd_agg_kernel<IO, G, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ag);
+            r = cudaFuncSetAttribute(scan_bwd_split_front_kernel<IO, G, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)fr);
         return r;
     });
     if (e != cudaSuccess) return e;
-    if (p.nchunk > 1) scan_bwd_ckpt_kernel<IO, G, Q, true><<<grid, kBwdThreads, ck, s>>>(p);
-    else scan_bwd_ckpt_kernel<IO, G, Q, false><<<grid, kBwdThreads, ck, s>>>(p);
-    if (p.nchunk > 1) {   // time split: the adjoint carries of chunks 1.., then both combines
-        scan_bwd_agg_kernel<IO, G, Q><<<dim3(grid.x, grid.y, grid.z - 1), kBwdThreads, ag, s>>>(p);
+    if (p.nchunk > 1) {   // time split: chunk-local checkpoints and adjoint carries, both combines
+        scan_bwd_split_front_kernel<IO, G, Q><<<dim3(grid.x, grid.y, 2 * grid.z - 1), kBwdThreads, fr, s>>>(p);
         const int64_t threads = p.Bt * p.Dm * (int64_t)(G * Q);
         bwd_chunk_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p, G * Q);
+        scan_bwd_kernel<IO, G, Q, true><<<grid, kBwdThreads, sms, s>>>(p);
+    } else {
+        scan_bwd_ckpt_kernel<IO, G, Q><<<grid, kBwdThreads, ck, s>>>(p);
+        scan_bwd_kernel<IO, G, Q, false><<<grid, kBwdThreads, sm, s>>>(p);
     }
-    if (p.nchunk > 1) scan_bwd_kernel<IO, G, Q, true><<<grid, kBwdThreads, sms, s>>>(p);
-    else scan_bwd_kernel<IO, G, Q, false><<<grid, kBwdThreads, sm, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -423,10 +423,11 @@ struct BwdRing {
 
 // Checkpoint pass: the forward recurrence, h stored before every S-step segment; the next
 // segments' raw inputs are in flight (in registers, or in the copy ring) while the current one
-// computes. SPLIT (a time-split chunk): held to 64 registers, as the aggregate pass, for eight
-// CTAs per SM, the density the time split aims at (one lane per channel keeps 128 channels'
-// staging slots per thread and gets more); unsplit grids (at least two CTAs per SM, at most a
-// few) keep the registers for the prefetch: 8% faster on 8 x 1536 x 2048 x 16.
+// computes. SPLIT (a time-split chunk, launched with the aggregate pass): 64 registers, for
+// eight CTAs per SM, the density the time split aims at (one lane per channel keeps 128
+// channels' staging slots per thread and gets more); the unsplit kernel (at least two CTAs
+// per SM, at most a few) keeps the registers for the prefetch: 8% faster on
+// 8 x 1536 x 2048 x 16.
 template <typename IO, int G, int Q>
 constexpr size_t bwd_ckpt_smem_bytes() {
     return (size_t)(BwdCfg<G, Q>::kOffU + BwdCfg<G, Q>::kChan + BwdCfg<G, Q>::kCpb) * sizeof(float) +
@@ -457,7 +458,7 @@ __device__ __forceinline__ void load_pairs(const float *p, float2 (&out)[P]) {
 }
 
 template <typename IO, int G, int Q, bool SPLIT>
-__global__ void __launch_bounds__(kBwdThreads, SPLIT ? (G >= 2 ? 8 : 4) : 1) scan_bwd_ckpt_kernel(const BwdParams p) {
+__device__ __forceinline__ void bwd_ckpt_body(const BwdParams &p, int kc) {
     using Cfg = BwdCfg<G, Q>;
     constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
     float *sm = reinterpret_cast<float *>(smem_bwd4);
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(kBwdThreads, SPLIT ? (G >= 2 ? 8 : 4) : 1) sca
     float *ck = p.ckpt + bd * (int64_t)p.nseg * kNP;
     // this CTA's chunk of segments; the state starts from 0 at the chunk (time split: the
     // true state is added to these checkpoints once the chunks' end states are combined)
-    const int kc = blockIdx.z, s0 = kc * p.seg_per_chunk, s1 = min(p.nseg, s0 + p.seg_per_chunk);
+    const int s0 = kc * p.seg_per_chunk, s1 = min(p.nseg, s0 + p.seg_per_chunk);
     float cum = 0.0f;                               // sum of dt from the chunk's first step
     using Ring = BwdRing<IO, G, Q, kRingCkpt>;
     float *sbias = sm + Cfg::kOffU + Cfg::kChan;    // the CTA's channels' dt bias (0 without one)
@@ -546,7 +547,7 @@ __global__ void __launch_bounds__(kBwdThreads, SPLIT ? (G >= 2 ? 8 : 4) : 1) sca
 // carry leaving its first step (cloc). The carry that actually enters each chunk is then
 // cin_{k-1} = (prod of a_t over chunk k) cin_k + cloc_k, with cin_{last} = dlast.
 template <typename IO, int G, int Q>
-__global__ void __launch_bounds__(kBwdThreads, G >= 2 ? 8 : 4) scan_bwd_agg_kernel(const BwdParams p) {
+__device__ __forceinline__ void bwd_agg_body(const BwdParams &p, int kc) {
     using Cfg = BwdCfg<G, Q>;
     constexpr int kS = Cfg::kS, kNP = Cfg::kNP, kQ = Cfg::kQ, kCpb = Cfg::kCpb, kP = Cfg::kP;
     float *sm = reinterpret_cast<float *>(smem_bwd4);
@@ -555,7 +556,7 @@ __global__ void __launch_bounds__(kBwdThreads, G >= 2 ? 8 : 4) scan_bwd_agg_kern
     const int64_t b = blockIdx.y, d0 = (int64_t)blockIdx.x * kCpb, d = d0 + cc;
     const bool valid = d < p.Dm;
     const int64_t bd = b * p.Dm + (valid ? d : 0);
-    const int kc = blockIdx.z + 1, s0 = kc * p.seg_per_chunk, s1 = min(p.nseg, s0 + p.seg_per_chunk);
+    const int s0 = kc * p.seg_per_chunk, s1 = min(p.nseg, s0 + p.seg_per_chunk);
     float2 Ap2[kP], c2[kP];
 #pragma unroll
     for (int k = 0; k < kP; ++k) {
@@ -614,6 +615,22 @@ __global__ void __launch_bounds__(kBwdThreads, G >= 2 ? 8 : 4) scan_bwd_agg_kern
             st_chk_g(p.cloc, bwd_chunk_bytes(p, kNP), cl + g + G * (2 * k + 1), c2[k].y);
         }
     }
+}
+
+// Unsplit checkpoint pass: one CTA per channel block and batch row.
+template <typename IO, int G, int Q>
+__global__ void __launch_bounds__(kBwdThreads, 1) scan_bwd_ckpt_kernel(const BwdParams p) {
+    bwd_ckpt_body<IO, G, Q, false>(p, 0);
+}
+
+// Time split, the two passes that need no combined carry, in one launch: grid.z < nchunk are
+// the checkpoint pass's chunks, the rest the aggregate pass's chunks 1 .. nchunk-1. The two
+// roles read the same rows and are both latency-bound; sharing the SMs evens out each one's
+// partial last wave. Held to 64 registers (eight CTAs per SM).
+template <typename IO, int G, int Q>
+__global__ void __launch_bounds__(kBwdThreads, G >= 2 ? 8 : 4) scan_bwd_split_front_kernel(const BwdParams p) {
+    if ((int)blockIdx.z < p.nchunk) bwd_ckpt_body<IO, G, Q, true>(p, (int)blockIdx.z);
+    else bwd_agg_body<IO, G, Q>(p, (int)blockIdx.z - p.nchunk + 1);
 }
 
 template <typename IO, int G, int Q, bool SPLIT>
