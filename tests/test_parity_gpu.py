@@ -222,6 +222,15 @@ def test_backward_gradients_time_split(Bt, D, L, N, io, gate, dskip, bias, dlast
         _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind)
 
 
+@pytest.mark.parametrize("L,chunks", [(560, 40), (512, 64), (560, 100)])
+def test_backward_time_split_many_chunks(L, chunks):
+    """Many chunks of one or two 8-step segments: 32 to 64 chunks take the combine's warp scan
+    (560 steps, 40 asked: 35 chunks of 2 segments, lanes past the last chunk; 512 steps: 64
+    chunks, every lane two), more than 64 its loop (560 steps, 100 asked: 70 chunks)."""
+    with ssm.plan_override(bwd_chunks=chunks):
+        _check_backward(2, 9, L, 16, "bf16", True, "normal", True, True, "scaled")
+
+
 @pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,bias,dlast,a_kind", [c for c in BWD_CASES if c[3] <= 32])
 def test_backward_time_split_two_states_per_lane(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind):
     with ssm.plan_override(bwd_chunks=3, bwd_states_per_lane=2):
