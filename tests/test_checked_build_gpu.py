@@ -221,6 +221,7 @@ BWD_CHECK_CASES = [
     (1, 20, 70, 32, "bf16", 1, 0, False),    # two-step loads, unsplit
     (2, 9, 70, 16, "bf16", 3, 0, True),      # inputs off alignment: single steps, split
     (1, 5, 40, 100, "f32", 1, 0, False),     # N = 100: 32 lanes per channel
+    (1, 9, 560, 16, "bf16", 40, 0, False),   # 35 chunks: the combine's warp scan
 ]
 
 
