@@ -718,6 +718,39 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
                            : make_float2(0.f, 0.f);
         cm = (valid && fold) ? ld_chk_g(p.cumdt, bwd_cum_bytes(p), p.cumdt + bd * p.nseg + seg) : 0.0f;
     };
+    // dB, dC of the segment starting at t0: sum the CTA's channels, one vector atomic per
+    // (state, 4 steps). Run for the previous segment between the next one's barriers (the
+    // staging touches other shared memory), which saves a barrier per segment.
+    auto reduce_dbc = [&](int64_t t0) {
+        constexpr int kItems = 2 * kNP * (kS / 4);
+        for (int e = tid; e < kItems; e += kBwdThreads) {
+            const int kind = e / (kNP * (kS / 4)), r = e % (kNP * (kS / 4)), n = r / (kS / 4), tq = r % (kS / 4);
+            if (n >= p.N) continue;
+            const float *src = sm + Cfg::kOffPart + kind * kCpb * Cfg::kPartCh + n * Cfg::kRow + 4 * tq;
+            float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+#pragma unroll 8
+            for (int ch = 0; ch < kCpb; ++ch) {
+                const float4 v = ld_chk_s(smem_bwd4, reinterpret_cast<const float4 *>(src + ch * Cfg::kPartCh));
+                lo = __fadd2_rn(lo, make_float2(v.x, v.y));
+                hi = __fadd2_rn(hi, make_float2(v.z, v.w));
+            }
+            const float4 acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+            const int64_t t = t0 + 4 * tq;
+            float *dst = (kind ? p.dC : p.dB) + (b * p.N + n) * p.L + t;
+            if (t + 3 < p.L && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+                if (SSM_CHK_G(kind ? p.dC : p.dB, bwd_bc_bytes(p, 4), dst, 16))
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc.x), "f"(acc.y),
+                                 "f"(acc.z), "f"(acc.w)
+                                 : "memory");
+            } else {
+                const float av[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (t + k < p.L && SSM_CHK_G(kind ? p.dC : p.dB, bwd_bc_bytes(p, 4), dst + k, 4))
+                        atomicAdd(dst + k, av[k]);
+            }
+        }
+    };
     float2 ckn[kP];
     float cumn = 0.0f;
     // this CTA's chunk of segments, walked backwards from its last
@@ -736,6 +769,7 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
         const int64_t t0 = (int64_t)seg * kS;
         if (p.ring) cp_async_wait<Ring::kStages - 2>();
         __syncthreads();                        // the previous segment is done with shared memory
+        if (seg < s1 - 1) reduce_dbc(t0 + kS);   // the previous (later) segment's terms
         if (p.ring) Ring::stage(p, ring, sm, sbias, seg, d0, ckn, cumn);
         else f.stage(p, sm, sbias, t0, d0);
         __syncthreads();
@@ -835,37 +869,9 @@ __global__ void __launch_bounds__(kBwdThreads, Q == 4 ? 3 : 4) scan_bwd_kernel(c
                 finish(grp * kGrp + g, t0, yhs, dus, dds);
             }
         }
-        // dB, dC of the segment: sum the CTA's channels, one vector atomic per (state, 4 steps)
-        __syncthreads();
-        constexpr int kItems = 2 * kNP * (kS / 4);
-        for (int e = tid; e < kItems; e += kBwdThreads) {
-            const int kind = e / (kNP * (kS / 4)), r = e % (kNP * (kS / 4)), n = r / (kS / 4), tq = r % (kS / 4);
-            if (n >= p.N) continue;
-            const float *src = sm + Cfg::kOffPart + kind * kCpb * Cfg::kPartCh + n * Cfg::kRow + 4 * tq;
-            float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
-#pragma unroll 8
-            for (int ch = 0; ch < kCpb; ++ch) {
-                const float4 v = ld_chk_s(smem_bwd4, reinterpret_cast<const float4 *>(src + ch * Cfg::kPartCh));
-                lo = __fadd2_rn(lo, make_float2(v.x, v.y));
-                hi = __fadd2_rn(hi, make_float2(v.z, v.w));
-            }
-            const float4 acc = make_float4(lo.x, lo.y, hi.x, hi.y);
-            const int64_t t = t0 + 4 * tq;
-            float *dst = (kind ? p.dC : p.dB) + (b * p.N + n) * p.L + t;
-            if (t + 3 < p.L && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-                if (SSM_CHK_G(kind ? p.dC : p.dB, bwd_bc_bytes(p, 4), dst, 16))
-                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc.x), "f"(acc.y),
-                                 "f"(acc.z), "f"(acc.w)
-                                 : "memory");
-            } else {
-                const float av[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (t + k < p.L && SSM_CHK_G(kind ? p.dC : p.dB, bwd_bc_bytes(p, 4), dst + k, 4))
-                        atomicAdd(dst + k, av[k]);
-            }
-        }
     }
+    __syncthreads();                            // the last segment's dB/dC terms are complete
+    reduce_dbc((int64_t)s0 * kS);
     // dA per state; dD and the dt bias summed over the channel's lanes first
 #pragma unroll
     for (int o = G / 2; o >= 1; o /= 2) {
