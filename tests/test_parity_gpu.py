@@ -203,6 +203,14 @@ def test_backward_full_size_sampled_channels(cfg):
 
 
 @pytest.mark.parametrize("chunks", [1, 3])
+@pytest.mark.parametrize("Bt,D,L,N,io,gate,dskip,bias,dlast,a_kind", BWD_CASES[:5])
+def test_backward_without_softplus(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind, chunks):
+    """delta_softplus = 0: dt = delta + bias directly, so ddelta = ddt (no sigmoid factor)."""
+    with ssm.plan_override(bwd_chunks=chunks):
+        _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind, softplus=False)
+
+
+@pytest.mark.parametrize("chunks", [1, 3])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_backward_rows_off_pair_alignment(io, chunks):
     """Even length with every input one element off a 2-element boundary: the rows are read
@@ -253,11 +261,15 @@ def _odd_offset(t):
     return v
 
 
-def _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind, odd_offset=False):
+def _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind, odd_offset=False, softplus=True):
     from oracle import backward as obwd
     cfg = gen.ScanConfig("bwd", Bt, D, L, N, io=io, gate=gate, dskip=dskip, bias=bias, seed=3 * L + N,
                          a_kind=a_kind)
     inp = gen.scan_inputs(cfg)
+    if not softplus:  # the raw step is the step itself: keep it positive
+        inp["delta"] = (inp["delta"].float().abs() * 0.2).to(inp["delta"].dtype)
+        if inp["delta_bias"] is not None:
+            inp["delta_bias"] = torch.full_like(inp["delta_bias"], 0.01)
     rng = np.random.default_rng(L + N)
     dy = torch.from_numpy(rng.standard_normal((Bt, D, L)).astype(np.float32)).to(inp["u"].dtype)
     dl = torch.from_numpy(rng.standard_normal((Bt, D, N)).astype(np.float32)) if dlast else None
@@ -268,12 +280,12 @@ def _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind, odd_offse
             g[k] = _odd_offset(g[k])
         dyd = _odd_offset(dyd)
     got = ssm.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dyd, D=g["D"], z=g["z"],
-                                 delta_bias=g["delta_bias"], delta_softplus=True,
+                                 delta_bias=g["delta_bias"], delta_softplus=softplus,
                                  dlast_state=None if dl is None else dl.cuda())
     torch.cuda.synchronize()
     f = gen.as_f64
     ref = obwd.scan_backward(f(inp["u"]), f(inp["delta"]), f(inp["A"]), f(inp["B"]), f(inp["C"]), D=f(inp["D"]),
-                             z=f(inp["z"]), delta_bias=f(inp["delta_bias"]), delta_softplus=True, dy=f(dy),
+                             z=f(inp["z"]), delta_bias=f(inp["delta_bias"]), delta_softplus=softplus, dy=f(dy),
                              dlast=None if dl is None else f(dl))
     # fp32: sums of up to L*N*D terms in fp32 with atomics, compared element by element;
     # bf16: the rounding of the bf16 inputs' products at 2^-9
