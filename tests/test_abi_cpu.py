@@ -108,6 +108,33 @@ def test_state_update_argument_errors(lib):
     assert f(ctypes.byref(ssm.dims(0, 8, 1, 16, 1)), None, None, None, None, None, None, None, None, None, None) == ssm.SSM_OK
 
 
+def test_backward_argument_errors(lib):
+    """ssm_selective_scan_bwd rejects bad arguments on the host, before any CUDA call (a caller
+    workspace is passed, so no default workspace is looked up)."""
+    f = lib.ssm_selective_scan_bwd
+    d = ssm.dims(1, 4, 64, 4, ssm.SSM_F32)
+
+    def call(dims=d, u=A, delta=A, Am=A, B=A, C=A, dy=A, du=A, ddelta=A, dA=A, dB=A, dC=A, ws=A, wsb=1 << 20):
+        return f(ctypes.byref(dims) if dims is not None else None, u, delta, Am, B, C, None, None, None, 1, dy,
+                 None, du, ddelta, dA, dB, dC, None, None, None, ws, wsb, None)
+    assert call(dims=None) == ssm.SSM_ERR_NULL
+    assert call(u=None) == ssm.SSM_ERR_NULL
+    assert call(dy=None) == ssm.SSM_ERR_NULL
+    assert call(dA=None) == ssm.SSM_ERR_NULL
+    assert call(dC=None) == ssm.SSM_ERR_NULL
+    assert call(u=MIS) == ssm.SSM_ERR_ALIGN
+    assert call(dB=MIS) == ssm.SSM_ERR_ALIGN
+    assert call(ws=MIS) == ssm.SSM_ERR_ALIGN
+    assert call(dims=ssm.dims(1, 4, 64, 4, 7)) == ssm.SSM_ERR_DTYPE
+    assert call(dims=ssm.dims(1, 4, -64, 4, 0)) == ssm.SSM_ERR_SHAPE
+    assert call(dims=ssm.dims(70000, 4, 64, 4, 0)) == ssm.SSM_ERR_UNSUPPORTED    # batch rows on grid.y
+    need = lib.ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(d))
+    assert need > 0
+    assert call(wsb=need - 16) == ssm.SSM_ERR_WORKSPACE
+    # nothing to do for an empty batch or channel count: OK without touching the GPU
+    assert call(dims=ssm.dims(0, 4, 64, 4, 0), u=None, dy=None) == ssm.SSM_OK
+
+
 def test_workspace_query(lib):
     # a sequence over too few channels to give every SM sub-partition two warps is cut into
     # chunks whose carries pass through the workspace; a batch wide enough needs none
