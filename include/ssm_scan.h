@@ -309,7 +309,8 @@ size_t ssm_conv_selective_scan_workspace_bytes(const ssm_dims_t *dims);
  *                least ssm_selective_scan_bwd_workspace_bytes(dims) bytes, 16-byte aligned.
  * Pointers need only their element alignment. Sums over channels, batch rows and time use
  * fp32 atomic additions, so results may differ in the last bits between runs.
- * Returns SSM_OK (also for an empty batch or channel count: the sums over them are zeroed);
+ * Returns SSM_OK (with nothing written for an empty batch or channel count; for an empty
+ * sequence dA, dD and ddelta_bias are zeroed);
  * SSM_ERR_NULL for a missing required pointer; SSM_ERR_ALIGN for a misaligned pointer or
  * workspace; SSM_ERR_SHAPE / SSM_ERR_DTYPE for bad dims; SSM_ERR_UNSUPPORTED for more than
  * 65535 batch rows or dstate > 128; SSM_ERR_WORKSPACE when a caller or registered workspace
