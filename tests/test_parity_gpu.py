@@ -230,6 +230,24 @@ def test_backward_gradients_time_split(Bt, D, L, N, io, gate, dskip, bias, dlast
         _check_backward(Bt, D, L, N, io, gate, dskip, bias, dlast, a_kind)
 
 
+def test_backward_empty_sequence():
+    """seqlen = 0: no step contributes, so the parameter gradients (dA, dD, d bias) come back
+    as zeros and nothing else is touched."""
+    g = {"u": torch.empty((2, 5, 0), dtype=torch.float32, device="cuda"),
+         "delta": torch.empty((2, 5, 0), dtype=torch.float32, device="cuda"),
+         "A": -torch.ones((5, 4), dtype=torch.float32, device="cuda"),
+         "B": torch.empty((2, 4, 0), dtype=torch.float32, device="cuda"),
+         "C": torch.empty((2, 4, 0), dtype=torch.float32, device="cuda"),
+         "D": torch.ones(5, dtype=torch.float32, device="cuda"),
+         "bias": torch.zeros(5, dtype=torch.float32, device="cuda")}
+    dy = torch.empty((2, 5, 0), dtype=torch.float32, device="cuda")
+    got = ssm.selective_scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], dy, D=g["D"], delta_bias=g["bias"])
+    torch.cuda.synchronize()
+    for k in ("A", "D", "delta_bias"):
+        assert torch.equal(got[k], torch.zeros_like(got[k])), k
+    assert ssm.stream_status() == ssm.SSM_OK
+
+
 @pytest.mark.parametrize("L,chunks", [(560, 40), (512, 64), (560, 100)])
 def test_backward_time_split_many_chunks(L, chunks):
     """Many chunks of one or two 8-step segments: 32 to 64 chunks take the combine's warp scan
