@@ -556,6 +556,28 @@ def test_registered_workspace():
     assert torch.equal(y3, y) and torch.equal(h3, h)
 
 
+def test_registered_workspace_backward():
+    """The backward with no workspace argument takes the registered one (time-split shape:
+    checkpoints plus the split's arrays, over stale bytes), returns SSM_ERR_WORKSPACE when the
+    registration is too small, and allocates again once it is removed."""
+    import ctypes
+    Bt, D, L, N = 1, 32, 2048, 16
+    dm = ssm.dims(Bt, D, L, N, ssm.SSM_BF16)
+    need = ssm.load().ssm_selective_scan_bwd_workspace_bytes(ctypes.byref(dm))
+    assert need > 4 * D * (L // 8) * N                    # the time split's arrays too
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    try:
+        ssm.set_workspace(ws)
+        _check_backward(Bt, D, L, N, "bf16", True, "ones", True, True, "random")
+        ssm.set_workspace(ws[: need // 2])
+        with pytest.raises(ssm.SsmError) as e:
+            _check_backward(Bt, D, L, N, "bf16", True, "ones", True, True, "random")
+        assert e.value.code == ssm.SSM_ERR_WORKSPACE
+    finally:
+        ssm.set_workspace(None)
+    _check_backward(Bt, D, L, N, "bf16", True, "ones", True, True, "random")
+
+
 @pytest.mark.parametrize("cfg", [gen.BLOCK512, gen.ScanConfig("h", 3, 70, 333, 16, io="f32", gate=True, seed=8)],
                          ids=["block512", "ragged_f32"])
 def test_host_buffer_entry(cfg):
